@@ -1,0 +1,486 @@
+#!/usr/bin/env python3
+"""Benchmark: FP8 paged decode attention, tokens/s and HBM GB/s.
+
+Workload (default): the concurrency-sweep point with 64 requests -- each
+request has an 8192-token prompt already quantised into an e4m3 paged cache
+(GQA 32 query / 8 KV heads, head_dim 128, page 16, pool sized for 64
+requests x (8192 + 1000) tokens) -- decoding one token per request per step.
+One step is the whole hot path on one batch:
+    kvq_append (quantise the step's new K/V into the pages)
+    kvq_check_tags (batched page-tag integrity check -> abort mask)
+    kvq_decode_attn (plan + split-K paged attention + combine).
+Step i appends generated token (offset + i) mod 1000 of every request, so
+the context during the default run is ~8.6k-8.8k tokens, the mean context of
+the 1000-token generation.  All inputs are seeded synthetic data drawn by
+fp8_paged_kv_attn_gb300.inputs.  The KV cache read per step (~1.1 GB) is
+larger than L2, so no explicit flush is needed between steps.
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload: each step is one request's decode step.
+
+Prints ONE JSON line (rank 0).  Multi-GPU (torchrun): every rank runs its own
+independent replica of the workload (requests are independent; no
+collective on the data path); value = all ranks' tokens / max rank time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 paged decode attention: tokens/s and HBM GB/s (% of GB300 peak)"
+DECODE_KERNEL_SOURCES = ["fp8_paged_kv_attn_gb300/csrc/decode_attn.cu",
+                         "fp8_paged_kv_attn_gb300/csrc/kvq_device.cuh"]
+TRAFFIC_PROFILE = "profiles/decode_attn_sweep_b64.md"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--kv", choices=["e4m3", "bf16"], default="e4m3")
+    ap.add_argument("--check", choices=["on", "off"], default="on")
+    ap.add_argument("--offset", type=int, default=400, help="first generated-token index")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--seed", type=int, default=2)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (barrier + max of times only)
+# ----------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+        return dist, rank, world, local
+    return None, rank, world, local
+
+
+def dist_max(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def decode_source_sha() -> str:
+    h = hashlib.sha256()
+    for p in DECODE_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per decode-attention call from the committed ncu summary,
+    only if it was taken on the current kernel source."""
+    try:
+        text = open(os.path.join(ROOT, TRAFFIC_PROFILE)).read()
+    except OSError:
+        return None
+    sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    tr = re.search(r"traffic_bytes_per_call:\s*([0-9.eE+]+)", text)
+    if not sha or not tr or sha.group(1) != decode_source_sha():
+        return None
+    return float(tr.group(1))
+
+
+def attn_bytes(lens, Hq, Hkv, D, P, es):
+    """Algorithmic bytes of one decode-attention call: every cached K and V
+    element once, q in, out (fp32), and the block-table entries read."""
+    lens = np.asarray(lens, dtype=np.int64)
+    return int((lens * Hkv * D * 2 * es).sum() + len(lens) * Hq * D * (2 + 4)
+               + ((lens + P - 1) // P * 4).sum())
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args, dist, rank, world, local):
+    import torch
+    from fp8_paged_kv_attn_gb300 import inputs, kvq
+
+    torch.cuda.set_device(local)
+    kvq.load()
+    kv_bytes = 1 if args.kv == "e4m3" else 2
+    w = inputs.sweep(args.batch, kv_bytes=kv_bytes, seed=args.seed + rank)
+    B, Hq, Hkv, D, P = w.B, w.Hq, w.Hkv, w.D, w.P
+    steps_total = args.warmup + args.steps
+
+    # --- cache: prompt K/V drawn on the host, quantised into pages on the GPU
+    sources = w.kv_sources(threads=os.cpu_count() or 8)
+    ks, vs = w.scales(sources)
+    shape = w.pool_shape()
+    pdt = torch.uint8 if kv_bytes == 1 else torch.bfloat16
+    cache = kvq.KVCache(torch.zeros(shape, dtype=pdt, device="cuda"),
+                        torch.zeros(shape, dtype=pdt, device="cuda"), float(ks), float(vs))
+    bt = torch.from_numpy(w.block_table).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    for b, (k, v) in enumerate(sources):
+        req, pos = w.context_tokens(b)
+        kvq.kvq_append(cache, bf16(k).cuda(), bf16(v).cuda(), torch.from_numpy(req).cuda(),
+                       torch.from_numpy(pos).cuda(), bt, err_word=err)
+    torch.cuda.synchronize()
+    del sources
+
+    # --- per-step inputs (device resident for the kernel-time loop)
+    gen = [(args.offset + i) % inputs.SWEEP_DECODE_STEPS for i in range(steps_total)]
+    host_q, host_k, host_v, host_pos, host_len = [], [], [], [], []
+    for gi in gen:
+        q, k_new, v_new, _, pos = w.step_inputs(gi)
+        host_q.append(bf16(q))
+        host_k.append(bf16(k_new))
+        host_v.append(bf16(v_new))
+        host_pos.append(torch.from_numpy(pos))
+        host_len.append(torch.from_numpy(w.seq_lens_after(gi)))
+    d_q = [t.cuda() for t in host_q]
+    d_k = [t.cuda() for t in host_k]
+    d_v = [t.cuda() for t in host_v]
+    d_pos = [t.cuda() for t in host_pos]
+    d_len = [t.cuda() for t in host_len]
+    req_idx = torch.arange(B, dtype=torch.int32, device="cuda")
+    tags = torch.from_numpy(w.page_tags.view(np.int32)).cuda()
+    exp_tags = torch.from_numpy(w.expected_tags.view(np.int32)).cuda()
+    mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+    ws = kvq.workspace(B, Hq, Hkv, D)
+    check = args.check == "on"
+    stream = torch.cuda.current_stream()
+
+    def step(i, q, kn, vn, pos, lens, ev=None):
+        kvq.kvq_append(cache, kn, vn, req_idx, pos, bt, err_word=err)
+        if check:
+            kvq.kvq_check_tags(bt, lens, P, tags, exp_tags, mask)
+        if ev is not None:
+            ev[0].record(stream)
+        kvq.kvq_decode_attn(cache, q, bt, lens, out, ws, abort_mask=mask if check else None,
+                            sm_scale=float(w.sm_scale), err_word=err)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i, d_q[i], d_k[i], d_v[i], d_pos[i], d_len[i])
+    torch.cuda.synchronize()
+
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    dist_barrier(dist)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    t_start.record(stream)
+    for j in range(args.steps):
+        i = args.warmup + j
+        step(i, d_q[i], d_k[i], d_v[i], d_pos[i], d_len[i], ev=attn_ev[j])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    dist_barrier(dist)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = dist_max(dist, elapsed_ms)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item()):#x}")
+    if check and int(mask.sum().item()) != 0:
+        raise RuntimeError("integrity check aborted requests on a clean workload")
+
+    bytes_per_call = [attn_bytes(host_len[args.warmup + j].numpy(), Hq, Hkv, D, P, kv_bytes)
+                      for j in range(args.steps)]
+    achieved = sum(bytes_per_call) / (sum(attn_ms) * 1e-3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+
+    # --- end to end: the step's inputs copied from pinned host memory, the
+    # result (out + abort mask) read back, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.pin_memory()  # noqa: E731
+        hq = [pin(t) for t in host_q]
+        hk = [pin(t) for t in host_k]
+        hv = [pin(t) for t in host_v]
+        hp = [pin(t) for t in host_pos]
+        hl = [pin(t) for t in host_len]
+        sq, sk, sv = torch.empty_like(d_q[0]), torch.empty_like(d_k[0]), torch.empty_like(d_v[0])
+        sp, sl = torch.empty_like(d_pos[0]), torch.empty_like(d_len[0])
+        h_out = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+        h_mask = torch.empty(B, dtype=torch.uint8).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq[0], hk[0], hv[0], hp[0], hl[0]))
+        d2h = h_out.numel() * 4 + h_mask.numel()
+        torch.cuda.synchronize()
+        dist_barrier(dist)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for j in range(args.steps):
+            i = args.warmup + j
+            sq.copy_(hq[i], non_blocking=True)
+            sk.copy_(hk[i], non_blocking=True)
+            sv.copy_(hv[i], non_blocking=True)
+            sp.copy_(hp[i], non_blocking=True)
+            sl.copy_(hl[i], non_blocking=True)
+            step(i, sq, sk, sv, sp, sl)
+            h_out.copy_(out, non_blocking=True)
+            h_mask.copy_(mask, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = dist_max(dist, e0.elapsed_time(e1))
+        e2e = {"value": round(world * B * args.steps / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    value = world * B * args.steps / (elapsed_ms * 1e-3)
+    ctx_mean = float(np.mean([host_len[args.warmup + j].numpy().mean()
+                              for j in range(args.steps)]))
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) bf16 K/V with 1% outliers x20, quantised to e4m3 "
+                "in the GPU's append kernel)",
+        "config": {
+            "workload": f"concurrency sweep point: {B} requests x 8192-token prompt + decode "
+                        f"(generated tokens {gen[args.warmup]}..{gen[-1]}), GQA {Hq}/{Hkv}, "
+                        f"head_dim {D}, page {P}, {args.kv} KV, integrity check {args.check}",
+            "batch": B, "mean_context": round(ctx_mean, 1), "kv_dtype": args.kv,
+            "pool_pages": w.num_pages, "page_size": P, "check": args.check,
+            "l2": "inputs larger than L2 (~1.1 GB of KV read per step); no flush",
+            "step": "kvq_append + kvq_check_tags + kvq_decode_attn",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "kvq_decode_attn (plan + split + combine), CUDA events around each call",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(),
+            "bytes_per_call": int(statistics.mean(bytes_per_call)),
+            "ms_per_call": round(statistics.mean(attn_ms), 5),
+        },
+        "gpu_launches": args.steps * (1 + (1 if check else 0) + 3),
+        "clocks": clk,
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args, w, ks, vs, args.cpu_seconds)
+    return result
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ----------------------------------------------------------------------------
+
+class OracleRequestStep:
+    """One request's decode step on the CPU oracle: append its new token,
+    check its page tags, attend for every query head."""
+
+    def __init__(self, w, b, ks, vs):
+        import oracle
+        self.oracle = oracle
+        self.w, self.b, self.ks, self.vs = w, b, ks, vs
+        shape = w.pool_shape()
+        self.kp = np.zeros(shape, dtype=np.uint8)
+        self.vp = np.zeros(shape, dtype=np.uint8)
+        k, v = w.kv_source(b)
+        req, pos = w.context_tokens(b)
+        oracle.quant_append(oracle.KV_E4M3, self.kp, self.vp, ks, vs, k, v, req, pos,
+                            w.block_table)
+        self.bt1 = w.block_table[b:b + 1]
+
+    def run(self, gen_index, nthreads):
+        o, w, b = self.oracle, self.w, self.b
+        q, k_new, v_new, _, pos = w.step_inputs(gen_index)
+        o.quant_append(o.KV_E4M3, self.kp, self.vp, self.ks, self.vs, k_new[b:b + 1],
+                       v_new[b:b + 1], np.zeros(1, np.int32), pos[b:b + 1], self.bt1)
+        lens = w.seq_lens_after(gen_index)[b:b + 1]
+        mask = o.check_tags(self.bt1, lens, w.P, w.page_tags, w.expected_tags[b:b + 1])
+        out, err = o.decode_attn(o.KV_E4M3, self.kp, self.vp, self.ks, self.vs, q[b:b + 1],
+                                 self.bt1, lens, abort_mask=mask, sm_scale=w.sm_scale,
+                                 nthreads=nthreads)
+        return out
+
+
+def oracle_threads():
+    import oracle
+    n = os.cpu_count() or 1
+    return n if oracle.has_openmp() else 1
+
+
+def cpu_baseline(args, w, ks, vs, seconds):
+    nthreads = oracle_threads()
+    done, t_total, b = 0, 0.0, 0
+    gi = args.offset
+    while t_total < seconds and b < w.B:
+        st = OracleRequestStep(w, b, ks, vs)
+        t0 = time.perf_counter()
+        st.run(gi, nthreads)
+        t_total += time.perf_counter() - t0
+        done += 1
+        b += 1
+    return {"value": round(done / t_total, 3), "unit": "tokens/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{done} requests' decode step (append + tag check + fp64 attention over "
+                      f"~{int(w.ctx_lens[0]) + gi + 1} tokens, {w.Hq} heads), "
+                      f"{t_total:.1f} s of CPU time"}
+
+
+def run_reference(args, rank):
+    from fp8_paged_kv_attn_gb300 import inputs
+    w = inputs.sweep(args.batch, kv_bytes=1, seed=args.seed)
+    # scales of the full workload need every request's prompt; the sample uses
+    # request 0's own amax, which is what per-tensor calibration of that
+    # request alone would give
+    k0, v0 = w.kv_source(0)
+    ks = inputs.scale_from_amax(inputs.amax_bf16(k0))
+    vs = inputs.scale_from_amax(inputs.amax_bf16(v0))
+    nthreads = oracle_threads()
+    st = OracleRequestStep(w, 0, ks, vs)
+    for i in range(args.warmup):
+        st.run((args.offset + i) % inputs.SWEEP_DECODE_STEPS, nthreads)
+    t0 = time.perf_counter()
+    for j in range(args.steps):
+        st.run((args.offset + args.warmup + j) % inputs.SWEEP_DECODE_STEPS, nthreads)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    sample = (f"each step: one request's decode step (append + tag check + fp64 attention, "
+              f"{w.Hq} heads, ~{8192 + args.offset} tokens) of the {args.batch}-request sweep")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"concurrency sweep point ({args.batch} requests), one request "
+                               f"per step on the CPU oracle", "batch": 1},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": nthreads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        # the CPU oracle runs on rank 0 only; other ranks exit without work
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(run_reference(args, 0)), flush=True)
+        return
+    dist, rank, world, local = dist_setup()
+    result = run_gpu(args, dist, rank, world, local)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

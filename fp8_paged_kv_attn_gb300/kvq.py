@@ -1,0 +1,226 @@
+"""Python binding of the kvq C ABI (include/kvq.h): argument marshalling only.
+
+Every function here checks tensor devices, dtypes and shapes, takes raw
+device pointers and the current CUDA stream, and calls the function of the
+same name in libkvq.so.  All computation happens in the library's kernels;
+there is no fallback: if the library cannot be built or loaded, every call
+raises.
+
+Tensor conventions (torch is used for device memory and streams only):
+  pools          uint8 (e4m3 codes) or bfloat16, [num_pages, Hkv, P, D]
+  q              bfloat16 [B, Hq, D]; out float32 [B, Hq, D]
+  k_new, v_new   bfloat16 [N, Hkv, D]
+  block_table    int32 [B, MP]; seq_lens, req_idx, pos int32
+  page_tags      int32/uint32 [num_pages]; expected_tags [B, MP]
+  abort_mask     uint8 [B]; err_word int32/uint32 [1]
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _build
+
+KV_E4M3 = 0
+KV_BF16 = 1
+
+ERRBIT_PAGE = 1 << 0
+ERRBIT_SEQLEN = 1 << 1
+ERRBIT_POS = 1 << 2
+ERRBIT_REQ = 1 << 3
+ERRBIT_TIMEOUT = 1 << 4
+
+STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_WORKSPACE", 3: "KVQ_ERR_CUDA",
+          4: "KVQ_ERR_UNSUPPORTED"}
+
+# every symbol include/kvq.h declares
+EXPORTS = ("kvq_append", "kvq_check_tags", "kvq_decode_attn_workspace_size", "kvq_decode_attn",
+           "kvq_status_string")
+
+
+class KvqError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+        self.status = status
+
+
+class CCache(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("kv_dtype", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libkvq.so (building it with nvcc first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"CUDA library missing: {_build.LIB}")
+    L = ctypes.CDLL(_build.LIB)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    cp = ctypes.POINTER(CCache)
+    L.kvq_append.argtypes = [cp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp]
+    L.kvq_append.restype = ctypes.c_int
+    L.kvq_check_tags.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp, vp, vp]
+    L.kvq_check_tags.restype = ctypes.c_int
+    L.kvq_decode_attn_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.kvq_decode_attn_workspace_size.restype = sz
+    L.kvq_decode_attn.argtypes = [cp, vp, i32, i32, vp, i32, vp, vp, f32, vp, vp, sz, vp, vp]
+    L.kvq_decode_attn.restype = ctypes.c_int
+    L.kvq_status_string.argtypes = [ctypes.c_int]
+    L.kvq_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtypes, ndim=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, has {t.dim()}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise KvqError(fn, status)
+
+
+I32 = (torch.int32,)
+U32 = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+U8 = (torch.uint8, torch.bool)
+BF16 = (torch.bfloat16,)
+
+
+@dataclass
+class KVCache:
+    """Caller-owned paged K/V pools ([num_pages, Hkv, P, D]) and their scales."""
+    k_pool: torch.Tensor
+    v_pool: torch.Tensor
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    @property
+    def kv_dtype(self) -> int:
+        return KV_E4M3 if self.k_pool.element_size() == 1 else KV_BF16
+
+    @property
+    def shape(self):
+        return tuple(self.k_pool.shape)
+
+    def c(self) -> CCache:
+        dt = (torch.uint8, torch.float8_e4m3fn, torch.bfloat16)
+        _dev(self.k_pool, "k_pool", dt, 4)
+        _dev(self.v_pool, "v_pool", dt, 4)
+        if self.k_pool.shape != self.v_pool.shape or self.k_pool.dtype != self.v_pool.dtype:
+            raise ValueError("k_pool and v_pool must match")
+        NP, H, P, D = self.k_pool.shape
+        return CCache(self.k_pool.data_ptr(), self.v_pool.data_ptr(), self.kv_dtype, NP, P, H, D,
+                      float(self.k_scale), float(self.v_scale))
+
+    @staticmethod
+    def empty(num_pages, num_kv_heads, page_size, head_dim, kv_dtype=KV_E4M3, k_scale=1.0,
+              v_scale=1.0, device="cuda"):
+        dt = torch.uint8 if kv_dtype == KV_E4M3 else torch.bfloat16
+        shape = (num_pages, num_kv_heads, page_size, head_dim)
+        return KVCache(torch.empty(shape, dtype=dt, device=device),
+                       torch.empty(shape, dtype=dt, device=device), k_scale, v_scale)
+
+
+# ----------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# ----------------------------------------------------------------------------
+
+def kvq_append(cache: KVCache, k_new, v_new, req_idx, pos, block_table, err_word=None,
+               stream=None) -> None:
+    L = load()
+    c = cache.c()
+    N = int(req_idx.shape[0])
+    B, MP = block_table.shape
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        if tuple(t.shape) != (N, c.num_kv_heads, c.head_dim):
+            raise ValueError(f"{n} must be [{N}, {c.num_kv_heads}, {c.head_dim}]")
+    st = L.kvq_append(ctypes.byref(c), _dev(k_new, "k_new", BF16, 3), _dev(v_new, "v_new", BF16, 3),
+                      _dev(req_idx, "req_idx", I32, 1), _dev(pos, "pos", I32, 1), N,
+                      _dev(block_table, "block_table", I32, 2), B, MP,
+                      _dev(err_word, "err_word", U32), _stream(stream))
+    _check("kvq_append", st)
+
+
+def kvq_check_tags(block_table, seq_lens, page_size: int, page_tags, expected_tags, abort_mask,
+                   stream=None) -> None:
+    L = load()
+    B, MP = block_table.shape
+    if tuple(expected_tags.shape) != (B, MP) or abort_mask.shape[0] != B:
+        raise ValueError("expected_tags must be [B, MP] and abort_mask [B]")
+    st = L.kvq_check_tags(_dev(block_table, "block_table", I32, 2), B, MP,
+                          _dev(seq_lens, "seq_lens", I32, 1), int(page_size),
+                          _dev(page_tags, "page_tags", U32, 1), int(page_tags.shape[0]),
+                          _dev(expected_tags, "expected_tags", U32, 2),
+                          _dev(abort_mask, "abort_mask", U8, 1), _stream(stream))
+    _check("kvq_check_tags", st)
+
+
+def kvq_decode_attn_workspace_size(B: int, Hq: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(load().kvq_decode_attn_workspace_size(B, Hq, num_kv_heads, head_dim))
+
+
+def workspace(B: int, Hq: int, num_kv_heads: int, head_dim: int, device="cuda") -> torch.Tensor:
+    """Allocate (with torch) a workspace of the size kvq_decode_attn needs."""
+    n = kvq_decode_attn_workspace_size(B, Hq, num_kv_heads, head_dim)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def kvq_decode_attn(cache: KVCache, q, block_table, seq_lens, out, workspace, abort_mask=None,
+                    sm_scale: Optional[float] = None, err_word=None, stream=None) -> None:
+    L = load()
+    c = cache.c()
+    B, Hq, D = q.shape
+    if D != c.head_dim or tuple(out.shape) != (B, Hq, D):
+        raise ValueError("q / out shapes do not match the cache")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table / seq_lens must have B rows")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    st = L.kvq_decode_attn(ctypes.byref(c), _dev(q, "q", BF16, 3), B, Hq,
+                           _dev(block_table, "block_table", I32, 2), int(block_table.shape[1]),
+                           _dev(seq_lens, "seq_lens", I32, 1),
+                           _dev(abort_mask, "abort_mask", U8, 1), float(sm_scale),
+                           _dev(out, "out", (torch.float32,), 3),
+                           _dev(workspace, "workspace", (torch.uint8,), 1),
+                           workspace.numel() * workspace.element_size(),
+                           _dev(err_word, "err_word", U32), _stream(stream))
+    _check("kvq_decode_attn", st)

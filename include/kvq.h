@@ -1,0 +1,158 @@
+/*
+ * kvq -- FP8 (e4m3) paged KV cache: quantise-and-append, batched page-tag
+ * integrity check, and single-query paged decode attention for NVIDIA GB300
+ * (sm_103a).  Plain C ABI: pointers, sizes, a CUDA stream.  No allocation.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [KVQ]   "大规模服务 Kimi 与 GLM：KV 缓存量化、权重压缩与缓存安全" (a translation
+ *           of "Smaller, faster, safer: running Kimi and GLM at scale"), section
+ *           "KV 缓存量化" (KV-cache quantisation): the decode cache holds K and V
+ *           as 8-bit e4m3 instead of BF16 (half the bytes, twice the tokens);
+ *           the FP8 attention kernel converts on read; prefill keeps BF16.  Its
+ *           decode table compares a BF16-KV and an FP8-KV attention kernel.
+ *   [GUARD] same page, section "共享 KV 缓存保护" (protecting the shared KV cache):
+ *           each physical page has a tag that changes on every reallocation;
+ *           the server records the page and tag each request expects; a
+ *           separate batched check (not fused into attention) compares them
+ *           before decode reads the cache, and a mismatching request is
+ *           aborted instead of being served another request's data; the check
+ *           is enabled per deployment, the default tracker does nothing.
+ *   The e4m3 bit format is the OCP 8-bit floating point E4M3 format (bias 7,
+ *   no infinities, S.1111.111 = NaN, largest finite 448).
+ *
+ * Conventions for every entry point
+ *   - Pointers named *_host are host memory; every other pointer is DEVICE
+ *     memory owned by the caller.  The library never allocates, frees or
+ *     synchronises; all work is enqueued on `stream` (0 = legacy default).
+ *   - Host-checkable argument errors return a status != KVQ_OK before any
+ *     launch and enqueue nothing.  A failed launch returns KVQ_ERR_CUDA.
+ *   - Data-dependent faults found on the device never trap: the kernel skips
+ *     the access and ORs a KVQ_ERRBIT_* value into *err_word (device uint32,
+ *     nullable; the caller zeroes it when it wants a fresh reading).
+ *   - Layouts are row-major:
+ *       pools        [num_pages][num_kv_heads][page_size][head_dim] elements
+ *                    (uint8 e4m3 codes, or bf16);
+ *       block_table  int32 [B][MP]: logical page i of request b lives in
+ *                    physical page block_table[b*MP + i];
+ *       q            bf16 [B][Hq][head_dim]; out fp32 [B][Hq][head_dim];
+ *       k_new/v_new  bf16 [n_tokens][num_kv_heads][head_dim].
+ *   - Query head h reads KV head h / (Hq / num_kv_heads).
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kvq_stream_t; /* == cudaStream_t */
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, bad scale */
+    KVQ_ERR_WORKSPACE = 2,   /* workspace too small or misaligned */
+    KVQ_ERR_CUDA = 3,        /* a kernel launch or device query failed */
+    KVQ_ERR_UNSUPPORTED = 4  /* shape outside the compiled set (see each call) */
+} kvq_status;
+
+typedef enum { KVQ_KV_E4M3 = 0, KVQ_KV_BF16 = 1 } kvq_kv_dtype;
+
+/* Bits ORed into *err_word by the kernels. */
+#define KVQ_ERRBIT_PAGE    (1u << 0) /* a block-table entry the call needs is outside [0, num_pages) */
+#define KVQ_ERRBIT_SEQLEN  (1u << 1) /* seq_lens[b] < 0 or > MP * page_size */
+#define KVQ_ERRBIT_POS     (1u << 2) /* append position outside [0, MP * page_size) */
+#define KVQ_ERRBIT_REQ     (1u << 3) /* append request index outside [0, B) */
+#define KVQ_ERRBIT_TIMEOUT (1u << 4) /* a bounded wait inside a kernel gave up (no result) */
+
+/* The paged cache ([KVQ]): two pools of identical shape, one for K, one for V.
+ * Supported: page_size in {16, 32, 64}; head_dim in {64, 128};
+ * k_scale/v_scale finite and > 0 (per-tensor; e4m3 only, ignored for bf16).
+ * Pools must be 16-byte aligned. */
+typedef struct {
+    void *k_pool;
+    void *v_pool;
+    int32_t kv_dtype; /* kvq_kv_dtype */
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    float k_scale;
+    float v_scale;
+} kvq_cache;
+
+/* Quantise-and-append ([KVQ]: the decode cache is stored as e4m3).
+ * For each token t < n_tokens, request r = req_idx[t], position p = pos[t]:
+ * page = block_table[r*MP + p/page_size], slot = p % page_size, and for every
+ * kv head h and dim d
+ *     k_pool[page][h][slot][d] = e4m3_rne_satfinite( float(k_new[t][h][d]) / k_scale )
+ * (one IEEE fp32 division, round to nearest even, |x| > 448 and inf -> +-448,
+ * NaN -> a NaN code), the same for V with v_scale.  For a bf16 cache the
+ * bf16 values are copied unchanged.  Nothing else in the pools is written.
+ * Invalid r, p or page: that token writes nothing and raises KVQ_ERRBIT_REQ,
+ * _POS or _PAGE.  Two tokens must not target the same slot (unspecified).
+ * n_tokens may be any size (a whole prompt in one call); n_tokens == 0 is a
+ * no-op.  k_new/v_new 16-byte aligned. */
+KVQ_API kvq_status kvq_append(const kvq_cache *cache, const void *k_new, const void *v_new,
+                      const int32_t *req_idx, const int32_t *pos, int32_t n_tokens,
+                      const int32_t *block_table, int32_t B, int32_t MP,
+                      uint32_t *err_word, kvq_stream_t stream);
+
+/* Batched page-tag integrity check ([GUARD]), a separate pass before decode.
+ * abort_mask[b] = 1 if, for some logical page i < ceil(seq_lens[b]/page_size),
+ * block_table[b*MP+i] is outside [0, num_pages) or
+ * page_tags[block_table[b*MP+i]] != expected_tags[b*MP+i]; also 1 when
+ * seq_lens[b] is outside [0, MP*page_size]; else 0.  Block-table entries past
+ * the request's length are not read.  page_tags uint32 [num_pages],
+ * expected_tags uint32 [B][MP], abort_mask uint8 [B]. */
+KVQ_API kvq_status kvq_check_tags(const int32_t *block_table, int32_t B, int32_t MP,
+                          const int32_t *seq_lens, int32_t page_size,
+                          const uint32_t *page_tags, int32_t num_pages,
+                          const uint32_t *expected_tags, uint8_t *abort_mask,
+                          kvq_stream_t stream);
+
+/* Bytes of device workspace kvq_decode_attn needs for these sizes (split
+ * partials and the per-call work plan).  Depends on B, Hq, num_kv_heads and
+ * head_dim only, not on the sequence lengths. */
+KVQ_API size_t kvq_decode_attn_workspace_size(int32_t B, int32_t Hq, int32_t num_kv_heads,
+                                      int32_t head_dim);
+
+/* Single-query paged decode attention over the cache ([KVQ]: e4m3 K/V are
+ * converted on read; a bf16 cache is the comparison kernel).
+ * For every request b and query head h, with L = seq_lens[b] tokens and
+ * kv head g = h / (Hq/num_kv_heads), token j's K/V at
+ * page block_table[b*MP + j/page_size], slot j % page_size:
+ *     s_j = sm_scale * sum_d q[b][h][d] * k_scale * e4m3(k_code_j[d])
+ *     out[b][h][:] = sum_j softmax(s)_j * v_scale * e4m3(v_code_j[:])
+ * accumulated in fp32 (split over the sequence, merged by log-sum-exp).
+ * abort_mask (uint8 [B], nullable; NULL = no check was run): a request with
+ * abort_mask[b] != 0 reads none of its pages and gets out[b] = 0 ([GUARD]:
+ * an aborted request is never served cache data).  L == 0 gives a zero row.
+ * A page id outside the pool or an invalid L raises KVQ_ERRBIT_PAGE /
+ * _SEQLEN and zeroes that request's rows without reading the bad page.
+ * Supported: Hq/num_kv_heads in {1, 2, 4, 8}, head_dim in {64, 128},
+ * page_size in {16, 32, 64}.  q 16-byte aligned; workspace 256-byte aligned
+ * with at least kvq_decode_attn_workspace_size() bytes; the workspace must not
+ * be shared by calls that can run at the same time. */
+KVQ_API kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int32_t B, int32_t Hq,
+                           const int32_t *block_table, int32_t MP, const int32_t *seq_lens,
+                           const uint8_t *abort_mask, float sm_scale, float *out,
+                           void *workspace, size_t workspace_bytes, uint32_t *err_word,
+                           kvq_stream_t stream);
+
+/* Human-readable name of a status. */
+KVQ_API const char *kvq_status_string(kvq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,151 @@
+"""GPU parity of kvq_append and kvq_check_tags against the oracle (bit-exact)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_paged_kv_attn_gb300 import inputs
+from gpu_harness import Run, dev, dev_bf16, dev_u32, SENTINEL
+
+pytestmark = pytest.mark.gpu
+
+SCALES = [1.0, 3.0, 0.1, 1.0 / 3.0, 0.0123, 37.5, 1e-3, 2.0 ** -20]
+
+
+def _exhaustive_tokens():
+    """All 65,536 bf16 bit patterns laid out as 512 tokens x 1 head x 128 dims."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(512, 1, 128)
+    return bits
+
+
+@pytest.mark.parametrize("scale", SCALES)
+def test_append_every_bf16_value(kvq, scale):
+    """Every bf16 input (including inf and NaN) at several scales: the same
+    e4m3 byte as the oracle; NaN inputs give a NaN code."""
+    bits = _exhaustive_tokens()
+    N, H, D, P = bits.shape[0], 1, 128, 16
+    MP = N // P
+    bt = np.random.default_rng(5).permutation(MP).astype(np.int32).reshape(1, MP)
+    req = np.zeros(N, dtype=np.int32)
+    pos = np.arange(N, dtype=np.int32)
+    s32 = np.float32(scale)
+    cache = kvq.KVCache(torch.full((MP, H, P, D), SENTINEL, dtype=torch.uint8, device="cuda"),
+                        torch.full((MP, H, P, D), SENTINEL, dtype=torch.uint8, device="cuda"),
+                        float(s32), float(s32 * 2))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.kvq_append(cache, dev_bf16(bits), dev_bf16(bits[::-1].copy()), dev(req), dev(pos), dev(bt),
+                   err_word=err)
+    hk = np.full((MP, H, P, D), SENTINEL, dtype=np.uint8)
+    hv = hk.copy()
+    assert oracle.quant_append(oracle.KV_E4M3, hk, hv, s32, s32 * 2, bits, bits[::-1].copy(),
+                               req, pos, bt) == 0
+    gk = cache.k_pool.cpu().numpy()
+    gv = cache.v_pool.cpu().numpy()
+    assert int(err.item()) == 0
+    for g, h in ((gk, hk), (gv, hv)):
+        nan = (h & 0x7F) == 0x7F
+        assert np.array_equal(g[~nan], h[~nan])
+        assert np.all((g[nan] & 0x7F) == 0x7F)
+
+
+def test_append_bf16_pool_copies(kvq):
+    w = inputs.uniform("bf16copy", 41, B=3, ctx=77, Hq=8, Hkv=2, D=128, P=16)
+    r = Run(w, kv_dtype=kvq.KV_BF16)
+    r.fill_context()
+    r.assert_pools_equal(w.ctx_lens, whole=True)
+    assert r.err_word() == 0
+
+
+@pytest.mark.parametrize("mk", [inputs.tiny,
+                                lambda: inputs.uniform("u64", 42, B=4, ctx=300, Hq=16, Hkv=2,
+                                                       D=64, P=64, outlier_frac=0.01),
+                                lambda: inputs.ragged(seed=43, B=7, total=5000, lo=1, hi=2000,
+                                                      Hq=8, Hkv=8, D=128, P=32)],
+                         ids=["tiny", "u64", "ragged"])
+def test_append_context_and_step(kvq, mk):
+    """Bulk prompt append then one decode-step append: the whole pool equals
+    the oracle's byte for byte (untouched bytes keep their sentinel)."""
+    w = mk()
+    r = Run(w)
+    r.fill_context()
+    r.assert_pools_equal(w.ctx_lens, whole=True)
+    r.append_step(0)
+    torch.cuda.synchronize()
+    r.assert_pools_equal(w.seq_lens_after(0), whole=True)
+    assert r.err_word() == 0
+
+
+def test_append_errors(kvq):
+    w = inputs.tiny()
+    r = Run(w)
+    k = np.ones((4, w.Hkv, w.D), dtype=np.uint16) * 0x3F80
+    req = np.array([5, 0, 0, -1], dtype=np.int32)
+    pos = np.array([0, -1, w.MP * w.P, 0], dtype=np.int32)
+    bt = w.block_table.copy()
+    kvq.kvq_append(r.cache, dev_bf16(k), dev_bf16(k), dev(req), dev(pos), dev(bt), err_word=r.err)
+    torch.cuda.synchronize()
+    assert r.err_word() == (kvq.ERRBIT_REQ | kvq.ERRBIT_POS)
+    r.err.zero_()
+    bt[0, 0] = w.num_pages
+    kvq.kvq_append(r.cache, dev_bf16(k[:1]), dev_bf16(k[:1]), dev(req[1:2]), dev(pos[3:4]),
+                   dev(bt), err_word=r.err)
+    torch.cuda.synchronize()
+    assert r.err_word() == kvq.ERRBIT_PAGE
+    gk, gv = r.pool_bytes()
+    assert np.all(gk == SENTINEL) and np.all(gv == SENTINEL)
+
+
+def test_append_invalid_args_return_status(kvq):
+    w = inputs.tiny()
+    r = Run(w)
+    k = dev_bf16(np.zeros((1, w.Hkv, w.D), dtype=np.uint16))
+    bad = kvq.KVCache(r.cache.k_pool, r.cache.v_pool, -1.0, 1.0)
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_append(bad, k, k, dev(np.zeros(1, np.int32)), dev(np.zeros(1, np.int32)), r.bt)
+
+
+# ----------------------------------------------------------------------------
+# tag check
+# ----------------------------------------------------------------------------
+
+def _gpu_check(kvq, w, lens, bt=None, tags=None, exp=None):
+    bt = w.block_table if bt is None else bt
+    tags = w.page_tags if tags is None else tags
+    exp = w.expected_tags if exp is None else exp
+    mask = torch.full((w.B,), 7, dtype=torch.uint8, device="cuda")
+    kvq.kvq_check_tags(dev(bt), dev(lens), w.P, dev_u32(tags), dev_u32(exp), mask)
+    return mask.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,frac,ppv", [(256, 0.001, 1), (256, 0.1, 3), (64, 0.5, 2)])
+def test_check_integrity_workload(kvq, oracle_mod, B, frac, ppv):
+    """The integrity workload at full size (256 requests of 1k-16k tokens,
+    page 16): the GPU mask equals the oracle's and flags exactly the
+    requests that received stale tags."""
+    w = inputs.integrity(B=B, stale_frac=frac, pages_per_victim=ppv)
+    lens = w.seq_lens_after(0)
+    got = _gpu_check(kvq, w, lens)
+    ref = oracle_mod.check_tags(w.block_table, lens, w.P, w.page_tags, w.expected_tags)
+    assert np.array_equal(got, ref)
+    assert set(np.nonzero(got)[0].tolist()) == set(w.stale)
+
+
+def test_check_edges(kvq, oracle_mod):
+    w = inputs.ragged(seed=44, B=9, total=3000, lo=1, hi=900, Hq=8, Hkv=8, D=64, P=16)
+    lens = w.seq_lens_after(0).copy()
+    lens[0] = 0
+    lens[1] = w.MP * w.P + 1          # over capacity
+    lens[2] = -5
+    lens[4] = 5                       # one page; the rest of its row is garbage
+    lens[6] = 17                      # two pages
+    bt = w.block_table.copy()
+    bt[3, 0] = w.num_pages            # page id out of range
+    bt[4, 1:] = -1                    # past the request's length: never read
+    exp = w.expected_tags.copy()
+    n5 = -(-int(lens[5]) // w.P)
+    exp[5, n5 - 1] ^= 1               # last checked page stale
+    exp[6, 2:] += 3                   # entries past the length are ignored
+    got = _gpu_check(kvq, w, lens, bt=bt, exp=exp)
+    ref = oracle_mod.check_tags(bt, lens, w.P, w.page_tags, exp)
+    assert np.array_equal(got, ref)
+    assert got[:6].tolist() == [0, 1, 1, 1, 0, 1]

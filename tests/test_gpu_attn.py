@@ -1,0 +1,243 @@
+"""GPU parity of kvq_decode_attn (FP8 and BF16 caches) against the fp64
+oracle: |gpu - ref| <= 1e-3 + 1e-3 |ref| elementwise, plus exact cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle_pins as pins
+from fp8_paged_kv_attn_gb300 import inputs
+from gpu_harness import Run, assert_close, dev, dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def step_and_compare(kvq, w, kv_dtype=None, rows=None, host_requests=None, abort=None,
+                     check_pools=True):
+    kv_dtype = kvq.KV_E4M3 if kv_dtype is None else kv_dtype
+    r = Run(w, kv_dtype=kv_dtype, host_requests=host_requests)
+    r.fill_context()
+    q = r.append_step(0)
+    lens = w.seq_lens_after(0)
+    got = r.attend(q, lens, abort=abort)
+    if check_pools:
+        r.assert_pools_equal(lens)
+    if rows is None:
+        rows = [(b, h) for b in r.host_requests for h in range(w.Hq)]
+    ref, err = r.oracle_rows(q, lens, rows, abort=abort)
+    assert err == 0 and r.err_word() == 0
+    for b, h in rows:
+        assert_close(got[b, h], ref[b, h], f"{w.name} row ({b},{h})")
+    return r, got, ref, q, lens
+
+
+def test_tiny_fp8(kvq):
+    step_and_compare(kvq, inputs.tiny())
+
+
+def test_tiny_bf16(kvq):
+    step_and_compare(kvq, inputs.tiny(), kv_dtype=kvq.KV_BF16)
+
+
+SHAPES = [(G, D, P) for G in (1, 2, 4, 8) for D in (64, 128) for P in (16, 32, 64)]
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "bf16"])
+@pytest.mark.parametrize("G,D,P", SHAPES, ids=[f"g{g}_d{d}_p{p}" for g, d, p in SHAPES])
+def test_shapes(kvq, G, D, P, dtype):
+    """Every compiled (group size, head dim, page size) with ragged lengths
+    that span several work items and end mid-page."""
+    Hkv = 2
+    w = inputs.ragged(seed=100 + G + D + P, B=4, total=2600, lo=1, hi=1500, Hq=G * Hkv, Hkv=Hkv,
+                      D=D, P=P)
+    step_and_compare(kvq, w, kv_dtype=kvq.KV_E4M3 if dtype == "e4m3" else kvq.KV_BF16)
+
+
+def test_ragged_many_items(kvq):
+    """Lengths from 1 to ~6000 in one batch: each request splits into a
+    different number of items, tails end mid-stage."""
+    w = inputs.ragged(seed=7, B=12, total=30000, lo=1, hi=6000, Hq=32, Hkv=8, D=128, P=16)
+    step_and_compare(kvq, w)
+
+
+def test_one_token_is_exact(kvq):
+    """A 1-token context gives exactly v_scale * e4m3(v) (softmax weight 1)."""
+    w = inputs.uniform("one", 9, B=3, ctx=0, Hq=16, Hkv=4, D=128, P=16, outlier_frac=0.01)
+    r = Run(w)
+    q = r.append_step(0)
+    lens = w.seq_lens_after(0)
+    got = r.attend(q, lens)
+    for b in range(w.B):
+        page = w.block_table[b, 0]
+        for h in range(w.Hq):
+            v = (pins.torch_decode(r.hv[page, h // w.G, 0, :]) * float(r.v_scale)).astype(np.float32)
+            assert np.array_equal(got[b, h], v), (b, h)
+
+
+def test_equal_keys_mean_of_v(kvq):
+    w = inputs.uniform("eqk", 10, B=2, ctx=333, Hq=8, Hkv=2, D=64, P=16)
+    r = Run(w)
+    r.fill_context()
+    r.cache.k_pool.fill_(0x3C)
+    r.hk[...] = 0x3C
+    q, *_ = w.step_inputs(0)
+    got = r.attend(q, w.ctx_lens)
+    for b in range(w.B):
+        L = int(w.ctx_lens[b])
+        j = np.arange(L)
+        v = pins.torch_decode(r.hv[w.block_table[b, j // w.P], :, j % w.P, :]) * float(r.v_scale)
+        for h in range(w.Hq):
+            assert_close(got[b, h], v[:, h // w.G].mean(axis=0), "mean of V")
+
+
+def test_page_permutation_bitwise_and_deterministic(kvq):
+    """Moving every page to another physical slot leaves the GPU output bit
+    for bit unchanged; repeated calls give identical bits."""
+    w = inputs.ragged(seed=11, B=6, total=9000, lo=1, hi=4000, Hq=32, Hkv=8, D=128, P=16)
+    r = Run(w)
+    r.fill_context()
+    q, *_ = w.step_inputs(0)
+    a = r.attend(q, w.ctx_lens)
+    b = r.attend(q, w.ctx_lens)
+    assert np.array_equal(a, b)
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(w.num_pages)).cuda()
+    kp = torch.empty_like(r.cache.k_pool)
+    vp = torch.empty_like(r.cache.v_pool)
+    kp[perm] = r.cache.k_pool
+    vp[perm] = r.cache.v_pool
+    r.cache.k_pool, r.cache.v_pool = kp, vp
+    bt = w.block_table
+    r.bt = dev(np.where(bt >= 0, perm.cpu().numpy()[np.maximum(bt, 0)], -1).astype(np.int32))
+    c = r.attend(q, w.ctx_lens)
+    assert np.array_equal(a, c)
+
+
+def test_abort_reads_nothing(kvq):
+    """An aborted request's pages are filled with NaN codes: its output rows
+    are exactly zero and every other row is unaffected."""
+    w = inputs.uniform("abort", 12, B=5, ctx=700, Hq=16, Hkv=4, D=128, P=16)
+    r = Run(w)
+    r.fill_context()
+    q, *_ = w.step_inputs(0)
+    base = r.attend(q, w.ctx_lens)
+    victims = [1, 3]
+    for b in victims:
+        n = -(-int(w.ctx_lens[b]) // w.P)
+        pages = torch.from_numpy(w.block_table[b, :n].astype(np.int64)).cuda()
+        r.cache.k_pool[pages] = 0x7F
+        r.cache.v_pool[pages] = 0xFF
+    mask = np.zeros(w.B, dtype=np.uint8)
+    mask[victims] = 1
+    got = r.attend(q, w.ctx_lens, abort=mask)
+    assert not np.isnan(got).any()
+    for b in range(w.B):
+        if b in victims:
+            assert not got[b].any()
+        else:
+            assert np.array_equal(got[b], base[b])
+    assert r.err_word() == 0
+
+
+def test_errors_zero_rows(kvq):
+    w = inputs.uniform("errs", 13, B=4, ctx=100, Hq=8, Hkv=2, D=64, P=16)
+    r = Run(w)
+    r.fill_context()
+    q, *_ = w.step_inputs(0)
+    lens = w.ctx_lens.copy()
+    base = r.attend(q, lens)
+    lens[0] = 0
+    lens[1] = w.MP * w.P + 1
+    bt = w.block_table.copy()
+    bt[2, 3] = w.num_pages + 1
+    r.bt = dev(bt)
+    r.err.zero_()
+    got = r.attend(q, lens)
+    assert not got[0].any() and not got[1].any() and not got[2].any()
+    assert np.array_equal(got[3], base[3])
+    assert r.err_word() == (kvq.ERRBIT_SEQLEN | kvq.ERRBIT_PAGE)
+
+
+def test_all_aborted_and_empty_batch(kvq):
+    w = inputs.uniform("none", 14, B=3, ctx=40, Hq=8, Hkv=2, D=64, P=16)
+    r = Run(w)
+    r.fill_context()
+    q, *_ = w.step_inputs(0)
+    got = r.attend(q, w.ctx_lens, abort=np.ones(w.B, dtype=np.uint8))
+    assert not got.any()
+    got = r.attend(q, np.zeros(w.B, dtype=np.int32))
+    assert not got.any()
+
+
+def test_invalid_args(kvq):
+    w = inputs.tiny()
+    r = Run(w)
+    q = dev_bf16(np.zeros((w.B, w.Hq, w.D), dtype=np.uint16))
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device="cuda")
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_decode_attn(r.cache, q, r.bt, dev(w.ctx_lens), out, small)
+    assert e.value.status == 2
+    ws = kvq.workspace(w.B, w.Hq, w.Hkv, w.D)
+    r3 = kvq.KVCache(r.cache.k_pool, r.cache.v_pool, float("nan"), 1.0)
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_decode_attn(r3, q, r.bt, dev(w.ctx_lens), out, ws)
+
+
+# ----------------------------------------------------------------------------
+# full-size workloads (sampled rows)
+# ----------------------------------------------------------------------------
+
+def test_full_8x8192(kvq):
+    """8 requests x 8192 cached tokens (+1 appended), 32/8 heads, D=128,
+    page 16, pool 2x: every row of requests 0, 3 and 7."""
+    w = inputs.cfg8x8k()
+    step_and_compare(kvq, w, host_requests=[0, 3, 7])
+
+
+def test_full_sweep_b64(kvq):
+    """The concurrency-sweep point the benchmark times (64 requests, 8192-token
+    prompts, page 16, FP8 pool of 64 requests' bytes), after the step that
+    appends token 8193: sampled requests, all heads."""
+    w = inputs.sweep(64)
+    step_and_compare(kvq, w, host_requests=[0, 21, 63],
+                     rows=[(b, h) for b in (0, 21, 63) for h in (0, 5, 13, 31)])
+
+
+def test_full_sweep_bf16_b32(kvq):
+    w = inputs.sweep(32, kv_bytes=2)
+    step_and_compare(kvq, w, kv_dtype=kvq.KV_BF16, host_requests=[2, 31],
+                     rows=[(b, h) for b in (2, 31) for h in (1, 30)])
+
+
+def test_full_ragged(kvq):
+    """64 requests, log-uniform 512..131072 tokens (~1.37M total), 64/8 heads,
+    page 64, fragmented pool: shortest, median and longest requests."""
+    w = inputs.ragged()
+    order = np.argsort(w.ctx_lens)
+    picks = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
+    rows = [(b, h) for b in picks for h in (0, 9, 63)]
+    step_and_compare(kvq, w, host_requests=picks, rows=rows)
+
+
+def test_full_integrity(kvq, oracle_mod):
+    """256 requests of 1k-16k tokens with one stale tag: the GPU check's mask
+    feeds the GPU attention; the stale request's rows are zero, sampled
+    survivors match the oracle."""
+    w = inputs.integrity()
+    lens = w.seq_lens_after(0)
+    mask_ref = oracle_mod.check_tags(w.block_table, lens, w.P, w.page_tags, w.expected_tags)
+    victim = w.stale[0]
+    picks = [0, victim, 128, 255]
+    r = Run(w, host_requests=picks)
+    r.fill_context()
+    q = r.append_step(0)
+    mask = torch.empty(w.B, dtype=torch.uint8, device="cuda")
+    from gpu_harness import dev_u32
+    kvq.kvq_check_tags(r.bt, dev(lens), w.P, dev_u32(w.page_tags), dev_u32(w.expected_tags), mask)
+    assert np.array_equal(mask.cpu().numpy(), mask_ref)
+    got = r.attend(q, lens, abort=mask.cpu().numpy())
+    rows = [(b, h) for b in picks for h in (0, 17, 31)]
+    ref, err = r.oracle_rows(q, lens, rows, abort=mask_ref)
+    assert err == 0
+    assert not got[victim].any()
+    for b, h in rows:
+        assert_close(got[b, h], ref[b, h], f"integrity row ({b},{h})")

@@ -267,11 +267,13 @@ def run_gpu(args, dist, rank, world, local):
     dist_barrier(dist)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
+    torch.cuda.nvtx.range_push("timed")
     t_start.record(stream)
     for j in range(args.steps):
         i = args.warmup + j
         step(i, d_q[i], d_k[i], d_v[i], d_pos[i], d_len[i], ev=attn_ev[j])
     t_end.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     clk = clocks.stop()
     dist_barrier(dist)

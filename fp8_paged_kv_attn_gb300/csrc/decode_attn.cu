@@ -190,7 +190,9 @@ struct Cfg {
   static constexpr int CI = (16 / G < ITERS) ? 16 / G : ITERS;  // iterations per softmax chunk
   static constexpr int KV_BYTES = TS * D * ES;            // one stage of K (or V)
   static constexpr int Q_BYTES = G * D * 2;
-  static constexpr int RED = G * D + 2 * G;               // floats per warp in the merge area
+  // floats per warp in the merge area: acc[G][D], m[G], l[G], padded so that
+  // every warp's area starts on a 16-byte boundary (float4 stores)
+  static constexpr int RED = G * D + (2 * G + 3) / 4 * 4;
   static constexpr int PART = G * (D + 2);                // floats per partial
 
   static constexpr size_t off_k = 0;
@@ -205,6 +207,7 @@ struct Cfg {
   static_assert(TS % TPI == 0 && ITERS % CI == 0, "stage mapping");
   static_assert(kTokQuant % TS == 0, "items must hold whole stages");
   static_assert(off_q % 16 == 0 && off_red % 16 == 0 && off_desc % 16 == 0, "alignment");
+  static_assert(RED % 4 == 0 && (G * D) % 4 == 0 && (EPL * ES) % 8 == 0, "vector alignment");
 };
 
 struct SplitArgs {

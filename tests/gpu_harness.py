@@ -56,7 +56,9 @@ class Run:
         self.k_scale, self.v_scale = w.scales(self.sources)
         shape = w.pool_shape()
         tdt = torch.uint8 if fp8 else torch.int16
-        fill = SENTINEL if fp8 else SENTINEL | (SENTINEL << 8)
+        # the same sentinel byte in every byte of the pool
+        fill = SENTINEL if fp8 else int(np.array([SENTINEL | (SENTINEL << 8)],
+                                                 dtype=np.uint16).view(np.int16)[0])
         kp = torch.full(shape, fill, dtype=tdt, device="cuda")
         vp = torch.full(shape, fill, dtype=tdt, device="cuda")
         if not fp8:

@@ -39,6 +39,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "FP8 paged decode attention: tokens/s and HBM GB/s (% of GB300 peak)"
 DECODE_KERNEL_SOURCES = ["fp8_paged_kv_attn_gb300/csrc/decode_attn.cu",
+                         "fp8_paged_kv_attn_gb300/csrc/decode_attn_mma.cuh",
                          "fp8_paged_kv_attn_gb300/csrc/kvq_device.cuh"]
 TRAFFIC_PROFILE = "profiles/decode_attn_sweep_b64.md"
 

@@ -27,6 +27,9 @@
 // KVQ_ERRBIT_TIMEOUT and the CTA leaves its loop.
 #include <cfloat>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -520,6 +523,12 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
   }
 }
 
+}  // namespace kvq
+
+#include "decode_attn_mma.cuh"
+
+namespace kvq {
+
 // ---------------------------------------------------------------------------
 // combine
 // ---------------------------------------------------------------------------
@@ -564,15 +573,31 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 // ---------------------------------------------------------------------------
 
 using SplitFn = void (*)(SplitArgs);
+using SplitTmaFn = void (*)(CUtensorMap, CUtensorMap, SplitArgs);
 
 struct SplitKernel {
-  SplitFn fn;
-  size_t smem;
+  SplitFn fn = nullptr;      // CUDA-core kernel (bulk copies)
+  SplitTmaFn tma = nullptr;  // tensor-core kernel (tiled TMA); used when set
+  size_t smem = 0;
+  const void *ptr() const {
+    return tma ? reinterpret_cast<const void *>(tma) : reinterpret_cast<const void *>(fn);
+  }
 };
 
 template <int D, int G, bool kFp8>
 SplitKernel make_split() {
-  return SplitKernel{split_kernel<D, G, kFp8>, Cfg<D, G, kFp8>::bytes};
+  SplitKernel k;
+  k.fn = split_kernel<D, G, kFp8>;
+  k.smem = Cfg<D, G, kFp8>::bytes;
+  return k;
+}
+
+template <int G>
+SplitKernel make_split_mma() {
+  SplitKernel k;
+  k.tma = split_mma_kernel<G>;
+  k.smem = MmaCfg<G>::bytes;
+  return k;
 }
 
 template <int D, bool kFp8>
@@ -587,6 +612,15 @@ bool pick_g(int G, SplitKernel *k) {
 }
 
 bool pick_split(int D, int G, bool fp8, SplitKernel *k) {
+  if (fp8 && D == 128) {
+    switch (G) {
+      case 1: *k = make_split_mma<1>(); return true;
+      case 2: *k = make_split_mma<2>(); return true;
+      case 4: *k = make_split_mma<4>(); return true;
+      case 8: *k = make_split_mma<8>(); return true;
+    }
+    return false;
+  }
   if (D == 64) return fp8 ? pick_g<64, true>(G, k) : pick_g<64, false>(G, k);
   if (D == 128) return fp8 ? pick_g<128, true>(G, k) : pick_g<128, false>(G, k);
   return false;
@@ -595,32 +629,61 @@ bool pick_split(int D, int G, bool fp8, SplitKernel *k) {
 // Per (device, kernel) launch set-up: opt into the dynamic shared memory and
 // read back how many CTAs fit on one SM.
 int split_ctas_per_sm(const SplitKernel &k) {
-  constexpr int kMaxDev = 64, kMaxFn = 32;
+  constexpr int kMaxDev = 64, kMaxFn = 64;
   static int cache_dev_fn[kMaxDev][kMaxFn];
-  static SplitFn fns[kMaxFn];
+  static const void *fns[kMaxFn];
   static int nfns = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  const void *f = k.ptr();
   int fi = -1;
   for (int i = 0; i < nfns; ++i)
-    if (fns[i] == k.fn) fi = i;
+    if (fns[i] == f) fi = i;
   if (fi < 0) {
     if (nfns >= kMaxFn) return 0;
     fi = nfns;
-    fns[nfns++] = k.fn;
+    fns[nfns++] = f;
   }
   if (cache_dev_fn[dev][fi] > 0) return cache_dev_fn[dev][fi];
-  if (cudaFuncSetAttribute(reinterpret_cast<const void *>(k.fn),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(k.smem)) != cudaSuccess)
     return 0;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void *>(k.fn),
-                                                    32 * (kConsumerWarps + 1),
-                                                    k.smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, f, 32 * (kConsumerWarps + 1), k.smem) !=
+      cudaSuccess)
     return 0;
   cache_dev_fn[dev][fi] = occ;
   return occ;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 4-D map over an e4m3 pool [num_pages][Hkv][P][D] (D = 128 bytes innermost);
+// one box is one page of one kv head, 128-byte swizzled.
+bool encode_pool_map(CUtensorMap *map, const void *pool, const kvq_cache &c) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t D = c.head_dim, P = c.page_size, H = c.num_kv_heads, NP = c.num_pages;
+  const cuuint64_t dims[4] = {D, P, H, NP};
+  const cuuint64_t strides[3] = {D, P * D, H * P * D};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(P), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(pool), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace kvq
@@ -691,7 +754,15 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   sa.Hq = Hq;
   sa.MP = MP;
   sa.q_scale = sm_scale * (fp8 ? cache->k_scale : 1.0f) * kLog2e;
-  sk.fn<<<sms * occ, 32 * (kConsumerWarps + 1), sk.smem, s>>>(sa);
+  if (sk.tma) {
+    CUtensorMap kmap, vmap;
+    if (!encode_pool_map(&kmap, cache->k_pool, *cache) ||
+        !encode_pool_map(&vmap, cache->v_pool, *cache))
+      return KVQ_ERR_CUDA;
+    sk.tma<<<sms * occ, 32 * (kConsumerWarps + 1), sk.smem, s>>>(kmap, vmap, sa);
+  } else {
+    sk.fn<<<sms * occ, 32 * (kConsumerWarps + 1), sk.smem, s>>>(sa);
+  }
 
   CombineArgs ca{n_items, base, bad, part, out, Hq, Hkv, G, D, fp8 ? cache->v_scale : 1.0f};
   combine_kernel<<<B * Hkv, 256, 0, s>>>(ca);

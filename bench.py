@@ -8,7 +8,7 @@ requests x (8192 + 1000) tokens) -- decoding one token per request per step.
 One step is the whole hot path on one batch:
     kvq_append (quantise the step's new K/V into the pages)
     kvq_check_tags (batched page-tag integrity check -> abort mask)
-    kvq_decode_attn (plan + split-K paged attention + combine).
+    kvq_decode_attn (plan + split paged attention with the merge fused).
 Step i appends generated token (offset + i) mod 1000 of every request, so
 the context during the default run is ~8.6k-8.8k tokens, the mean context of
 the 1000-token generation.  All inputs are seeded synthetic data drawn by
@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "FP8 paged decode attention: tokens/s and HBM GB/s (% of GB300 peak)"
 DECODE_KERNEL_SOURCES = ["fp8_paged_kv_attn_gb300/csrc/decode_attn.cu",
                          "fp8_paged_kv_attn_gb300/csrc/decode_attn_mma.cuh",
+                         "fp8_paged_kv_attn_gb300/csrc/decode_common.cuh",
                          "fp8_paged_kv_attn_gb300/csrc/kvq_device.cuh"]
 TRAFFIC_PROFILE = "profiles/decode_attn_sweep_b64.md"
 
@@ -356,7 +357,7 @@ def run_gpu(args, dist, rank, world, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "kvq_decode_attn (plan + split + combine), CUDA events around each call",
+            "kernel": "kvq_decode_attn (plan + split), CUDA events around each call",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -367,7 +368,7 @@ def run_gpu(args, dist, rank, world, local):
             "bytes_per_call": int(statistics.mean(bytes_per_call)),
             "ms_per_call": round(statistics.mean(attn_ms), 5),
         },
-        "gpu_launches": args.steps * (1 + (1 if check else 0) + 3),
+        "gpu_launches": args.steps * (1 + (1 if check else 0) + 2),
         "clocks": clk,
     }
     if e2e is not None:

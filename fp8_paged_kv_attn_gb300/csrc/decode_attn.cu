@@ -7,21 +7,25 @@
 // token than the BF16 kernel it is compared with in the section's table).
 // The pages give no kernel design; this one is written for GB300:
 //
-//   plan     1 CTA: per-request split counts so that the whole batch becomes
-//            about kItemTarget equal work items of T tokens (T a multiple of
-//            64), plus a flat item list (b, kv head, token range).
-//   split    persistent, (#SMs x resident CTAs) CTAs of 5 warps.  Warp 4 is a
-//            producer: it takes items from an atomic counter, reads the block
-//            table and issues 1-D bulk copies (TMA engine) of each page's
-//            contiguous [slot][dim] chunk for this kv head into a 4-stage
-//            shared-memory ring (mbarrier-tracked, L2 evict-first).  Warps 0-3
-//            consume the ring: e4m3 -> fp32 in registers, q.k for the G query
-//            heads that share the kv head (each cached element is converted
-//            once and used G times), online softmax in the log2 domain with
-//            lazy rescaling, p.v accumulation; at the end of an item the four
-//            warps merge and write one partial (acc[G][D], m[G], l[G]).
-//   combine  1 CTA per (request, kv head): log-sum-exp merge of the request's
-//            partials, times v_scale; aborted / empty / invalid rows are 0.
+//   plan   1 CTA: per-request unit counts (64-token units), their prefix sum,
+//          where each persistent CTA starts, and zeroed per-row counters;
+//          rows of aborted / empty / invalid requests are written as zeros.
+//   split  persistent grid of (#SMs x resident CTAs), launched as a
+//          programmatic dependent of the plan so its set-up overlaps it.
+//          Each CTA owns an equal run of units (see decode_common.cuh).  Warp
+//          4 produces: it reads the block table and stages every page's
+//          contiguous [slot][dim] chunk of the row's kv head into a 4-stage
+//          shared-memory ring with TMA-engine copies (mbarrier-tracked, L2
+//          evict-first).  Warps 0-3 consume: convert, q.k for the G query
+//          heads sharing the kv head (each cached element converted once, used
+//          G times), online softmax in the log2 domain with lazy rescaling,
+//          p.v; at the end of a segment they merge and either write the
+//          output row or a partial that the row's last CTA merges.
+//   Two split kernels exist: a tensor-core one for e4m3 with head_dim 128
+//   (decode_attn_mma.cuh: rows are groups of up to 8 kv heads, 16-token
+//   units, one consumer warp per kv head, no combine step for whole rows)
+//   and a CUDA-core one for bf16 caches and head_dim 64 (rows are single kv
+//   heads, 64-token units, four consumer warps per row).
 //
 // Every wait is bounded (see mbar_wait); a wait that gives up raises
 // KVQ_ERRBIT_TIMEOUT and the CTA leaves its loop.
@@ -31,23 +35,16 @@
 #include <cudaTypedefs.h>
 
 #include "kvq_internal.h"
+#include "decode_common.cuh"
 
 namespace kvq {
-
-constexpr int kItemTarget = 4096;  // work items a call aims for
-constexpr int kTokQuant = 64;      // item boundaries are multiples of this
-constexpr int kConsumerWarps = 4;
-constexpr int kStages = 4;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 
 // ---------------------------------------------------------------------------
 // workspace layout
 // ---------------------------------------------------------------------------
 
 struct WsLayout {
-  size_t hdr, n_items, base, bad, items, part, total;
-  int64_t max_items;
+  size_t hdr, prefix, start, done, bad, part, total;
 };
 
 inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -55,20 +52,22 @@ inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 inline WsLayout ws_layout(int B, int Hq, int Hkv, int D) {
   WsLayout w;
   const int G = Hq / Hkv;
-  w.max_items = kItemTarget + static_cast<int64_t>(B) * Hkv;
+  const size_t rows = static_cast<size_t>(B) * Hkv;
   size_t off = 0;
   w.hdr = off;
-  off = round256(off + 64 * sizeof(int32_t));
-  w.n_items = off;
-  off = round256(off + static_cast<size_t>(B) * sizeof(int32_t));
-  w.base = off;
-  off = round256(off + static_cast<size_t>(B) * sizeof(int32_t));
+  off = round256(off + 16 * sizeof(int32_t));
+  w.prefix = off;
+  off = round256(off + (static_cast<size_t>(B) + 1) * sizeof(int32_t));
+  w.start = off;
+  off = round256(off + static_cast<size_t>(kMaxCtas) * sizeof(int4));
+  w.done = off;
+  off = round256(off + rows * sizeof(int32_t));
   w.bad = off;
-  off = round256(off + static_cast<size_t>(B) * sizeof(int32_t));
-  w.items = off;
-  off = round256(off + static_cast<size_t>(w.max_items) * sizeof(int4));
+  off = round256(off + rows * sizeof(int32_t));
+  // partial slots: row + CTA for every row split across CTAs; a tensor-core
+  // row holds up to 8 kv heads, a CUDA-core row one
   w.part = off;
-  off = round256(off + static_cast<size_t>(w.max_items) * G * (D + 2) * sizeof(float));
+  off = round256(off + (rows + 8ull * kMaxCtas) * G * (D + 2) * sizeof(float));
   w.total = off;
   return w;
 }
@@ -77,59 +76,44 @@ inline WsLayout ws_layout(int B, int Hq, int Hkv, int D) {
 // plan
 // ---------------------------------------------------------------------------
 
+constexpr int kPlanSmemPrefix = 4096;
+
 struct PlanArgs {
   const int32_t *seq_lens;
   const uint8_t *abort_mask;
-  int32_t *hdr, *n_items, *base, *bad;
-  int4 *items;
+  int32_t *hdr, *prefix;
+  int4 *start;
+  int32_t *done, *bad;
+  float *out;
   uint32_t *err_word;
-  int32_t B, Hkv, MP, P;
+  int32_t B, Hq, D, MP, P, nctas;
+  int32_t rows_per_req;  // rows of work per request (kv heads or kv-head groups)
+  int32_t unit;          // tokens per scheduling unit
 };
 
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
-  __shared__ long long s_sum[32];
+  allow_dependents();  // the split grid may start its set-up now
   __shared__ int s_scan[32];
   __shared__ int s_carry;
+  __shared__ int s_prefix[kPlanSmemPrefix];
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
-  const int nwarps = nt >> 5;
   const long long cap = static_cast<long long>(a.MP) * a.P;
-
-  // tokens of every request that will be read
-  long long sum = 0;
-  for (int b = tid; b < a.B; b += nt) {
-    const int L = a.seq_lens[b];
-    const bool aborted = a.abort_mask && a.abort_mask[b];
-    if (!aborted) {
-      if (L < 0 || L > cap)
-        report(a.err_word, KVQ_ERRBIT_SEQLEN);
-      else
-        sum += L;
-    }
-  }
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane == 0) s_sum[warp] = sum;
   if (tid == 0) s_carry = 0;
   __syncthreads();
-  long long total_tokens = 0;
-  for (int w = 0; w < nwarps; ++w) total_tokens += s_sum[w];
 
-  // tokens per item: the batch's kv-head work spread over ~kItemTarget items
-  const long long work = total_tokens * a.Hkv;
-  long long T = (work + kItemTarget - 1) / kItemTarget;
-  T = (T + kTokQuant - 1) / kTokQuant * kTokQuant;
-  if (T < kTokQuant) T = kTokQuant;
-
-  // per-request split counts and an exclusive scan of their item counts
   for (int b0 = 0; b0 < a.B; b0 += nt) {
     const int b = b0 + tid;
-    int n = 0;
+    int units = 0;
     if (b < a.B) {
       const int L = a.seq_lens[b];
       const bool aborted = a.abort_mask && a.abort_mask[b];
-      if (!aborted && L > 0 && L <= cap) n = static_cast<int>((L + T - 1) / T);
+      const bool in_range = L >= 0 && L <= cap;
+      if (!aborted && !in_range) report(a.err_word, KVQ_ERRBIT_SEQLEN);
+      if (!aborted && in_range) units = (L + a.unit - 1) / a.unit;
     }
-    const int cnt = n * a.Hkv;
+    const int cnt = units * a.rows_per_req;
     int incl = cnt;
+#pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
@@ -138,45 +122,62 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     __syncthreads();
     int warp_off = 0;
     for (int w = 0; w < warp; ++w) warp_off += s_scan[w];
-    const int base = s_carry + warp_off + incl - cnt;
+    const int pre = s_carry + warp_off + incl - cnt;
     if (b < a.B) {
-      a.n_items[b] = n;
-      a.base[b] = base;
-      a.bad[b] = 0;
+      a.prefix[b] = pre;
+      if (b < kPlanSmemPrefix) s_prefix[b] = pre;
+      for (int h = 0; h < a.rows_per_req; ++h) {
+        a.done[b * a.rows_per_req + h] = 0;
+        a.bad[b * a.rows_per_req + h] = 0;
+      }
+      if (units == 0) {  // aborted, empty or invalid: the rows are zero
+        float4 *o = reinterpret_cast<float4 *>(a.out + static_cast<int64_t>(b) * a.Hq * a.D);
+        for (int i = 0; i < a.Hq * a.D / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     __syncthreads();
-    if (tid == nt - 1) s_carry = base + cnt;
+    if (tid == nt - 1) s_carry = pre + cnt;
     __syncthreads();
   }
-  const int total_items = s_carry;
+  const int S = s_carry;
+  const int U = S > 0 ? (S + a.nctas - 1) / a.nctas : 1;
+  if (tid == 0) {
+    a.prefix[a.B] = S;
+    if (a.B < kPlanSmemPrefix) s_prefix[a.B] = S;
+  }
+  __syncthreads();
 
-  // flat item list: item i belongs to the last request whose base is <= i
-  for (int i = tid; i < total_items; i += nt) {
+  // where each CTA starts: the request whose units contain u = c * U
+  const bool in_smem = a.B < kPlanSmemPrefix;
+  for (int c = tid; c < a.nctas; c += nt) {
+    const long long u = static_cast<long long>(c) * U;
+    if (u >= S) {
+      a.start[c] = make_int4(-1, 0, 0, 0);
+      continue;
+    }
     int lo = 0, hi = a.B - 1;
-    while (lo < hi) {
+    while (lo < hi) {  // last b with prefix[b] <= u (it owns unit u)
       const int mid = (lo + hi + 1) >> 1;
-      if (__ldcg(a.base + mid) <= i)
+      const int pm = in_smem ? s_prefix[mid] : __ldcg(a.prefix + mid);
+      if (pm <= u)
         lo = mid;
       else
         hi = mid - 1;
     }
-    const int b = lo;
-    const int n = __ldcg(a.n_items + b);
-    const int r = i - __ldcg(a.base + b);
-    const int kvh = r / n, s = r % n;
-    const long long t0 = static_cast<long long>(s) * T;
-    const long long t1 = min(t0 + T, static_cast<long long>(a.seq_lens[b]));
-    a.items[i] = make_int4(b, kvh, static_cast<int>(t0), static_cast<int>(t1));
+    const int p0 = in_smem ? s_prefix[lo] : __ldcg(a.prefix + lo);
+    const int p1 = in_smem ? s_prefix[lo + 1] : __ldcg(a.prefix + lo + 1);
+    const int units_b = (p1 - p0) / a.rows_per_req;
+    const int r = static_cast<int>(u - p0);
+    a.start[c] = make_int4(lo, r / units_b, r % units_b, 0);
   }
   if (tid == 0) {
-    a.hdr[0] = 0;  // work counter for the split kernel
-    a.hdr[1] = total_items;
-    a.hdr[2] = static_cast<int>(T);
+    a.hdr[0] = S;
+    a.hdr[1] = U;
   }
 }
 
 // ---------------------------------------------------------------------------
-// split
+// CUDA-core split kernel (bf16 caches, head_dim 64)
 // ---------------------------------------------------------------------------
 
 template <int D, int G, bool kFp8>
@@ -196,47 +197,19 @@ struct Cfg {
   // floats per warp in the merge area: acc[G][D], m[G], l[G], padded so that
   // every warp's area starts on a 16-byte boundary (float4 stores)
   static constexpr int RED = G * D + (2 * G + 3) / 4 * 4;
-  static constexpr int PART = G * (D + 2);                // floats per partial
 
   static constexpr size_t off_k = 0;
   static constexpr size_t off_v = off_k + static_cast<size_t>(NS) * KV_BYTES;
   static constexpr size_t off_q = off_v + static_cast<size_t>(NS) * KV_BYTES;
   static constexpr size_t off_red = off_q + static_cast<size_t>(NS) * Q_BYTES;
-  static constexpr size_t off_desc = off_red + 2ull * NCW * RED * sizeof(float);
-  static constexpr size_t off_bar = off_desc + NS * sizeof(int4);
-  static constexpr size_t bytes = off_bar + (2 * NS + 2) * sizeof(uint64_t) + 16;
+  static constexpr size_t off_ctl = off_red + 2ull * NCW * RED * sizeof(float);
+  static constexpr size_t bytes = off_ctl + sizeof(Ctrl);
 
   static_assert(D % EPL == 0 && 32 % LPT == 0, "lane mapping");
   static_assert(TS % TPI == 0 && ITERS % CI == 0, "stage mapping");
-  static_assert(kTokQuant % TS == 0, "items must hold whole stages");
-  static_assert(off_q % 16 == 0 && off_red % 16 == 0 && off_desc % 16 == 0, "alignment");
+  static_assert(off_q % 16 == 0 && off_red % 16 == 0 && off_ctl % 16 == 0, "alignment");
   static_assert(RED % 4 == 0 && (G * D) % 4 == 0 && (EPL * ES) % 8 == 0, "vector alignment");
 };
-
-struct SplitArgs {
-  const uint8_t *k_pool, *v_pool;
-  const uint16_t *q;
-  const int32_t *block_table;
-  const int32_t *hdr;
-  int32_t *hdr_counter;
-  const int4 *items;
-  int32_t *bad;
-  float *part;
-  uint32_t *err_word;
-  int32_t num_pages, P, Hkv, Hq, MP;
-  float q_scale;  // sm_scale * k_scale * log2(e)
-};
-
-// desc.w packs the number of valid tokens (low 16 bits) and flags
-constexpr int kFirst = 1 << 16;
-constexpr int kLast = 1 << 17;
-
-// 2^x on the SFU (relative error ~2^-22; exactly 1 at x = 0)
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 template <int D, int G, bool kFp8, int EPL>
 __device__ __forceinline__ void load_row(const uint8_t *p, float *x) {
@@ -269,99 +242,28 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
   uint8_t *vbuf = smem + C::off_v;
   uint8_t *qbuf = smem + C::off_q;
   float *red = reinterpret_cast<float *>(smem + C::off_red);
-  int4 *desc = reinterpret_cast<int4 *>(smem + C::off_desc);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::off_bar);
-  uint64_t *empty = full + C::NS;
-  uint64_t *fin = empty + C::NS;
-  volatile int *fail = reinterpret_cast<volatile int *>(fin + 2);
+  Ctrl &ctl = *reinterpret_cast<Ctrl *>(smem + C::off_ctl);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::NCW);
-    }
-    mbar_init(&fin[0], C::NCW);
-    mbar_init(&fin[1], C::NCW);
-    *fail = 0;
-    fence_barrier_init();
-  }
+  if (threadIdx.x == 0) ctrl_init(ctl, C::NS, C::NCW);
   __syncthreads();
+  grid_dependency_wait();  // the plan's outputs are visible from here on
 
   if (warp == C::NCW) {
-    // ------------------------------------------------------------- producer
-    const int total_items = a.hdr[1];
     const uint32_t copy_tokens = C::TS > a.P ? a.P : C::TS;
     const uint32_t copy_bytes = copy_tokens * D * C::ES;
     const uint64_t pol = policy_evict_first();
-    uint32_t g = 0;  // stages issued by this CTA
-    bool ok = true;
-    while (ok) {
-      int item = 0;
-      if (lane == 0) item = atomicAdd(a.hdr_counter, 1);
-      item = __shfl_sync(0xffffffffu, item, 0);
-      const bool done = item >= total_items;
-      int4 it = make_int4(0, 0, 0, 0);
-      if (!done) it = a.items[item];
-      const int nstages = done ? 1 : (it.w - it.z + C::TS - 1) / C::TS;
-      for (int st = 0; st < nstages; ++st, ++g) {
-        const int slot = g % C::NS;
-        if (lane == 0 && g >= C::NS) {
-          if (*fail || !mbar_wait(&empty[slot], ((g / C::NS) - 1) & 1)) {
-            if (!*fail) report(a.err_word, KVQ_ERRBIT_TIMEOUT);
-            *fail = 1;
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, *fail, 0) == 0;
-        if (!ok) break;
-        if (done) {
-          if (lane == 0) {
-            desc[slot] = make_int4(-1, 0, 0, 0);
-            mbar_arrive(&full[slot]);
-          }
-          ok = false;
-          break;
-        }
-        const int b = it.x, kvh = it.y;
-        const int tok0 = it.z + st * C::TS;
-        const int ntok = min(C::TS, it.w - tok0);
-        const int npages = C::TS > a.P ? (ntok + a.P - 1) / a.P : 1;
-        int page = -1;
-        if (lane < npages) {
-          page = __ldg(a.block_table + static_cast<int64_t>(b) * a.MP + tok0 / a.P + lane);
-          if (page < 0 || page >= a.num_pages) {
-            atomicOr(a.bad + b, 1);
-            report(a.err_word, KVQ_ERRBIT_PAGE);
-            page = -1;
-          }
-        }
-        const unsigned valid_mask = __ballot_sync(0xffffffffu, page >= 0);
-        const bool first = st == 0, last = st == nstages - 1;
-        if (lane == 0) {
-          desc[slot] = make_int4(item, b * a.Hkv + kvh, tok0,
-                                 ntok | (first ? kFirst : 0) | (last ? kLast : 0));
-          const uint32_t tx = 2u * __popc(valid_mask) * copy_bytes + (first ? C::Q_BYTES : 0u);
-          mbar_arrive_expect_tx(&full[slot], tx);
-          if (first)
-            bulk_g2s(qbuf + slot * C::Q_BYTES,
-                     a.q + (static_cast<int64_t>(b) * a.Hq + kvh * G) * D, C::Q_BYTES,
-                     &full[slot]);
-        }
-        __syncwarp();  // the transaction count is armed before any page copy is issued
-        // lanes holding a valid page issue its K and V copies
-        if (page >= 0) {
+    producer_loop<C::TS, C::Q_BYTES, G, D>(
+        a, ctl, qbuf, lane, copy_bytes, [&](int slot, int l, int page, int kvh, int tok0) {
           const int64_t in_page = C::TS > a.P ? 0 : (tok0 % a.P);
-          const int64_t src = ((static_cast<int64_t>(page) * a.Hkv + kvh) * a.P + in_page) * D *
-                              C::ES;
-          const uint32_t dst = lane * copy_bytes;
+          const int64_t src =
+              ((static_cast<int64_t>(page) * a.Hkv + kvh) * a.P + in_page) * D * C::ES;
+          const uint32_t dst = l * copy_bytes;
           bulk_g2s_hint(kbuf + slot * C::KV_BYTES + dst, a.k_pool + src, copy_bytes,
-                        &full[slot], pol);
+                        &ctl.full[slot], pol);
           bulk_g2s_hint(vbuf + slot * C::KV_BYTES + dst, a.v_pool + src, copy_bytes,
-                        &full[slot], pol);
-        }
-        __syncwarp();
-      }
-    }
+                        &ctl.full[slot], pol);
+        });
     return;
   }
 
@@ -371,21 +273,17 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
   float q[G][C::EPL];
   float acc[G][C::EPL];
   float m_run[G], l_run[G];
-  uint32_t g = 0, n_items_done = 0;
-  int cur_item = 0;
+  uint32_t g = 0, segs = 0, csync_count = 0;
+  bool seg_bad = false;
 
   while (true) {
     const int slot = g % C::NS;
-    if (*fail || !mbar_wait(&full[slot], (g / C::NS) & 1)) {
-      if (!*fail) report(a.err_word, KVQ_ERRBIT_TIMEOUT);
-      *fail = 1;
-      break;
-    }
-    const int4 d = desc[slot];
-    if (d.x < 0) break;
-    const int ntok = d.w & 0xFFFF;
-    if (d.w & kFirst) {
-      cur_item = d.x;
+    if (!ctl_wait(ctl, &ctl.full[slot], (g / C::NS) & 1, a.err_word)) break;
+    const int4 d0 = ctl.desc[slot][0];
+    if (d0.x < 0) break;
+    const int4 d1 = ctl.desc[slot][1];
+    const int ntok = d0.z & 0xFFFF;
+    if (d0.z & kFirst) {
       const uint16_t *qs = reinterpret_cast<const uint16_t *>(qbuf + slot * C::Q_BYTES);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
@@ -401,7 +299,9 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
         m_run[h] = -INFINITY;
         l_run[h] = 0.f;
       }
+      seg_bad = false;
     }
+    seg_bad |= (d0.z & kBad) != 0;
 
     const uint8_t *ks = kbuf + slot * C::KV_BYTES;
     const uint8_t *vs = vbuf + slot * C::KV_BYTES;
@@ -456,10 +356,10 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (lane == 0) mbar_arrive(&ctl.empty[slot]);
 
-    if (d.w & kLast) {
-      // merge the warp's token groups
+    if (d0.z & kLast) {
+      // merge the warp's token groups, then the four warps
 #pragma unroll
       for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -469,7 +369,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
           for (int e = 0; e < C::EPL; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], o);
         }
       }
-      const int rb = n_items_done & 1;
+      const int rb = segs & 1;
       float *my = red + (rb * C::NCW + warp) * C::RED;
       if (lane < C::LPT) {
 #pragma unroll
@@ -487,37 +387,12 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&fin[rb]);
-      if (*fail || !mbar_wait(&fin[rb], (n_items_done >> 1) & 1)) {
-        if (!*fail) report(a.err_word, KVQ_ERRBIT_TIMEOUT);
-        *fail = 1;
-        break;
-      }
-      // merge the four warps and write the item's partial
-      const float *rr = red + rb * C::NCW * C::RED;
-      float *out = a.part + static_cast<int64_t>(cur_item) * C::PART;
-      const int ctid = warp * 32 + lane;
-      for (int idx = ctid; idx < G * D + G; idx += C::NCW * 32) {
-        const int h = idx < G * D ? idx / D : idx - G * D;
-        float mstar = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < C::NCW; ++w) mstar = fmaxf(mstar, rr[w * C::RED + G * D + h]);
-        float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < C::NCW; ++w) {
-          const float mw = rr[w * C::RED + G * D + h];
-          const float f = mw == -INFINITY ? 0.f : exp2f(mw - mstar);
-          const float v = idx < G * D ? rr[w * C::RED + idx] : rr[w * C::RED + G * D + G + h];
-          sum = fmaf(f, v, sum);
-        }
-        if (idx < G * D) {
-          out[idx] = sum;
-        } else {
-          out[G * D + h] = mstar;
-          out[G * D + G + h] = sum;
-        }
-      }
-      ++n_items_done;
+      if (lane == 0) mbar_arrive(&ctl.fin[rb]);
+      if (!ctl_wait(ctl, &ctl.fin[rb], (segs >> 1) & 1, a.err_word)) break;
+      finish_segment<G, D, C::RED>(a, ctl, red + rb * C::NCW * C::RED, d0, d1, seg_bad, lane,
+                                   csync_count);
+      if (ctl.fail) break;
+      ++segs;
     }
     ++g;
   }
@@ -530,45 +405,6 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
 namespace kvq {
 
 // ---------------------------------------------------------------------------
-// combine
-// ---------------------------------------------------------------------------
-
-struct CombineArgs {
-  const int32_t *n_items, *base, *bad;
-  const float *part;
-  float *out;
-  int32_t Hq, Hkv, G, D;
-  float v_scale;
-};
-
-__global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
-  const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv;
-  const int n = a.n_items[b];
-  const bool zero = n == 0 || a.bad[b] != 0;
-  const int GD = a.G * a.D;
-  const int stride = a.G * (a.D + 2);
-  float *out = a.out + (static_cast<int64_t>(b) * a.Hq + kvh * a.G) * a.D;
-  const float *p0 = a.part + static_cast<int64_t>(a.base[b] + kvh * n) * stride;
-  for (int idx = threadIdx.x; idx < GD; idx += blockDim.x) {
-    if (zero) {
-      out[idx] = 0.f;
-      continue;
-    }
-    const int h = idx / a.D;
-    float mstar = -INFINITY;
-    for (int s = 0; s < n; ++s) mstar = fmaxf(mstar, p0[s * stride + GD + h]);
-    float num = 0.f, den = 0.f;
-    for (int s = 0; s < n; ++s) {
-      const float ms = p0[s * stride + GD + h];
-      const float f = ms == -INFINITY ? 0.f : exp2f(ms - mstar);
-      num = fmaf(f, p0[s * stride + idx], num);
-      den = fmaf(f, p0[s * stride + GD + a.G + h], den);
-    }
-    out[idx] = num / den * a.v_scale;
-  }
-}
-
-// ---------------------------------------------------------------------------
 // host dispatch
 // ---------------------------------------------------------------------------
 
@@ -579,6 +415,9 @@ struct SplitKernel {
   SplitFn fn = nullptr;      // CUDA-core kernel (bulk copies)
   SplitTmaFn tma = nullptr;  // tensor-core kernel (tiled TMA); used when set
   size_t smem = 0;
+  int threads = 0;
+  int hg = 1;        // kv heads per row
+  int unit = kUnit;  // tokens per scheduling unit
   const void *ptr() const {
     return tma ? reinterpret_cast<const void *>(tma) : reinterpret_cast<const void *>(fn);
   }
@@ -589,15 +428,28 @@ SplitKernel make_split() {
   SplitKernel k;
   k.fn = split_kernel<D, G, kFp8>;
   k.smem = Cfg<D, G, kFp8>::bytes;
+  k.threads = 32 * (kConsumerWarps + 1);
+  return k;
+}
+
+template <int G, int HG>
+SplitKernel make_split_hg() {
+  SplitKernel k;
+  k.tma = split_hg_kernel<G, HG>;
+  k.smem = HgCfg<G, HG>::bytes;
+  k.threads = 32 * (HG + 1);
+  k.hg = HG;
+  k.unit = kTile;
   return k;
 }
 
 template <int G>
-SplitKernel make_split_mma() {
-  SplitKernel k;
-  k.tma = split_mma_kernel<G>;
-  k.smem = MmaCfg<G>::bytes;
-  return k;
+bool pick_hg(int Hkv, SplitKernel *k) {
+  if (Hkv % 8 == 0) { *k = make_split_hg<G, 8>(); return true; }
+  if (Hkv % 4 == 0) { *k = make_split_hg<G, 4>(); return true; }
+  if (Hkv % 2 == 0) { *k = make_split_hg<G, 2>(); return true; }
+  *k = make_split_hg<G, 1>();
+  return true;
 }
 
 template <int D, bool kFp8>
@@ -611,13 +463,13 @@ bool pick_g(int G, SplitKernel *k) {
   return false;
 }
 
-bool pick_split(int D, int G, bool fp8, SplitKernel *k) {
+bool pick_split(int D, int G, int Hkv, bool fp8, SplitKernel *k) {
   if (fp8 && D == 128) {
     switch (G) {
-      case 1: *k = make_split_mma<1>(); return true;
-      case 2: *k = make_split_mma<2>(); return true;
-      case 4: *k = make_split_mma<4>(); return true;
-      case 8: *k = make_split_mma<8>(); return true;
+      case 1: return pick_hg<1>(Hkv, k);
+      case 2: return pick_hg<2>(Hkv, k);
+      case 4: return pick_hg<4>(Hkv, k);
+      case 8: return pick_hg<8>(Hkv, k);
     }
     return false;
   }
@@ -649,8 +501,7 @@ int split_ctas_per_sm(const SplitKernel &k) {
                            static_cast<int>(k.smem)) != cudaSuccess)
     return 0;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, f, 32 * (kConsumerWarps + 1), k.smem) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, f, k.threads, k.smem) != cudaSuccess)
     return 0;
   cache_dev_fn[dev][fi] = occ;
   return occ;
@@ -672,14 +523,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 4-D map over an e4m3 pool [num_pages][Hkv][P][D] (D = 128 bytes innermost);
-// one box is one page of one kv head, 128-byte swizzled.
-bool encode_pool_map(CUtensorMap *map, const void *pool, const kvq_cache &c) {
+// one box is 16 slots of `hg` consecutive kv heads of one page, 128-byte
+// swizzled.
+bool encode_pool_map(CUtensorMap *map, const void *pool, const kvq_cache &c, int hg) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t D = c.head_dim, P = c.page_size, H = c.num_kv_heads, NP = c.num_pages;
   const cuuint64_t dims[4] = {D, P, H, NP};
   const cuuint64_t strides[3] = {D, P * D, H * P * D};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(P), 1, 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(kTile),
+                             static_cast<cuuint32_t>(hg), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(pool), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -710,11 +563,11 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   if (Hq % Hkv) return KVQ_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
   if (!q || !block_table || !seq_lens || !out || !workspace) return KVQ_ERR_INVALID_ARG;
-  if (!aligned16(q)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARG;
   if (static_cast<int64_t>(MP) * cache->page_size > INT32_MAX) return KVQ_ERR_INVALID_ARG;
   SplitKernel sk;
-  if (!pick_split(D, G, cache->kv_dtype == KVQ_KV_E4M3, &sk)) return KVQ_ERR_UNSUPPORTED;
+  if (!pick_split(D, G, Hkv, cache->kv_dtype == KVQ_KV_E4M3, &sk)) return KVQ_ERR_UNSUPPORTED;
   const WsLayout ws = ws_layout(B, Hq, Hkv, D);
   if (!aligned256(workspace) || workspace_bytes < ws.total) return KVQ_ERR_WORKSPACE;
 
@@ -722,19 +575,20 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   if (device_sm_count(&sms) != KVQ_OK) return KVQ_ERR_CUDA;
   const int occ = split_ctas_per_sm(sk);
   if (occ <= 0) return KVQ_ERR_CUDA;
+  const int nctas = sms * occ < kMaxCtas ? sms * occ : kMaxCtas;
 
   uint8_t *w = static_cast<uint8_t *>(workspace);
   int32_t *hdr = reinterpret_cast<int32_t *>(w + ws.hdr);
-  int32_t *n_items = reinterpret_cast<int32_t *>(w + ws.n_items);
-  int32_t *base = reinterpret_cast<int32_t *>(w + ws.base);
+  int32_t *prefix = reinterpret_cast<int32_t *>(w + ws.prefix);
+  int4 *start = reinterpret_cast<int4 *>(w + ws.start);
+  int32_t *done = reinterpret_cast<int32_t *>(w + ws.done);
   int32_t *bad = reinterpret_cast<int32_t *>(w + ws.bad);
-  int4 *items = reinterpret_cast<int4 *>(w + ws.items);
   float *part = reinterpret_cast<float *>(w + ws.part);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool fp8 = cache->kv_dtype == KVQ_KV_E4M3;
 
-  PlanArgs pa{seq_lens, abort_mask, hdr, n_items, base, bad, items, err_word,
-              B, Hkv, MP, cache->page_size};
+  PlanArgs pa{seq_lens, abort_mask, hdr, prefix, start, done, bad, out, err_word,
+              B, Hq, D, MP, cache->page_size, nctas, Hkv / sk.hg, sk.unit};
   plan_kernel<<<1, 1024, 0, s>>>(pa);
 
   SplitArgs sa;
@@ -742,29 +596,47 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   sa.v_pool = static_cast<const uint8_t *>(cache->v_pool);
   sa.q = static_cast<const uint16_t *>(q);
   sa.block_table = block_table;
+  sa.seq_lens = seq_lens;
   sa.hdr = hdr;
-  sa.hdr_counter = hdr;
-  sa.items = items;
+  sa.prefix = prefix;
+  sa.start = start;
+  sa.done = done;
   sa.bad = bad;
   sa.part = part;
+  sa.out = out;
   sa.err_word = err_word;
   sa.num_pages = cache->num_pages;
   sa.P = cache->page_size;
   sa.Hkv = Hkv;
   sa.Hq = Hq;
   sa.MP = MP;
+  sa.B = B;
   sa.q_scale = sm_scale * (fp8 ? cache->k_scale : 1.0f) * kLog2e;
+  sa.v_scale = fp8 ? cache->v_scale : 1.0f;
+
+  // the split grid is a programmatic dependent of the plan: its CTAs start
+  // (shared-memory and barrier set-up) while the plan finishes, and wait for
+  // the plan's results with griddepcontrol.wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nctas);
+  cfg.blockDim = dim3(sk.threads);
+  cfg.dynamicSmemBytes = sk.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (sk.tma) {
     CUtensorMap kmap, vmap;
-    if (!encode_pool_map(&kmap, cache->k_pool, *cache) ||
-        !encode_pool_map(&vmap, cache->v_pool, *cache))
+    if (!encode_pool_map(&kmap, cache->k_pool, *cache, sk.hg) ||
+        !encode_pool_map(&vmap, cache->v_pool, *cache, sk.hg))
       return KVQ_ERR_CUDA;
-    sk.tma<<<sms * occ, 32 * (kConsumerWarps + 1), sk.smem, s>>>(kmap, vmap, sa);
+    e = cudaLaunchKernelEx(&cfg, sk.tma, kmap, vmap, sa);
   } else {
-    sk.fn<<<sms * occ, 32 * (kConsumerWarps + 1), sk.smem, s>>>(sa);
+    e = cudaLaunchKernelEx(&cfg, sk.fn, sa);
   }
-
-  CombineArgs ca{n_items, base, bad, part, out, Hq, Hkv, G, D, fp8 ? cache->v_scale : 1.0f};
-  combine_kernel<<<B * Hkv, 256, 0, s>>>(ca);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -1,17 +1,23 @@
 // Tensor-core split kernel for an e4m3 cache with head_dim 128 (included by
-// decode_attn.cu; shares its plan, workspace, partial format and combine).
+// decode_attn.cu; shares its plan and partial-merge conventions).
 //
-// Same producer/consumer structure as the CUDA-core kernel, but:
-//  * pages are staged with tiled TMA copies (cp.async.bulk.tensor, 4-D map
-//    over the pool [page][kv head][slot][dim], 128-byte swizzle), so the
-//    fragment loads below are free of shared-memory bank conflicts;
-//  * q.k and p.v run on the tensor cores with mma.sync m16n8k16 (f16 in,
-//    fp32 accumulate).  Every e4m3 value is exactly representable in f16 and
-//    the query is bf16 scaled by a power of two into f16 range, so q.k is
-//    exact up to fp32 accumulation; the softmax weights are rounded to f16
-//    (relative error 2^-11) for p.v.
+// A CTA works on rows of (request, group of HG kv heads).  One stage is 16
+// cached tokens of all HG heads of the group: the pool layout
+// [page][kv head][slot][dim] makes those 16 x HG x 128 bytes one contiguous
+// block per page, so a single tiled TMA copy (cp.async.bulk.tensor, 4-D map,
+// box [128 dims][16 slots][HG heads][1 page], 128-byte swizzle) stages all of
+// K and one stages all of V.  Consumer warp w owns kv head w of the group:
+// it keeps that head's G query rows, softmax state and output accumulators in
+// registers, so no consumer warp ever waits for another except when a row
+// split across CTAs is merged.  Warp HG is the producer.
 //
-// Fragment layout of one consumer warp (16 tokens of the stage, lane = 4g+t):
+// q.k and p.v run on the tensor cores with mma.sync m16n8k16 (f16 in, fp32
+// accumulate).  Every e4m3 value is exactly representable in f16 and the
+// query is bf16 scaled by a power of two into f16 range, so q.k is exact up
+// to fp32 accumulation; the softmax weights are rounded to f16 (relative
+// error 2^-11) for p.v.
+//
+// Fragment layout of one consumer warp (16 tokens, lane = 4g+t):
 //   S[head][token]   = Q[head][dim] * K^T[dim][token]    (2 n-tiles of 8 tokens)
 //       k-step s (16 dims): thread t supplies dims 32t+4s .. 32t+4s+3, so its
 //       B operand is one 32-bit word of its K row (no shuffles, no permutes);
@@ -20,6 +26,8 @@
 //       V^T from rows 2t,2t+1,2t+8,2t+9 at dims 16g..16g+15 with byte permutes;
 //       m-tile i, row g is dim 16g+2i and row g+8 is dim 16g+2i+1.
 // Query heads occupy rows 0..G-1 of S (G <= 8) and columns 0..G-1 of O^T.
+// A row r of the 16-token tile sits at byte r*128 of the head's 2 KB block
+// with its 16-byte chunk c stored at chunk c ^ (r % 8) (TMA 128-byte swizzle).
 #pragma once
 
 namespace kvq {
@@ -58,124 +66,294 @@ __device__ __forceinline__ uint4 lds128(const uint8_t *p) {
   return *reinterpret_cast<const uint4 *>(p);
 }
 
-template <int G>
-struct MmaCfg {
+constexpr int kTile = 16;  // tokens per stage of the tensor-core kernel
+
+template <int G, int HG>
+struct HgCfg {
   static constexpr int D = 128;
-  static constexpr int TS = 64;  // tokens per stage: 4 consumer warps x 16
-  static constexpr int NS = kStages;
-  static constexpr int NCW = kConsumerWarps;
-  static constexpr int KV_BYTES = TS * D;  // one stage of K (or V), e4m3
-  static constexpr int Q_BYTES = G * D * 2;
-  static constexpr int RED = G * D + (2 * G + 3) / 4 * 4;
-  static constexpr int PART = G * (D + 2);
-  static constexpr size_t off_k = 0;  // 1024-byte aligned (128-byte swizzle atoms)
+  static constexpr int NS = (HG * G >= 64) ? 5 : 6;     // stages in the ring
+  static constexpr int HEAD_TILE = kTile * D;           // 2 KB: 16 tokens of one head
+  static constexpr int KV_BYTES = HG * HEAD_TILE;       // one stage of K (or V)
+  static constexpr int Q_BYTES = HG * G * D * 2;        // the group's query rows (bf16)
+  static constexpr int PART = HG * G * (D + 2);         // floats per partial slot
+  static constexpr size_t off_k = 0;                    // 1024-byte aligned
   static constexpr size_t off_v = off_k + static_cast<size_t>(NS) * KV_BYTES;
   static constexpr size_t off_q = off_v + static_cast<size_t>(NS) * KV_BYTES;
-  static constexpr size_t off_red = off_q + static_cast<size_t>(NS) * Q_BYTES;
-  static constexpr size_t off_desc = off_red + 2ull * NCW * RED * sizeof(float);
-  static constexpr size_t off_bar = off_desc + NS * sizeof(int4);
-  static constexpr size_t bytes = off_bar + (2 * NS + 2) * sizeof(uint64_t) + 16 + 1024;
-  static_assert(G >= 1 && G <= 8, "query heads per kv head");
-  static_assert(KV_BYTES % 1024 == 0 && off_red % 16 == 0 && off_desc % 16 == 0, "alignment");
-  static_assert(TS == NCW * 16 && kTokQuant % TS == 0, "stage mapping");
+  static constexpr size_t off_ctl = off_q + 2ull * Q_BYTES;
+  static constexpr size_t bytes = off_ctl + sizeof(Ctrl) + 1024;  // + alignment slack
+  static_assert(G >= 1 && G <= 8 && HG >= 1 && HG <= 8, "group sizes");
+  static_assert(KV_BYTES % 1024 == 0 && off_q % 1024 == 0 && off_ctl % 16 == 0, "alignment");
+  static_assert(NS <= kMaxStages, "control block");
+  static_assert(bytes <= 227 * 1024, "shared memory");
 };
 
+// One consumer warp's state for its kv head.
+struct HeadState {
+  uint32_t qa0[8], qa2[8];  // Q A-fragments (rows gq), per k-step
+  float o[8][4];            // O^T accumulators, per 16-dim m-tile
+  float m_run, l_run;       // softmax state of head gq (lanes with gq < G)
+  float qk_scale;
+};
+
+// q rows of this warp's kv head (bf16 in shared memory) -> f16 fragments,
+// scaled by 2^e so that the largest |q| of the head group sits in [2^14, 2^15).
 template <int G>
-__global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2)
-    split_mma_kernel(const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap vmap, SplitArgs a) {
-  using C = MmaCfg<G>;
+__device__ __forceinline__ void load_q(HeadState &st, const uint8_t *qhead, float q_scale, int gq,
+                                       int tq) {
+  float qf[32];
+  float qmax = 0.f;
+  if (gq < G) {
+    const uint8_t *qs = qhead + (gq * 128 + 32 * tq) * 2;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 w4 = lds128(qs + 16 * c);
+      bf16x2_to_f32(w4.x, qf + 8 * c);
+      bf16x2_to_f32(w4.y, qf + 8 * c + 2);
+      bf16x2_to_f32(w4.z, qf + 8 * c + 4);
+      bf16x2_to_f32(w4.w, qf + 8 * c + 6);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) qmax = fmaxf(qmax, fabsf(qf[i]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) qf[i] = 0.f;
+  }
+#pragma unroll
+  for (int o2 = 16; o2 > 0; o2 >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o2));
+  int e = (qmax > 0.f && qmax < INFINITY) ? 14 - ilogbf(qmax) : 0;
+  e = max(-100, min(100, e));
+  const float up = ldexpf(1.f, e);
+  st.qk_scale = q_scale * ldexpf(1.f, -e);
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    st.qa0[s] = f32x2_to_f16x2(qf[4 * s] * up, qf[4 * s + 1] * up);
+    st.qa2[s] = f32x2_to_f16x2(qf[4 * s + 2] * up, qf[4 * s + 3] * up);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+  st.m_run = -INFINITY;
+  st.l_run = 0.f;
+}
+
+// One 16-token tile of one kv head: ks / vs are the head's 2 KB swizzled
+// blocks, ntok (1..16) the valid tokens.
+template <int G>
+__device__ __forceinline__ void tile_step(HeadState &st, const uint8_t *ks, const uint8_t *vs,
+                                          int ntok, int gq, int tq) {
+  // ---- S = Q K^T for tokens gq (n-tile 0) and 8+gq (n-tile 1); row % 8 == gq
+  const uint8_t *k0 = ks + gq * 128;
+  const uint8_t *k1 = k0 + 8 * 128;
+  const int c0 = ((2 * tq) ^ gq) * 16, c1 = ((2 * tq + 1) ^ gq) * 16;
+  const uint4 k0a = lds128(k0 + c0), k0b = lds128(k0 + c1);
+  const uint4 k1a = lds128(k1 + c0), k1b = lds128(k1 + c1);
+  const uint32_t kw0[8] = {k0a.x, k0a.y, k0a.z, k0a.w, k0b.x, k0b.y, k0b.z, k0b.w};
+  const uint32_t kw1[8] = {k1a.x, k1a.y, k1a.z, k1a.w, k1b.x, k1b.y, k1b.z, k1b.w};
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    mma_16816(s0, st.qa0[s], 0u, st.qa2[s], 0u, e4m3x2_to_f16x2(kw0[s] & 0xFFFFu),
+              e4m3x2_to_f16x2(kw0[s] >> 16));
+    mma_16816(s1, st.qa0[s], 0u, st.qa2[s], 0u, e4m3x2_to_f16x2(kw1[s] & 0xFFFFu),
+              e4m3x2_to_f16x2(kw1[s] >> 16));
+  }
+  // ---- online softmax for head gq over the 16 tokens (log2 domain)
+  const bool row_ok = gq < G;
+  const int t0 = 2 * tq, t1 = 8 + 2 * tq;
+  const float x00 = (row_ok && t0 < ntok) ? s0[0] * st.qk_scale : -INFINITY;
+  const float x01 = (row_ok && t0 + 1 < ntok) ? s0[1] * st.qk_scale : -INFINITY;
+  const float x10 = (row_ok && t1 < ntok) ? s1[0] * st.qk_scale : -INFINITY;
+  const float x11 = (row_ok && t1 + 1 < ntok) ? s1[1] * st.qk_scale : -INFINITY;
+  float mx = fmaxf(fmaxf(x00, x01), fmaxf(x10, x11));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const bool grow = mx > st.m_run + kRescaleThreshold;
+  if (__any_sync(0xffffffffu, grow)) {
+    const float f = grow ? exp2f(st.m_run - mx) : 1.f;  // 0 when m_run is -inf
+    if (grow) {
+      st.m_run = mx;
+      st.l_run *= f;
+    }
+    // O^T columns 2t and 2t+1 belong to heads whose rows live in lanes 8t, 8t+4
+    const float fa = __shfl_sync(0xffffffffu, f, 8 * tq);
+    const float fb = __shfl_sync(0xffffffffu, f, 8 * tq + 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      st.o[i][0] *= fa;
+      st.o[i][1] *= fb;
+      st.o[i][2] *= fa;
+      st.o[i][3] *= fb;
+    }
+  }
+  const float p00 = x00 == -INFINITY ? 0.f : fast_exp2(x00 - st.m_run);
+  const float p01 = x01 == -INFINITY ? 0.f : fast_exp2(x01 - st.m_run);
+  const float p10 = x10 == -INFINITY ? 0.f : fast_exp2(x10 - st.m_run);
+  const float p11 = x11 == -INFINITY ? 0.f : fast_exp2(x11 - st.m_run);
+  st.l_run += (p00 + p01) + (p10 + p11);
+  const uint32_t pb0 = f32x2_to_f16x2(p00, p01);
+  const uint32_t pb1 = f32x2_to_f16x2(p10, p11);
+
+  // ---- O^T += V^T P^T: rows 2t, 2t+1, 2t+8, 2t+9 at logical chunk gq
+  const uint8_t *vr = vs + (2 * tq) * 128;
+  uint4 va = lds128(vr + ((gq ^ (2 * tq)) * 16));
+  uint4 vb = lds128(vr + 128 + ((gq ^ (2 * tq + 1)) * 16));
+  uint4 vc = lds128(vr + 8 * 128 + ((gq ^ (2 * tq)) * 16));
+  uint4 vd = lds128(vr + 9 * 128 + ((gq ^ (2 * tq + 1)) * 16));
+  if (ntok < kTile) {  // tail: cached bytes past the sequence may be anything
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    if (t0 >= ntok) va = z;
+    if (t0 + 1 >= ntok) vb = z;
+    if (t1 >= ntok) vc = z;
+    if (t1 + 1 >= ntok) vd = z;
+  }
+  const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+  const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes (a.b, b.b, a.b+1, b.b+1)
+    const uint32_t x = prmt(wa[i >> 1], wb[i >> 1], sel);
+    const uint32_t y = prmt(wc[i >> 1], wd[i >> 1], sel);
+    mma_16816(st.o[i], e4m3x2_to_f16x2(x & 0xFFFFu), e4m3x2_to_f16x2(x >> 16),
+              e4m3x2_to_f16x2(y & 0xFFFFu), e4m3x2_to_f16x2(y >> 16), pb0, pb1);
+  }
+}
+
+template <int G, int HG>
+__global__ void __launch_bounds__(32 * (HG + 1))
+    split_hg_kernel(const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap, SplitArgs a) {
+  using C = HgCfg<G, HG>;
+  constexpr int NS = C::NS;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // TMA 128-byte swizzle needs 1024-byte aligned destinations
   uint8_t *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   uint8_t *kbuf = smem + C::off_k;
   uint8_t *vbuf = smem + C::off_v;
   uint8_t *qbuf = smem + C::off_q;
-  float *red = reinterpret_cast<float *>(smem + C::off_red);
-  int4 *desc = reinterpret_cast<int4 *>(smem + C::off_desc);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::off_bar);
-  uint64_t *empty = full + C::NS;
-  uint64_t *fin = empty + C::NS;
-  volatile int *fail = reinterpret_cast<volatile int *>(fin + 2);
+  Ctrl &ctl = *reinterpret_cast<Ctrl *>(smem + C::off_ctl);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::NCW);
-    }
-    mbar_init(&fin[0], C::NCW);
-    mbar_init(&fin[1], C::NCW);
-    *fail = 0;
-    fence_barrier_init();
+    ctrl_init(ctl, NS, HG);
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
   }
   __syncthreads();
+  grid_dependency_wait();  // the plan's outputs are visible from here on
 
-  if (warp == C::NCW) {
+  const int S = a.hdr[0], U = a.hdr[1];
+  const int c = blockIdx.x;
+  const int groups = a.Hkv / HG;  // rows per request
+
+  if (warp == HG) {
     // ------------------------------------------------------------- producer
-    const int total_items = a.hdr[1];
-    const uint32_t page_box = static_cast<uint32_t>(a.P) * C::D;  // bytes of one page box
+    long long u = static_cast<long long>(c) * U;
+    const long long u_end = min(u + U, static_cast<long long>(S));
+    int b = 0, grp = 0, s = 0;
+    if (u < u_end) {
+      const int4 st = a.start[c];
+      b = st.x;
+      grp = st.y;
+      s = st.z;
+    }
     const uint64_t pol = policy_evict_first();
-    uint32_t g = 0;
+    // block-table window of the current request: lane i holds logical page
+    // win+i (cur) and win+32+i (nxt, loaded one window ahead)
+    int win_b = -1, win = 0, cur = -1, nxt = -1;
+    const int32_t *bt_row = a.block_table;
+    auto bt_load = [&](int lp) -> int { return lp < a.MP ? __ldg(bt_row + lp) : -1; };
+    uint32_t g = 0, nseg = 0;
     bool ok = true;
-    while (ok) {
-      int item = 0;
-      if (lane == 0) item = atomicAdd(a.hdr_counter, 1);
-      item = __shfl_sync(0xffffffffu, item, 0);
-      const bool done = item >= total_items;
-      int4 it = make_int4(0, 0, 0, 0);
-      if (!done) it = a.items[item];
-      const int nstages = done ? 1 : (it.w - it.z + C::TS - 1) / C::TS;
+    while (ok && u < u_end) {
+      const int p0 = __ldg(a.prefix + b), p1 = __ldg(a.prefix + b + 1);
+      const int units_b = (p1 - p0) / groups;
+      const int L = __ldg(a.seq_lens + b);
+      const int row = b * groups + grp;
+      const long long ur = static_cast<long long>(p0) + static_cast<long long>(grp) * units_b;
+      const int c_lo = static_cast<int>(ur / U);
+      const int nparts = static_cast<int>((ur + units_b - 1) / U) - c_lo + 1;
+      const int seg_units = static_cast<int>(min(static_cast<long long>(units_b - s), u_end - u));
+      const int t_begin = s * kTile;
+      const int t_end = min((s + seg_units) * kTile, L);
+      const int nstages = (t_end - t_begin + kTile - 1) / kTile;
+      const int lp0 = t_begin / a.P;
+      if (b != win_b || lp0 < win || lp0 >= win + 32) {
+        win_b = b;
+        win = lp0;
+        bt_row = a.block_table + static_cast<int64_t>(b) * a.MP;
+        cur = bt_load(win + lane);
+        nxt = bt_load(win + 32 + lane);
+      }
+      // the group's query rows, double-buffered per segment
+      const int qs = nseg & 1;
+      if (lane == 0) {
+        bool w_ok = true;
+        if (nseg >= 2) w_ok = ctl_wait(ctl, &ctl.qempty[qs], ((nseg >> 1) - 1) & 1, a.err_word);
+        if (w_ok) {
+          mbar_arrive_expect_tx(&ctl.qfull[qs], C::Q_BYTES);
+          bulk_g2s(qbuf + qs * C::Q_BYTES,
+                   a.q + (static_cast<int64_t>(b) * a.Hq + grp * HG * G) * C::D, C::Q_BYTES,
+                   &ctl.qfull[qs]);
+        }
+      }
       for (int st = 0; st < nstages; ++st, ++g) {
-        const int slot = g % C::NS;
-        if (lane == 0 && g >= C::NS) {
-          if (*fail || !mbar_wait(&empty[slot], ((g / C::NS) - 1) & 1)) {
-            if (!*fail) report(a.err_word, KVQ_ERRBIT_TIMEOUT);
-            *fail = 1;
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, *fail, 0) == 0;
+        const int slot = g % NS;
+        bool waited = true;
+        if (lane == 0 && g >= NS)
+          waited = ctl_wait(ctl, &ctl.empty[slot], ((g / NS) - 1) & 1, a.err_word);
+        ok = __shfl_sync(0xffffffffu, waited ? 1 : 0, 0) != 0 &&
+             !*reinterpret_cast<volatile int *>(&ctl.fail);
         if (!ok) break;
-        if (done) {
-          if (lane == 0) {
-            desc[slot] = make_int4(-1, 0, 0, 0);
-            mbar_arrive(&full[slot]);
-          }
-          ok = false;
-          break;
+        const int tok0 = t_begin + st * kTile;
+        const int ntok = min(kTile, t_end - tok0);
+        const int lp = tok0 / a.P;
+        while (lp >= win + 32) {  // slide the window by 32 pages
+          win += 32;
+          cur = nxt;
+          nxt = bt_load(win + 32 + lane);
         }
-        const int b = it.x, kvh = it.y;
-        const int tok0 = it.z + st * C::TS;
-        const int ntok = min(C::TS, it.w - tok0);
-        const int npages = (ntok + a.P - 1) / a.P;  // page_size <= TS
-        int page = -1;
-        if (lane < npages) {
-          page = __ldg(a.block_table + static_cast<int64_t>(b) * a.MP + tok0 / a.P + lane);
-          if (page < 0 || page >= a.num_pages) {
-            atomicOr(a.bad + b, 1);
-            report(a.err_word, KVQ_ERRBIT_PAGE);
-            page = -1;
-          }
-        }
-        const unsigned valid_mask = __ballot_sync(0xffffffffu, page >= 0);
-        const bool first = st == 0, last = st == nstages - 1;
+        const int page = __shfl_sync(0xffffffffu, cur, lp - win);
+        const bool bad_page = page < 0 || page >= a.num_pages;
         if (lane == 0) {
-          desc[slot] = make_int4(item, b * a.Hkv + kvh, tok0,
-                                 ntok | (first ? kFirst : 0) | (last ? kLast : 0));
-          const uint32_t tx = 2u * __popc(valid_mask) * page_box + (first ? C::Q_BYTES : 0u);
-          mbar_arrive_expect_tx(&full[slot], tx);
-          if (first)
-            bulk_g2s(qbuf + slot * C::Q_BYTES,
-                     a.q + (static_cast<int64_t>(b) * a.Hq + kvh * G) * C::D, C::Q_BYTES,
-                     &full[slot]);
-        }
-        __syncwarp();  // the transaction count is armed before any page copy is issued
-        if (page >= 0) {
-          const uint32_t dst = lane * page_box;
-          tma_load_4d(kbuf + slot * C::KV_BYTES + dst, &kmap, 0, 0, kvh, page, &full[slot], pol);
-          tma_load_4d(vbuf + slot * C::KV_BYTES + dst, &vmap, 0, 0, kvh, page, &full[slot], pol);
+          if (bad_page) {
+            atomicOr(a.bad + row, 1);
+            report(a.err_word, KVQ_ERRBIT_PAGE);
+          }
+          ctl.desc[slot][0] = make_int4(
+              row, tok0,
+              ntok | (st == 0 ? kFirst : 0) | (st == nstages - 1 ? kLast : 0) |
+                  (bad_page ? kBad : 0),
+              nparts);
+          ctl.desc[slot][1] = make_int4(row + c, c_lo, b, grp | (qs << 16));
+          mbar_arrive_expect_tx(&ctl.full[slot], bad_page ? 0u : 2u * C::KV_BYTES);
+          if (!bad_page) {
+            const int y = tok0 % a.P;
+            tma_load_4d(kbuf + slot * C::KV_BYTES, &kmap, 0, y, grp * HG, page, &ctl.full[slot],
+                        pol);
+            tma_load_4d(vbuf + slot * C::KV_BYTES, &vmap, 0, y, grp * HG, page, &ctl.full[slot],
+                        pol);
+          }
         }
         __syncwarp();
+      }
+      ++nseg;
+      u += seg_units;
+      s = 0;
+      if (++grp == groups) {
+        grp = 0;
+        ++b;
+        // requests without work (aborted, empty or invalid) own no units
+        while (b < a.B && __ldg(a.prefix + b + 1) == __ldg(a.prefix + b)) ++b;
+      }
+    }
+    // tell the consumers there is nothing more
+    if (ok) {
+      const int slot = g % NS;
+      bool waited = true;
+      if (lane == 0 && g >= NS)
+        waited = ctl_wait(ctl, &ctl.empty[slot], ((g / NS) - 1) & 1, a.err_word);
+      if (lane == 0 && waited) {
+        ctl.desc[slot][0] = make_int4(-1, 0, 0, 0);
+        mbar_arrive(&ctl.full[slot]);
       }
     }
     return;
@@ -184,195 +362,145 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2)
   // --------------------------------------------------------------- consumers
   const int gq = lane >> 2;  // fragment row group
   const int tq = lane & 3;   // thread in group
-  uint32_t qa0[8], qa2[8];   // Q A-fragments (rows gq), per k-step
-  float o[8][4];             // O^T accumulators, per 16-dim m-tile
-  float m_run = -INFINITY, l_run = 0.f;  // softmax state of head gq (lanes with gq < G)
-  float qk_scale = 0.f;
-  uint32_t g = 0, n_items_done = 0;
-  int cur_item = 0;
+  HeadState hs;
+  uint32_t g = 0, nseg = 0, csync_count = 0;
+  bool seg_bad = false;
 
   while (true) {
-    const int slot = g % C::NS;
-    if (*fail || !mbar_wait(&full[slot], (g / C::NS) & 1)) {
-      if (!*fail) report(a.err_word, KVQ_ERRBIT_TIMEOUT);
-      *fail = 1;
-      break;
+    const int slot = g % NS;
+    if (!ctl_wait(ctl, &ctl.full[slot], (g / NS) & 1, a.err_word)) break;
+    const int4 d0 = ctl.desc[slot][0];
+    if (d0.x < 0) break;
+    const int4 d1 = ctl.desc[slot][1];
+    const int ntok = d0.z & 0xFFFF;
+    if (d0.z & kFirst) {
+      const int qs = (d1.w >> 16) & 1;
+      if (!ctl_wait(ctl, &ctl.qfull[qs], (nseg >> 1) & 1, a.err_word)) break;
+      load_q<G>(hs, qbuf + qs * C::Q_BYTES + warp * G * C::D * 2, a.q_scale, gq, tq);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.qempty[qs]);
+      seg_bad = false;
     }
-    const int4 d = desc[slot];
-    if (d.x < 0) break;
-    const int ntok = d.w & 0xFFFF;
-    if (d.w & kFirst) {
-      cur_item = d.x;
-      // query rows gq < G, dims 32t..32t+31 (bf16) -> f16 scaled by 2^e so the
-      // largest |q| of the group sits in [2^14, 2^15)
-      float qf[32];
-      float qmax = 0.f;
-      if (gq < G) {
-        const uint8_t *qs = qbuf + slot * C::Q_BYTES + (gq * C::D + 32 * tq) * 2;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 w4 = lds128(qs + 16 * c);
-          bf16x2_to_f32(w4.x, qf + 8 * c);
-          bf16x2_to_f32(w4.y, qf + 8 * c + 2);
-          bf16x2_to_f32(w4.z, qf + 8 * c + 4);
-          bf16x2_to_f32(w4.w, qf + 8 * c + 6);
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) qmax = fmaxf(qmax, fabsf(qf[i]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) qf[i] = 0.f;
-      }
-#pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o2));
-      int e = (qmax > 0.f && qmax < INFINITY) ? 14 - ilogbf(qmax) : 0;
-      e = max(-100, min(100, e));
-      const float up = ldexpf(1.f, e);
-      qk_scale = a.q_scale * ldexpf(1.f, -e);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        qa0[s] = f32x2_to_f16x2(qf[4 * s] * up, qf[4 * s + 1] * up);
-        qa2[s] = f32x2_to_f16x2(qf[4 * s + 2] * up, qf[4 * s + 3] * up);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-      m_run = -INFINITY;
-      l_run = 0.f;
-    }
+    seg_bad |= (d0.z & kBad) != 0;
+    if (!(d0.z & kBad))
+      tile_step<G>(hs, kbuf + slot * C::KV_BYTES + warp * C::HEAD_TILE,
+                   vbuf + slot * C::KV_BYTES + warp * C::HEAD_TILE, ntok, gq, tq);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.empty[slot]);
 
-    const int tl0 = warp * 16;  // this warp's first token in the stage
-    if (tl0 < ntok) {
-      const uint8_t *ks = kbuf + slot * C::KV_BYTES;
-      const uint8_t *vs = vbuf + slot * C::KV_BYTES;
-      // ---- S = Q K^T for tokens tl0+gq (n-tile 0) and tl0+8+gq (n-tile 1);
-      // swizzled 16-byte chunk c of row r sits at chunk c ^ (r % 8), r % 8 == gq
-      const uint8_t *k0 = ks + (tl0 + gq) * C::D;
-      const uint8_t *k1 = k0 + 8 * C::D;
-      const int c0 = ((2 * tq) ^ gq) * 16, c1 = ((2 * tq + 1) ^ gq) * 16;
-      const uint4 k0a = lds128(k0 + c0), k0b = lds128(k0 + c1);
-      const uint4 k1a = lds128(k1 + c0), k1b = lds128(k1 + c1);
-      const uint32_t kw0[8] = {k0a.x, k0a.y, k0a.z, k0a.w, k0b.x, k0b.y, k0b.z, k0b.w};
-      const uint32_t kw1[8] = {k1a.x, k1a.y, k1a.z, k1a.w, k1b.x, k1b.y, k1b.z, k1b.w};
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        mma_16816(s0, qa0[s], 0u, qa2[s], 0u, e4m3x2_to_f16x2(kw0[s] & 0xFFFFu),
-                  e4m3x2_to_f16x2(kw0[s] >> 16));
-        mma_16816(s1, qa0[s], 0u, qa2[s], 0u, e4m3x2_to_f16x2(kw1[s] & 0xFFFFu),
-                  e4m3x2_to_f16x2(kw1[s] >> 16));
-      }
-      // ---- online softmax for head gq over this warp's 16 tokens (log2 domain)
-      const bool row_ok = gq < G;
-      const int t0 = tl0 + 2 * tq, t1 = tl0 + 8 + 2 * tq;
-      const float x00 = (row_ok && t0 < ntok) ? s0[0] * qk_scale : -INFINITY;
-      const float x01 = (row_ok && t0 + 1 < ntok) ? s0[1] * qk_scale : -INFINITY;
-      const float x10 = (row_ok && t1 < ntok) ? s1[0] * qk_scale : -INFINITY;
-      const float x11 = (row_ok && t1 + 1 < ntok) ? s1[1] * qk_scale : -INFINITY;
-      float mx = fmaxf(fmaxf(x00, x01), fmaxf(x10, x11));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const bool grow = mx > m_run + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, grow)) {
-        const float f = grow ? exp2f(m_run - mx) : 1.f;  // 0 when m_run is -inf
-        if (grow) {
-          m_run = mx;
-          l_run *= f;
-        }
-        // O^T columns 2t and 2t+1 belong to heads whose rows live in lanes 8t, 8t+4
-        const float fa = __shfl_sync(0xffffffffu, f, 8 * tq);
-        const float fb = __shfl_sync(0xffffffffu, f, 8 * tq + 4);
+    if (d0.z & kLast) {
+      const int row = d0.x, nparts = d0.w, pslot = d1.x, c_lo = d1.y, b = d1.z;
+      const int kvh = (d1.w & 0xFFFF) * HG + warp;
+      hs.l_run += __shfl_xor_sync(0xffffffffu, hs.l_run, 1);
+      hs.l_run += __shfl_xor_sync(0xffffffffu, hs.l_run, 2);
+      // heads 2t and 2t+1 of the O^T columns: their m, l live in lanes 8t, 8t+4
+      const float la = __shfl_sync(0xffffffffu, hs.l_run, 8 * tq);
+      const float lb = __shfl_sync(0xffffffffu, hs.l_run, 8 * tq + 4);
+      const float ma = __shfl_sync(0xffffffffu, hs.m_run, 8 * tq);
+      const float mb = __shfl_sync(0xffffffffu, hs.m_run, 8 * tq + 4);
+      const int ha = 2 * tq, hb = 2 * tq + 1;
+      float *out = a.out + (static_cast<int64_t>(b) * a.Hq + kvh * G) * C::D;
+      if (nparts == 1) {
+        const float sa = seg_bad ? 0.f : a.v_scale / la;
+        const float sb = seg_bad ? 0.f : a.v_scale / lb;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          o[i][0] *= fa;
-          o[i][1] *= fb;
-          o[i][2] *= fa;
-          o[i][3] *= fb;
+          const int dim = 16 * gq + 2 * i;
+          if (ha < G)
+            *reinterpret_cast<float2 *>(out + ha * C::D + dim) =
+                make_float2(hs.o[i][0] * sa, hs.o[i][2] * sa);
+          if (hb < G)
+            *reinterpret_cast<float2 *>(out + hb * C::D + dim) =
+                make_float2(hs.o[i][1] * sb, hs.o[i][3] * sb);
+        }
+      } else {
+        // partial of this head: acc[G][D], then m[G], l[G]
+        float *mine = a.part + static_cast<int64_t>(pslot) * C::PART +
+                      static_cast<int64_t>(warp) * G * (C::D + 2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int dim = 16 * gq + 2 * i;
+          if (ha < G)
+            *reinterpret_cast<float2 *>(mine + ha * C::D + dim) =
+                make_float2(hs.o[i][0], hs.o[i][2]);
+          if (hb < G)
+            *reinterpret_cast<float2 *>(mine + hb * C::D + dim) =
+                make_float2(hs.o[i][1], hs.o[i][3]);
+        }
+        if (gq == 0) {
+          if (ha < G) {
+            mine[G * C::D + ha] = ma;
+            mine[G * C::D + G + ha] = la;
+          }
+          if (hb < G) {
+            mine[G * C::D + hb] = mb;
+            mine[G * C::D + G + hb] = lb;
+          }
+        }
+        __threadfence();
+        if (!consumer_sync(ctl, csync_count, lane, a.err_word)) break;
+        if (warp == 0 && lane == 0) {
+          const int prev = atomicAdd(a.done + row, 1);
+          ctl.last = prev == nparts - 1;
+        }
+        if (!consumer_sync(ctl, csync_count, lane, a.err_word)) break;
+        if (ctl.last) {
+          __threadfence();
+          const bool row_bad = __ldcg(a.bad + row) != 0;
+          // consecutive CTAs of one row wrote consecutive slots (slot = row + CTA)
+          const float *p0 = a.part + static_cast<int64_t>(row + c_lo) * C::PART +
+                            static_cast<int64_t>(warp) * G * (C::D + 2);
+          float msa = -INFINITY, msb = -INFINITY;
+          for (int p = 0; p < nparts; ++p) {
+            const float *pp = p0 + static_cast<int64_t>(p) * C::PART;
+            if (ha < G) msa = fmaxf(msa, __ldcg(pp + G * C::D + ha));
+            if (hb < G) msb = fmaxf(msb, __ldcg(pp + G * C::D + hb));
+          }
+          float acc[8][4] = {};
+          float dena = 0.f, denb = 0.f;
+          for (int p = 0; p < nparts; ++p) {
+            const float *pp = p0 + static_cast<int64_t>(p) * C::PART;
+            float fa = 0.f, fb = 0.f;
+            if (ha < G) {
+              const float m = __ldcg(pp + G * C::D + ha);
+              fa = m == -INFINITY ? 0.f : exp2f(m - msa);
+              dena = fmaf(fa, __ldcg(pp + G * C::D + G + ha), dena);
+            }
+            if (hb < G) {
+              const float m = __ldcg(pp + G * C::D + hb);
+              fb = m == -INFINITY ? 0.f : exp2f(m - msb);
+              denb = fmaf(fb, __ldcg(pp + G * C::D + G + hb), denb);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int dim = 16 * gq + 2 * i;
+              if (ha < G) {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(pp + ha * C::D + dim));
+                acc[i][0] = fmaf(fa, v.x, acc[i][0]);
+                acc[i][2] = fmaf(fa, v.y, acc[i][2]);
+              }
+              if (hb < G) {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(pp + hb * C::D + dim));
+                acc[i][1] = fmaf(fb, v.x, acc[i][1]);
+                acc[i][3] = fmaf(fb, v.y, acc[i][3]);
+              }
+            }
+          }
+          const float sa = row_bad ? 0.f : a.v_scale / dena;
+          const float sb = row_bad ? 0.f : a.v_scale / denb;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int dim = 16 * gq + 2 * i;
+            if (ha < G)
+              *reinterpret_cast<float2 *>(out + ha * C::D + dim) =
+                  make_float2(acc[i][0] * sa, acc[i][2] * sa);
+            if (hb < G)
+              *reinterpret_cast<float2 *>(out + hb * C::D + dim) =
+                  make_float2(acc[i][1] * sb, acc[i][3] * sb);
+          }
         }
       }
-      const float p00 = x00 == -INFINITY ? 0.f : fast_exp2(x00 - m_run);
-      const float p01 = x01 == -INFINITY ? 0.f : fast_exp2(x01 - m_run);
-      const float p10 = x10 == -INFINITY ? 0.f : fast_exp2(x10 - m_run);
-      const float p11 = x11 == -INFINITY ? 0.f : fast_exp2(x11 - m_run);
-      l_run += (p00 + p01) + (p10 + p11);
-      const uint32_t pb0 = f32x2_to_f16x2(p00, p01);
-      const uint32_t pb1 = f32x2_to_f16x2(p10, p11);
-
-      // ---- O^T += V^T P^T: rows tl0+2t, +1, +8, +9 at logical chunk gq
-      const uint8_t *vr = vs + (tl0 + 2 * tq) * C::D;
-      uint4 va = lds128(vr + ((gq ^ (2 * tq)) * 16));
-      uint4 vb = lds128(vr + C::D + ((gq ^ (2 * tq + 1)) * 16));
-      uint4 vc = lds128(vr + 8 * C::D + ((gq ^ (2 * tq)) * 16));
-      uint4 vd = lds128(vr + 9 * C::D + ((gq ^ (2 * tq + 1)) * 16));
-      if (tl0 + 16 > ntok) {  // tail: cached bytes past the sequence may be anything
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        if (t0 >= ntok) va = z;
-        if (t0 + 1 >= ntok) vb = z;
-        if (t1 >= ntok) vc = z;
-        if (t1 + 1 >= ntok) vd = z;
-      }
-      const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
-      const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes (a.b, b.b, a.b+1, b.b+1)
-        const uint32_t x = prmt(wa[i >> 1], wb[i >> 1], sel);
-        const uint32_t y = prmt(wc[i >> 1], wd[i >> 1], sel);
-        mma_16816(o[i], e4m3x2_to_f16x2(x & 0xFFFFu), e4m3x2_to_f16x2(x >> 16),
-                  e4m3x2_to_f16x2(y & 0xFFFFu), e4m3x2_to_f16x2(y >> 16), pb0, pb1);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
-
-    if (d.w & kLast) {
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-      const int rb = n_items_done & 1;
-      float *my = red + (rb * C::NCW + warp) * C::RED;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int dim = 16 * gq + 2 * i;
-        if (2 * tq < G)
-          *reinterpret_cast<float2 *>(my + (2 * tq) * C::D + dim) = make_float2(o[i][0], o[i][2]);
-        if (2 * tq + 1 < G)
-          *reinterpret_cast<float2 *>(my + (2 * tq + 1) * C::D + dim) =
-              make_float2(o[i][1], o[i][3]);
-      }
-      if (tq == 0 && gq < G) {
-        my[G * C::D + gq] = m_run;
-        my[G * C::D + G + gq] = l_run;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&fin[rb]);
-      if (*fail || !mbar_wait(&fin[rb], (n_items_done >> 1) & 1)) {
-        if (!*fail) report(a.err_word, KVQ_ERRBIT_TIMEOUT);
-        *fail = 1;
-        break;
-      }
-      const float *rr = red + rb * C::NCW * C::RED;
-      float *out = a.part + static_cast<int64_t>(cur_item) * C::PART;
-      const int ctid = warp * 32 + lane;
-      for (int idx = ctid; idx < G * C::D + G; idx += C::NCW * 32) {
-        const int h = idx < G * C::D ? idx / C::D : idx - G * C::D;
-        float mstar = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < C::NCW; ++w) mstar = fmaxf(mstar, rr[w * C::RED + G * C::D + h]);
-        float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < C::NCW; ++w) {
-          const float mw = rr[w * C::RED + G * C::D + h];
-          const float f = mw == -INFINITY ? 0.f : exp2f(mw - mstar);
-          const float v = idx < G * C::D ? rr[w * C::RED + idx] : rr[w * C::RED + G * C::D + G + h];
-          sum = fmaf(f, v, sum);
-        }
-        if (idx < G * C::D) {
-          out[idx] = sum;
-        } else {
-          out[G * C::D + h] = mstar;
-          out[G * C::D + G + h] = sum;
-        }
-      }
-      ++n_items_done;
+      ++nseg;
     }
     ++g;
   }

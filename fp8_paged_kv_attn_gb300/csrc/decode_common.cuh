@@ -1,0 +1,309 @@
+// Scheduling, staging and merge code shared by the two decode-attention split
+// kernels (CUDA-core and tensor-core).  Included by decode_attn.cu.
+//
+// Work split ("stream-K" over the sequence): every (request b, kv head)
+// pair is a row of ceil(L_b / 64) units of 64 tokens.  The rows are laid end
+// to end and each of the C persistent CTAs takes the same number U of
+// consecutive units, so the load is balanced to within one unit whatever the
+// length mix.  A CTA's range cuts rows into segments; a row owned by one CTA
+// is normalised and written directly, otherwise every CTA writes a partial
+// (acc[G][D], m[G], l[G]) and the last one to finish the row (an atomic
+// counter, no waiting) merges them by log-sum-exp.
+#pragma once
+
+namespace kvq {
+
+constexpr int kUnit = 64;           // tokens per scheduling unit (CUDA-core kernel)
+constexpr int kMaxCtas = 1024;      // upper bound on the persistent grid
+constexpr int kConsumerWarps = 4;   // consumer warps of the CUDA-core kernel
+constexpr int kStages = 4;          // ring stages of the CUDA-core kernel
+constexpr int kMaxStages = 6;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+
+// stage descriptor flags (packed above the 16-bit token count)
+constexpr int kFirst = 1 << 16;  // first stage of a segment
+constexpr int kLast = 1 << 17;   // last stage of a segment
+constexpr int kBad = 1 << 18;    // a page of this stage was outside the pool
+
+struct SplitArgs {
+  const uint8_t *k_pool, *v_pool;
+  const uint16_t *q;
+  const int32_t *block_table, *seq_lens;
+  const int32_t *hdr;     // [0] total units S, [1] units per CTA U
+  const int32_t *prefix;  // [B+1]: units before request b, over all its kv heads
+  const int4 *start;      // [C]: (b, kv head, unit in row) where CTA c begins
+  int32_t *done;          // [B*Hkv] CTAs finished per row (zeroed by the plan)
+  int32_t *bad;           // [B*Hkv] a page of the row was outside the pool
+  float *part;            // [B*Hkv + C][G][D+2] partials
+  float *out;             // [B][Hq][D]
+  uint32_t *err_word;
+  int32_t num_pages, P, Hkv, Hq, MP, B;
+  float q_scale;  // sm_scale * k_scale * log2(e)
+  float v_scale;
+};
+
+// Shared-memory control block.
+struct Ctrl {
+  int4 desc[kMaxStages][2];  // {row, tok0, ntok|flags, nparts}, {slot, c_lo, b, kvh or group}
+  uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t qfull[2], qempty[2];  // double-buffered query rows (tensor-core kernel)
+  uint64_t fin[2];               // per-segment merge of the consumer warps (CUDA-core kernel)
+  uint64_t csync;                // consumer-wide barrier for the split-row hand-off
+  int fail;
+  int last;
+};
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 2^x on the SFU (relative error ~2^-22; exactly 1 at x = 0)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ns ring stages, nc consumer warps (each consumer warp arrives once per phase)
+__device__ __forceinline__ void ctrl_init(Ctrl &ctl, int ns, int nc) {
+  for (int s = 0; s < ns; ++s) {
+    mbar_init(&ctl.full[s], 1);
+    mbar_init(&ctl.empty[s], nc);
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&ctl.qfull[i], 1);
+    mbar_init(&ctl.qempty[i], nc);
+    mbar_init(&ctl.fin[i], nc);
+  }
+  mbar_init(&ctl.csync, nc);
+  ctl.fail = 0;
+  ctl.last = 0;
+  fence_barrier_init();
+}
+
+// Bounded wait shared by every role: on timeout the error bit is raised once
+// and the CTA's fail flag tells everybody to leave.
+__device__ __forceinline__ bool ctl_wait(Ctrl &ctl, uint64_t *bar, uint32_t parity,
+                                         uint32_t *err_word) {
+  volatile int *fail = &ctl.fail;
+  if (*fail) return false;
+  if (mbar_wait(bar, parity)) return true;
+  if (atomicExch(&ctl.fail, 1) == 0) report(err_word, KVQ_ERRBIT_TIMEOUT);
+  return false;
+}
+
+// All consumer warps meet (every consumer warp calls this the same number of
+// times; `count` is that number so far, kept per warp).
+__device__ __forceinline__ bool consumer_sync(Ctrl &ctl, uint32_t &count, int lane,
+                                              uint32_t *err_word) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ctl.csync);
+  const bool ok = ctl_wait(ctl, &ctl.csync, count & 1, err_word);
+  ++count;
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ---------------------------------------------------------------------------
+// producer: walk this CTA's units, one stage (TS tokens of one row) at a time
+// ---------------------------------------------------------------------------
+
+// CopyPages(slot, lane, page, kvh, tok0) issues the K and V copies of page
+// `page` (the lane-th page of the stage) into the stage's buffers; each copy
+// moves `copy_bytes`.
+template <int TS, int QBYTES, int G, int D, typename CopyPages>
+__device__ __forceinline__ void producer_loop(const SplitArgs &a, Ctrl &ctl, uint8_t *qbuf,
+                                              int lane, uint32_t copy_bytes, CopyPages copy) {
+  static_assert(kUnit % TS == 0, "a unit holds whole stages");
+  const int S = a.hdr[0], U = a.hdr[1];
+  const int c = blockIdx.x;
+  long long u = static_cast<long long>(c) * U;
+  const long long u_end = min(u + U, static_cast<long long>(S));
+  int b = 0, kvh = 0, s = 0;
+  if (u < u_end) {
+    const int4 st = a.start[c];
+    b = st.x;
+    kvh = st.y;
+    s = st.z;
+  }
+  uint32_t g = 0;  // stages issued
+  // Block-table window of the current request: lane i holds logical page
+  // win+i in `cur` and win+32+i in `nxt`; `nxt` is loaded one window ahead so
+  // the page ids of a stage never wait on memory.
+  int win_b = -1, win = 0, cur = -1, nxt = -1;
+  const int32_t *bt_row = a.block_table;
+  auto bt_load = [&](int lp) -> int { return lp < a.MP ? __ldg(bt_row + lp) : -1; };
+  bool ok = true;
+  while (ok) {
+    const bool done = u >= u_end;
+    int units_b = 0, L = 0, row = 0, nparts = 1, c_lo = c;
+    if (!done) {
+      const int p0 = __ldg(a.prefix + b), p1 = __ldg(a.prefix + b + 1);
+      units_b = (p1 - p0) / a.Hkv;
+      L = __ldg(a.seq_lens + b);
+      row = b * a.Hkv + kvh;
+      const long long ur = static_cast<long long>(p0) + static_cast<long long>(kvh) * units_b;
+      c_lo = static_cast<int>(ur / U);
+      nparts = static_cast<int>((ur + units_b - 1) / U) - c_lo + 1;
+      const int lp0 = s * kUnit / a.P;
+      if (b != win_b || lp0 < win || lp0 >= win + 32) {
+        win_b = b;
+        win = lp0;
+        bt_row = a.block_table + static_cast<int64_t>(b) * a.MP;
+        cur = bt_load(win + lane);
+        nxt = bt_load(win + 32 + lane);
+      }
+    }
+    const int seg_units = done ? 0 : static_cast<int>(min(static_cast<long long>(units_b - s),
+                                                          u_end - u));
+    const int t_begin = s * kUnit;
+    const int t_end = done ? 0 : min((s + seg_units) * kUnit, L);
+    const int nstages = done ? 1 : (t_end - t_begin + TS - 1) / TS;
+    for (int st = 0; st < nstages; ++st, ++g) {
+      const int slot = g % kStages;
+      bool waited = true;
+      if (lane == 0 && g >= kStages)
+        waited = ctl_wait(ctl, &ctl.empty[slot], ((g / kStages) - 1) & 1, a.err_word);
+      ok = __shfl_sync(0xffffffffu, waited ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      if (done) {
+        if (lane == 0) {
+          ctl.desc[slot][0] = make_int4(-1, 0, 0, 0);
+          mbar_arrive(&ctl.full[slot]);
+        }
+        ok = false;
+        break;
+      }
+      const int tok0 = t_begin + st * TS;
+      const int ntok = min(TS, t_end - tok0);
+      const int npages = TS > a.P ? (ntok + a.P - 1) / a.P : 1;
+      const int lp = tok0 / a.P;  // first logical page of the stage
+      while (lp + npages > win + 32) {  // slide the window by 32 pages
+        win += 32;
+        cur = nxt;
+        nxt = bt_load(win + 32 + lane);
+      }
+      const int idx = lp - win + lane;  // < 64 for lane < npages
+      const int from_cur = __shfl_sync(0xffffffffu, cur, idx & 31);
+      const int from_nxt = __shfl_sync(0xffffffffu, nxt, idx & 31);
+      int page = -1;
+      bool bad_page = false;
+      if (lane < npages) {
+        page = idx < 32 ? from_cur : from_nxt;
+        if (page < 0 || page >= a.num_pages) {
+          bad_page = true;
+          page = -1;
+          atomicOr(a.bad + row, 1);
+          report(a.err_word, KVQ_ERRBIT_PAGE);
+        }
+      }
+      const unsigned valid_mask = __ballot_sync(0xffffffffu, page >= 0);
+      const bool any_bad = __any_sync(0xffffffffu, bad_page);
+      const bool first = st == 0, last = st == nstages - 1;
+      if (lane == 0) {
+        ctl.desc[slot][0] = make_int4(row, tok0,
+                                      ntok | (first ? kFirst : 0) | (last ? kLast : 0) |
+                                          (any_bad ? kBad : 0),
+                                      nparts);
+        ctl.desc[slot][1] = make_int4(row + c, c_lo, b, kvh);
+        const uint32_t tx = 2u * __popc(valid_mask) * copy_bytes + (first ? QBYTES : 0u);
+        mbar_arrive_expect_tx(&ctl.full[slot], tx);
+        if (first)
+          bulk_g2s(qbuf + slot * QBYTES, a.q + (static_cast<int64_t>(b) * a.Hq + kvh * G) * D,
+                   QBYTES, &ctl.full[slot]);
+      }
+      __syncwarp();  // the transaction count is armed before any page copy is issued
+      if (page >= 0) copy(slot, lane, page, kvh, tok0);
+      __syncwarp();
+    }
+    if (!done) {
+      u += seg_units;
+      s = 0;
+      if (++kvh == a.Hkv) {
+        kvh = 0;
+        ++b;
+        // requests without work (aborted, empty or invalid) own no units
+        while (b < a.B && __ldg(a.prefix + b + 1) == __ldg(a.prefix + b)) ++b;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// consumers: finish a segment from the warps' merge areas
+// red: [kConsumerWarps][RED] floats, each acc[G][D] then m[G], l[G]
+// ---------------------------------------------------------------------------
+
+template <int G, int D, int RED>
+__device__ __forceinline__ void finish_segment(const SplitArgs &a, Ctrl &ctl, const float *red,
+                                               int4 d0, int4 d1, bool seg_bad, int lane,
+                                               uint32_t &csync_count) {
+  const int ctid = (threadIdx.x >> 5) * 32 + lane;
+  const int row = d0.x, nparts = d0.w, slot = d1.x, c_lo = d1.y, b = d1.z, kvh = d1.w;
+  constexpr int GD = G * D;
+  constexpr int PART = G * (D + 2);
+  float *out = a.out + (static_cast<int64_t>(b) * a.Hq + kvh * G) * D;
+  float *mine = a.part + static_cast<int64_t>(slot) * PART;
+  for (int idx = ctid; idx < GD; idx += kConsumerWarps * 32) {
+    const int h = idx / D;
+    float mstar = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) mstar = fmaxf(mstar, red[w * RED + GD + h]);
+    float acc = 0.f, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = red[w * RED + GD + h];
+      const float f = mw == -INFINITY ? 0.f : exp2f(mw - mstar);
+      acc = fmaf(f, red[w * RED + idx], acc);
+      l = fmaf(f, red[w * RED + GD + G + h], l);
+    }
+    if (nparts == 1) {
+      out[idx] = seg_bad ? 0.f : acc / l * a.v_scale;
+    } else {
+      mine[idx] = acc;
+      if (idx % D == 0) {
+        mine[GD + h] = mstar;
+        mine[GD + G + h] = l;
+      }
+    }
+  }
+  if (nparts == 1) return;
+
+  // split row: publish the partial, count it; the last CTA merges the row
+  __threadfence();
+  if (!consumer_sync(ctl, csync_count, lane, a.err_word)) return;
+  if (ctid == 0) {
+    const int prev = atomicAdd(a.done + row, 1);
+    ctl.last = prev == nparts - 1;
+  }
+  if (!consumer_sync(ctl, csync_count, lane, a.err_word)) return;
+  if (!ctl.last) return;
+  __threadfence();
+  const bool row_bad = __ldcg(a.bad + row) != 0;
+  const float *p0 = a.part + static_cast<int64_t>(row + c_lo) * PART;  // slot of CTA c_lo
+  for (int idx = ctid; idx < GD; idx += kConsumerWarps * 32) {
+    if (row_bad) {
+      out[idx] = 0.f;
+      continue;
+    }
+    const int h = idx / D;
+    float mstar = -INFINITY;
+    for (int p = 0; p < nparts; ++p) mstar = fmaxf(mstar, __ldcg(p0 + p * PART + GD + h));
+    float num = 0.f, den = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+      // consecutive CTAs of one row write consecutive slots (slot = row + CTA)
+      const float *pp = p0 + p * PART;
+      const float ms = __ldcg(pp + GD + h);
+      const float f = ms == -INFINITY ? 0.f : exp2f(ms - mstar);
+      num = fmaf(f, __ldcg(pp + idx), num);
+      den = fmaf(f, __ldcg(pp + GD + G + h), den);
+    }
+    out[idx] = num / den * a.v_scale;
+  }
+}
+
+}  // namespace kvq

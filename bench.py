@@ -59,6 +59,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seed", type=int, default=2)
+    ap.add_argument("--sweep", action="store_true",
+                    help="concurrency sweep 1/8/16/32/64 requests, e4m3 and bf16 KV at equal pool "
+                         "bytes; one JSON line per point (not the headline line)")
     return ap.parse_args()
 
 
@@ -471,8 +474,89 @@ def run_reference(args, rank):
     }
 
 
+def run_sweep(args):
+    """FP8 vs BF16 KV over 1..64 concurrent requests at equal pool bytes (the
+    pages' decode table shape).  Each point times `steps` decode steps
+    (append + attention, no tag check) after `warmup` steps."""
+    import torch
+    from fp8_paged_kv_attn_gb300 import inputs, kvq
+
+    kvq.load()
+    peak, _ = measured_hbm_peak()
+    ref = inputs.sweep(64, kv_bytes=1, seed=args.seed)
+    sources = ref.kv_sources(threads=os.cpu_count() or 8)
+    ks, vs = ref.scales(sources)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    for kv in ("e4m3", "bf16"):
+        kv_bytes = 1 if kv == "e4m3" else 2
+        for B in (1, 8, 16, 32, 64):
+            try:
+                w = inputs.sweep(B, kv_bytes=kv_bytes, seed=args.seed)
+            except MemoryError as e:
+                print(json.dumps({"sweep": True, "kv": kv, "batch": B, "result": "OOM",
+                                  "why": str(e)}), flush=True)
+                continue
+            shape = w.pool_shape()
+            pdt = torch.uint8 if kv_bytes == 1 else torch.bfloat16
+            cache = kvq.KVCache(torch.zeros(shape, dtype=pdt, device="cuda"),
+                                torch.zeros(shape, dtype=pdt, device="cuda"), float(ks), float(vs))
+            bt = torch.from_numpy(w.block_table).cuda()
+            for b in range(B):
+                k, v = sources[b]
+                req, pos = w.context_tokens(b)
+                kvq.kvq_append(cache, bf16(k).cuda(), bf16(v).cuda(), torch.from_numpy(req).cuda(),
+                               torch.from_numpy(pos).cuda(), bt)
+            n = args.warmup + args.steps
+            gen = [(args.offset + i) % inputs.SWEEP_DECODE_STEPS for i in range(n)]
+            st = [w.step_inputs(gi) for gi in gen]
+            d_q = [bf16(x[0]).cuda() for x in st]
+            d_k = [bf16(x[1]).cuda() for x in st]
+            d_v = [bf16(x[2]).cuda() for x in st]
+            d_pos = [torch.from_numpy(x[4]).cuda() for x in st]
+            lens = [w.seq_lens_after(gi) for gi in gen]
+            d_len = [torch.from_numpy(x).cuda() for x in lens]
+            req_idx = torch.arange(B, dtype=torch.int32, device="cuda")
+            out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device="cuda")
+            ws = kvq.workspace(B, w.Hq, w.Hkv, w.D)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            stream = torch.cuda.current_stream()
+            for i in range(n):
+                if i == args.warmup:
+                    t0.record(stream)
+                kvq.kvq_append(cache, d_k[i], d_v[i], req_idx, d_pos[i], bt)
+                evs[i][0].record(stream)
+                kvq.kvq_decode_attn(cache, d_q[i], bt, d_len[i], out, ws,
+                                    sm_scale=float(w.sm_scale))
+                evs[i][1].record(stream)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            step_ms = t0.elapsed_time(t1) / args.steps
+            attn_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.warmup, n)]
+            byts = [attn_bytes(lens[i], w.Hq, w.Hkv, w.D, w.P, kv_bytes)
+                    for i in range(args.warmup, n)]
+            gbs = sum(byts) / (sum(attn_ms) * 1e-3) / 1e9
+            print(json.dumps({"sweep": True, "kv": kv, "batch": B,
+                              "tokens_per_s": round(B / (step_ms * 1e-3), 1),
+                              "ms_per_step": round(step_ms, 5),
+                              "attn_us": round(statistics.mean(attn_ms) * 1e3, 2),
+                              "attn_GBs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                              "pool_pages": w.num_pages,
+                              "mean_context": round(float(np.mean([x.mean() for x in lens[args.warmup:]])), 1)}),
+                  flush=True)
+            del cache
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         # the CPU oracle runs on rank 0 only; other ranks exit without work
         if int(os.environ.get("RANK", "0")) == 0:

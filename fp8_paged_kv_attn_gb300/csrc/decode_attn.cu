@@ -44,7 +44,7 @@ namespace kvq {
 // ---------------------------------------------------------------------------
 
 struct WsLayout {
-  size_t hdr, prefix, start, done, bad, part, total;
+  size_t hdr, prefix, start, done, bad, comb, part, total;
 };
 
 inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -64,10 +64,12 @@ inline WsLayout ws_layout(int B, int Hq, int Hkv, int D) {
   off = round256(off + rows * sizeof(int32_t));
   w.bad = off;
   off = round256(off + rows * sizeof(int32_t));
+  w.comb = off;  // rows the combine kernel merges
+  off = round256(off + rows * sizeof(int32_t));
   // partial slots: row + CTA for every row split across CTAs; a tensor-core
   // row holds up to 8 kv heads, a CUDA-core row one
   w.part = off;
-  off = round256(off + (rows + 8ull * kMaxCtas) * G * (D + 2) * sizeof(float));
+  off = round256(off + (rows + 8ull * kMaxCtas) * part_stride(G, D) * sizeof(float));
   w.total = off;
   return w;
 }
@@ -83,7 +85,7 @@ struct PlanArgs {
   const uint8_t *abort_mask;
   int32_t *hdr, *prefix;
   int4 *start;
-  int32_t *done, *bad;
+  int32_t *done, *bad, *comb;
   float *out;
   uint32_t *err_word;
   int32_t B, Hq, D, MP, P, nctas;
@@ -170,9 +172,26 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     const int r = static_cast<int>(u - p0);
     a.start[c] = make_int4(lo, r / units_b, r % units_b, 0);
   }
+  // rows split over more than kFusedMergeMax CTAs go to the combine kernel
+  __shared__ int s_ncomb;
+  if (tid == 0) s_ncomb = 0;
+  __syncthreads();
+  for (int b = tid; b < a.B; b += nt) {
+    const int p0 = in_smem ? s_prefix[b] : __ldcg(a.prefix + b);
+    const int p1 = in_smem ? s_prefix[b + 1] : __ldcg(a.prefix + b + 1);
+    const int units_b = (p1 - p0) / a.rows_per_req;
+    if (units_b == 0) continue;
+    for (int r = 0; r < a.rows_per_req; ++r) {
+      const long long ur = static_cast<long long>(p0) + static_cast<long long>(r) * units_b;
+      const int nparts = static_cast<int>((ur + units_b - 1) / U - ur / U) + 1;
+      if (nparts > kFusedMergeMax) a.comb[atomicAdd(&s_ncomb, 1)] = b * a.rows_per_req + r;
+    }
+  }
+  __syncthreads();
   if (tid == 0) {
     a.hdr[0] = S;
     a.hdr[1] = U;
+    a.hdr[2] = s_ncomb;
   }
 }
 
@@ -248,6 +267,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
   if (threadIdx.x == 0) ctrl_init(ctl, C::NS, C::NCW);
   __syncthreads();
   grid_dependency_wait();  // the plan's outputs are visible from here on
+  allow_dependents();      // the combine grid may become resident and wait
 
   if (warp == C::NCW) {
     const uint32_t copy_tokens = C::TS > a.P ? a.P : C::TS;
@@ -395,6 +415,103 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
       ++segs;
     }
     ++g;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// combine: rows split over more than kFusedMergeMax CTAs
+// ---------------------------------------------------------------------------
+
+struct CombineArgs {
+  const int32_t *hdr, *prefix, *bad, *comb;
+  const float *part;
+  float *out;
+  int32_t B, Hq, Hkv, G, D, hg, rows_per_req;
+  float v_scale;
+};
+
+constexpr int kCombineSubsets = 16;  // part subsets per combine CTA (32 lanes each)
+
+// Work item = one output row (query head) of one listed kv-head row, 512
+// threads: thread t merges dims 4*(t%32)..+3 over the parts p = t/32,
+// t/32 + 16, ... with a running maximum; the 16 subsets are then merged
+// through shared memory.  Launched as a programmatic dependent of the split
+// kernel; with no listed rows it exits after reading the count.
+__global__ void __launch_bounds__(32 * kCombineSubsets) combine_kernel(CombineArgs a) {
+  __shared__ float s_m[kCombineSubsets], s_l[kCombineSubsets];
+  __shared__ float4 s_acc[kCombineSubsets][32];
+  grid_dependency_wait();
+  const int ncomb = a.hdr[2];
+  if (ncomb == 0) return;
+  const int U = a.hdr[1];
+  const int tid = threadIdx.x, sub = tid >> 5, lane = tid & 31;
+  const int heads_per_row = a.hg * a.G;
+  const int64_t kpart = part_stride(a.G, a.D);  // 16-byte multiple
+  const int64_t slot_floats = a.hg * kpart;
+  const int GD = a.G * a.D;
+  const bool active = 4 * lane < a.D;
+  for (int item = blockIdx.x; item < ncomb * heads_per_row; item += gridDim.x) {
+    const int row = a.comb[item / heads_per_row];
+    const int hr = item % heads_per_row;  // query head within the row
+    const int b = row / a.rows_per_req, rin = row % a.rows_per_req;
+    const int kvh_in = hr / a.G, hq = hr % a.G;
+    const int p0 = a.prefix[b], p1 = a.prefix[b + 1];
+    const int units_b = (p1 - p0) / a.rows_per_req;
+    const long long ur = static_cast<long long>(p0) + static_cast<long long>(rin) * units_b;
+    const int c_lo = static_cast<int>(ur / U);
+    const int nparts = static_cast<int>((ur + units_b - 1) / U) - c_lo + 1;
+    float *out = a.out + (static_cast<int64_t>(b) * a.Hq + (rin * a.hg + kvh_in) * a.G + hq) * a.D;
+    if (a.bad[row]) {
+      for (int d = tid; d < a.D; d += blockDim.x) out[d] = 0.f;
+      continue;
+    }
+    const float *base = a.part + static_cast<int64_t>(row + c_lo) * slot_floats + kvh_in * kpart;
+    float m = -INFINITY, l = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+    for (int p = sub; p < nparts; p += kCombineSubsets) {
+      const float *pp = base + p * slot_floats;
+      const float mp = __ldcg(pp + GD + hq);
+      const float lp = __ldcg(pp + GD + a.G + hq);
+      const float4 v = active ? __ldcg(reinterpret_cast<const float4 *>(pp + hq * a.D) + lane)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (mp == -INFINITY) continue;
+      const float mn = fmaxf(m, mp);
+      const float fo = m == -INFINITY ? 0.f : exp2f(m - mn);
+      const float fp = exp2f(mp - mn);
+      acc.x = acc.x * fo + v.x * fp;
+      acc.y = acc.y * fo + v.y * fp;
+      acc.z = acc.z * fo + v.z * fp;
+      acc.w = acc.w * fo + v.w * fp;
+      l = l * fo + lp * fp;
+      m = mn;
+    }
+    if (lane == 0) {
+      s_m[sub] = m;
+      s_l[sub] = l;
+    }
+    s_acc[sub][lane] = acc;
+    __syncthreads();
+    if (sub == 0 && active) {
+      float mstar = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kCombineSubsets; ++i) mstar = fmaxf(mstar, s_m[i]);
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 0.f;
+#pragma unroll
+      for (int i = 0; i < kCombineSubsets; ++i) {
+        const float f = s_m[i] == -INFINITY ? 0.f : exp2f(s_m[i] - mstar);
+        const float4 v = s_acc[i][lane];
+        o.x = fmaf(f, v.x, o.x);
+        o.y = fmaf(f, v.y, o.y);
+        o.z = fmaf(f, v.z, o.z);
+        o.w = fmaf(f, v.w, o.w);
+        den = fmaf(f, s_l[i], den);
+      }
+      const float sc = a.v_scale / den;
+      reinterpret_cast<float4 *>(out)[lane] = make_float4(o.x * sc, o.y * sc, o.z * sc, o.w * sc);
+    }
+    __syncthreads();
   }
 }
 
@@ -583,11 +700,12 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   int4 *start = reinterpret_cast<int4 *>(w + ws.start);
   int32_t *done = reinterpret_cast<int32_t *>(w + ws.done);
   int32_t *bad = reinterpret_cast<int32_t *>(w + ws.bad);
+  int32_t *comb = reinterpret_cast<int32_t *>(w + ws.comb);
   float *part = reinterpret_cast<float *>(w + ws.part);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool fp8 = cache->kv_dtype == KVQ_KV_E4M3;
 
-  PlanArgs pa{seq_lens, abort_mask, hdr, prefix, start, done, bad, out, err_word,
+  PlanArgs pa{seq_lens, abort_mask, hdr, prefix, start, done, bad, comb, out, err_word,
               B, Hq, D, MP, cache->page_size, nctas, Hkv / sk.hg, sk.unit};
   plan_kernel<<<1, 1024, 0, s>>>(pa);
 
@@ -638,5 +756,17 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
     e = cudaLaunchKernelEx(&cfg, sk.fn, sa);
   }
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
+
+  // rows split over many CTAs are merged across the GPU by combine_kernel;
+  // it is a programmatic dependent of the split grid and exits at once for
+  // rows the split kernel already finished
+  CombineArgs ca{hdr, prefix, bad, comb, part, out, B, Hq, Hkv, G, D, sk.hg, Hkv / sk.hg,
+                 fp8 ? cache->v_scale : 1.0f};
+  cudaLaunchConfig_t ccfg = cfg;
+  const int crows = B * Hq;
+  ccfg.gridDim = dim3(crows < 2 * sms ? crows : 2 * sms);
+  ccfg.blockDim = dim3(32 * kCombineSubsets);
+  ccfg.dynamicSmemBytes = 0;
+  if (cudaLaunchKernelEx(&ccfg, combine_kernel, ca) != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

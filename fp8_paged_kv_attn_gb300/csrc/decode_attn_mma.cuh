@@ -75,7 +75,8 @@ struct HgCfg {
   static constexpr int HEAD_TILE = kTile * D;           // 2 KB: 16 tokens of one head
   static constexpr int KV_BYTES = HG * HEAD_TILE;       // one stage of K (or V)
   static constexpr int Q_BYTES = HG * G * D * 2;        // the group's query rows (bf16)
-  static constexpr int PART = HG * G * (D + 2);         // floats per partial slot
+  static constexpr int KPART = part_stride(G, D);       // floats per kv head in a slot
+  static constexpr int PART = HG * KPART;               // floats per partial slot
   static constexpr size_t off_k = 0;                    // 1024-byte aligned
   static constexpr size_t off_v = off_k + static_cast<size_t>(NS) * KV_BYTES;
   static constexpr size_t off_q = off_v + static_cast<size_t>(NS) * KV_BYTES;
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
   }
   __syncthreads();
   grid_dependency_wait();  // the plan's outputs are visible from here on
+  allow_dependents();      // the combine grid may become resident and wait
 
   const int S = a.hdr[0], U = a.hdr[1];
   const int c = blockIdx.x;
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
       } else {
         // partial of this head: acc[G][D], then m[G], l[G]
         float *mine = a.part + static_cast<int64_t>(pslot) * C::PART +
-                      static_cast<int64_t>(warp) * G * (C::D + 2);
+                      static_cast<int64_t>(warp) * C::KPART;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int dim = 16 * gq + 2 * i;
@@ -437,6 +439,11 @@ __global__ void __launch_bounds__(32 * (HG + 1))
             mine[G * C::D + G + hb] = lb;
           }
         }
+        if (nparts > kFusedMergeMax) {  // merged by combine_kernel
+          ++nseg;
+          ++g;
+          continue;
+        }
         __threadfence();
         if (!consumer_sync(ctl, csync_count, lane, a.err_word)) break;
         if (warp == 0 && lane == 0) {
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
           const bool row_bad = __ldcg(a.bad + row) != 0;
           // consecutive CTAs of one row wrote consecutive slots (slot = row + CTA)
           const float *p0 = a.part + static_cast<int64_t>(row + c_lo) * C::PART +
-                            static_cast<int64_t>(warp) * G * (C::D + 2);
+                            static_cast<int64_t>(warp) * C::KPART;
           float msa = -INFINITY, msb = -INFINITY;
           for (int p = 0; p < nparts; ++p) {
             const float *pp = p0 + static_cast<int64_t>(p) * C::PART;

@@ -1,14 +1,16 @@
 // Scheduling, staging and merge code shared by the two decode-attention split
 // kernels (CUDA-core and tensor-core).  Included by decode_attn.cu.
 //
-// Work split ("stream-K" over the sequence): every (request b, kv head)
-// pair is a row of ceil(L_b / 64) units of 64 tokens.  The rows are laid end
-// to end and each of the C persistent CTAs takes the same number U of
-// consecutive units, so the load is balanced to within one unit whatever the
-// length mix.  A CTA's range cuts rows into segments; a row owned by one CTA
-// is normalised and written directly, otherwise every CTA writes a partial
-// (acc[G][D], m[G], l[G]) and the last one to finish the row (an atomic
-// counter, no waiting) merges them by log-sum-exp.
+// Work split ("stream-K" over the sequence): every request is cut into
+// rows (its kv heads, or groups of kv heads), each a run of units of a fixed
+// number of tokens.  The rows are laid end to end and each of the C
+// persistent CTAs takes the same number U of consecutive units, so the load
+// is balanced to within one unit whatever the length mix.  A CTA's range cuts
+// rows into segments; a row owned by one CTA is normalised and written
+// directly, otherwise every CTA writes a partial (acc[G][D], m[G], l[G] per
+// kv head) and the row is merged by log-sum-exp: by the last CTA to finish
+// it (an atomic counter, no waiting) when it has few parts, else by the
+// combine kernel, whose CTAs each merge one output row.
 #pragma once
 
 namespace kvq {
@@ -42,6 +44,14 @@ struct SplitArgs {
   float q_scale;  // sm_scale * k_scale * log2(e)
   float v_scale;
 };
+
+// Floats of one kv head's partial: acc[G][D], m[G], l[G], padded to a
+// multiple of four floats so every head's block is 16-byte aligned.
+__host__ __device__ constexpr int part_stride(int G, int D) { return G * D + (2 * G + 3) / 4 * 4; }
+
+// Rows split over at most this many CTAs are merged by the last of them;
+// rows split further are merged by combine_kernel, spread over the GPU.
+constexpr int kFusedMergeMax = 8;
 
 // Shared-memory control block.
 struct Ctrl {
@@ -245,7 +255,7 @@ __device__ __forceinline__ void finish_segment(const SplitArgs &a, Ctrl &ctl, co
   const int ctid = (threadIdx.x >> 5) * 32 + lane;
   const int row = d0.x, nparts = d0.w, slot = d1.x, c_lo = d1.y, b = d1.z, kvh = d1.w;
   constexpr int GD = G * D;
-  constexpr int PART = G * (D + 2);
+  constexpr int PART = part_stride(G, D);
   float *out = a.out + (static_cast<int64_t>(b) * a.Hq + kvh * G) * D;
   float *mine = a.part + static_cast<int64_t>(slot) * PART;
   for (int idx = ctid; idx < GD; idx += kConsumerWarps * 32) {
@@ -271,7 +281,7 @@ __device__ __forceinline__ void finish_segment(const SplitArgs &a, Ctrl &ctl, co
       }
     }
   }
-  if (nparts == 1) return;
+  if (nparts == 1 || nparts > kFusedMergeMax) return;
 
   // split row: publish the partial, count it; the last CTA merges the row
   __threadfence();

@@ -241,3 +241,18 @@ def test_full_integrity(kvq, oracle_mod):
     assert not got[victim].any()
     for b, h in rows:
         assert_close(got[b, h], ref[b, h], f"integrity row ({b},{h})")
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "bf16"])
+@pytest.mark.parametrize("lens", [[8000], [5000, 20, 3000], [1, 12000]], ids=["one", "mix", "two"])
+def test_few_long_requests(kvq, dtype, lens):
+    """Few requests with long contexts: every row is split over many CTAs and
+    merged across the GPU by the combine kernel (rows with few parts are
+    merged inside the split kernel; both paths are covered by the other
+    tests)."""
+    B = len(lens)
+    w = inputs.uniform("few", 50 + B, B=B, ctx=max(lens), Hq=32, Hkv=8, D=128, P=16,
+                       outlier_frac=0.01)
+    w.ctx_lens = np.array(lens, dtype=np.int32)
+    step_and_compare(kvq, w, kv_dtype=kvq.KV_E4M3 if dtype == "e4m3" else kvq.KV_BF16,
+                     rows=[(b, h) for b in range(B) for h in (0, 3, 17, 31)])

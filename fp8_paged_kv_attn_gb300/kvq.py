@@ -40,7 +40,8 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_WORKSPACE", 3: "KVQ
 
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_append", "kvq_check_tags", "kvq_decode_attn_workspace_size", "kvq_decode_attn",
-           "kvq_status_string")
+           "kvq_decode_attn_static", "kvq_status_string")
+STATIC_SCRATCH_BYTES = 64 << 20
 
 
 class KvqError(RuntimeError):
@@ -84,6 +85,8 @@ def load(build_if_missing: bool = True):
     L.kvq_decode_attn_workspace_size.restype = sz
     L.kvq_decode_attn.argtypes = [cp, vp, i32, i32, vp, i32, vp, vp, f32, vp, vp, sz, vp, vp]
     L.kvq_decode_attn.restype = ctypes.c_int
+    L.kvq_decode_attn_static.argtypes = [cp, vp, i32, i32, vp, i32, vp, vp, f32, vp, vp, vp]
+    L.kvq_decode_attn_static.restype = ctypes.c_int
     L.kvq_status_string.argtypes = [ctypes.c_int]
     L.kvq_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -224,3 +227,26 @@ def kvq_decode_attn(cache: KVCache, q, block_table, seq_lens, out, workspace, ab
                            workspace.numel() * workspace.element_size(),
                            _dev(err_word, "err_word", U32), _stream(stream))
     _check("kvq_decode_attn", st)
+
+
+def kvq_decode_attn_static(cache: KVCache, q, block_table, seq_lens, out, abort_mask=None,
+                           sm_scale: Optional[float] = None, err_word=None, stream=None) -> None:
+    """kvq_decode_attn with the library's own static scratch instead of a
+    caller workspace, for callers that cannot allocate device memory (see
+    include/kvq.h).  Calls that can overlap on the GPU must not be issued."""
+    L = load()
+    c = cache.c()
+    B, Hq, D = q.shape
+    if D != c.head_dim or tuple(out.shape) != (B, Hq, D):
+        raise ValueError("q / out shapes do not match the cache")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table / seq_lens must have B rows")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    st = L.kvq_decode_attn_static(ctypes.byref(c), _dev(q, "q", BF16, 3), B, Hq,
+                                  _dev(block_table, "block_table", I32, 2),
+                                  int(block_table.shape[1]), _dev(seq_lens, "seq_lens", I32, 1),
+                                  _dev(abort_mask, "abort_mask", U8, 1), float(sm_scale),
+                                  _dev(out, "out", (torch.float32,), 3),
+                                  _dev(err_word, "err_word", U32), _stream(stream))
+    _check("kvq_decode_attn_static", st)

@@ -148,6 +148,29 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int32_
                            void *workspace, size_t workspace_bytes, uint32_t *err_word,
                            kvq_stream_t stream);
 
+/* kvq_decode_attn without a caller workspace.  The pages have no counterpart
+ * to this call: it exists for callers that cannot allocate device memory (a
+ * runtime that reserves all memory up front and serves it only from its own
+ * pool, a plugin host that forbids allocation in its execute callback, a
+ * latency-bound loop that cannot afford cudaMalloc).  It computes exactly what
+ * kvq_decode_attn computes, with the workspace taken from a static device
+ * array of KVQ_STATIC_SCRATCH_BYTES owned by the library (held on every GPU
+ * that loads it, until exit).  It allocates nothing.
+ * - Shapes whose kvq_decode_attn_workspace_size() exceeds
+ *   KVQ_STATIC_SCRATCH_BYTES return KVQ_ERR_WORKSPACE before any launch.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, that device current); make that first call before
+ *   any stream capture.
+ * - All calls share the one array: calls whose kernels can overlap on the GPU
+ *   (different streams or host threads without ordering) race and must not be
+ *   issued.  Stale contents from an earlier call are harmless. */
+#define KVQ_STATIC_SCRATCH_BYTES (64u << 20)
+KVQ_API kvq_status kvq_decode_attn_static(const kvq_cache *cache, const void *q, int32_t B,
+                                          int32_t Hq, const int32_t *block_table, int32_t MP,
+                                          const int32_t *seq_lens, const uint8_t *abort_mask,
+                                          float sm_scale, float *out, uint32_t *err_word,
+                                          kvq_stream_t stream);
+
 /* Human-readable name of a status. */
 KVQ_API const char *kvq_status_string(kvq_status status);
 

@@ -21,11 +21,10 @@
 //          G times), online softmax in the log2 domain with lazy rescaling,
 //          p.v; at the end of a segment they merge and either write the
 //          output row or a partial that the row's last CTA merges.
-//   Two split kernels exist: a tensor-core one for e4m3 with head_dim 128
-//   (decode_attn_mma.cuh: rows are groups of up to 8 kv heads, 16-token
-//   units, one consumer warp per kv head, no combine step for whole rows)
-//   and a CUDA-core one for bf16 caches and head_dim 64 (rows are single kv
-//   heads, 64-token units, four consumer warps per row).
+//   Two split kernels exist: a tensor-core one for head_dim 128, e4m3 or
+//   bf16 (decode_attn_mma.cuh: rows are groups of up to 8 kv heads, 16-token
+//   units, one consumer warp per kv head) and a CUDA-core one for head_dim 64
+//   (rows are single kv heads, 64-token units, four consumer warps per row).
 //
 // Every wait is bounded (see mbar_wait); a wait that gives up raises
 // KVQ_ERRBIT_TIMEOUT and the CTA leaves its loop.
@@ -196,7 +195,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// CUDA-core split kernel (bf16 caches, head_dim 64)
+// CUDA-core split kernel (head_dim 64)
 // ---------------------------------------------------------------------------
 
 template <int D, int G, bool kFp8>
@@ -549,24 +548,35 @@ SplitKernel make_split() {
   return k;
 }
 
-template <int G, int HG>
+template <int G, int HG, bool kBf16>
 SplitKernel make_split_hg() {
   SplitKernel k;
-  k.tma = split_hg_kernel<G, HG>;
-  k.smem = HgCfg<G, HG>::bytes;
+  k.tma = split_hg_kernel<G, HG, kBf16>;
+  k.smem = HgCfg<G, HG, kBf16>::bytes;
   k.threads = 32 * (HG + 1);
   k.hg = HG;
   k.unit = kTile;
   return k;
 }
 
-template <int G>
+template <int G, bool kBf16>
 bool pick_hg(int Hkv, SplitKernel *k) {
-  if (Hkv % 8 == 0) { *k = make_split_hg<G, 8>(); return true; }
-  if (Hkv % 4 == 0) { *k = make_split_hg<G, 4>(); return true; }
-  if (Hkv % 2 == 0) { *k = make_split_hg<G, 2>(); return true; }
-  *k = make_split_hg<G, 1>();
+  if (Hkv % 8 == 0) { *k = make_split_hg<G, 8, kBf16>(); return true; }
+  if (Hkv % 4 == 0) { *k = make_split_hg<G, 4, kBf16>(); return true; }
+  if (Hkv % 2 == 0) { *k = make_split_hg<G, 2, kBf16>(); return true; }
+  *k = make_split_hg<G, 1, kBf16>();
   return true;
+}
+
+template <bool kBf16>
+bool pick_hg_g(int G, int Hkv, SplitKernel *k) {
+  switch (G) {
+    case 1: return pick_hg<1, kBf16>(Hkv, k);
+    case 2: return pick_hg<2, kBf16>(Hkv, k);
+    case 4: return pick_hg<4, kBf16>(Hkv, k);
+    case 8: return pick_hg<8, kBf16>(Hkv, k);
+  }
+  return false;
 }
 
 template <int D, bool kFp8>
@@ -581,15 +591,7 @@ bool pick_g(int G, SplitKernel *k) {
 }
 
 bool pick_split(int D, int G, int Hkv, bool fp8, SplitKernel *k) {
-  if (fp8 && D == 128) {
-    switch (G) {
-      case 1: return pick_hg<1>(Hkv, k);
-      case 2: return pick_hg<2>(Hkv, k);
-      case 4: return pick_hg<4>(Hkv, k);
-      case 8: return pick_hg<8>(Hkv, k);
-    }
-    return false;
-  }
+  if (D == 128) return fp8 ? pick_hg_g<false>(G, Hkv, k) : pick_hg_g<true>(G, Hkv, k);
   if (D == 64) return fp8 ? pick_g<64, true>(G, k) : pick_g<64, false>(G, k);
   if (D == 128) return fp8 ? pick_g<128, true>(G, k) : pick_g<128, false>(G, k);
   return false;
@@ -639,19 +641,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 4-D map over an e4m3 pool [num_pages][Hkv][P][D] (D = 128 bytes innermost);
-// one box is 16 slots of `hg` consecutive kv heads of one page, 128-byte
-// swizzled.
+// 4-D map over a pool [num_pages][Hkv][P][D] (D innermost); one box is 128
+// bytes of dims x 16 slots x `hg` consecutive kv heads of one page, 128-byte
+// swizzled (all of D for e4m3, half of it for bf16).
 bool encode_pool_map(CUtensorMap *map, const void *pool, const kvq_cache &c, int hg) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
+  const bool bf16 = c.kv_dtype == KVQ_KV_BF16;
+  const cuuint64_t es = bf16 ? 2 : 1;
   const cuuint64_t D = c.head_dim, P = c.page_size, H = c.num_kv_heads, NP = c.num_pages;
   const cuuint64_t dims[4] = {D, P, H, NP};
-  const cuuint64_t strides[3] = {D, P * D, H * P * D};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(kTile),
+  const cuuint64_t strides[3] = {D * es, P * D * es, H * P * D * es};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(kTile),
                              static_cast<cuuint32_t>(hg), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(pool), dims, strides, box,
+  return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+             const_cast<void *>(pool), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -28,6 +28,14 @@
 // Query heads occupy rows 0..G-1 of S (G <= 8) and columns 0..G-1 of O^T.
 // A row r of the 16-token tile sits at byte r*128 of the head's 2 KB block
 // with its 16-byte chunk c stored at chunk c ^ (r % 8) (TMA 128-byte swizzle).
+//
+// The bf16 variant (the comparison kernel for an uncompressed cache) stages
+// each head as two such 128-byte-wide planes (dims 0-63 and 64-127, two TMA
+// boxes), runs q.k as exact bf16 MMAs (thread t supplies dims 16t..16t+15 of
+// each plane) and gets V^T straight from ldmatrix.trans (m-tile i is dims
+// 16i..16i+15: row g is dim 16i+g, row g+8 is dim 16i+8+g).  The softmax
+// weights are split into a bf16 head and a bf16 remainder, p = hi + lo, and
+// p.v runs as two MMAs, so the weights keep about 16 significant bits.
 #pragma once
 
 namespace kvq {
@@ -66,14 +74,40 @@ __device__ __forceinline__ uint4 lds128(const uint8_t *p) {
   return *reinterpret_cast<const uint4 *>(p);
 }
 
-constexpr int kTile = 16;  // tokens per stage of the tensor-core kernel
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
-template <int G, int HG>
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const uint8_t *p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+constexpr int kTile = 16;  // tokens per stage of the tensor-core kernel
+constexpr int kPlane = kTile * 128;  // 2 KB: 16 tokens x 128 bytes of one head
+
+template <int G, int HG, bool kBf16>
 struct HgCfg {
   static constexpr int D = 128;
-  static constexpr int NS = (HG * G >= 64) ? 5 : 6;     // stages in the ring
-  static constexpr int HEAD_TILE = kTile * D;           // 2 KB: 16 tokens of one head
-  static constexpr int KV_BYTES = HG * HEAD_TILE;       // one stage of K (or V)
+  static constexpr int PLANES = kBf16 ? 2 : 1;          // 128-byte-wide planes per head
+  static constexpr int PLANE = HG * kPlane;             // one plane of the head group
+  static constexpr int TILES = 1;                       // 16-token tiles per stage
+  static constexpr int TILE_BYTES = PLANES * PLANE;     // one tile of K (or V)
+  static constexpr int KV_BYTES = TILES * TILE_BYTES;   // one stage of K (or V)
+  // stages in the ring: 192 KB of K+V in flight per SM for 8-head groups
+  static constexpr int NS = kBf16 ? 3 : ((HG * G >= 64) ? 5 : 6);
   static constexpr int Q_BYTES = HG * G * D * 2;        // the group's query rows (bf16)
   static constexpr int KPART = part_stride(G, D);       // floats per kv head in a slot
   static constexpr int PART = HG * KPART;               // floats per partial slot
@@ -84,7 +118,7 @@ struct HgCfg {
   static constexpr size_t bytes = off_ctl + sizeof(Ctrl) + 1024;  // + alignment slack
   static_assert(G >= 1 && G <= 8 && HG >= 1 && HG <= 8, "group sizes");
   static_assert(KV_BYTES % 1024 == 0 && off_q % 1024 == 0 && off_ctl % 16 == 0, "alignment");
-  static_assert(NS <= kMaxStages, "control block");
+  static_assert(NS <= kMaxStages && TILES <= 2, "control block");
   static_assert(bytes <= 227 * 1024, "shared memory");
 };
 
@@ -218,11 +252,120 @@ __device__ __forceinline__ void tile_step(HeadState &st, const uint8_t *ks, cons
   }
 }
 
-template <int G, int HG>
+// bf16 query rows -> bf16 fragments (exact, no scaling); thread t supplies
+// dims 16t+4s.. of plane 0 (k-steps 0-3) and 64+16t+4(s-4).. (k-steps 4-7).
+template <int G>
+__device__ __forceinline__ void load_q_bf16(HeadState &st, const uint8_t *qhead, float q_scale,
+                                            int gq, int tq) {
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int dim = (s < 4) ? 16 * tq + 4 * s : 64 + 16 * tq + 4 * (s - 4);
+    if (gq < G) {
+      st.qa0[s] = *reinterpret_cast<const uint32_t *>(qhead + (gq * 128 + dim) * 2);
+      st.qa2[s] = *reinterpret_cast<const uint32_t *>(qhead + (gq * 128 + dim + 2) * 2);
+    } else {
+      st.qa0[s] = st.qa2[s] = 0u;
+    }
+  }
+  st.qk_scale = q_scale;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+  st.m_run = -INFINITY;
+  st.l_run = 0.f;
+}
+
+// One 16-token tile of one kv head with a bf16 cache: k0/k1 (v0/v1) are the
+// head's two 2 KB planes (dims 0-63, 64-127).
+template <int G>
+__device__ __forceinline__ void tile_step_bf16(HeadState &st, const uint8_t *k0, const uint8_t *k1,
+                                               const uint8_t *v0, const uint8_t *v1, int ntok,
+                                               int gq, int tq, int lane) {
+  float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {  // n-tile j: token 8j+gq, row % 8 == gq
+    const int r = 8 * j + gq;
+    const int ca = ((2 * tq) ^ gq) * 16, cb = ((2 * tq + 1) ^ gq) * 16;
+    const uint4 a = lds128(k0 + r * 128 + ca), b = lds128(k0 + r * 128 + cb);
+    const uint4 c = lds128(k1 + r * 128 + ca), d = lds128(k1 + r * 128 + cb);
+    const uint32_t w[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w,
+                            c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int s = 0; s < 8; ++s) mma_16816_bf16(sc[j], st.qa0[s], 0u, st.qa2[s], 0u, w[2 * s], w[2 * s + 1]);
+  }
+  const bool row_ok = gq < G;
+  const int t0 = 2 * tq, t1 = 8 + 2 * tq;
+  const float x00 = (row_ok && t0 < ntok) ? sc[0][0] * st.qk_scale : -INFINITY;
+  const float x01 = (row_ok && t0 + 1 < ntok) ? sc[0][1] * st.qk_scale : -INFINITY;
+  const float x10 = (row_ok && t1 < ntok) ? sc[1][0] * st.qk_scale : -INFINITY;
+  const float x11 = (row_ok && t1 + 1 < ntok) ? sc[1][1] * st.qk_scale : -INFINITY;
+  float mx = fmaxf(fmaxf(x00, x01), fmaxf(x10, x11));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const bool grow = mx > st.m_run + kRescaleThreshold;
+  if (__any_sync(0xffffffffu, grow)) {
+    const float f = grow ? exp2f(st.m_run - mx) : 1.f;
+    if (grow) {
+      st.m_run = mx;
+      st.l_run *= f;
+    }
+    const float fa = __shfl_sync(0xffffffffu, f, 8 * tq);
+    const float fb = __shfl_sync(0xffffffffu, f, 8 * tq + 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      st.o[i][0] *= fa;
+      st.o[i][1] *= fb;
+      st.o[i][2] *= fa;
+      st.o[i][3] *= fb;
+    }
+  }
+  const float p00 = x00 == -INFINITY ? 0.f : fast_exp2(x00 - st.m_run);
+  const float p01 = x01 == -INFINITY ? 0.f : fast_exp2(x01 - st.m_run);
+  const float p10 = x10 == -INFINITY ? 0.f : fast_exp2(x10 - st.m_run);
+  const float p11 = x11 == -INFINITY ? 0.f : fast_exp2(x11 - st.m_run);
+  st.l_run += (p00 + p01) + (p10 + p11);
+  // p = hi + lo, both bf16
+  const uint32_t h0 = f32x2_to_bf16x2(p00, p01), h1 = f32x2_to_bf16x2(p10, p11);
+  const uint32_t l0 = f32x2_to_bf16x2(p00 - __uint_as_float(h0 << 16),
+                                      p01 - __uint_as_float(h0 & 0xFFFF0000u));
+  const uint32_t l1 = f32x2_to_bf16x2(p10 - __uint_as_float(h1 << 16),
+                                      p11 - __uint_as_float(h1 & 0xFFFF0000u));
+
+  // ---- O^T += V^T P^T; ldmatrix.trans lane l addresses row (l%8) + 8*(l>=16)
+  // of 16-byte chunk 2(i%4) + ((l/8)&1) in plane i/4
+  const int lrow = (lane & 7) + ((lane >> 4) << 3);
+  const int lchunk = (lane >> 3) & 1;
+  const bool tail = ntok < kTile;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint8_t *vp = (i < 4 ? v0 : v1) + lrow * 128 + (((2 * (i & 3) + lchunk) ^ (lrow & 7)) * 16);
+    uint32_t a[4];
+    ldsm_x4_trans(a, vp);
+    if (tail) {  // cached values past the sequence may be anything: zero them
+      const uint32_t m0 = (t0 < ntok ? 0xFFFFu : 0u) | (t0 + 1 < ntok ? 0xFFFF0000u : 0u);
+      const uint32_t m1 = (t1 < ntok ? 0xFFFFu : 0u) | (t1 + 1 < ntok ? 0xFFFF0000u : 0u);
+      a[0] &= m0;
+      a[1] &= m0;
+      a[2] &= m1;
+      a[3] &= m1;
+    }
+    mma_16816_bf16(st.o[i], a[0], a[1], a[2], a[3], h0, h1);
+    mma_16816_bf16(st.o[i], a[0], a[1], a[2], a[3], l0, l1);
+  }
+}
+
+// Output dims held by thread (g,t) in m-tile i: rows g and g+8 of O^T.
+template <bool kBf16>
+__device__ __forceinline__ int dim_lo(int i, int gq) { return kBf16 ? 16 * i + gq : 16 * gq + 2 * i; }
+template <bool kBf16>
+__device__ __forceinline__ int dim_hi(int i, int gq) {
+  return kBf16 ? 16 * i + 8 + gq : 16 * gq + 2 * i + 1;
+}
+
+template <int G, int HG, bool kBf16>
 __global__ void __launch_bounds__(32 * (HG + 1))
     split_hg_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, SplitArgs a) {
-  using C = HgCfg<G, HG>;
+  using C = HgCfg<G, HG, kBf16>;
   constexpr int NS = C::NS;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // TMA 128-byte swizzle needs 1024-byte aligned destinations
@@ -276,7 +419,8 @@ __global__ void __launch_bounds__(32 * (HG + 1))
       const int seg_units = static_cast<int>(min(static_cast<long long>(units_b - s), u_end - u));
       const int t_begin = s * kTile;
       const int t_end = min((s + seg_units) * kTile, L);
-      const int nstages = (t_end - t_begin + kTile - 1) / kTile;
+      constexpr int kStageTok = kTile * C::TILES;
+      const int nstages = (t_end - t_begin + kStageTok - 1) / kStageTok;
       const int lp0 = t_begin / a.P;
       if (b != win_b || lp0 < win || lp0 >= win + 32) {
         win_b = b;
@@ -305,34 +449,86 @@ __global__ void __launch_bounds__(32 * (HG + 1))
         ok = __shfl_sync(0xffffffffu, waited ? 1 : 0, 0) != 0 &&
              !*reinterpret_cast<volatile int *>(&ctl.fail);
         if (!ok) break;
-        const int tok0 = t_begin + st * kTile;
-        const int ntok = min(kTile, t_end - tok0);
-        const int lp = tok0 / a.P;
-        while (lp >= win + 32) {  // slide the window by 32 pages
+        const int tok0 = t_begin + st * kStageTok;
+        const int ntok = min(kStageTok, t_end - tok0);
+        const int lp_first = tok0 / a.P;
+        while (lp_first >= win + 32) {  // slide the window by 32 pages
           win += 32;
           cur = nxt;
           nxt = bt_load(win + 32 + lane);
         }
-        const int page = __shfl_sync(0xffffffffu, cur, lp - win);
-        const bool bad_page = page < 0 || page >= a.num_pages;
-        if (lane == 0) {
-          if (bad_page) {
-            atomicOr(a.bad + row, 1);
-            report(a.err_word, KVQ_ERRBIT_PAGE);
+        if constexpr (C::TILES == 1) {
+          const int page = __shfl_sync(0xffffffffu, cur, lp_first - win);
+          const bool bad_page = page < 0 || page >= a.num_pages;
+          if (lane == 0) {
+            if (bad_page) {
+              atomicOr(a.bad + row, 1);
+              report(a.err_word, KVQ_ERRBIT_PAGE);
+            }
+            ctl.desc[slot][0] = make_int4(
+                row, tok0,
+                ntok | (st == 0 ? kFirst : 0) | (st == nstages - 1 ? kLast : 0) |
+                    (bad_page ? kBad : 0),
+                nparts);
+            ctl.desc[slot][1] = make_int4(row + c, c_lo, b, grp | (qs << 16));
+            mbar_arrive_expect_tx(&ctl.full[slot], bad_page ? 0u : 2u * C::KV_BYTES);
+            if (!bad_page) {
+              const int y = tok0 % a.P;
+#pragma unroll
+              for (int pl = 0; pl < C::PLANES; ++pl) {  // plane pl: 128 bytes from x = 64*pl
+                const uint32_t off = slot * C::KV_BYTES + pl * C::PLANE;
+                tma_load_4d(kbuf + off, &kmap, 64 * pl, y, grp * HG, page, &ctl.full[slot], pol);
+                tma_load_4d(vbuf + off, &vmap, 64 * pl, y, grp * HG, page, &ctl.full[slot], pol);
+              }
+            }
           }
-          ctl.desc[slot][0] = make_int4(
-              row, tok0,
-              ntok | (st == 0 ? kFirst : 0) | (st == nstages - 1 ? kLast : 0) |
-                  (bad_page ? kBad : 0),
-              nparts);
-          ctl.desc[slot][1] = make_int4(row + c, c_lo, b, grp | (qs << 16));
-          mbar_arrive_expect_tx(&ctl.full[slot], bad_page ? 0u : 2u * C::KV_BYTES);
-          if (!bad_page) {
-            const int y = tok0 % a.P;
-            tma_load_4d(kbuf + slot * C::KV_BYTES, &kmap, 0, y, grp * HG, page, &ctl.full[slot],
-                        pol);
-            tma_load_4d(vbuf + slot * C::KV_BYTES, &vmap, 0, y, grp * HG, page, &ctl.full[slot],
-                        pol);
+        } else {
+          // tile k of the stage: tokens tok0+16k.., logical page (tok0+16k)/P,
+          // which lies in [win, win+64): cur or nxt
+          int tile_page[C::TILES];
+          int bad_bits = 0;
+#pragma unroll
+          for (int k = 0; k < C::TILES; ++k) {
+            const int lpk = (tok0 + kTile * k) / a.P - win;
+            const int from_cur = __shfl_sync(0xffffffffu, cur, lpk & 31);
+            const int from_nxt = __shfl_sync(0xffffffffu, nxt, lpk & 31);
+            tile_page[k] = -1;
+            if (kTile * k < ntok) {
+              const int page = lpk < 32 ? from_cur : from_nxt;
+              if (page < 0 || page >= a.num_pages)
+                bad_bits |= kBad << k;
+              else
+                tile_page[k] = page;
+            }
+          }
+          if (lane == 0) {
+            if (bad_bits) {
+              atomicOr(a.bad + row, 1);
+              report(a.err_word, KVQ_ERRBIT_PAGE);
+            }
+            ctl.desc[slot][0] = make_int4(
+                row, tok0,
+                ntok | (st == 0 ? kFirst : 0) | (st == nstages - 1 ? kLast : 0) | bad_bits,
+                nparts);
+            ctl.desc[slot][1] = make_int4(row + c, c_lo, b, grp | (qs << 16));
+            uint32_t tx = 0;
+#pragma unroll
+            for (int k = 0; k < C::TILES; ++k)
+              if (tile_page[k] >= 0) tx += 2u * C::TILE_BYTES;
+            mbar_arrive_expect_tx(&ctl.full[slot], tx);
+#pragma unroll
+            for (int k = 0; k < C::TILES; ++k) {
+              if (tile_page[k] < 0) continue;
+              const int y = (tok0 + kTile * k) % a.P;
+#pragma unroll
+              for (int pl = 0; pl < C::PLANES; ++pl) {
+                const uint32_t off = slot * C::KV_BYTES + k * C::TILE_BYTES + pl * C::PLANE;
+                tma_load_4d(kbuf + off, &kmap, 64 * pl, y, grp * HG, tile_page[k],
+                            &ctl.full[slot], pol);
+                tma_load_4d(vbuf + off, &vmap, 64 * pl, y, grp * HG, tile_page[k],
+                            &ctl.full[slot], pol);
+              }
+            }
           }
         }
         __syncwarp();
@@ -378,15 +574,42 @@ __global__ void __launch_bounds__(32 * (HG + 1))
     if (d0.z & kFirst) {
       const int qs = (d1.w >> 16) & 1;
       if (!ctl_wait(ctl, &ctl.qfull[qs], (nseg >> 1) & 1, a.err_word)) break;
-      load_q<G>(hs, qbuf + qs * C::Q_BYTES + warp * G * C::D * 2, a.q_scale, gq, tq);
+      if constexpr (kBf16)
+        load_q_bf16<G>(hs, qbuf + qs * C::Q_BYTES + warp * G * C::D * 2, a.q_scale, gq, tq);
+      else
+        load_q<G>(hs, qbuf + qs * C::Q_BYTES + warp * G * C::D * 2, a.q_scale, gq, tq);
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.qempty[qs]);
       seg_bad = false;
     }
-    seg_bad |= (d0.z & kBad) != 0;
-    if (!(d0.z & kBad))
-      tile_step<G>(hs, kbuf + slot * C::KV_BYTES + warp * C::HEAD_TILE,
-                   vbuf + slot * C::KV_BYTES + warp * C::HEAD_TILE, ntok, gq, tq);
+    if constexpr (C::TILES == 1) {
+      seg_bad |= (d0.z & kBad) != 0;
+      if (!(d0.z & kBad)) {
+        const uint8_t *kt = kbuf + slot * C::KV_BYTES + warp * kPlane;
+        const uint8_t *vt = vbuf + slot * C::KV_BYTES + warp * kPlane;
+        if constexpr (kBf16)
+          tile_step_bf16<G>(hs, kt, kt + C::PLANE, vt, vt + C::PLANE, ntok, gq, tq, lane);
+        else
+          tile_step<G>(hs, kt, vt, ntok, gq, tq);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < C::TILES; ++k) {
+        const int nt = ntok - kTile * k;
+        if (nt <= 0) break;
+        if (d0.z & (kBad << k)) {
+          seg_bad = true;
+          continue;
+        }
+        const uint8_t *kt = kbuf + slot * C::KV_BYTES + k * C::TILE_BYTES + warp * kPlane;
+        const uint8_t *vt = vbuf + slot * C::KV_BYTES + k * C::TILE_BYTES + warp * kPlane;
+        if constexpr (kBf16)
+          tile_step_bf16<G>(hs, kt, kt + C::PLANE, vt, vt + C::PLANE, min(nt, kTile), gq, tq,
+                            lane);
+        else
+          tile_step<G>(hs, kt, vt, min(nt, kTile), gq, tq);
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl.empty[slot]);
 
@@ -407,13 +630,24 @@ __global__ void __launch_bounds__(32 * (HG + 1))
         const float sb = seg_bad ? 0.f : a.v_scale / lb;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int dim = 16 * gq + 2 * i;
-          if (ha < G)
-            *reinterpret_cast<float2 *>(out + ha * C::D + dim) =
-                make_float2(hs.o[i][0] * sa, hs.o[i][2] * sa);
-          if (hb < G)
-            *reinterpret_cast<float2 *>(out + hb * C::D + dim) =
-                make_float2(hs.o[i][1] * sb, hs.o[i][3] * sb);
+          const int dl = dim_lo<kBf16>(i, gq), dh = dim_hi<kBf16>(i, gq);
+          if constexpr (!kBf16) {  // dims dl, dl+1: one 8-byte store
+            if (ha < G)
+              *reinterpret_cast<float2 *>(out + ha * C::D + dl) =
+                  make_float2(hs.o[i][0] * sa, hs.o[i][2] * sa);
+            if (hb < G)
+              *reinterpret_cast<float2 *>(out + hb * C::D + dl) =
+                  make_float2(hs.o[i][1] * sb, hs.o[i][3] * sb);
+          } else {
+            if (ha < G) {
+              out[ha * C::D + dl] = hs.o[i][0] * sa;
+              out[ha * C::D + dh] = hs.o[i][2] * sa;
+            }
+            if (hb < G) {
+              out[hb * C::D + dl] = hs.o[i][1] * sb;
+              out[hb * C::D + dh] = hs.o[i][3] * sb;
+            }
+          }
         }
       } else {
         // partial of this head: acc[G][D], then m[G], l[G]
@@ -421,13 +655,24 @@ __global__ void __launch_bounds__(32 * (HG + 1))
                       static_cast<int64_t>(warp) * C::KPART;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int dim = 16 * gq + 2 * i;
-          if (ha < G)
-            *reinterpret_cast<float2 *>(mine + ha * C::D + dim) =
-                make_float2(hs.o[i][0], hs.o[i][2]);
-          if (hb < G)
-            *reinterpret_cast<float2 *>(mine + hb * C::D + dim) =
-                make_float2(hs.o[i][1], hs.o[i][3]);
+          const int dl = dim_lo<kBf16>(i, gq), dh = dim_hi<kBf16>(i, gq);
+          if constexpr (!kBf16) {  // dims dl, dl+1: one 8-byte store
+            if (ha < G)
+              *reinterpret_cast<float2 *>(mine + ha * C::D + dl) =
+                  make_float2(hs.o[i][0], hs.o[i][2]);
+            if (hb < G)
+              *reinterpret_cast<float2 *>(mine + hb * C::D + dl) =
+                  make_float2(hs.o[i][1], hs.o[i][3]);
+          } else {
+            if (ha < G) {
+              mine[ha * C::D + dl] = hs.o[i][0];
+              mine[ha * C::D + dh] = hs.o[i][2];
+            }
+            if (hb < G) {
+              mine[hb * C::D + dl] = hs.o[i][1];
+              mine[hb * C::D + dh] = hs.o[i][3];
+            }
+          }
         }
         if (gq == 0) {
           if (ha < G) {
@@ -480,30 +725,47 @@ __global__ void __launch_bounds__(32 * (HG + 1))
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const int dim = 16 * gq + 2 * i;
-              if (ha < G) {
-                const float2 v = __ldcg(reinterpret_cast<const float2 *>(pp + ha * C::D + dim));
-                acc[i][0] = fmaf(fa, v.x, acc[i][0]);
-                acc[i][2] = fmaf(fa, v.y, acc[i][2]);
+              const int dl = dim_lo<kBf16>(i, gq), dh = dim_hi<kBf16>(i, gq);
+              float2 va, vb;
+              if constexpr (!kBf16) {  // dims dl, dl+1: one 8-byte load
+                va = ha < G ? __ldcg(reinterpret_cast<const float2 *>(pp + ha * C::D + dl))
+                            : make_float2(0.f, 0.f);
+                vb = hb < G ? __ldcg(reinterpret_cast<const float2 *>(pp + hb * C::D + dl))
+                            : make_float2(0.f, 0.f);
+              } else {
+                va = ha < G ? make_float2(__ldcg(pp + ha * C::D + dl), __ldcg(pp + ha * C::D + dh))
+                            : make_float2(0.f, 0.f);
+                vb = hb < G ? make_float2(__ldcg(pp + hb * C::D + dl), __ldcg(pp + hb * C::D + dh))
+                            : make_float2(0.f, 0.f);
               }
-              if (hb < G) {
-                const float2 v = __ldcg(reinterpret_cast<const float2 *>(pp + hb * C::D + dim));
-                acc[i][1] = fmaf(fb, v.x, acc[i][1]);
-                acc[i][3] = fmaf(fb, v.y, acc[i][3]);
-              }
+              acc[i][0] = fmaf(fa, va.x, acc[i][0]);
+              acc[i][2] = fmaf(fa, va.y, acc[i][2]);
+              acc[i][1] = fmaf(fb, vb.x, acc[i][1]);
+              acc[i][3] = fmaf(fb, vb.y, acc[i][3]);
             }
           }
           const float sa = row_bad ? 0.f : a.v_scale / dena;
           const float sb = row_bad ? 0.f : a.v_scale / denb;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int dim = 16 * gq + 2 * i;
-            if (ha < G)
-              *reinterpret_cast<float2 *>(out + ha * C::D + dim) =
-                  make_float2(acc[i][0] * sa, acc[i][2] * sa);
-            if (hb < G)
-              *reinterpret_cast<float2 *>(out + hb * C::D + dim) =
-                  make_float2(acc[i][1] * sb, acc[i][3] * sb);
+            const int dl = dim_lo<kBf16>(i, gq), dh = dim_hi<kBf16>(i, gq);
+            if constexpr (!kBf16) {
+              if (ha < G)
+                *reinterpret_cast<float2 *>(out + ha * C::D + dl) =
+                    make_float2(acc[i][0] * sa, acc[i][2] * sa);
+              if (hb < G)
+                *reinterpret_cast<float2 *>(out + hb * C::D + dl) =
+                    make_float2(acc[i][1] * sb, acc[i][3] * sb);
+            } else {
+              if (ha < G) {
+                out[ha * C::D + dl] = acc[i][0] * sa;
+                out[ha * C::D + dh] = acc[i][2] * sa;
+              }
+              if (hb < G) {
+                out[hb * C::D + dl] = acc[i][1] * sb;
+                out[hb * C::D + dh] = acc[i][3] * sb;
+              }
+            }
           }
         }
       }

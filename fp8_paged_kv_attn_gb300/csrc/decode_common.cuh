@@ -26,7 +26,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max g
 // stage descriptor flags (packed above the 16-bit token count)
 constexpr int kFirst = 1 << 16;  // first stage of a segment
 constexpr int kLast = 1 << 17;   // last stage of a segment
-constexpr int kBad = 1 << 18;    // a page of this stage was outside the pool
+constexpr int kBad = 1 << 18;    // a page of this stage (of its tile k: kBad << k) was outside the pool
 
 struct SplitArgs {
   const uint8_t *k_pool, *v_pool;

@@ -360,7 +360,7 @@ def run_gpu(args, dist, rank, world, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "kvq_decode_attn (plan + split), CUDA events around each call",
+            "kernel": "kvq_decode_attn (plan + split + combine), CUDA events around each call",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -371,7 +371,7 @@ def run_gpu(args, dist, rank, world, local):
             "bytes_per_call": int(statistics.mean(bytes_per_call)),
             "ms_per_call": round(statistics.mean(attn_ms), 5),
         },
-        "gpu_launches": args.steps * (1 + (1 if check else 0) + 2),
+        "gpu_launches": args.steps * (1 + (1 if check else 0) + 3),
         "clocks": clk,
     }
     if e2e is not None:

@@ -59,6 +59,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seed", type=int, default=2)
+    ap.add_argument("--workload", choices=["ragged", "integrity", "8x8192"], default=None,
+                    help="time one of the other decode workloads (pools filled with random "
+                         "finite e4m3 codes on the GPU; one JSON line, not the headline)")
     ap.add_argument("--sweep", action="store_true",
                     help="concurrency sweep 1/8/16/32/64 requests, e4m3 and bf16 KV at equal pool "
                          "bytes; one JSON line per point (not the headline line)")
@@ -552,8 +555,84 @@ def run_sweep(args):
             del cache
 
 
+def run_workload(args):
+    """Decode-step timing on the ragged (page 64, 8 query heads per kv head),
+    integrity (256 requests, stale tags, check -> mask -> attention) or 8x8192
+    workloads.  The cache holds random finite e4m3 codes written on the GPU
+    (timing only; the parity tests cover these workloads with real data).  For
+    the integrity workload it also times the same steps without the check and
+    reports the check's share of the step."""
+    import torch
+    from fp8_paged_kv_attn_gb300 import inputs, kvq
+
+    kvq.load()
+    peak, _ = measured_hbm_peak()
+    w = {"ragged": inputs.ragged, "integrity": inputs.integrity,
+         "8x8192": inputs.cfg8x8k}[args.workload]()
+    B, Hq, Hkv, D, P = w.B, w.Hq, w.Hkv, w.D, w.P
+    shape = w.pool_shape()
+    gen = torch.Generator(device="cuda").manual_seed(args.seed)
+    pools = [torch.randint(0, 0x77, shape, dtype=torch.uint8, device="cuda", generator=gen)
+             for _ in range(2)]
+    cache = kvq.KVCache(pools[0], pools[1], 0.01, 0.01)
+    bt = torch.from_numpy(w.block_table).cuda()
+    tags = torch.from_numpy(w.page_tags.view(np.int32)).cuda()
+    exp_tags = torch.from_numpy(w.expected_tags.view(np.int32)).cuda()
+    lens_np = w.seq_lens_after(0)
+    lens = torch.from_numpy(lens_np).cuda()
+    q, k_new, v_new, req, pos = w.step_inputs(0)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    d_q, d_k, d_v = bf16(q), bf16(k_new), bf16(v_new)
+    d_req, d_pos = torch.from_numpy(req).cuda(), torch.from_numpy(pos).cuda()
+    mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+    ws = kvq.workspace(B, Hq, Hkv, D)
+    stream = torch.cuda.current_stream()
+
+    def run(check, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(n):
+            kvq.kvq_append(cache, d_k, d_v, d_req, d_pos, bt)
+            if check:
+                kvq.kvq_check_tags(bt, lens, P, tags, exp_tags, mask)
+            ev[i][0].record(stream)
+            kvq.kvq_decode_attn(cache, d_q, bt, lens, out, ws, abort_mask=mask if check else None,
+                                sm_scale=float(w.sm_scale))
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / n, statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    run(True, args.warmup)
+    run(False, args.warmup)
+    step_on, attn_on = run(True, args.steps)
+    step_off, attn_off = run(False, args.steps)
+    aborted = int(mask.sum().item())
+    alive = (mask.cpu().numpy() == 0)
+    byts = attn_bytes(lens_np[alive], Hq, Hkv, D, P, 1)
+    res = {"workload": w.name, "batch": B, "tokens": int(lens_np.sum()), "Hq": Hq, "Hkv": Hkv,
+           "page_size": P, "steps": args.steps,
+           "step_ms_with_check": round(step_on, 5), "attn_us_with_check": round(attn_on * 1e3, 2),
+           "attn_GBs": round(byts / (attn_on * 1e-3) / 1e9, 1),
+           "frac_of_measured_peak": round(byts / (attn_on * 1e-3) / 1e9 / peak, 4),
+           "aborted_requests": aborted}
+    if args.workload == "integrity":
+        res["step_ms_without_check"] = round(step_off, 5)
+        res["check_overhead_pct_of_step"] = round(100 * (step_on - step_off) / step_off, 2)
+    print(json.dumps(res), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.workload:
+        run_workload(args)
+        return
     if args.sweep:
         run_sweep(args)
         return

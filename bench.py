@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--check", choices=["on", "off"], default="on")
     ap.add_argument("--offset", type=int, default=400, help="first generated-token index")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="call the library per operation instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seed", type=int, default=2)
@@ -195,6 +197,157 @@ def attn_bytes(lens, Hq, Hkv, D, P, es):
 
 
 # ----------------------------------------------------------------------------
+# the decode step: packed inputs, eager calls or a replayed CUDA graph
+# ----------------------------------------------------------------------------
+
+class StepInputs:
+    """The inputs of one decode step (q, k_new, v_new, pos, seq_lens) packed
+    into one byte row, every field 256-byte aligned, so that a step's inputs
+    are staged with a single copy (device to device, or host to device)."""
+
+    def __init__(self, torch, B, Hq, Hkv, D):
+        self.torch = torch
+        spec = [("q", torch.bfloat16, (B, Hq, D), 2), ("k", torch.bfloat16, (B, Hkv, D), 2),
+                ("v", torch.bfloat16, (B, Hkv, D), 2), ("pos", torch.int32, (B,), 4),
+                ("lens", torch.int32, (B,), 4)]
+        self.fields, off = [], 0
+        for name, dt, shape, es in spec:
+            n = int(np.prod(shape)) * es
+            self.fields.append((name, off, n, dt, shape))
+            off += -(-n // 256) * 256
+        self.nbytes = off
+
+    def views(self, row):
+        return {name: row[o:o + n].view(dt).view(shape) for name, o, n, dt, shape in self.fields}
+
+    def pack(self, steps):
+        """steps: per step a dict field -> numpy array (bf16 fields as 16-bit
+        bit patterns).  Returns a uint8 host tensor [len(steps), nbytes]."""
+        torch = self.torch
+        host = torch.zeros((len(steps), self.nbytes), dtype=torch.uint8)
+        for i, st in enumerate(steps):
+            for name, o, n, _, _ in self.fields:
+                raw = np.ascontiguousarray(st[name]).view(np.uint8).reshape(-1)
+                assert raw.size == n, (name, raw.size, n)
+                host[i, o:o + n] = torch.from_numpy(raw)
+        return host
+
+
+class DecodeStep:
+    """One decode step over a packed input row: kvq_append, kvq_check_tags
+    (when `check`; it writes `mask`) and kvq_decode_attn (which skips the
+    requests `mask` flags, when a mask is given), through the library's
+    Python binding.
+
+    graph=True captures the step once over static buffers into a CUDA graph
+    (the five kernels are chained as programmatic dependents, which the
+    capture keeps as programmatic edges); each step then stages its inputs
+    with one copy into the static row and replays the graph.  A second graph
+    holds the attention call alone, for timing it by itself.  graph=False
+    calls the library eagerly on the step's own row."""
+
+    def __init__(self, torch, kvq, cache, bt, P, sm_scale, packer, out, ws, err=None,
+                 check=False, tags=None, exp_tags=None, mask=None, graph=True):
+        self.torch, self.kvq, self.cache, self.bt, self.P = torch, kvq, cache, bt, P
+        self.sm_scale, self.packer, self.out, self.ws, self.err = sm_scale, packer, out, ws, err
+        self.check, self.tags, self.exp_tags, self.mask = check, tags, exp_tags, mask
+        self.graph = graph
+        B = bt.shape[0]
+        self.req_idx = torch.arange(B, dtype=torch.int32, device="cuda")
+        self.row = torch.zeros(packer.nbytes, dtype=torch.uint8, device="cuda")
+        self.static = packer.views(self.row)
+        self.g_step = self.g_attn = None
+
+    # -- the library calls
+    def append_check(self, v):
+        kvq = self.kvq
+        kvq.kvq_append(self.cache, v["k"], v["v"], self.req_idx, v["pos"], self.bt,
+                       err_word=self.err)
+        if self.check:
+            kvq.kvq_check_tags(self.bt, v["lens"], self.P, self.tags, self.exp_tags, self.mask)
+
+    def attn(self, v):
+        self.kvq.kvq_decode_attn(self.cache, v["q"], self.bt, v["lens"], self.out, self.ws,
+                                 abort_mask=self.mask, sm_scale=self.sm_scale, err_word=self.err)
+
+    def eager(self, v):
+        self.append_check(v)
+        self.attn(v)
+
+    # -- graphs
+    def capture(self, warm_row):
+        """Runs the step eagerly on `warm_row` (fills the library's per-device
+        caches), then captures both graphs on the static row."""
+        torch = self.torch
+        self.row.copy_(warm_row)
+        self.eager(self.static)
+        torch.cuda.synchronize()
+        self.g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_step):
+            self.eager(self.static)
+        self.g_attn = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_attn):
+            self.attn(self.static)
+        torch.cuda.synchronize()
+
+    def run(self, row):
+        """One whole step on a device row (staged into the graph's buffers)."""
+        if self.graph:
+            self.row.copy_(row, non_blocking=True)
+            self.g_step.replay()
+        else:
+            self.eager(self.packer.views(row))
+
+    def run_staged(self, host_row):
+        """One whole step whose inputs come from pinned host memory."""
+        self.row.copy_(host_row, non_blocking=True)
+        if self.graph:
+            self.g_step.replay()
+        else:
+            self.eager(self.static)
+
+    def run_attn_timed(self, row, ev, stream):
+        """The step's attention call alone between two recorded events (for
+        the graph, the step's inputs are staged before the first event)."""
+        if self.graph:
+            self.row.copy_(row, non_blocking=True)
+            ev[0].record(stream)
+            self.g_attn.replay()
+        else:
+            self.append_check(self.packer.views(row))
+            ev[0].record(stream)
+            self.attn(self.packer.views(row))
+        ev[1].record(stream)
+
+
+def time_steps(torch, step, d_rows, warmup, steps):
+    """Warm-up steps, then `steps` whole steps timed as one region (ms per
+    step), then each step's attention call timed alone (ms per call)."""
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        step.eager(step.packer.views(d_rows[i]))
+    if step.graph:
+        step.capture(d_rows[max(warmup - 1, 0)])
+        step.run(d_rows[max(warmup - 1, 0)])
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0.record(stream)
+    for j in range(steps):
+        if step.graph:
+            step.run(d_rows[warmup + j])
+        else:
+            step.run_attn_timed(d_rows[warmup + j], ev[j], stream)
+    t1.record(stream)
+    if step.graph:
+        for j in range(steps):
+            step.run_attn_timed(d_rows[warmup + j], ev[j], stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps, [a.elapsed_time(b) for a, b in ev]
+
+
+# ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
 
@@ -229,43 +382,37 @@ def run_gpu(args, dist, rank, world, local):
     torch.cuda.synchronize()
     del sources
 
-    # --- per-step inputs (device resident for the kernel-time loop)
+    # --- per-step inputs, packed one row per step (device resident for the
+    # kernel-time loop, pinned host memory for the end-to-end loop)
     gen = [(args.offset + i) % inputs.SWEEP_DECODE_STEPS for i in range(steps_total)]
-    host_q, host_k, host_v, host_pos, host_len = [], [], [], [], []
+    packer = StepInputs(torch, B, Hq, Hkv, D)
+    host_len = []
+    rows = []
     for gi in gen:
         q, k_new, v_new, _, pos = w.step_inputs(gi)
-        host_q.append(bf16(q))
-        host_k.append(bf16(k_new))
-        host_v.append(bf16(v_new))
-        host_pos.append(torch.from_numpy(pos))
-        host_len.append(torch.from_numpy(w.seq_lens_after(gi)))
-    d_q = [t.cuda() for t in host_q]
-    d_k = [t.cuda() for t in host_k]
-    d_v = [t.cuda() for t in host_v]
-    d_pos = [t.cuda() for t in host_pos]
-    d_len = [t.cuda() for t in host_len]
-    req_idx = torch.arange(B, dtype=torch.int32, device="cuda")
+        host_len.append(w.seq_lens_after(gi))
+        rows.append({"q": q, "k": k_new, "v": v_new, "pos": pos, "lens": host_len[-1]})
+    h_rows = packer.pack(rows)
+    d_rows = h_rows.cuda()
+    del rows
     tags = torch.from_numpy(w.page_tags.view(np.int32)).cuda()
     exp_tags = torch.from_numpy(w.expected_tags.view(np.int32)).cuda()
     mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
     out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
     ws = kvq.workspace(B, Hq, Hkv, D)
     check = args.check == "on"
+    graph = not args.eager
     stream = torch.cuda.current_stream()
-
-    def step(i, q, kn, vn, pos, lens, ev=None):
-        kvq.kvq_append(cache, kn, vn, req_idx, pos, bt, err_word=err)
-        if check:
-            kvq.kvq_check_tags(bt, lens, P, tags, exp_tags, mask)
-        if ev is not None:
-            ev[0].record(stream)
-        kvq.kvq_decode_attn(cache, q, bt, lens, out, ws, abort_mask=mask if check else None,
-                            sm_scale=float(w.sm_scale), err_word=err)
-        if ev is not None:
-            ev[1].record(stream)
+    step = DecodeStep(torch, kvq, cache, bt, P, float(w.sm_scale), packer, out, ws, err=err,
+                      check=check, tags=tags, exp_tags=exp_tags, mask=mask if check else None,
+                      graph=graph)
 
     for i in range(args.warmup):
-        step(i, d_q[i], d_k[i], d_v[i], d_pos[i], d_len[i])
+        step.eager(packer.views(d_rows[i]))
+    if graph:
+        last = d_rows[max(args.warmup - 1, 0)]
+        step.capture(last)
+        step.run(last)  # first replay (graph upload) outside the timed region
     torch.cuda.synchronize()
 
     attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -278,11 +425,21 @@ def run_gpu(args, dist, rank, world, local):
     torch.cuda.nvtx.range_push("timed")
     t_start.record(stream)
     for j in range(args.steps):
-        i = args.warmup + j
-        step(i, d_q[i], d_k[i], d_v[i], d_pos[i], d_len[i], ev=attn_ev[j])
+        if graph:
+            step.run(d_rows[args.warmup + j])
+        else:  # the eager loop times each attention call inside the step
+            step.run_attn_timed(d_rows[args.warmup + j], attn_ev[j], stream)
     t_end.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
+    if graph:
+        # the attention graph alone over the same steps' inputs (every token
+        # it reads was appended by the timed steps), events around each replay
+        torch.cuda.nvtx.range_push("attn")
+        for j in range(args.steps):
+            step.run_attn_timed(d_rows[args.warmup + j], attn_ev[j], stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
     clk = clocks.stop()
     dist_barrier(dist)
     elapsed_ms = t_start.elapsed_time(t_end)
@@ -293,7 +450,7 @@ def run_gpu(args, dist, rank, world, local):
     if check and int(mask.sum().item()) != 0:
         raise RuntimeError("integrity check aborted requests on a clean workload")
 
-    bytes_per_call = [attn_bytes(host_len[args.warmup + j].numpy(), Hq, Hkv, D, P, kv_bytes)
+    bytes_per_call = [attn_bytes(host_len[args.warmup + j], Hq, Hkv, D, P, kv_bytes)
                       for j in range(args.steps)]
     achieved = sum(bytes_per_call) / (sum(attn_ms) * 1e-3) / 1e9
     peak, peak_kind = measured_hbm_peak()
@@ -302,17 +459,10 @@ def run_gpu(args, dist, rank, world, local):
     # result (out + abort mask) read back, inside the timed region
     e2e = None
     if not args.no_e2e:
-        pin = lambda t: t.pin_memory()  # noqa: E731
-        hq = [pin(t) for t in host_q]
-        hk = [pin(t) for t in host_k]
-        hv = [pin(t) for t in host_v]
-        hp = [pin(t) for t in host_pos]
-        hl = [pin(t) for t in host_len]
-        sq, sk, sv = torch.empty_like(d_q[0]), torch.empty_like(d_k[0]), torch.empty_like(d_v[0])
-        sp, sl = torch.empty_like(d_pos[0]), torch.empty_like(d_len[0])
+        h_pinned = h_rows.pin_memory()
         h_out = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
         h_mask = torch.empty(B, dtype=torch.uint8).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (hq[0], hk[0], hv[0], hp[0], hl[0]))
+        h2d = packer.nbytes
         d2h = h_out.numel() * 4 + h_mask.numel()
         torch.cuda.synchronize()
         dist_barrier(dist)
@@ -320,13 +470,7 @@ def run_gpu(args, dist, rank, world, local):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for j in range(args.steps):
-            i = args.warmup + j
-            sq.copy_(hq[i], non_blocking=True)
-            sk.copy_(hk[i], non_blocking=True)
-            sv.copy_(hv[i], non_blocking=True)
-            sp.copy_(hp[i], non_blocking=True)
-            sl.copy_(hl[i], non_blocking=True)
-            step(i, sq, sk, sv, sp, sl)
+            step.run_staged(h_pinned[args.warmup + j])
             h_out.copy_(out, non_blocking=True)
             h_mask.copy_(mask, non_blocking=True)
         e1.record(stream)
@@ -336,8 +480,7 @@ def run_gpu(args, dist, rank, world, local):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     value = world * B * args.steps / (elapsed_ms * 1e-3)
-    ctx_mean = float(np.mean([host_len[args.warmup + j].numpy().mean()
-                              for j in range(args.steps)]))
+    ctx_mean = float(np.mean([host_len[args.warmup + j].mean() for j in range(args.steps)]))
     result = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -360,10 +503,14 @@ def run_gpu(args, dist, rank, world, local):
             "pool_pages": w.num_pages, "page_size": P, "check": args.check,
             "l2": "inputs larger than L2 (~1.1 GB of KV read per step); no flush",
             "step": "kvq_append + kvq_check_tags + kvq_decode_attn",
+            "launch": "CUDA graph per step (inputs staged with one device copy; the five "
+                      "kernels chained as programmatic dependents)" if graph
+                      else "eager library calls",
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "kvq_decode_attn (plan + split + combine), CUDA events around each call",
+            "kernel": "kvq_decode_attn (plan + split + combine), CUDA events around each call"
+                      + (" (its own graph, replayed per step)" if graph else ""),
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -514,33 +661,18 @@ def run_sweep(args):
                                torch.from_numpy(pos).cuda(), bt)
             n = args.warmup + args.steps
             gen = [(args.offset + i) % inputs.SWEEP_DECODE_STEPS for i in range(n)]
-            st = [w.step_inputs(gi) for gi in gen]
-            d_q = [bf16(x[0]).cuda() for x in st]
-            d_k = [bf16(x[1]).cuda() for x in st]
-            d_v = [bf16(x[2]).cuda() for x in st]
-            d_pos = [torch.from_numpy(x[4]).cuda() for x in st]
+            packer = StepInputs(torch, B, w.Hq, w.Hkv, w.D)
             lens = [w.seq_lens_after(gi) for gi in gen]
-            d_len = [torch.from_numpy(x).cuda() for x in lens]
-            req_idx = torch.arange(B, dtype=torch.int32, device="cuda")
+            rows = []
+            for gi, ln in zip(gen, lens):
+                q, k_new, v_new, _, pos = w.step_inputs(gi)
+                rows.append({"q": q, "k": k_new, "v": v_new, "pos": pos, "lens": ln})
+            d_rows = packer.pack(rows).cuda()
             out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device="cuda")
             ws = kvq.workspace(B, w.Hq, w.Hkv, w.D)
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(n)]
-            t0 = torch.cuda.Event(enable_timing=True)
-            t1 = torch.cuda.Event(enable_timing=True)
-            stream = torch.cuda.current_stream()
-            for i in range(n):
-                if i == args.warmup:
-                    t0.record(stream)
-                kvq.kvq_append(cache, d_k[i], d_v[i], req_idx, d_pos[i], bt)
-                evs[i][0].record(stream)
-                kvq.kvq_decode_attn(cache, d_q[i], bt, d_len[i], out, ws,
-                                    sm_scale=float(w.sm_scale))
-                evs[i][1].record(stream)
-            t1.record(stream)
-            torch.cuda.synchronize()
-            step_ms = t0.elapsed_time(t1) / args.steps
-            attn_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.warmup, n)]
+            step = DecodeStep(torch, kvq, cache, bt, w.P, float(w.sm_scale), packer, out, ws,
+                              graph=not args.eager)
+            step_ms, attn_ms = time_steps(torch, step, d_rows, args.warmup, args.steps)
             byts = [attn_bytes(lens[i], w.Hq, w.Hkv, w.D, w.P, kv_bytes)
                     for i in range(args.warmup, n)]
             gbs = sum(byts) / (sum(attn_ms) * 1e-3) / 1e9
@@ -560,8 +692,9 @@ def run_workload(args):
     integrity (256 requests, stale tags, check -> mask -> attention) or 8x8192
     workloads.  The cache holds random finite e4m3 codes written on the GPU
     (timing only; the parity tests cover these workloads with real data).  For
-    the integrity workload it also times the same steps without the check and
-    reports the check's share of the step."""
+    the integrity workload it also times the same steps without the check
+    (attention still skipping the requests the check aborted) and reports the
+    check's share of the step."""
     import torch
     from fp8_paged_kv_attn_gb300 import inputs, kvq
 
@@ -579,40 +712,26 @@ def run_workload(args):
     tags = torch.from_numpy(w.page_tags.view(np.int32)).cuda()
     exp_tags = torch.from_numpy(w.expected_tags.view(np.int32)).cuda()
     lens_np = w.seq_lens_after(0)
-    lens = torch.from_numpy(lens_np).cuda()
     q, k_new, v_new, req, pos = w.step_inputs(0)
-
-    def bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
-
-    d_q, d_k, d_v = bf16(q), bf16(k_new), bf16(v_new)
-    d_req, d_pos = torch.from_numpy(req).cuda(), torch.from_numpy(pos).cuda()
+    assert np.array_equal(req, np.arange(B, dtype=np.int32))
+    packer = StepInputs(torch, B, Hq, Hkv, D)
+    rows = packer.pack([{"q": q, "k": k_new, "v": v_new, "pos": pos, "lens": lens_np}]).cuda()
+    rows = rows.expand(args.warmup + args.steps, -1)  # the same step inputs every step
     mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
     out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
     ws = kvq.workspace(B, Hq, Hkv, D)
-    stream = torch.cuda.current_stream()
 
-    def run(check, n):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(n)]
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for i in range(n):
-            kvq.kvq_append(cache, d_k, d_v, d_req, d_pos, bt)
-            if check:
-                kvq.kvq_check_tags(bt, lens, P, tags, exp_tags, mask)
-            ev[i][0].record(stream)
-            kvq.kvq_decode_attn(cache, d_q, bt, lens, out, ws, abort_mask=mask if check else None,
-                                sm_scale=float(w.sm_scale))
-            ev[i][1].record(stream)
-        t1.record(stream)
-        torch.cuda.synchronize()
-        return t0.elapsed_time(t1) / n, statistics.mean(a.elapsed_time(b) for a, b in ev)
+    def run(check):
+        step = DecodeStep(torch, kvq, cache, bt, P, float(w.sm_scale), packer, out, ws,
+                          check=check, tags=tags, exp_tags=exp_tags, mask=mask,
+                          graph=not args.eager)
+        step_ms, attn_ms = time_steps(torch, step, rows, args.warmup, args.steps)
+        return step_ms, statistics.mean(attn_ms)
 
-    run(True, args.warmup)
-    run(False, args.warmup)
-    step_on, attn_on = run(True, args.steps)
-    step_off, attn_off = run(False, args.steps)
+    # with the check, then without it but with the mask it produced, so that
+    # both attend the same requests and the difference is the check alone
+    step_on, attn_on = run(True)
+    step_off, attn_off = run(False)
     aborted = int(mask.sum().item())
     alive = (mask.cpu().numpy() == 0)
     byts = attn_bytes(lens_np[alive], Hq, Hkv, D, P, 1)

@@ -10,6 +10,8 @@
 // 8 bf16 values) of one (token, kv head) row, so loads of the bf16 source
 // (32 B) and stores to the page (16 B) are vectorised and coalesced.  The
 // grid strides, so one launch handles a single decode token or a whole prompt.
+// It is launched as a programmatic dependent of the work before it on the
+// stream (launch_dependent), so it waits for that work before any access.
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -32,6 +34,8 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   const int64_t per_tensor = a.n_tokens * per_token;
   const int64_t total = 2 * per_tensor;
   const int64_t cap = static_cast<int64_t>(a.MP) * a.P;
+  grid_dependency_wait();  // earlier work on the stream is complete and visible
+  allow_dependents();
 
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -134,9 +138,7 @@ extern "C" kvq_status kvq_append(const kvq_cache *cache, const void *k_new, cons
   const int64_t want = (total + threads - 1) / threads;
   const int blocks = static_cast<int>(want < 16LL * sms ? want : 16LL * sms);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (fp8)
-    append_kernel<true><<<blocks, threads, 0, s>>>(a);
-  else
-    append_kernel<false><<<blocks, threads, 0, s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  const cudaError_t e = fp8 ? launch_dependent(append_kernel<true>, blocks, threads, 0, s, a)
+                            : launch_dependent(append_kernel<false>, blocks, threads, 0, s, a);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -11,7 +11,9 @@
 // One CTA per request (grid-strided): its threads stride over the request's
 // logical pages, compare the recorded tag with the page's current tag, and a
 // block-wide OR gives the request's abort flag.  Integer work only: the
-// result is exact by construction.
+// result is exact by construction.  Launched as a programmatic dependent of
+// the work before it on the stream, so in a decode step its launch overlaps
+// the append kernel.
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -25,6 +27,8 @@ struct CheckArgs {
 
 __global__ void __launch_bounds__(256) check_tags_kernel(CheckArgs a) {
   const int64_t cap = static_cast<int64_t>(a.MP) * a.P;
+  grid_dependency_wait();  // earlier work on the stream is complete and visible
+  allow_dependents();
   for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
     const int L = a.seq_lens[b];
     int bad = (L < 0 || L > cap) ? 1 : 0;
@@ -66,6 +70,7 @@ extern "C" kvq_status kvq_check_tags(const int32_t *block_table, int32_t B, int3
   int sms = 0;
   if (device_sm_count(&sms) != KVQ_OK) return KVQ_ERR_CUDA;
   const int blocks = B < 32 * sms ? B : 32 * sms;
-  check_tags_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  const cudaError_t e = launch_dependent(check_tags_kernel, blocks, 256, 0,
+                                         reinterpret_cast<cudaStream_t>(stream), a);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -7,6 +7,11 @@
 // token than the BF16 kernel it is compared with in the section's table).
 // The pages give no kernel design; this one is written for GB300:
 //
+//   Every kernel of the call is launched as a programmatic dependent of the
+//   one before it (the first of them of whatever precedes the call on the
+//   stream, e.g. the tag check), so launch latency overlaps the previous
+//   kernel's tail; each waits for its predecessor before touching memory.
+//
 //   plan   1 CTA: per-request unit counts (64-token units), their prefix sum,
 //          where each persistent CTA starts, and zeroed per-row counters;
 //          rows of aborted / empty / invalid requests are written as zeros.
@@ -63,8 +68,8 @@ inline WsLayout ws_layout(int B, int Hq, int Hkv, int D) {
   off = round256(off + rows * sizeof(int32_t));
   w.bad = off;
   off = round256(off + rows * sizeof(int32_t));
-  w.comb = off;  // rows the combine kernel merges
-  off = round256(off + rows * sizeof(int32_t));
+  w.comb = off;  // rows the combine kernel merges: {row, first CTA, parts, request}
+  off = round256(off + rows * sizeof(int4));
   // partial slots: row + CTA for every row split across CTAs; a tensor-core
   // row holds up to 8 kv heads, a CUDA-core row one
   w.part = off;
@@ -84,7 +89,8 @@ struct PlanArgs {
   const uint8_t *abort_mask;
   int32_t *hdr, *prefix;
   int4 *start;
-  int32_t *done, *bad, *comb;
+  int32_t *done, *bad;
+  int4 *comb;
   float *out;
   uint32_t *err_word;
   int32_t B, Hq, D, MP, P, nctas;
@@ -93,7 +99,8 @@ struct PlanArgs {
 };
 
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
-  allow_dependents();  // the split grid may start its set-up now
+  grid_dependency_wait();  // e.g. the tag check's abort mask is visible from here on
+  allow_dependents();      // the split grid may start its set-up now
   __shared__ int s_scan[32];
   __shared__ int s_carry;
   __shared__ int s_prefix[kPlanSmemPrefix];
@@ -183,7 +190,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     for (int r = 0; r < a.rows_per_req; ++r) {
       const long long ur = static_cast<long long>(p0) + static_cast<long long>(r) * units_b;
       const int nparts = static_cast<int>((ur + units_b - 1) / U - ur / U) + 1;
-      if (nparts > kFusedMergeMax) a.comb[atomicAdd(&s_ncomb, 1)] = b * a.rows_per_req + r;
+      if (nparts > kFusedMergeMax)
+        a.comb[atomicAdd(&s_ncomb, 1)] =
+            make_int4(b * a.rows_per_req + r, static_cast<int>(ur / U), nparts, b);
     }
   }
   __syncthreads();
@@ -422,7 +431,8 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
 // ---------------------------------------------------------------------------
 
 struct CombineArgs {
-  const int32_t *hdr, *prefix, *bad, *comb;
+  const int32_t *hdr, *bad;
+  const int4 *comb;
   const float *part;
   float *out;
   int32_t B, Hq, Hkv, G, D, hg, rows_per_req;
@@ -430,82 +440,118 @@ struct CombineArgs {
 };
 
 constexpr int kCombineSubsets = 16;  // part subsets per combine CTA (32 lanes each)
+constexpr int kCombineThreads = 32 * kCombineSubsets;
 
-// Work item = one output row (query head) of one listed kv-head row, 512
-// threads: thread t merges dims 4*(t%32)..+3 over the parts p = t/32,
-// t/32 + 16, ... with a running maximum; the 16 subsets are then merged
-// through shared memory.  Launched as a programmatic dependent of the split
-// kernel; with no listed rows it exits after reading the count.
-__global__ void __launch_bounds__(32 * kCombineSubsets) combine_kernel(CombineArgs a) {
-  __shared__ float s_m[kCombineSubsets], s_l[kCombineSubsets];
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float *s_red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, u) : v + u;
+  }
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  v = s_red[0];
+#pragma unroll
+  for (int w = 1; w < kCombineSubsets; ++w) v = is_max ? fmaxf(v, s_red[w]) : v + s_red[w];
+  __syncthreads();  // s_red may be reused
+  return v;
+}
+
+// Work item = one output row (query head) of one listed kv-head row; 512
+// threads.  The merge is written for latency (a row of a short batch can
+// have hundreds of parts): (1) every part's running max m_p and sum l_p are
+// loaded at once, one part per thread, and reduced to the row maximum M and
+// the denominator sum_p 2^(m_p - M) l_p; (2) thread t accumulates dims
+// 4*(t%32)..+3 of sum_p 2^(m_p - M) acc_p over the parts p = t/32, t/32 + 16,
+// ... with weights read from shared memory, so its loads are independent of
+// one another; (3) the 16 subsets are summed through shared memory.  A part
+// whose maximum is -inf carries no weight and its values are not used.
+// Launched as a programmatic dependent of the split kernel; with no listed
+// rows it exits after reading the count.
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
+  __shared__ float s_w[kMaxCtas], s_l[kMaxCtas];
+  __shared__ float s_red[kCombineSubsets];
   __shared__ float4 s_acc[kCombineSubsets][32];
   grid_dependency_wait();
-  const int ncomb = a.hdr[2];
-  if (ncomb == 0) return;
-  const int U = a.hdr[1];
+  allow_dependents();  // e.g. the next step's append may be scheduled
   const int tid = threadIdx.x, sub = tid >> 5, lane = tid & 31;
   const int heads_per_row = a.hg * a.G;
+  const int nrows = a.B * a.rows_per_req;
+  // the first item's descriptor is loaded together with the count (the
+  // descriptor array has a slot for every row, so the load is in bounds
+  // even when the slot is not in use)
+  int item = blockIdx.x;
+  int4 cd = item / heads_per_row < nrows ? __ldcg(a.comb + item / heads_per_row)
+                                         : make_int4(0, 0, 0, 0);
+  const int ncomb = __ldcg(a.hdr + 2);
+  if (ncomb == 0) return;
   const int64_t kpart = part_stride(a.G, a.D);  // 16-byte multiple
   const int64_t slot_floats = a.hg * kpart;
   const int GD = a.G * a.D;
   const bool active = 4 * lane < a.D;
-  for (int item = blockIdx.x; item < ncomb * heads_per_row; item += gridDim.x) {
-    const int row = a.comb[item / heads_per_row];
+  for (; item < ncomb * heads_per_row; item += gridDim.x) {
+    if (item != static_cast<int>(blockIdx.x)) cd = __ldcg(a.comb + item / heads_per_row);
+    const int row = cd.x, c_lo = cd.y, nparts = cd.z, b = cd.w;  // nparts <= kMaxCtas
     const int hr = item % heads_per_row;  // query head within the row
-    const int b = row / a.rows_per_req, rin = row % a.rows_per_req;
+    const int rin = row % a.rows_per_req;
     const int kvh_in = hr / a.G, hq = hr % a.G;
-    const int p0 = a.prefix[b], p1 = a.prefix[b + 1];
-    const int units_b = (p1 - p0) / a.rows_per_req;
-    const long long ur = static_cast<long long>(p0) + static_cast<long long>(rin) * units_b;
-    const int c_lo = static_cast<int>(ur / U);
-    const int nparts = static_cast<int>((ur + units_b - 1) / U) - c_lo + 1;
     float *out = a.out + (static_cast<int64_t>(b) * a.Hq + (rin * a.hg + kvh_in) * a.G + hq) * a.D;
-    if (a.bad[row]) {
+    const float *base = a.part + static_cast<int64_t>(row + c_lo) * slot_floats + kvh_in * kpart;
+    const int row_bad = __ldcg(a.bad + row);  // uniform over the CTA
+
+    // (1) maxima and sums of all parts
+    float m_loc = -INFINITY;
+    for (int p = tid; p < nparts; p += blockDim.x) {
+      const float *pp = base + p * slot_floats;
+      const float mp = __ldcg(pp + GD + hq);
+      s_w[p] = mp;
+      s_l[p] = __ldcg(pp + GD + a.G + hq);
+      m_loc = fmaxf(m_loc, mp);
+    }
+    const float M = block_reduce(m_loc, true, s_red);
+    if (row_bad) {  // a page of the row was out of range: the output is zero
       for (int d = tid; d < a.D; d += blockDim.x) out[d] = 0.f;
       continue;
     }
-    const float *base = a.part + static_cast<int64_t>(row + c_lo) * slot_floats + kvh_in * kpart;
-    float m = -INFINITY, l = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-    for (int p = sub; p < nparts; p += kCombineSubsets) {
-      const float *pp = base + p * slot_floats;
-      const float mp = __ldcg(pp + GD + hq);
-      const float lp = __ldcg(pp + GD + a.G + hq);
-      const float4 v = active ? __ldcg(reinterpret_cast<const float4 *>(pp + hq * a.D) + lane)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-      if (mp == -INFINITY) continue;
-      const float mn = fmaxf(m, mp);
-      const float fo = m == -INFINITY ? 0.f : exp2f(m - mn);
-      const float fp = exp2f(mp - mn);
-      acc.x = acc.x * fo + v.x * fp;
-      acc.y = acc.y * fo + v.y * fp;
-      acc.z = acc.z * fo + v.z * fp;
-      acc.w = acc.w * fo + v.w * fp;
-      l = l * fo + lp * fp;
-      m = mn;
+    float l_loc = 0.f;
+    for (int p = tid; p < nparts; p += blockDim.x) {
+      const float mp = s_w[p];
+      const float w = mp == -INFINITY ? 0.f : exp2f(mp - M);
+      s_w[p] = w;
+      l_loc += w != 0.f ? w * s_l[p] : 0.f;
     }
-    if (lane == 0) {
-      s_m[sub] = m;
-      s_l[sub] = l;
+    const float den = block_reduce(l_loc, false, s_red);  // also orders the s_w writes
+
+    // (2) weighted sum of the parts' accumulators
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (active) {
+      const float4 *vbase = reinterpret_cast<const float4 *>(base + hq * a.D) + lane;
+      const int64_t vstride = slot_floats / 4;
+#pragma unroll 8
+      for (int p = sub; p < nparts; p += kCombineSubsets) {
+        const float w = s_w[p];
+        float4 v = __ldcg(vbase + p * vstride);
+        if (w == 0.f) v = make_float4(0.f, 0.f, 0.f, 0.f);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
     }
     s_acc[sub][lane] = acc;
     __syncthreads();
+
+    // (3) the subsets
     if (sub == 0 && active) {
-      float mstar = -INFINITY;
+      float4 o = s_acc[0][lane];
 #pragma unroll
-      for (int i = 0; i < kCombineSubsets; ++i) mstar = fmaxf(mstar, s_m[i]);
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      float den = 0.f;
-#pragma unroll
-      for (int i = 0; i < kCombineSubsets; ++i) {
-        const float f = s_m[i] == -INFINITY ? 0.f : exp2f(s_m[i] - mstar);
+      for (int i = 1; i < kCombineSubsets; ++i) {
         const float4 v = s_acc[i][lane];
-        o.x = fmaf(f, v.x, o.x);
-        o.y = fmaf(f, v.y, o.y);
-        o.z = fmaf(f, v.z, o.z);
-        o.w = fmaf(f, v.w, o.w);
-        den = fmaf(f, s_l[i], den);
+        o.x += v.x;
+        o.y += v.y;
+        o.z += v.z;
+        o.w += v.w;
       }
       const float sc = a.v_scale / den;
       reinterpret_cast<float4 *>(out)[lane] = make_float4(o.x * sc, o.y * sc, o.z * sc, o.w * sc);
@@ -705,14 +751,14 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   int4 *start = reinterpret_cast<int4 *>(w + ws.start);
   int32_t *done = reinterpret_cast<int32_t *>(w + ws.done);
   int32_t *bad = reinterpret_cast<int32_t *>(w + ws.bad);
-  int32_t *comb = reinterpret_cast<int32_t *>(w + ws.comb);
+  int4 *comb = reinterpret_cast<int4 *>(w + ws.comb);
   float *part = reinterpret_cast<float *>(w + ws.part);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool fp8 = cache->kv_dtype == KVQ_KV_E4M3;
 
   PlanArgs pa{seq_lens, abort_mask, hdr, prefix, start, done, bad, comb, out, err_word,
               B, Hq, D, MP, cache->page_size, nctas, Hkv / sk.hg, sk.unit};
-  plan_kernel<<<1, 1024, 0, s>>>(pa);
+  if (launch_dependent(plan_kernel, 1, 1024, 0, s, pa) != cudaSuccess) return KVQ_ERR_CUDA;
 
   SplitArgs sa;
   sa.k_pool = static_cast<const uint8_t *>(cache->k_pool);
@@ -740,38 +786,26 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   // the split grid is a programmatic dependent of the plan: its CTAs start
   // (shared-memory and barrier set-up) while the plan finishes, and wait for
   // the plan's results with griddepcontrol.wait
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nctas);
-  cfg.blockDim = dim3(sk.threads);
-  cfg.dynamicSmemBytes = sk.smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   cudaError_t e;
   if (sk.tma) {
     CUtensorMap kmap, vmap;
     if (!encode_pool_map(&kmap, cache->k_pool, *cache, sk.hg) ||
         !encode_pool_map(&vmap, cache->v_pool, *cache, sk.hg))
       return KVQ_ERR_CUDA;
-    e = cudaLaunchKernelEx(&cfg, sk.tma, kmap, vmap, sa);
+    e = launch_dependent(sk.tma, nctas, sk.threads, sk.smem, s, kmap, vmap, sa);
   } else {
-    e = cudaLaunchKernelEx(&cfg, sk.fn, sa);
+    e = launch_dependent(sk.fn, nctas, sk.threads, sk.smem, s, sa);
   }
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
 
   // rows split over many CTAs are merged across the GPU by combine_kernel;
   // it is a programmatic dependent of the split grid and exits at once for
   // rows the split kernel already finished
-  CombineArgs ca{hdr, prefix, bad, comb, part, out, B, Hq, Hkv, G, D, sk.hg, Hkv / sk.hg,
+  CombineArgs ca{hdr, bad, comb, part, out, B, Hq, Hkv, G, D, sk.hg, Hkv / sk.hg,
                  fp8 ? cache->v_scale : 1.0f};
-  cudaLaunchConfig_t ccfg = cfg;
   const int crows = B * Hq;
-  ccfg.gridDim = dim3(crows < 2 * sms ? crows : 2 * sms);
-  ccfg.blockDim = dim3(32 * kCombineSubsets);
-  ccfg.dynamicSmemBytes = 0;
-  if (cudaLaunchKernelEx(&ccfg, combine_kernel, ca) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_dependent(combine_kernel, crows < 2 * sms ? crows : 2 * sms, kCombineThreads, 0, s,
+                       ca) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -64,14 +64,6 @@ struct Ctrl {
   int last;
 };
 
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ void allow_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // 2^x on the SFU (relative error ~2^-22; exactly 1 at x = 0)
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -22,6 +22,20 @@ __device__ __forceinline__ void report(uint32_t *err_word, uint32_t bit) {
 // shared-memory addresses and mbarriers
 // ---------------------------------------------------------------------------
 
+// Programmatic dependent launch.  A kernel launched as a dependent (see
+// launch_dependent) may become resident before the work ahead of it on the
+// stream has finished; grid_dependency_wait() returns once that work has
+// completed and its memory is visible, so it precedes every global-memory
+// access of such a kernel.  allow_dependents() lets the next dependent
+// launch be scheduled; it orders nothing by itself.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -3,6 +3,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "kvq.h"
@@ -15,6 +16,28 @@ inline bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) &
 
 // Number of SMs of the current device (cached per device).
 kvq_status device_sm_count(int *sms);
+
+// Launches `kernel` as a programmatic dependent of the work ahead of it on
+// `stream`: its CTAs may be scheduled as soon as the previous kernel has let
+// dependents go (or has finished), which hides the launch latency between
+// the kernels of a decode step.  The kernel must call grid_dependency_wait()
+// before it touches global memory, which keeps plain stream order for the
+// data.  Captured into a CUDA graph, the launch becomes a programmatic edge.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Checks of the cache descriptor common to every entry point.
 inline kvq_status validate_cache(const kvq_cache *c) {

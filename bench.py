@@ -61,7 +61,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seed", type=int, default=2)
-    ap.add_argument("--workload", choices=["ragged", "integrity", "8x8192"], default=None,
+    ap.add_argument("--workload", choices=["ragged", "integrity", "8x8192", "prefill"],
+                    default=None,
                     help="time one of the other decode workloads (pools filled with random "
                          "finite e4m3 codes on the GPU; one JSON line, not the headline)")
     ap.add_argument("--sweep", action="store_true",
@@ -747,8 +748,68 @@ def run_workload(args):
     print(json.dumps(res), flush=True)
 
 
+def run_prefill(args):
+    """The prefill -> decode handoff: the `--batch` (default 64) requests'
+    whole 8192-token BF16 prompts (at 64: 524,288 tokens, 1.07 GB each of K
+    and V) quantised into e4m3 pages by ONE kvq_append call, timed with CUDA
+    events per call; then the same into a BF16 pool of as many pages (a
+    paged copy), for comparison."""
+    import torch
+    from fp8_paged_kv_attn_gb300 import inputs, kvq
+
+    kvq.load()
+    peak, _ = measured_hbm_peak()
+    w = inputs.sweep(args.batch, kv_bytes=1, seed=args.seed)
+    sources = w.kv_sources(threads=os.cpu_count() or 8)
+    ks, vs = w.scales(sources)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    k_all = bf16(np.concatenate([k for k, _ in sources]))
+    v_all = bf16(np.concatenate([v for _, v in sources]))
+    toks = [w.context_tokens(b) for b in range(w.B)]
+    req = torch.from_numpy(np.concatenate([t[0] for t in toks])).cuda()
+    pos = torch.from_numpy(np.concatenate([t[1] for t in toks])).cuda()
+    del sources, toks
+    N = int(req.shape[0])
+    bt = torch.from_numpy(w.block_table).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for kv, es, pdt in (("e4m3", 1, torch.uint8), ("bf16", 2, torch.bfloat16)):
+        shape = w.pool_shape()
+        cache = kvq.KVCache(torch.zeros(shape, dtype=pdt, device="cuda"),
+                            torch.zeros(shape, dtype=pdt, device="cuda"), float(ks), float(vs))
+        for _ in range(args.warmup):
+            kvq.kvq_append(cache, k_all, v_all, req, pos, bt, err_word=err)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for e in ev:
+            e[0].record(stream)
+            kvq.kvq_append(cache, k_all, v_all, req, pos, bt, err_word=err)
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item()):#x}")
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        # K and V read as bf16, written as codes; req_idx and pos read
+        byts = N * w.Hkv * w.D * 2 * (2 + es) + N * 8
+        print(json.dumps({"workload": f"prefill_handoff_{w.B}x8192", "kv": kv, "tokens": N,
+                          "Hkv": w.Hkv, "D": w.D, "page_size": w.P, "steps": args.steps,
+                          "us_per_call": round(ms * 1e3, 2),
+                          "tokens_per_s": round(N / (ms * 1e-3), 1),
+                          "GBs": round(byts / (ms * 1e-3) / 1e9, 1),
+                          "frac_of_measured_peak": round(byts / (ms * 1e-3) / 1e9 / peak, 4),
+                          "bytes_per_call": byts}), flush=True)
+        del cache
+
+
 def main():
     args = parse_args()
+    if args.workload == "prefill":
+        run_prefill(args)
+        return
     if args.workload:
         run_workload(args)
         return

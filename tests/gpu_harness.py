@@ -87,6 +87,31 @@ class Run:
                 assert e == 0
         torch.cuda.synchronize()
 
+    def fill_context_one_call(self):
+        """The prompt handoff: every request's whole prompt quantised into the
+        pages by ONE kvq_append call (N = sum of the prompt lengths)."""
+        ks, vs, reqs, poss = [], [], [], []
+        for b, (k, v) in enumerate(self.sources):
+            if k.shape[0] == 0:
+                continue
+            req, pos = self.w.context_tokens(b)
+            ks.append(k)
+            vs.append(v)
+            reqs.append(req)
+            poss.append(pos)
+        k, v = np.concatenate(ks), np.concatenate(vs)
+        req, pos = np.concatenate(reqs), np.concatenate(poss)
+        kvq.kvq_append(self.cache, dev_bf16(k), dev_bf16(v), dev(req), dev(pos), self.bt,
+                       err_word=self.err)
+        sel = np.isin(req, np.array(self.host_requests, dtype=np.int32))
+        e = oracle.quant_append(self.oracle_dtype, self.hk, self.hv, self.k_scale, self.v_scale,
+                                np.ascontiguousarray(k[sel]), np.ascontiguousarray(v[sel]),
+                                np.ascontiguousarray(req[sel]), np.ascontiguousarray(pos[sel]),
+                                self.w.block_table)
+        assert e == 0
+        torch.cuda.synchronize()
+        return int(req.shape[0])
+
     def append_step(self, step: int):
         q, k_new, v_new, req, pos = self.w.step_inputs(step)
         kvq.kvq_append(self.cache, dev_bf16(k_new), dev_bf16(v_new), dev(req), dev(pos), self.bt,

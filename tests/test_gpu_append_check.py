@@ -10,6 +10,18 @@ from gpu_harness import Run, dev, dev_bf16, dev_u32, SENTINEL
 pytestmark = pytest.mark.gpu
 
 SCALES = [1.0, 3.0, 0.1, 1.0 / 3.0, 0.0123, 37.5, 1e-3, 2.0 ** -20]
+# the kernel's reciprocal fast path is exact only while 1/scale is a normal
+# float: scales at and past both ends of that range, and seeded random
+# scales over 2^-40 .. 2^40
+EDGE_SCALES = [2.0 ** -126, 1e-38, 1e-45, 2.0 ** 126, 3.0e38, 3.4028235e38]
+RANDOM_SCALES = [float(np.float32(2.0 ** e))
+                 for e in np.random.default_rng(11).uniform(-40, 40, 12)]
+
+
+def _v_scale(s32):
+    """Twice the K scale (exact), or the K scale where twice would overflow."""
+    v = 2.0 * float(s32)
+    return v if v <= float(np.finfo(np.float32).max) else float(s32)
 
 
 def _exhaustive_tokens():
@@ -18,7 +30,7 @@ def _exhaustive_tokens():
     return bits
 
 
-@pytest.mark.parametrize("scale", SCALES)
+@pytest.mark.parametrize("scale", SCALES + EDGE_SCALES + RANDOM_SCALES)
 def test_append_every_bf16_value(kvq, scale):
     """Every bf16 input (including inf and NaN) at several scales: the same
     e4m3 byte as the oracle; NaN inputs give a NaN code."""
@@ -31,13 +43,14 @@ def test_append_every_bf16_value(kvq, scale):
     s32 = np.float32(scale)
     cache = kvq.KVCache(torch.full((MP, H, P, D), SENTINEL, dtype=torch.uint8, device="cuda"),
                         torch.full((MP, H, P, D), SENTINEL, dtype=torch.uint8, device="cuda"),
-                        float(s32), float(s32 * 2))
+                        float(s32), _v_scale(s32))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     kvq.kvq_append(cache, dev_bf16(bits), dev_bf16(bits[::-1].copy()), dev(req), dev(pos), dev(bt),
                    err_word=err)
     hk = np.full((MP, H, P, D), SENTINEL, dtype=np.uint8)
     hv = hk.copy()
-    assert oracle.quant_append(oracle.KV_E4M3, hk, hv, s32, s32 * 2, bits, bits[::-1].copy(),
+    assert oracle.quant_append(oracle.KV_E4M3, hk, hv, np.float32(cache.k_scale),
+                               np.float32(cache.v_scale), bits, bits[::-1].copy(),
                                req, pos, bt) == 0
     gk = cache.k_pool.cpu().numpy()
     gv = cache.v_pool.cpu().numpy()
@@ -72,6 +85,30 @@ def test_append_context_and_step(kvq, mk):
     r.append_step(0)
     torch.cuda.synchronize()
     r.assert_pools_equal(w.seq_lens_after(0), whole=True)
+    assert r.err_word() == 0
+
+
+@pytest.mark.parametrize("kv_dtype", ["e4m3", "bf16"])
+def test_prompt_handoff_one_call_8x8192(kvq, kv_dtype):
+    """The prefill -> decode handoff at the 8-request x 8192-token size: all
+    65,536 prompt tokens quantised by one call, every byte of both pools equal
+    to the oracle's (pages no request uses keep their sentinel)."""
+    w = inputs.cfg8x8k()
+    r = Run(w, kv_dtype=kvq.KV_E4M3 if kv_dtype == "e4m3" else kvq.KV_BF16)
+    assert r.fill_context_one_call() == int(w.ctx_lens.sum())
+    r.assert_pools_equal(w.ctx_lens, whole=True)
+    assert r.err_word() == 0
+
+
+def test_prompt_handoff_one_call_64x8192(kvq):
+    """The handoff at the 64-request sweep size (524,288 tokens, 1.07 GB of bf16
+    K and of V, in one call): every page of 6 sampled requests equals the
+    oracle's byte for byte."""
+    w = inputs.sweep(64, kv_bytes=1)
+    sel = [0, 13, 27, 40, 52, 63]
+    r = Run(w, host_requests=sel, sources=w.kv_sources(threads=16))
+    assert r.fill_context_one_call() == 64 * 8192
+    r.assert_pools_equal(w.ctx_lens)
     assert r.err_word() == 0
 
 

@@ -1,7 +1,7 @@
 """CPU oracle for the FP8 paged-KV decode path -- TEST INFRASTRUCTURE ONLY.
 
 Thin ctypes wrappers over ``kvq_oracle.c`` (plain C, fp64 attention, scalar
-e4m3 codec, linear-scan tag check).  Only the tests, the smoke check and the
+e4m3 codec, linear-scan tag check, sequential page allocator).  Only the tests, the smoke check and the
 benchmark's CPU-baseline / reference arm may import this package; the
 product library never does.  It shares no code with the CUDA path.
 
@@ -28,6 +28,7 @@ ERR_PAGE = 1 << 0
 ERR_SEQLEN = 1 << 1
 ERR_POS = 1 << 2
 ERR_REQ = 1 << 3
+ERR_EXHAUSTED = 1 << 5
 
 _lib = None
 
@@ -70,6 +71,9 @@ def _load(path):
     L.oracle_quant_append.restype = u32
     L.oracle_check_tags.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp, vp]
     L.oracle_check_tags.restype = None
+    L.oracle_pages_update.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, vp, vp, i32,
+                                      vp, vp, vp, i32, vp]
+    L.oracle_pages_update.restype = u32
     L.oracle_decode_attn.argtypes = [i32, vp, vp, i32, i32, i32, i32, f32, f32,
                                      vp, i32, i32, vp, i32, vp, vp, f32, vp,
                                      vp, i32, i32, vp, i64]
@@ -148,6 +152,51 @@ def check_tags(block_table, seq_lens, page_size, page_tags, expected_tags) -> np
                             _ptr(page_tags), page_tags.shape[0], _ptr(expected_tags),
                             _ptr(out))
     return out
+
+
+class PageState:
+    """The page allocator's state (host arrays, updated in place by
+    pages_update): free_stack [num_pages] int32 with free_count live entries
+    (top = last), page_tags [num_pages] uint32, block_table [B, MP] int32 and
+    expected_tags [B, MP] uint32."""
+
+    def __init__(self, free_stack, free_count, page_tags, block_table, expected_tags):
+        self.free_stack = np.ascontiguousarray(free_stack, dtype=np.int32)
+        self.free_count = np.array([free_count], dtype=np.int32)
+        self.page_tags = np.ascontiguousarray(page_tags, dtype=np.uint32)
+        self.block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+        self.expected_tags = np.ascontiguousarray(expected_tags, dtype=np.uint32)
+
+    @staticmethod
+    def fresh(num_pages, B, MP, order=None):
+        stack = np.arange(num_pages, dtype=np.int32) if order is None else order
+        return PageState(stack, num_pages, np.zeros(num_pages, np.uint32),
+                         np.full((B, MP), -1, np.int32), np.zeros((B, MP), np.uint32))
+
+    def copy(self):
+        return PageState(self.free_stack.copy(), int(self.free_count[0]), self.page_tags.copy(),
+                         self.block_table.copy(), self.expected_tags.copy())
+
+
+def pages_update(state: PageState, rel_req=(), rel_npages=(), acq_req=(), acq_first=(),
+                 acq_npages=()):
+    """One batch of releases then acquisitions on `state` (in place).
+    Returns (acq_ok uint8 [n_acq], error bits)."""
+    rel_req = _c(np.asarray(rel_req, dtype=np.int32), np.int32)
+    rel_npages = _c(np.asarray(rel_npages, dtype=np.int32), np.int32)
+    acq_req = _c(np.asarray(acq_req, dtype=np.int32), np.int32)
+    acq_first = _c(np.asarray(acq_first, dtype=np.int32), np.int32)
+    acq_npages = _c(np.asarray(acq_npages, dtype=np.int32), np.int32)
+    assert rel_req.shape == rel_npages.shape
+    assert acq_req.shape == acq_first.shape == acq_npages.shape
+    ok = np.zeros(acq_req.shape[0], dtype=np.uint8)
+    B, MP = state.block_table.shape
+    err = lib().oracle_pages_update(
+        _ptr(state.free_stack), _ptr(state.free_count), _ptr(state.page_tags),
+        state.page_tags.shape[0], _ptr(state.block_table), _ptr(state.expected_tags), B, MP,
+        _ptr(rel_req), _ptr(rel_npages), rel_req.shape[0], _ptr(acq_req), _ptr(acq_first),
+        _ptr(acq_npages), acq_req.shape[0], _ptr(ok))
+    return ok, int(err)
 
 
 def decode_attn(kv_dtype, k_pool, v_pool, k_scale, v_scale, q, block_table, seq_lens,

@@ -30,7 +30,11 @@
  *   - query head h reads kv head h / (Hq/Hkv); logits scaled by sm_scale; no
  *     soft-cap, window or bias;
  *   - only logical pages i < ceil(L/P) of a request are read or checked;
- *   - an aborted, empty or invalid request gives an all-zero output row.
+ *   - an aborted, empty or invalid request gives an all-zero output row;
+ *   - the page allocator (the step before the check): a page's tag is
+ *     incremented when the page is handed to a new owner, free pages form a
+ *     last-in-first-out stack, a batch releases before it acquires, and
+ *     acquisitions are served in order until the first that does not fit.
  *
  * Every floating-point result of the attention is computed in fp64 and only
  * the final output is rounded to fp32.  Build with -ffp-contract=off and
@@ -48,7 +52,8 @@
 #define ORACLE_ERR_PAGE   (1u << 0) /* a block-table entry the call needs is outside [0, num_pages) */
 #define ORACLE_ERR_SEQLEN (1u << 1) /* seq_lens[b] < 0 or > MP * page_size */
 #define ORACLE_ERR_POS    (1u << 2) /* append position outside [0, MP * page_size) */
-#define ORACLE_ERR_REQ    (1u << 3) /* append request index outside [0, B) */
+#define ORACLE_ERR_REQ    (1u << 3) /* request index outside [0, B) */
+#define ORACLE_ERR_EXHAUSTED (1u << 5) /* an acquisition found too few free pages */
 
 #define ORACLE_KV_E4M3 0
 #define ORACLE_KV_BF16 1
@@ -210,6 +215,95 @@ void oracle_check_tags(const int32_t *block_table, int B, int MP, const int32_t 
         }
         abort_mask[b] = (uint8_t)bad;
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Page allocator and tag tracker                                            */
+/* ------------------------------------------------------------------------ */
+
+/* [GUARD] The allocator side of the tag check: a page's tag changes every
+ * time the page is handed to a new owner, and the server records, for each
+ * request, the (page, tag) pairs it was given.
+ *
+ * State: a stack of free page ids free_stack[0 .. *free_count) (the top is
+ * the last one), page_tags[num_pages], and for each request slot b its
+ * block-table row and expected-tag row (MP entries each).
+ *
+ * One call is a batch of releases followed by a batch of acquisitions.
+ *  Release: for j = 0, 1, ... in order, request rel_req[j] returns its
+ *    logical pages k = 0 .. rel_npages[j]-1 in order; each page id is pushed
+ *    on the stack and the block-table entry becomes -1 (tags are unchanged).
+ *    All or nothing: if any request index is outside [0, B), any count is
+ *    outside [0, MP], any returned entry is not a page id, or the pushes would
+ *    overfill the stack, nothing is released and error bits are returned.
+ *  Acquire: for i = 0, 1, ... in order, request acq_req[i] asks for logical
+ *    pages acq_first[i] .. acq_first[i] + acq_npages[i] - 1.  A request with
+ *    an invalid index (ERR_REQ) or range (ERR_POS) gets nothing.  Valid
+ *    requests are served in order: each pops its pages off the top of the
+ *    stack in logical order, increments the popped page's tag (mod 2^32) and
+ *    records the page and its new tag in its block-table and expected-tag
+ *    rows.  The first valid request that finds too few free pages, and every
+ *    valid request after it, get nothing (ERR_EXHAUSTED).  acq_ok[i] says
+ *    whether request i was served.  A popped entry that is not a page id is
+ *    consumed without being mapped (ERR_PAGE).
+ * A free count outside [0, num_pages] changes nothing (ERR_PAGE).
+ * Returns the OR of the error bits. */
+uint32_t oracle_pages_update(int32_t *free_stack, int32_t *free_count, uint32_t *page_tags,
+                             int num_pages, int32_t *block_table, uint32_t *expected_tags,
+                             int B, int MP, const int32_t *rel_req, const int32_t *rel_npages,
+                             int n_rel, const int32_t *acq_req, const int32_t *acq_first,
+                             const int32_t *acq_npages, int n_acq, uint8_t *acq_ok)
+{
+    uint32_t err = 0;
+    int count = *free_count;
+    for (int i = 0; i < n_acq; ++i) acq_ok[i] = 0;
+    if (count < 0 || count > num_pages) return ORACLE_ERR_PAGE;
+
+    /* release: validate the whole batch, then push */
+    uint32_t rel_err = 0;
+    int64_t pushes = 0;
+    for (int j = 0; j < n_rel; ++j) {
+        int b = rel_req[j], n = rel_npages[j];
+        if (b < 0 || b >= B) { rel_err |= ORACLE_ERR_REQ; continue; }
+        if (n < 0 || n > MP) { rel_err |= ORACLE_ERR_POS; continue; }
+        for (int k = 0; k < n; ++k) {
+            int page = block_table[(int64_t)b * MP + k];
+            if (page < 0 || page >= num_pages) rel_err |= ORACLE_ERR_PAGE;
+        }
+        pushes += n;
+    }
+    if (rel_err == 0 && count + pushes > num_pages) rel_err |= ORACLE_ERR_PAGE;
+    if (rel_err) {
+        err |= rel_err;
+    } else {
+        for (int j = 0; j < n_rel; ++j) {
+            int b = rel_req[j], n = rel_npages[j];
+            for (int k = 0; k < n; ++k) {
+                int32_t *entry = &block_table[(int64_t)b * MP + k];
+                free_stack[count++] = *entry;
+                *entry = -1;
+            }
+        }
+    }
+
+    /* acquire: in order, until the first valid request that does not fit */
+    int stopped = 0;
+    for (int i = 0; i < n_acq; ++i) {
+        int b = acq_req[i], first = acq_first[i], n = acq_npages[i];
+        if (b < 0 || b >= B) { err |= ORACLE_ERR_REQ; continue; }
+        if (first < 0 || n < 0 || (int64_t)first + n > MP) { err |= ORACLE_ERR_POS; continue; }
+        if (stopped || n > count) { stopped = 1; err |= ORACLE_ERR_EXHAUSTED; continue; }
+        for (int k = 0; k < n; ++k) {
+            int page = free_stack[--count];
+            if (page < 0 || page >= num_pages) { err |= ORACLE_ERR_PAGE; continue; }
+            page_tags[page] += 1u;
+            block_table[(int64_t)b * MP + first + k] = page;
+            expected_tags[(int64_t)b * MP + first + k] = page_tags[page];
+        }
+        acq_ok[i] = 1;
+    }
+    *free_count = count;
+    return err;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -445,3 +445,231 @@ def pin_attn_abort_and_errors(oracle):
     part, _ = _attend(oracle, w, oracle.KV_E4M3, kp, vp, ks, vs, q, lens, rows=rows)
     for b, h in rows:
         assert np.array_equal(part[b, h], full[b, h])
+
+
+# ----------------------------------------------------------------------------
+# page allocator
+# ----------------------------------------------------------------------------
+
+GOLDEN_PAGES = __import__("os").path.join(__import__("os").path.dirname(__file__), "golden",
+                                          "page_allocator_example.json")
+
+
+def _golden_pages():
+    import json
+    with open(GOLDEN_PAGES) as f:
+        return json.load(f)
+
+
+def _state_from(oracle, g, B, MP):
+    n = len(g["tags"])
+    stack = np.full(n, -7, dtype=np.int32)  # entries above the count are never read
+    stack[:len(g["stack"])] = g["stack"]
+    return oracle.PageState(stack, g["count"], np.array(g["tags"], dtype=np.uint32),
+                            np.full((B, MP), -1, np.int32), np.zeros((B, MP), np.uint32))
+
+
+def _assert_expect(st, ok, err, e, what):
+    assert err == e["err"], (what, "err", err, e["err"])
+    assert list(ok) == e["ok"], (what, "ok", list(ok), e["ok"])
+    c = int(st.free_count[0])
+    assert c == e["count"], (what, "count", c, e["count"])
+    if "stack" in e:
+        assert list(st.free_stack[:c]) == e["stack"], (what, "stack", list(st.free_stack[:c]))
+    assert list(st.page_tags) == e["tags"], (what, "tags", list(st.page_tags), e["tags"])
+    for b, row in e["bt"].items():
+        assert list(st.block_table[int(b)]) == row, (what, "bt", b, list(st.block_table[int(b)]))
+    for b, row in e["exp"].items():
+        assert list(st.expected_tags[int(b)]) == row, (what, "exp", b,
+                                                       list(st.expected_tags[int(b)]))
+
+
+def _run_golden_op(oracle, st, op):
+    rel = op.get("release", [])
+    acq = op.get("acquire", [])
+    return oracle.pages_update(st, [r[0] for r in rel], [r[1] for r in rel],
+                               [a[0] for a in acq], [a[1] for a in acq], [a[2] for a in acq])
+
+
+def pin_pages_golden(oracle):
+    """The hand-worked allocator example (tests/golden/page_allocator_example.json):
+    every op's error bits, served flags, stack, tags, block-table and
+    expected-tag rows; the tag check after op 2 (live requests pass, a stale
+    copy of a released request fails); uint32 tag wrap-around."""
+    g = _golden_pages()
+    B, MP, P = g["B"], g["MP"], g["page_size"]
+    st = _state_from(oracle, g["initial"], B, MP)
+    snapshot = None
+    for n, op in enumerate(g["ops"]):
+        if n == 1:
+            snapshot = st.copy()
+        ok, err = _run_golden_op(oracle, st, op)
+        _assert_expect(st, ok, err, op["expect"], f"op {n + 1}")
+        if "check" in op:
+            live = op["check"]["live"]
+            rq = live["requests"]
+            ab = oracle.check_tags(st.block_table[rq], np.array(live["seq_lens"], np.int32), P,
+                                   st.page_tags, st.expected_tags[rq])
+            assert list(ab) == live["abort"], ("live check", list(ab))
+            stale = op["check"]["stale"]
+            assert list(snapshot.block_table[0]) == stale["bt"]
+            assert list(snapshot.expected_tags[0]) == stale["exp"]
+            ab = oracle.check_tags(np.array([stale["bt"]], np.int32),
+                                   np.array([stale["seq_len"]], np.int32), P, st.page_tags,
+                                   np.array([stale["exp"]], np.uint32))
+            assert list(ab) == [stale["abort"]], ("stale check", list(ab))
+    w = g["wrap"]
+    st = _state_from(oracle, w["initial"], w["B"], w["MP"])
+    ok, err = _run_golden_op(oracle, st, w)
+    _assert_expect(st, ok, err, w["expect"], "wrap")
+
+
+def mapped_prefix(block_table):
+    """Per request slot, how many leading block-table entries are mapped."""
+    unm = block_table < 0
+    return np.where(unm.any(axis=1), unm.argmax(axis=1), block_table.shape[1])
+
+
+def next_page_ops(rng, block_table, fail_often=False, bad_release=False):
+    """One seeded (release, acquire) batch for the current mapping, keeping
+    the allocator's preconditions (a request returns exactly its mapped
+    prefix, acquires only unmapped entries, appears at most once per list):
+    some live requests finish, some grow by a page or two, some free slots
+    admit a new request.  `fail_often` asks for three times as many pages;
+    `bad_release` makes one release reach past its mapped prefix (which the
+    allocator must refuse as a batch)."""
+    B, MP = block_table.shape
+    held = mapped_prefix(block_table)
+    rel_req, rel_n = [], []
+    for b in np.nonzero(held > 0)[0]:
+        if rng.random() < 0.15:
+            rel_req.append(int(b))
+            rel_n.append(int(held[b]))
+    if bad_release and rel_req and held[rel_req[0]] < MP:
+        rel_n[0] += 1
+    acq = []
+    for b in rng.permutation(B):
+        b = int(b)
+        if b in rel_req:
+            continue
+        if held[b] > 0 and held[b] < MP and rng.random() < 0.4:
+            n = int(rng.integers(1, 3))
+        elif held[b] == 0 and rng.random() < 0.3:
+            n = int(rng.integers(1, max(2, MP // 2)))
+        else:
+            continue
+        if fail_often:
+            n *= 3
+        acq.append((b, int(held[b]), int(min(MP - held[b], n))))
+    return (rel_req, rel_n, [a[0] for a in acq], [a[1] for a in acq], [a[2] for a in acq])
+
+
+def pin_pages_invariants(oracle, seed=3, num_pages=64, B=12, MP=10, n_ops=60):
+    """Properties every op must keep, whatever the implementation:
+    conservation (the free stack and the live block-table entries hold every
+    page exactly once), LIFO order (the pages an op hands out are the top of
+    the stack after its releases, in pop order), one tag increment per page
+    handed out and none otherwise, served requests = the valid requests in
+    order up to the first that does not fit, expected tag = current tag on
+    every live entry (so the check passes every live request and fails a
+    stale copy of a request whose pages were handed out again)."""
+    for fail_often in (False, True):
+        rng = np.random.default_rng(seed)
+        order = rng.permutation(num_pages).astype(np.int32)
+        st = oracle.PageState.fresh(num_pages, B, MP, order=order)
+        stale = []
+        for step in range(n_ops):
+            rel_req, rel_n, acq_req, acq_first, acq_n = next_page_ops(
+                rng, st.block_table, fail_often, bad_release=fail_often and step % 7 == 3)
+            before = st.copy()
+            # releases of entries that were never mapped are refused as a batch
+            rel_ok = all(np.all(before.block_table[b, :n] >= 0) for b, n in zip(rel_req, rel_n))
+            if rel_ok:
+                for b in rel_req:
+                    stale.append((before.block_table[b].copy(), before.expected_tags[b].copy()))
+            ok, err = oracle.pages_update(st, rel_req, rel_n, acq_req, acq_first, acq_n)
+            # after the releases (if accepted): the stack as the acquisitions see it
+            stack = list(before.free_stack[:before.free_count[0]])
+            if rel_ok:
+                for b, n in zip(rel_req, rel_n):
+                    stack.extend(int(p) for p in before.block_table[b, :n])
+            else:
+                assert err & oracle.ERR_PAGE
+            # served = valid requests in order until the first that does not fit
+            avail = len(stack)
+            expect_ok, stopped, handed = [], False, []
+            for b, f, n in zip(acq_req, acq_first, acq_n):
+                if stopped or n > avail:
+                    stopped = True
+                    expect_ok.append(0)
+                    continue
+                expect_ok.append(1)
+                for k in range(n):
+                    handed.append((b, f + k, stack[len(stack) - 1 - (len(handed))]))
+                avail -= n
+            assert list(ok) == expect_ok, (list(ok), expect_ok)
+            assert bool(err & oracle.ERR_EXHAUSTED) == stopped
+            assert int(st.free_count[0]) == len(stack) - len(handed)
+            assert list(st.free_stack[:st.free_count[0]]) == stack[:len(stack) - len(handed)]
+            # tags: +1 for each page handed out, unchanged otherwise
+            bump = np.zeros(num_pages, dtype=np.uint32)
+            for _, _, p in handed:
+                bump[p] += 1
+            assert np.array_equal(st.page_tags, before.page_tags + bump)
+            for b, k, p in handed:
+                assert st.block_table[b, k] == p
+                assert st.expected_tags[b, k] == st.page_tags[p]
+            if rel_ok:
+                for b, n in zip(rel_req, rel_n):
+                    assert np.all(st.block_table[b, :n] < 0)
+            else:
+                for b in rel_req:
+                    assert np.array_equal(st.block_table[b], before.block_table[b])
+            # conservation
+            live = st.block_table[st.block_table >= 0]
+            allp = np.sort(np.concatenate([st.free_stack[:st.free_count[0]], live]))
+            assert np.array_equal(allp, np.arange(num_pages)), "a page was lost or duplicated"
+            # expected tag = current tag on every live entry: the check passes
+            # every request over its mapped prefix
+            for b in range(B):
+                row = st.block_table[b]
+                n = int(np.argmax(row < 0)) if np.any(row < 0) else MP
+                if n == 0:
+                    continue
+                ab = oracle.check_tags(row[None, :], np.array([n * 4], np.int32), 4,
+                                       st.page_tags, st.expected_tags[b][None, :])
+                assert ab[0] == 0
+        # a stale copy of a released request fails the check once one of its
+        # pages has been handed out again
+        flagged = 0
+        for bt_row, exp_row in stale:
+            n = int(np.argmax(bt_row < 0)) if np.any(bt_row < 0) else MP
+            if n == 0:
+                continue
+            reused = any(st.page_tags[p] != exp_row[i] for i, p in enumerate(bt_row[:n]))
+            ab = oracle.check_tags(bt_row[None, :], np.array([n * 4], np.int32), 4,
+                                   st.page_tags, exp_row[None, :])
+            assert ab[0] == int(reused)
+            flagged += int(reused)
+        assert flagged > 0
+
+
+def pin_pages_overflow_and_state(oracle):
+    """A release that would push more pages than the pool holds is refused as
+    a whole (page error); so is a call on a free count outside [0, pages]."""
+    st = oracle.PageState.fresh(4, 2, 4)
+    st.block_table[0, :2] = [1, 2]  # a mapping to pages that are also free
+    before = st.copy()
+    ok, err = oracle.pages_update(st, [0], [2], [1], [0], [1])
+    assert err & oracle.ERR_PAGE
+    # the release is refused but the acquisition still runs on the full stack
+    assert list(ok) == [1] and st.block_table[0, 0] == 1
+    assert int(st.free_count[0]) == 3 and st.block_table[1, 0] == before.free_stack[3]
+    bad = oracle.PageState.fresh(4, 2, 4)
+    bad.free_count[0] = 5
+    snap = bad.copy()
+    ok, err = oracle.pages_update(bad, [], [], [0], [0], [1])
+    assert err == oracle.ERR_PAGE and list(ok) == [0]
+    assert np.array_equal(bad.free_stack, snap.free_stack)
+    assert np.array_equal(bad.page_tags, snap.page_tags)
+    assert int(bad.free_count[0]) == 5

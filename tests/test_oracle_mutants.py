@@ -49,6 +49,19 @@ MUTANTS = {
     "attn_no_normalise": ("o[d] = (float)(acc[d] / denom);", "o[d] = (float)(acc[d]);"),
     "attn_slot": ("int64_t base = (((int64_t)page * H + kvh) * P + j % P) * D;\n        double s",
                   "int64_t base = (((int64_t)page * H + kvh) * P + (j + 1) % P) * D;\n        double s"),
+    "pages_bump_on_release": ("free_stack[count++] = *entry;\n                *entry = -1;",
+                              "free_stack[count++] = *entry;\n                page_tags[*entry] += 1u;\n                *entry = -1;"),
+    "pages_no_bump": ("page_tags[page] += 1u;", "page_tags[page] += 0u;"),
+    "pages_pop_order": ("int page = free_stack[--count];",
+                        "int page = free_stack[count - n + k];\n            if (k == n - 1) count -= n;"),
+    "pages_keep_entry": ("                *entry = -1;\n", "\n"),
+    "pages_no_stop": ("if (stopped || n > count) { stopped = 1;", "if (n > count) { stopped = 1;"),
+    "pages_old_tag": ("expected_tags[(int64_t)b * MP + first + k] = page_tags[page];",
+                      "expected_tags[(int64_t)b * MP + first + k] = page_tags[page] - 1u;"),
+    "pages_partial_release": ("    if (rel_err) {\n        err |= rel_err;\n    } else {",
+                              "    err |= rel_err;\n    {"),
+    "pages_first_ignored": ("block_table[(int64_t)b * MP + first + k] = page;",
+                            "block_table[(int64_t)b * MP + k] = page;"),
     "attn_bf16_scaled": ("double ks = (kv_dtype == ORACLE_KV_E4M3) ? (double)k_scale : 1.0;",
                          "double ks = (double)k_scale;"),
 }
@@ -76,6 +89,9 @@ def run_all_pins():
         ("attn_one_token", lambda: pins.pin_attn_one_token(oracle)),
         ("attn_equal_keys", lambda: pins.pin_attn_equal_keys(oracle)),
         ("attn_abort", lambda: pins.pin_attn_abort_and_errors(oracle)),
+        ("pages_golden", lambda: pins.pin_pages_golden(oracle)),
+        ("pages_invariants", lambda: pins.pin_pages_invariants(oracle, n_ops=30)),
+        ("pages_overflow", lambda: pins.pin_pages_overflow_and_state(oracle)),
     ]
     failed = []
     for name, fn in checks:

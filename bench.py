@@ -61,7 +61,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seed", type=int, default=2)
-    ap.add_argument("--workload", choices=["ragged", "integrity", "8x8192", "prefill"],
+    ap.add_argument("--workload", choices=["ragged", "integrity", "8x8192", "prefill", "pages"],
                     default=None,
                     help="time one of the other decode workloads (pools filled with random "
                          "finite e4m3 codes on the GPU; one JSON line, not the headline)")
@@ -805,8 +805,108 @@ def run_prefill(args):
         del cache
 
 
+def run_pages(args):
+    """The page allocator (kvq_pages_update), one line per scenario: the
+    batches of a decode step and of admission.  Each scenario is K calls
+    captured in one CUDA graph; the allocator state is restored from a
+    snapshot before every replay and only the replay is timed (CUDA events),
+    so the per-call figure is device time, not the Python binding's."""
+    import torch
+    from fp8_paged_kv_attn_gb300 import kvq
+
+    kvq.load()
+    rng = np.random.default_rng(args.seed)
+    stream = torch.cuda.current_stream()
+
+    def state(num_pages, B, MP):
+        return kvq.PageState(
+            torch.from_numpy(rng.permutation(num_pages).astype(np.int32)).cuda(),
+            torch.tensor([num_pages], dtype=torch.int32, device="cuda"),
+            torch.zeros(num_pages, dtype=torch.int32, device="cuda"),
+            torch.full((B, MP), -1, dtype=torch.int32, device="cuda"),
+            torch.zeros((B, MP), dtype=torch.int32, device="cuda"))
+
+    def i32(x):
+        return torch.tensor(x, dtype=torch.int32, device="cuda")
+
+    def timed(name, st, calls, pages_per_call, reps=20):
+        """calls: list of kwargs for kvq_pages_update, run in order."""
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        snap = [t.clone() for t in (st.free_stack, st.free_count, st.page_tags, st.block_table,
+                                    st.expected_tags)]
+
+        def restore():
+            for t, s0 in zip((st.free_stack, st.free_count, st.page_tags, st.block_table,
+                              st.expected_tags), snap):
+                t.copy_(s0)
+
+        def run():
+            for kw in calls:
+                kvq.kvq_pages_update(st, err_word=err, **kw)
+
+        run()  # eager warm-up (also checks the calls)
+        torch.cuda.synchronize()
+        bad = int(err.item()) & ~kvq.ERRBIT_EXHAUSTED
+        if bad:
+            raise RuntimeError(f"{name}: device error bits {bad:#x}")
+        restore()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for e in ev:
+            restore()
+            e[0].record(stream)
+            g.replay()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3 / len(calls)
+        print(json.dumps({"workload": f"pages_{name}", "calls_per_graph": len(calls),
+                          "us_per_call": round(us, 3), "pages_per_call": pages_per_call,
+                          "pages_per_s": round(pages_per_call / (us * 1e-6), 1),
+                          "reps": reps}), flush=True)
+
+    # decode-step growth: 16 of 256 live requests cross into a new page
+    st = state(65536, 256, 1024)
+    live = rng.choice(256, 16, replace=False).astype(np.int32)
+    calls = [dict(acq_req=i32(live), acq_first=i32(np.full(16, c, np.int32)),
+                  acq_npages=i32(np.ones(16, np.int32)),
+                  acq_ok=torch.zeros(16, dtype=torch.uint8, device="cuda")) for c in range(50)]
+    timed("grow_16x1", st, calls, 16)
+
+    # turnover: a finished 8k-token request (512 pages) leaves, a new one arrives
+    st = state(65536, 256, 1024)
+    setup_ok = torch.zeros(1, dtype=torch.uint8, device="cuda")
+    kvq.kvq_pages_update(st, acq_req=i32([0]), acq_first=i32([0]), acq_npages=i32([512]),
+                         acq_ok=setup_ok)
+    calls = []
+    for c in range(50):
+        a, b = (0, 1) if c % 2 == 0 else (1, 0)
+        calls.append(dict(rel_req=i32([a]), rel_npages=i32([512]), acq_req=i32([b]),
+                          acq_first=i32([0]), acq_npages=i32([512]),
+                          acq_ok=torch.zeros(1, dtype=torch.uint8, device="cuda")))
+    timed("turnover_512", st, calls, 1024)
+
+    # admission of 64 requests x 575 pages (the sweep pool), then its release
+    st = state(36800, 64, 575)
+    timed("admit_64x575", st, [dict(acq_req=i32(np.arange(64)), acq_first=i32(np.zeros(64)),
+                                    acq_npages=i32(np.full(64, 575)),
+                                    acq_ok=torch.zeros(64, dtype=torch.uint8, device="cuda"))],
+          36800)
+    st = state(36800, 64, 575)
+    kvq.kvq_pages_update(st, acq_req=i32(np.arange(64)), acq_first=i32(np.zeros(64)),
+                         acq_npages=i32(np.full(64, 575)),
+                         acq_ok=torch.zeros(64, dtype=torch.uint8, device="cuda"))
+    timed("release_64x575", st, [dict(rel_req=i32(np.arange(64)),
+                                      rel_npages=i32(np.full(64, 575)))], 36800)
+
+
 def main():
     args = parse_args()
+    if args.workload == "pages":
+        run_pages(args)
+        return
     if args.workload == "prefill":
         run_prefill(args)
         return

@@ -34,13 +34,14 @@ ERRBIT_SEQLEN = 1 << 1
 ERRBIT_POS = 1 << 2
 ERRBIT_REQ = 1 << 3
 ERRBIT_TIMEOUT = 1 << 4
+ERRBIT_EXHAUSTED = 1 << 5
 
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_WORKSPACE", 3: "KVQ_ERR_CUDA",
           4: "KVQ_ERR_UNSUPPORTED"}
 
 # every symbol include/kvq.h declares
-EXPORTS = ("kvq_append", "kvq_check_tags", "kvq_decode_attn_workspace_size", "kvq_decode_attn",
-           "kvq_decode_attn_static", "kvq_status_string")
+EXPORTS = ("kvq_append", "kvq_check_tags", "kvq_pages_update", "kvq_decode_attn_workspace_size",
+           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_status_string")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -81,6 +82,9 @@ def load(build_if_missing: bool = True):
     L.kvq_append.restype = ctypes.c_int
     L.kvq_check_tags.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp, vp, vp]
     L.kvq_check_tags.restype = ctypes.c_int
+    L.kvq_pages_update.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, vp, vp, i32, vp, vp, vp,
+                                   i32, vp, vp, vp]
+    L.kvq_pages_update.restype = ctypes.c_int
     L.kvq_decode_attn_workspace_size.argtypes = [i32, i32, i32, i32]
     L.kvq_decode_attn_workspace_size.restype = sz
     L.kvq_decode_attn.argtypes = [cp, vp, i32, i32, vp, i32, vp, vp, f32, vp, vp, sz, vp, vp]
@@ -195,6 +199,51 @@ def kvq_check_tags(block_table, seq_lens, page_size: int, page_tags, expected_ta
                           _dev(expected_tags, "expected_tags", U32, 2),
                           _dev(abort_mask, "abort_mask", U8, 1), _stream(stream))
     _check("kvq_check_tags", st)
+
+
+@dataclass
+class PageState:
+    """The page allocator's device state (include/kvq.h, kvq_pages_update):
+    free_stack int32 [num_pages] with free_count[0] live entries (top = last),
+    page_tags int32/uint32 [num_pages], block_table int32 [B, MP] and
+    expected_tags int32/uint32 [B, MP] (the tables kvq_check_tags reads)."""
+    free_stack: torch.Tensor
+    free_count: torch.Tensor
+    page_tags: torch.Tensor
+    block_table: torch.Tensor
+    expected_tags: torch.Tensor
+
+
+def kvq_pages_update(state: PageState, rel_req=None, rel_npages=None, acq_req=None,
+                     acq_first=None, acq_npages=None, acq_ok=None, err_word=None,
+                     stream=None) -> None:
+    """One batch of page releases then acquisitions (see include/kvq.h)."""
+    L = load()
+    num_pages = int(state.free_stack.shape[0])
+    B, MP = state.block_table.shape
+    if tuple(state.page_tags.shape) != (num_pages,) or state.free_count.numel() != 1:
+        raise ValueError("page_tags must be [num_pages] and free_count [1]")
+    if tuple(state.expected_tags.shape) != (B, MP):
+        raise ValueError("expected_tags must match block_table")
+    n_rel = 0 if rel_req is None else int(rel_req.shape[0])
+    n_acq = 0 if acq_req is None else int(acq_req.shape[0])
+    if n_rel and rel_npages.shape != rel_req.shape:
+        raise ValueError("rel_npages must match rel_req")
+    if n_acq and (acq_first.shape != acq_req.shape or acq_npages.shape != acq_req.shape or
+                  acq_ok is None or acq_ok.shape != acq_req.shape):
+        raise ValueError("acq_first, acq_npages and acq_ok must match acq_req")
+    st = L.kvq_pages_update(_dev(state.free_stack, "free_stack", I32, 1),
+                            _dev(state.free_count, "free_count", I32),
+                            _dev(state.page_tags, "page_tags", U32, 1), num_pages,
+                            _dev(state.block_table, "block_table", I32, 2),
+                            _dev(state.expected_tags, "expected_tags", U32, 2), B, MP,
+                            _dev(rel_req, "rel_req", I32, 1), _dev(rel_npages, "rel_npages", I32, 1),
+                            n_rel, _dev(acq_req, "acq_req", I32, 1),
+                            _dev(acq_first, "acq_first", I32, 1),
+                            _dev(acq_npages, "acq_npages", I32, 1), n_acq,
+                            _dev(acq_ok, "acq_ok", U8, 1), _dev(err_word, "err_word", U32),
+                            _stream(stream))
+    _check("kvq_pages_update", st)
 
 
 def kvq_decode_attn_workspace_size(B: int, Hq: int, num_kv_heads: int, head_dim: int) -> int:

@@ -1,7 +1,8 @@
 /*
  * kvq -- FP8 (e4m3) paged KV cache: quantise-and-append, batched page-tag
- * integrity check, and single-query paged decode attention for NVIDIA GB300
- * (sm_103a).  Plain C ABI: pointers, sizes, a CUDA stream.  No allocation.
+ * integrity check, the page allocator that sets the tags, and single-query
+ * paged decode attention for NVIDIA GB300 (sm_103a).  Plain C ABI: pointers,
+ * sizes, a CUDA stream.  The library allocates no memory.
  *
  * Sources (web pages, cited by title and section):
  *   [KVQ]   "大规模服务 Kimi 与 GLM：KV 缓存量化、权重压缩与缓存安全" (a translation
@@ -70,8 +71,9 @@ typedef enum { KVQ_KV_E4M3 = 0, KVQ_KV_BF16 = 1 } kvq_kv_dtype;
 #define KVQ_ERRBIT_PAGE    (1u << 0) /* a block-table entry the call needs is outside [0, num_pages) */
 #define KVQ_ERRBIT_SEQLEN  (1u << 1) /* seq_lens[b] < 0 or > MP * page_size */
 #define KVQ_ERRBIT_POS     (1u << 2) /* append position outside [0, MP * page_size) */
-#define KVQ_ERRBIT_REQ     (1u << 3) /* append request index outside [0, B) */
+#define KVQ_ERRBIT_REQ     (1u << 3) /* request index outside [0, B) (append, pages update) */
 #define KVQ_ERRBIT_TIMEOUT (1u << 4) /* a bounded wait inside a kernel gave up (no result) */
+#define KVQ_ERRBIT_EXHAUSTED (1u << 5) /* kvq_pages_update: an acquisition found too few free pages */
 
 /* The paged cache ([KVQ]): two pools of identical shape, one for K, one for V.
  * Supported: page_size in {16, 32, 64}; head_dim in {64, 128};
@@ -118,6 +120,48 @@ KVQ_API kvq_status kvq_check_tags(const int32_t *block_table, int32_t B, int32_t
                           const uint32_t *page_tags, int32_t num_pages,
                           const uint32_t *expected_tags, uint8_t *abort_mask,
                           kvq_stream_t stream);
+
+/* Batched page release and acquisition with per-page tags: the allocator
+ * side of the check ([GUARD]: a page's tag changes whenever the page is
+ * reallocated, and the server records the (page, tag) pairs each request was
+ * given).  The state is caller-owned device memory:
+ *   free_stack   int32 [num_pages]: free page ids in free_stack[0 .. *free_count)
+ *                (the top is the last one); free_count int32 [1];
+ *   page_tags    uint32 [num_pages];
+ *   block_table  int32 [B][MP] and expected_tags uint32 [B][MP] (the same
+ *                tables kvq_check_tags reads).
+ * One call is a batch of releases, then a batch of acquisitions:
+ *  - Release: for j = 0 .. n_rel-1 in order, request rel_req[j] returns its
+ *    logical pages 0 .. rel_npages[j]-1 in order: each page id is pushed on
+ *    the stack and its block-table entry becomes -1; tags are unchanged.  All
+ *    or nothing: if any request index is outside [0, B) (KVQ_ERRBIT_REQ), any
+ *    count outside [0, MP] (_POS), any returned entry is not a page id
+ *    (_PAGE), or the pushes would overfill the stack (_PAGE), nothing is
+ *    released.
+ *  - Acquire: for i = 0 .. n_acq-1 in order, request acq_req[i] asks for
+ *    logical pages acq_first[i] .. acq_first[i] + acq_npages[i] - 1.  An
+ *    invalid request index (_REQ) or range (_POS) gets nothing.  Valid
+ *    requests are served in order: each pops its pages off the top of the
+ *    stack in logical order; the popped page's tag is incremented (mod 2^32)
+ *    and the request's block-table and expected-tag entries get the page and
+ *    its new tag.  The first valid request that finds too few free pages,
+ *    and every valid request after it, get nothing (KVQ_ERRBIT_EXHAUSTED).
+ *    acq_ok[i] (uint8 [n_acq]) is 1 if request i was served, else 0.  A
+ *    popped entry that is not a page id is consumed unmapped (_PAGE).
+ * A *free_count outside [0, num_pages] changes nothing (_PAGE).
+ * Preconditions (unchecked; the result is unspecified otherwise): a request
+ * appears at most once in each list, releases exactly entries it holds, and
+ * acquires only entries it does not hold.  Freshly set up state: free_stack
+ * any permutation of the page ids, *free_count = num_pages, tags any values.
+ * The lists may be empty (their pointers may then be NULL). */
+KVQ_API kvq_status kvq_pages_update(int32_t *free_stack, int32_t *free_count, uint32_t *page_tags,
+                                    int32_t num_pages, int32_t *block_table,
+                                    uint32_t *expected_tags, int32_t B, int32_t MP,
+                                    const int32_t *rel_req, const int32_t *rel_npages,
+                                    int32_t n_rel, const int32_t *acq_req,
+                                    const int32_t *acq_first, const int32_t *acq_npages,
+                                    int32_t n_acq, uint8_t *acq_ok, uint32_t *err_word,
+                                    kvq_stream_t stream);
 
 /* Bytes of device workspace kvq_decode_attn needs for these sizes (split
  * partials and the per-call work plan).  Depends on B, Hq, num_kv_heads and

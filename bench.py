@@ -321,9 +321,29 @@ class DecodeStep:
         ev[1].record(stream)
 
 
-def time_steps(torch, step, d_rows, warmup, steps):
-    """Warm-up steps, then `steps` whole steps timed as one region (ms per
-    step), then each step's attention call timed alone (ms per call)."""
+class L2Flush:
+    """Writes a buffer twice the size of L2 before a timed step whose inputs
+    would otherwise stay L2-resident from one step to the next."""
+
+    def __init__(self, torch):
+        self.l2 = int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+        self.buf = torch.empty(self.l2 // 2, dtype=torch.int32, device="cuda")  # 2 x L2 bytes
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+    @staticmethod
+    def needed(torch, kv_bytes_per_step):
+        l2 = int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+        return kv_bytes_per_step < 2 * l2
+
+
+def time_steps(torch, step, d_rows, warmup, steps, flush=None):
+    """Warm-up steps, then `steps` whole steps, then each step's attention
+    call timed alone.  Returns (ms per step, [ms per attention call]).
+    Without `flush` the whole steps run back to back in one timed region;
+    with it, L2 is flushed before every timed step and every attention call,
+    and each is timed by its own pair of events."""
     stream = torch.cuda.current_stream()
     for i in range(warmup):
         step.eager(step.packer.views(d_rows[i]))
@@ -331,21 +351,40 @@ def time_steps(torch, step, d_rows, warmup, steps):
         step.capture(d_rows[max(warmup - 1, 0)])
         step.run(d_rows[max(warmup - 1, 0)])
     torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    t0.record(stream)
-    for j in range(steps):
-        if step.graph:
-            step.run(d_rows[warmup + j])
-        else:
-            step.run_attn_timed(d_rows[warmup + j], ev[j], stream)
-    t1.record(stream)
-    if step.graph:
+
+    def pairs():
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(steps)]
+
+    ev, es = pairs(), pairs()
+    if flush is None:
+        es[0][0].record(stream)
         for j in range(steps):
+            if step.graph:
+                step.run(d_rows[warmup + j])
+            else:  # the eager loop times each attention call inside the step
+                step.run_attn_timed(d_rows[warmup + j], ev[j], stream)
+        es[0][1].record(stream)
+    else:
+        for j in range(steps):
+            flush()
+            es[j][0].record(stream)
+            if step.graph:
+                step.run(d_rows[warmup + j])
+            else:
+                step.eager(step.packer.views(d_rows[warmup + j]))
+            es[j][1].record(stream)
+    if step.graph or flush is not None:
+        for j in range(steps):
+            if flush is not None:
+                flush()
             step.run_attn_timed(d_rows[warmup + j], ev[j], stream)
     torch.cuda.synchronize()
-    return t0.elapsed_time(t1) / steps, [a.elapsed_time(b) for a, b in ev]
+    if flush is None:
+        step_ms = es[0][0].elapsed_time(es[0][1]) / steps
+    else:
+        step_ms = statistics.mean(a.elapsed_time(b) for a, b in es)
+    return step_ms, [a.elapsed_time(b) for a, b in ev]
 
 
 # ----------------------------------------------------------------------------
@@ -416,8 +455,15 @@ def run_gpu(args, dist, rank, world, local):
         step.run(last)  # first replay (graph upload) outside the timed region
     torch.cuda.synchronize()
 
-    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+    def pairs():
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+
+    # a step's KV smaller than 2 x L2 would stay cached from step to step:
+    # then L2 is flushed before every timed step and each step is timed alone
+    kv_step = attn_bytes(host_len[args.warmup], Hq, Hkv, D, P, kv_bytes)
+    flush = L2Flush(torch) if L2Flush.needed(torch, kv_step) else None
+    attn_ev, step_ev = pairs(), pairs()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     dist_barrier(dist)
@@ -426,10 +472,15 @@ def run_gpu(args, dist, rank, world, local):
     torch.cuda.nvtx.range_push("timed")
     t_start.record(stream)
     for j in range(args.steps):
+        if flush is not None:
+            flush()
+            step_ev[j][0].record(stream)
         if graph:
             step.run(d_rows[args.warmup + j])
         else:  # the eager loop times each attention call inside the step
             step.run_attn_timed(d_rows[args.warmup + j], attn_ev[j], stream)
+        if flush is not None:
+            step_ev[j][1].record(stream)
     t_end.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
@@ -438,12 +489,17 @@ def run_gpu(args, dist, rank, world, local):
         # it reads was appended by the timed steps), events around each replay
         torch.cuda.nvtx.range_push("attn")
         for j in range(args.steps):
+            if flush is not None:
+                flush()
             step.run_attn_timed(d_rows[args.warmup + j], attn_ev[j], stream)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
     clk = clocks.stop()
     dist_barrier(dist)
-    elapsed_ms = t_start.elapsed_time(t_end)
+    if flush is None:
+        elapsed_ms = t_start.elapsed_time(t_end)
+    else:
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
     elapsed_ms = dist_max(dist, elapsed_ms)
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
     if int(err.item()) != 0:
@@ -469,14 +525,22 @@ def run_gpu(args, dist, rank, world, local):
         dist_barrier(dist)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        e2e_ev = pairs()
         e0.record(stream)
         for j in range(args.steps):
+            if flush is not None:
+                flush()
+                e2e_ev[j][0].record(stream)
             step.run_staged(h_pinned[args.warmup + j])
             h_out.copy_(out, non_blocking=True)
             h_mask.copy_(mask, non_blocking=True)
+            if flush is not None:
+                e2e_ev[j][1].record(stream)
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = dist_max(dist, e0.elapsed_time(e1))
+        e2e_ms = e0.elapsed_time(e1) if flush is None else \
+            sum(a.elapsed_time(b) for a, b in e2e_ev)
+        e2e_ms = dist_max(dist, e2e_ms)
         e2e = {"value": round(world * B * args.steps / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
@@ -502,7 +566,10 @@ def run_gpu(args, dist, rank, world, local):
                         f"head_dim {D}, page {P}, {args.kv} KV, integrity check {args.check}",
             "batch": B, "mean_context": round(ctx_mean, 1), "kv_dtype": args.kv,
             "pool_pages": w.num_pages, "page_size": P, "check": args.check,
-            "l2": "inputs larger than L2 (~1.1 GB of KV read per step); no flush",
+            "l2": (f"inputs larger than L2 ({kv_step / 1e9:.2f} GB of KV read per step); no flush"
+                   if flush is None else
+                   f"L2 ({flush.l2 >> 20} MB) flushed before every timed step and attention "
+                   f"call ({kv_step / 1e6:.0f} MB of KV per step); each timed by its own events"),
             "step": "kvq_append + kvq_check_tags + kvq_decode_attn",
             "launch": "CUDA graph per step (inputs staged with one device copy; the five "
                       "kernels chained as programmatic dependents)" if graph
@@ -521,6 +588,8 @@ def run_gpu(args, dist, rank, world, local):
             "traffic": profiled_traffic(),
             "bytes_per_call": int(statistics.mean(bytes_per_call)),
             "ms_per_call": round(statistics.mean(attn_ms), 5),
+            "ms_per_call_median": round(statistics.median(attn_ms), 5),
+            "ms_per_call_p95": round(float(np.percentile(attn_ms, 95)), 5),
         },
         "gpu_launches": args.steps * (1 + (1 if check else 0) + 3),
         "clocks": clk,
@@ -673,18 +742,25 @@ def run_sweep(args):
             ws = kvq.workspace(B, w.Hq, w.Hkv, w.D)
             step = DecodeStep(torch, kvq, cache, bt, w.P, float(w.sm_scale), packer, out, ws,
                               graph=not args.eager)
-            step_ms, attn_ms = time_steps(torch, step, d_rows, args.warmup, args.steps)
             byts = [attn_bytes(lens[i], w.Hq, w.Hkv, w.D, w.P, kv_bytes)
                     for i in range(args.warmup, n)]
+            flush = L2Flush(torch) if L2Flush.needed(torch, byts[0]) else None
+            step_ms, attn_ms = time_steps(torch, step, d_rows, args.warmup, args.steps, flush)
             gbs = sum(byts) / (sum(attn_ms) * 1e-3) / 1e9
-            print(json.dumps({"sweep": True, "kv": kv, "batch": B,
-                              "tokens_per_s": round(B / (step_ms * 1e-3), 1),
-                              "ms_per_step": round(step_ms, 5),
-                              "attn_us": round(statistics.mean(attn_ms) * 1e3, 2),
-                              "attn_GBs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
-                              "pool_pages": w.num_pages,
-                              "mean_context": round(float(np.mean([x.mean() for x in lens[args.warmup:]])), 1)}),
-                  flush=True)
+            line = {"sweep": True, "kv": kv, "batch": B,
+                    "tokens_per_s": round(B / (step_ms * 1e-3), 1),
+                    "ms_per_step": round(step_ms, 5),
+                    "attn_us": round(statistics.mean(attn_ms) * 1e3, 2),
+                    "attn_us_p95": round(float(np.percentile(attn_ms, 95)) * 1e3, 2),
+                    "attn_GBs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                    "l2": "flushed before each step" if flush else "KV larger than 2 x L2; no flush",
+                    "pool_pages": w.num_pages,
+                    "mean_context": round(float(np.mean([x.mean() for x in lens[args.warmup:]])), 1)}
+            if flush is not None:  # the same steps back to back, L2 warm, for comparison
+                wstep, wattn = time_steps(torch, step, d_rows, args.warmup, args.steps)
+                line["tokens_per_s_warm"] = round(B / (wstep * 1e-3), 1)
+                line["attn_us_warm"] = round(statistics.mean(wattn) * 1e3, 2)
+            print(json.dumps(line), flush=True)
             del cache
 
 
@@ -722,11 +798,14 @@ def run_workload(args):
     out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
     ws = kvq.workspace(B, Hq, Hkv, D)
 
+    flush = L2Flush(torch) if L2Flush.needed(torch, attn_bytes(lens_np, Hq, Hkv, D, P, 1)) \
+        else None
+
     def run(check):
         step = DecodeStep(torch, kvq, cache, bt, P, float(w.sm_scale), packer, out, ws,
                           check=check, tags=tags, exp_tags=exp_tags, mask=mask,
                           graph=not args.eager)
-        step_ms, attn_ms = time_steps(torch, step, rows, args.warmup, args.steps)
+        step_ms, attn_ms = time_steps(torch, step, rows, args.warmup, args.steps, flush)
         return step_ms, statistics.mean(attn_ms)
 
     # with the check, then without it but with the mask it produced, so that
@@ -741,7 +820,8 @@ def run_workload(args):
            "step_ms_with_check": round(step_on, 5), "attn_us_with_check": round(attn_on * 1e3, 2),
            "attn_GBs": round(byts / (attn_on * 1e-3) / 1e9, 1),
            "frac_of_measured_peak": round(byts / (attn_on * 1e-3) / 1e9 / peak, 4),
-           "aborted_requests": aborted}
+           "aborted_requests": aborted,
+           "l2": "flushed before each step" if flush else "KV larger than 2 x L2; no flush"}
     if args.workload == "integrity":
         res["step_ms_without_check"] = round(step_off, 5)
         res["check_overhead_pct_of_step"] = round(100 * (step_on - step_off) / step_off, 2)

@@ -71,6 +71,8 @@ def _load(path):
     L.oracle_quant_append.restype = u32
     L.oracle_check_tags.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp, vp]
     L.oracle_check_tags.restype = None
+    L.oracle_wq_gemm.argtypes = [i32, vp, vp, vp, vp, i32, i32, i32, i32]
+    L.oracle_wq_gemm.restype = None
     L.oracle_pages_update.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, vp, vp, i32,
                                       vp, vp, vp, i32, vp]
     L.oracle_pages_update.restype = u32
@@ -197,6 +199,31 @@ def pages_update(state: PageState, rel_req=(), rel_npages=(), acq_req=(), acq_fi
         _ptr(rel_req), _ptr(rel_npages), rel_req.shape[0], _ptr(acq_req), _ptr(acq_first),
         _ptr(acq_npages), acq_req.shape[0], _ptr(ok))
     return ok, int(err)
+
+
+W_INT4 = 0
+W_E4M3 = 1
+
+
+def wq_gemm(wdtype, w, scales, x, group=128) -> np.ndarray:
+    """y fp32 [M, N] = x [M, K] (bf16 bits) times the quantised weights
+    w [N, K/2] (INT4, two nibbles a byte) or [N, K] (e4m3 codes), with bf16
+    group scales [N, K/group] (INT4) or fp32 channel scales [N] (e4m3)."""
+    w = _c(w, np.uint8)
+    x = _c(x, np.uint16)
+    M, K = x.shape
+    N = w.shape[0]
+    if wdtype == W_INT4:
+        assert w.shape == (N, K // 2) and K % group == 0
+        scales = _c(scales, np.uint16)
+        assert scales.shape == (N, K // group)
+    else:
+        assert w.shape == (N, K)
+        scales = _c(scales, np.float32)
+        assert scales.shape == (N,)
+    y = np.empty((M, N), dtype=np.float32)
+    lib().oracle_wq_gemm(wdtype, _ptr(w), _ptr(scales), _ptr(x), _ptr(y), M, N, K, group)
+    return y
 
 
 def decode_attn(kv_dtype, k_pool, v_pool, k_scale, v_scale, q, block_table, seq_lens,

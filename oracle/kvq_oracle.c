@@ -307,6 +307,57 @@ uint32_t oracle_pages_update(int32_t *free_stack, int32_t *free_count, uint32_t 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Weight-only quantised matrix product (decode GEMV / skinny GEMM)          */
+/* ------------------------------------------------------------------------ */
+
+#define ORACLE_W_INT4 0
+#define ORACLE_W_E4M3 1
+
+/* The signed 4-bit value held in nibble k of a row of packed INT4 weights:
+ * byte k/2, low nibble for even k, high nibble for odd k, two's complement
+ * (0x8 .. 0xF are -8 .. -1). */
+static int int4_value(const uint8_t *row, int64_t k)
+{
+    uint8_t byte = row[k / 2];
+    int nib = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+    return nib >= 8 ? nib - 16 : nib;
+}
+
+/* [KVQ] section "模型权重压缩" (weight compression): the decode pool keeps the
+ * weights as 4-bit integers (from FP8); every generated token reads them all,
+ * so decode is bound by memory bandwidth; INT4 weights are widened to a
+ * higher precision before they take part in the computation.  The format is
+ * not stated; read as weight-only, symmetric, per-group:
+ *   INT4: w[n][k] = int4(n, k) * s[n][k / group]   (s bf16 [N][K/group])
+ *   E4M3: w[n][k] = e4m3(code[n][k]) * s[n]         (s fp32 [N], the FP8 path
+ *         the pages compare against)
+ * and y[m][n] = sum_k x[m][k] * w[n][k] with x bf16 [M][K], summed in fp64
+ * and rounded to fp32 once. */
+void oracle_wq_gemm(int wdtype, const uint8_t *w, const void *scales, const uint16_t *x,
+                    float *y, int M, int N, int K, int group)
+{
+    for (int n = 0; n < N; ++n) {
+        const uint8_t *row = w + (int64_t)n * (wdtype == ORACLE_W_INT4 ? K / 2 : K);
+        for (int m = 0; m < M; ++m) {
+            const uint16_t *xm = x + (int64_t)m * K;
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double wv;
+                if (wdtype == ORACLE_W_INT4) {
+                    const uint16_t *s = (const uint16_t *)scales + (int64_t)n * (K / group);
+                    wv = (double)int4_value(row, k) * (double)bf16_to_float(s[k / group]);
+                } else {
+                    const float *s = (const float *)scales;
+                    wv = oracle_e4m3_decode(row[k]) * (double)s[n];
+                }
+                acc += (double)bf16_to_float(xm[k]) * wv;
+            }
+            y[(int64_t)m * N + n] = (float)acc;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Single-query paged attention                                              */
 /* ------------------------------------------------------------------------ */
 

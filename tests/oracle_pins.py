@@ -673,3 +673,86 @@ def pin_pages_overflow_and_state(oracle):
     assert np.array_equal(bad.free_stack, snap.free_stack)
     assert np.array_equal(bad.page_tags, snap.page_tags)
     assert int(bad.free_count[0]) == 5
+
+
+# ----------------------------------------------------------------------------
+# weight-only quantised matrix product
+# ----------------------------------------------------------------------------
+
+def _bf16_to_f64(bits):
+    return (np.asarray(bits, dtype=np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def numpy_int4_weights(w, scales, group):
+    """Dequantised INT4 weights [N, K] in float64, unpacked with numpy bit
+    operations (independent of the oracle): even k = low nibble, odd k = high
+    nibble, two's complement."""
+    w = np.asarray(w, dtype=np.uint8)
+    lo = (w & 0x0F).astype(np.int64)
+    hi = (w >> 4).astype(np.int64)
+    q = np.empty((w.shape[0], w.shape[1] * 2), dtype=np.int64)
+    q[:, 0::2], q[:, 1::2] = lo, hi
+    q = np.where(q >= 8, q - 16, q)
+    s = np.repeat(_bf16_to_f64(scales), group, axis=1)
+    return q.astype(np.float64) * s
+
+
+def random_wq_case(rng, wdtype, M, N, K, group=128):
+    x = inputs.normal_bf16(rng, (M, K))
+    if wdtype == 0:
+        w = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+        amax = np.abs(rng.standard_normal((N, K // group))).astype(np.float32) * 0.02 + 1e-3
+        s = (amax.view(np.uint32) >> 16).astype(np.uint16)  # bf16 scales
+    else:
+        w = rng.integers(0, 256, (N, K), dtype=np.uint8)
+        w[(w & 0x7F) == 0x7F] ^= 0x01  # no NaN codes in weights
+        s = (np.abs(rng.standard_normal(N)) * 0.01 + 1e-3).astype(np.float32)
+    return w, s, x
+
+
+def pin_int4_nibbles(oracle):
+    """Every byte value: with a one-hot x picking k = 0 or k = 1 and scale 1,
+    y is the low or high nibble read as a signed 4-bit number."""
+    b = np.arange(256, dtype=np.uint8)
+    w = np.zeros((256, 64), dtype=np.uint8)
+    w[:, 0] = b
+    one = np.uint16(0x3F80)
+    s = np.full((256, 1), one, dtype=np.uint16)
+    for k, nib in ((0, b & 0x0F), (1, b >> 4)):
+        x = np.zeros((1, 128), dtype=np.uint16)
+        x[0, k] = one
+        y = oracle.wq_gemm(oracle.W_INT4, w, s, x)[0]
+        want = np.where(nib >= 8, nib.astype(np.int64) - 16, nib.astype(np.int64))
+        assert np.array_equal(y, want.astype(np.float32)), k
+
+
+def pin_wq_vs_numpy(oracle):
+    """Random INT4 and e4m3 weights: the oracle equals a float64 matmul of
+    weights dequantised independently (numpy nibbles; torch's float8_e4m3fn),
+    to within the last fp32 bit (the two sum in different orders)."""
+    rng = np.random.default_rng(31)
+    for M, N, K in ((1, 16, 128), (5, 33, 384), (16, 64, 1024)):
+        w, s, x = random_wq_case(rng, 0, M, N, K)
+        ref = _bf16_to_f64(x) @ numpy_int4_weights(w, s, 128).T
+        got = oracle.wq_gemm(oracle.W_INT4, w, s, x)
+        np.testing.assert_allclose(got, ref, rtol=2e-7, atol=1e-30)
+        w, s, x = random_wq_case(rng, 1, M, N, K)
+        wd = torch.from_numpy(w).view(E4M3).to(torch.float64).numpy() * s.astype(np.float64)[:, None]
+        ref = _bf16_to_f64(x) @ wd.T
+        got = oracle.wq_gemm(oracle.W_E4M3, w, s, x)
+        np.testing.assert_allclose(got, ref, rtol=2e-7, atol=1e-30)
+
+
+def pin_wq_single_weight(oracle):
+    """One nonzero weight: y is exactly x times that weight times its scale,
+    in the row and the group the weight sits in; other outputs are 0."""
+    K, N = 256, 3
+    x = inputs.normal_bf16(np.random.default_rng(32), (2, K))
+    w = np.zeros((N, K // 2), dtype=np.uint8)
+    w[1, 150 // 2] = 0x30  # k = 151 (high nibble) holds 3; k = 150 holds 0
+    s = np.full((N, K // 128), 0x3F80, dtype=np.uint16)
+    s[1, 1] = 0x4040  # 3.0 for group 1 (k 128..255)
+    y = oracle.wq_gemm(oracle.W_INT4, w, s, x)
+    want = _bf16_to_f64(x[:, 151]) * 3 * 3.0
+    assert np.array_equal(y[:, 1], want.astype(np.float32))
+    assert not y[:, 0].any() and not y[:, 2].any()

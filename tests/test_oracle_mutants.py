@@ -62,6 +62,12 @@ MUTANTS = {
                               "    err |= rel_err;\n    {"),
     "pages_first_ignored": ("block_table[(int64_t)b * MP + first + k] = page;",
                             "block_table[(int64_t)b * MP + k] = page;"),
+    "wq_nibble_order": ("int nib = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);",
+                        "int nib = (k % 2 == 0) ? (byte >> 4) : (byte & 0x0F);"),
+    "wq_unsigned": ("return nib >= 8 ? nib - 16 : nib;", "return nib - 8;"),
+    "wq_group": ("(double)bf16_to_float(s[k / group]);", "(double)bf16_to_float(s[k / 64]);"),
+    "wq_no_e4m3_scale": ("wv = oracle_e4m3_decode(row[k]) * (double)s[n];",
+                         "wv = oracle_e4m3_decode(row[k]);"),
     "attn_bf16_scaled": ("double ks = (kv_dtype == ORACLE_KV_E4M3) ? (double)k_scale : 1.0;",
                          "double ks = (double)k_scale;"),
 }
@@ -89,6 +95,9 @@ def run_all_pins():
         ("attn_one_token", lambda: pins.pin_attn_one_token(oracle)),
         ("attn_equal_keys", lambda: pins.pin_attn_equal_keys(oracle)),
         ("attn_abort", lambda: pins.pin_attn_abort_and_errors(oracle)),
+        ("int4_nibbles", lambda: pins.pin_int4_nibbles(oracle)),
+        ("wq_vs_numpy", lambda: pins.pin_wq_vs_numpy(oracle)),
+        ("wq_single", lambda: pins.pin_wq_single_weight(oracle)),
         ("pages_golden", lambda: pins.pin_pages_golden(oracle)),
         ("pages_invariants", lambda: pins.pin_pages_invariants(oracle, n_ops=30)),
         ("pages_overflow", lambda: pins.pin_pages_overflow_and_state(oracle)),

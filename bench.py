@@ -61,10 +61,17 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seed", type=int, default=2)
-    ap.add_argument("--workload", choices=["ragged", "integrity", "8x8192", "prefill", "pages"],
+    ap.add_argument("--workload", choices=["ragged", "integrity", "8x8192", "prefill", "pages",
+                                           "wq"],
                     default=None,
                     help="time one of the other decode workloads (pools filled with random "
                          "finite e4m3 codes on the GPU; one JSON line, not the headline)")
+    ap.add_argument("--wq-kind", choices=["stack", "large", "all"], default="all",
+                    help="--workload wq: which weight set to time")
+    ap.add_argument("--wq-m", type=int, default=0,
+                    help="--workload wq: one token count instead of 1, 8, 16, 32, 64")
+    ap.add_argument("--wq-w", choices=["int4", "e4m3", "both"], default="both",
+                    help="--workload wq: which weight format")
     ap.add_argument("--sweep", action="store_true",
                     help="concurrency sweep 1/8/16/32/64 requests, e4m3 and bf16 KV at equal pool "
                          "bytes; one JSON line per point (not the headline line)")
@@ -982,8 +989,98 @@ def run_pages(args):
                                       rel_npages=i32(np.full(64, 575)))], 36800)
 
 
+# GLM-like projection shapes at 8-way tensor parallelism (synthetic): hidden
+# 5120, 96 query + 8 kv heads of 128, dense MLP 12288: (N, K) per layer
+WQ_LAYER = [("qkv", 1792, 5120), ("o", 5120, 1536), ("gate_up", 3072, 5120), ("down", 5120, 1536)]
+WQ_LAYERS = 40
+
+
+def run_wq(args):
+    """Weight-only INT4 vs e4m3 decode matrix products (kvq_wq_gemm), the
+    pages' second decode workload: every generated token streams all the
+    weights.  Per M (tokens in flight): (a) one decode step's projections of a
+    40-layer stack of GLM-like shapes (distinct weights, 812 MB INT4 / 1.6 GB
+    e4m3: larger than L2), captured as one CUDA graph and replayed; (b) one
+    large projection (28672 x 5120) cycled over 8 weight copies.  Weights and
+    activations are seeded random data (no trained weights); each product's
+    output is discarded, so this times weight streaming, not a model."""
+    import torch
+    from fp8_paged_kv_attn_gb300 import kvq
+
+    kvq.load()
+    peak, _ = measured_hbm_peak()
+    gen = torch.Generator(device="cuda").manual_seed(args.seed)
+    stream = torch.cuda.current_stream()
+
+    def weights(wdtype, N, K):
+        if wdtype == kvq.W_INT4:
+            w = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=gen)
+            s = torch.full((N, K // 128), 0x3C00, dtype=torch.int16, device="cuda")
+            return w, s, N * K // 2 + N * (K // 128) * 2
+        w = torch.randint(0, 0x77, (N, K), dtype=torch.uint8, device="cuda", generator=gen)
+        s = torch.full((N,), 0.01, dtype=torch.float32, device="cuda")
+        return w, s, N * K + N * 4
+
+    def timed(calls, reps=20):
+        """Capture the calls once, replay `reps` times; median ms per replay."""
+        for f in calls:
+            f()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for f in calls:
+                f()
+        g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for e in ev:
+            e[0].record(stream)
+            g.replay()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    kinds = ("stack", "large") if args.wq_kind == "all" else (args.wq_kind,)
+    formats = [(kvq.W_E4M3, "e4m3"), (kvq.W_INT4, "int4")]
+    if args.wq_w != "both":
+        formats = [f for f in formats if f[1] == args.wq_w]
+    ms_list = (args.wq_m,) if args.wq_m else (1, 8, 16, 32, 64)
+    for kind in kinds:
+        res = {}
+        for wdtype, name in formats:
+            if kind == "stack":
+                mats = [weights(wdtype, N, K) + (N, K) for _ in range(WQ_LAYERS)
+                        for _, N, K in WQ_LAYER]
+            else:
+                mats = [weights(wdtype, 28672, 5120) + (28672, 5120) for _ in range(8)]
+            nbytes = sum(m[2] for m in mats)
+            for M in ms_list:
+                xs = {K: torch.randn((M, K), device="cuda", generator=gen).to(torch.bfloat16)
+                      for K in {m[4] for m in mats}}
+                ys = [torch.empty((M, m[3]), dtype=torch.float32, device="cuda") for m in mats]
+                calls = [(lambda m=m, y=y: kvq.kvq_wq_gemm(wdtype, m[0], m[1], xs[m[4]], y))
+                         for m, y in zip(mats, ys)]
+                ms = timed(calls)
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                res[(name, M)] = ms
+                line = {"workload": f"wq_{kind}", "w": name, "M": M, "products": len(mats),
+                        "weight_bytes": nbytes, "ms_per_step": round(ms, 4),
+                        "tokens_per_s": round(M / (ms * 1e-3), 1), "GBs": round(gbs, 1),
+                        "frac_of_measured_peak": round(gbs / peak, 4),
+                        "flops_TFs": round(2.0 * M * sum(m[3] * m[4] for m in mats) /
+                                           (ms * 1e-3) / 1e12, 1)}
+                if name == "int4" and ("e4m3", M) in res:
+                    line["speedup_vs_e4m3"] = round(res[("e4m3", M)] / ms, 3)
+                print(json.dumps(line), flush=True)
+            del mats
+
+
 def main():
     args = parse_args()
+    if args.workload == "wq":
+        run_wq(args)
+        return
     if args.workload == "pages":
         run_pages(args)
         return

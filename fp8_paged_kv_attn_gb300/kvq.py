@@ -28,6 +28,8 @@ from . import _build
 
 KV_E4M3 = 0
 KV_BF16 = 1
+W_INT4 = 0
+W_E4M3 = 1
 
 ERRBIT_PAGE = 1 << 0
 ERRBIT_SEQLEN = 1 << 1
@@ -41,7 +43,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_WORKSPACE", 3: "KVQ
 
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_append", "kvq_check_tags", "kvq_pages_update", "kvq_decode_attn_workspace_size",
-           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_status_string")
+           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_wq_gemm", "kvq_status_string")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -85,6 +87,8 @@ def load(build_if_missing: bool = True):
     L.kvq_pages_update.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, vp, vp, i32, vp, vp, vp,
                                    i32, vp, vp, vp]
     L.kvq_pages_update.restype = ctypes.c_int
+    L.kvq_wq_gemm.argtypes = [i32, vp, vp, vp, vp, i32, i32, i32, vp]
+    L.kvq_wq_gemm.restype = ctypes.c_int
     L.kvq_decode_attn_workspace_size.argtypes = [i32, i32, i32, i32]
     L.kvq_decode_attn_workspace_size.restype = sz
     L.kvq_decode_attn.argtypes = [cp, vp, i32, i32, vp, i32, vp, vp, f32, vp, vp, sz, vp, vp]
@@ -244,6 +248,28 @@ def kvq_pages_update(state: PageState, rel_req=None, rel_npages=None, acq_req=No
                             _dev(acq_ok, "acq_ok", U8, 1), _dev(err_word, "err_word", U32),
                             _stream(stream))
     _check("kvq_pages_update", st)
+
+
+def kvq_wq_gemm(w_dtype: int, w, scales, x, y, stream=None) -> None:
+    """y [M, N] fp32 = x [M, K] bf16 times the quantised weights (include/kvq.h):
+    W_INT4: w uint8 [N, K/2], scales bf16 (or int16 bits) [N, K/128];
+    W_E4M3: w uint8 [N, K], scales fp32 [N]."""
+    L = load()
+    M, K = x.shape
+    N = int(w.shape[0])
+    if tuple(y.shape) != (M, N):
+        raise ValueError("y must be [M, N]")
+    if w_dtype == W_INT4:
+        if tuple(w.shape) != (N, K // 2) or tuple(scales.shape) != (N, K // 128):
+            raise ValueError("INT4 weights must be [N, K/2] with scales [N, K/128]")
+        sc = _dev(scales, "scales", (torch.bfloat16, torch.int16), 2)
+    else:
+        if tuple(w.shape) != (N, K) or tuple(scales.shape) != (N,):
+            raise ValueError("e4m3 weights must be [N, K] with scales [N]")
+        sc = _dev(scales, "scales", (torch.float32,), 1)
+    st = L.kvq_wq_gemm(int(w_dtype), _dev(w, "w", U8, 2), sc, _dev(x, "x", BF16, 2),
+                       _dev(y, "y", (torch.float32,), 2), M, N, K, _stream(stream))
+    _check("kvq_wq_gemm", st)
 
 
 def kvq_decode_attn_workspace_size(B: int, Hq: int, num_kv_heads: int, head_dim: int) -> int:

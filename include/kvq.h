@@ -1,7 +1,8 @@
 /*
  * kvq -- FP8 (e4m3) paged KV cache: quantise-and-append, batched page-tag
- * integrity check, the page allocator that sets the tags, and single-query
- * paged decode attention for NVIDIA GB300 (sm_103a).  Plain C ABI: pointers,
+ * integrity check, the page allocator that sets the tags, single-query
+ * paged decode attention, and the weight-only INT4 / FP8 decode matrix
+ * product, for NVIDIA GB300 (sm_103a).  Plain C ABI: pointers,
  * sizes, a CUDA stream.  The library allocates no memory.
  *
  * Sources (web pages, cited by title and section):
@@ -66,6 +67,7 @@ typedef enum {
 } kvq_status;
 
 typedef enum { KVQ_KV_E4M3 = 0, KVQ_KV_BF16 = 1 } kvq_kv_dtype;
+typedef enum { KVQ_W_INT4 = 0, KVQ_W_E4M3 = 1 } kvq_w_dtype;
 
 /* Bits ORed into *err_word by the kernels. */
 #define KVQ_ERRBIT_PAGE    (1u << 0) /* a block-table entry the call needs is outside [0, num_pages) */
@@ -162,6 +164,24 @@ KVQ_API kvq_status kvq_pages_update(int32_t *free_stack, int32_t *free_count, ui
                                     const int32_t *acq_first, const int32_t *acq_npages,
                                     int32_t n_acq, uint8_t *acq_ok, uint32_t *err_word,
                                     kvq_stream_t stream);
+
+/* Weight-only quantised matrix product for decode ([KVQ] section "模型权重压缩":
+ * the decode pool keeps the weights as 4-bit integers instead of FP8; every
+ * token reads all of them, so decode is bandwidth-bound; INT4 values are
+ * widened before they are multiplied):
+ *     y[m][n] = sum_k x[m][k] * W[n][k]
+ * x bf16 [M][K] (row-major), y fp32 [M][N] (row-major, overwritten), and
+ *   KVQ_W_INT4: w uint8 [N][K/2], two signed 4-bit values a byte (two's
+ *     complement; k even in the low nibble); scales bf16 [N][K/128]:
+ *     W[n][k] = int4(n, k) * scales[n][k/128];
+ *   KVQ_W_E4M3: w uint8 e4m3 codes [N][K]; scales fp32 [N]:
+ *     W[n][k] = e4m3(w[n][k]) * scales[n].
+ * Products are exact and sums fp32 (split over k: the order of the partial
+ * sums varies from run to run); for e4m3 weights x is rounded to f16, which is
+ * exact for |x| in [2^-14, 65504].  Supported: 1 <= M <= 64, K a multiple of
+ * 128.  w and x 16-byte aligned, scales 4-byte aligned. */
+KVQ_API kvq_status kvq_wq_gemm(int32_t w_dtype, const void *w, const void *scales, const void *x,
+                               float *y, int32_t M, int32_t N, int32_t K, kvq_stream_t stream);
 
 /* Bytes of device workspace kvq_decode_attn needs for these sizes (split
  * partials and the per-call work plan).  Depends on B, Hq, num_kv_heads and

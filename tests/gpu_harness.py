@@ -150,13 +150,18 @@ class Run:
         assert np.array_equal(gk, hk), "K pool bytes differ from the oracle"
         assert np.array_equal(gv, hv), "V pool bytes differ from the oracle"
 
-    def attend(self, q_bits, lens, abort=None, sm_scale=None):
+    def attend(self, q_bits, lens, abort=None, sm_scale=None, ws=None, bt=None):
+        """kvq_decode_attn on this cache; `ws` is a workspace to reuse (a fresh
+        zeroed one by default), `bt` a block table to use instead of the
+        workload's (device tensor)."""
         w = self.w
         qd = dev_bf16(q_bits)
         out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32, device="cuda")
-        ws = kvq.workspace(w.B, w.Hq, w.Hkv, w.D)
+        if ws is None:
+            ws = kvq.workspace(w.B, w.Hq, w.Hkv, w.D)
         ab = None if abort is None else dev(abort.astype(np.uint8))
-        kvq.kvq_decode_attn(self.cache, qd, self.bt, dev(lens), out, ws, abort_mask=ab,
+        kvq.kvq_decode_attn(self.cache, qd, self.bt if bt is None else bt, dev(lens), out, ws,
+                            abort_mask=ab,
                             sm_scale=float(w.sm_scale if sm_scale is None else sm_scale),
                             err_word=self.err)
         return out.cpu().numpy()

@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import oracle_pins as pins
 from fp8_paged_kv_attn_gb300 import inputs
 from gpu_harness import Run, assert_close, dev, dev_bf16
@@ -256,3 +257,61 @@ def test_few_long_requests(kvq, dtype, lens):
     w.ctx_lens = np.array(lens, dtype=np.int32)
     step_and_compare(kvq, w, kv_dtype=kvq.KV_E4M3 if dtype == "e4m3" else kvq.KV_BF16,
                      rows=[(b, h) for b in range(B) for h in (0, 3, 17, 31)])
+
+
+def test_workspace_reused_across_calls(kvq):
+    """One workspace serves a mixed sequence of calls of different shapes
+    (every call's plan rewrites the per-call state: row counters, bad-page
+    flags, the list of rows merged across the GPU): rows merged by the combine
+    kernel (A), rows merged inside the split kernel with two aborted requests
+    and an out-of-pool page (B), and the head_dim-64 CUDA-core kernel (C),
+    each checked against the oracle, repeats bit-identical."""
+    wa = inputs.uniform("reuseA", 71, B=2, ctx=9000, Hq=32, Hkv=8, D=128, P=16, outlier_frac=0.01)
+    wa.ctx_lens = np.array([9000, 4100], dtype=np.int32)
+    wb = inputs.uniform("reuseB", 72, B=64, ctx=1200, Hq=32, Hkv=8, D=128, P=16)
+    wc = inputs.uniform("reuseC", 73, B=16, ctx=2000, Hq=16, Hkv=4, D=64, P=16)
+    runs = {}
+    for name, w in (("A", wa), ("B", wb), ("C", wc)):
+        r = Run(w, host_requests={"A": [0, 1], "B": [0, 3, 5, 11, 40], "C": [0, 3, 9, 15]}[name])
+        r.fill_context()
+        q = r.append_step(0)
+        runs[name] = (r, q, w.seq_lens_after(0))
+    size = max(kvq.kvq_decode_attn_workspace_size(w.B, w.Hq, w.Hkv, w.D) for w in (wa, wb, wc))
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    # B: requests 3 and 11 aborted; request 5 has an out-of-pool page (a row
+    # split over several CTAs sets its bad-page flag)
+    abort_b = np.zeros(wb.B, dtype=np.uint8)
+    abort_b[[3, 11]] = 1
+    bt_b = wb.block_table.copy()
+    bt_b[5, 40] = wb.num_pages + 7
+    ref = {}
+    for name in ("A", "B", "C"):
+        r, q, lens = runs[name]
+        rows = [(b, h) for b in r.host_requests for h in range(0, r.w.Hq, 5)]
+        if name == "B":
+            want, err = oracle.decode_attn(oracle.KV_E4M3, r.hk, r.hv, r.k_scale, r.v_scale, q,
+                                           bt_b, lens, abort_mask=abort_b, sm_scale=r.w.sm_scale,
+                                           rows=rows, nthreads=16)
+            assert err == kvq.ERRBIT_PAGE
+        else:
+            want, err = r.oracle_rows(q, lens, rows)
+            assert err == 0
+        ref[name] = (want, rows)
+    first = {}
+    for name in ("A", "B", "C", "A", "B", "C", "A"):
+        r, q, lens = runs[name]
+        r.err.zero_()
+        if name == "B":
+            got = r.attend(q, lens, abort=abort_b, ws=ws, bt=dev(bt_b))
+            assert r.err_word() == kvq.ERRBIT_PAGE
+            assert not got[3].any() and not got[11].any() and not got[5].any()
+        else:
+            got = r.attend(q, lens, ws=ws)
+            assert r.err_word() == 0
+        want, rows = ref[name]
+        for b, h in rows:
+            assert_close(got[b, h], want[b, h], f"{name} row ({b},{h})")
+        if name in first:
+            assert np.array_equal(got, first[name]), f"{name}: repeated call differs"
+        else:
+            first[name] = got

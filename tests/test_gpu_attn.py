@@ -245,12 +245,14 @@ def test_full_integrity(kvq, oracle_mod):
 
 
 @pytest.mark.parametrize("dtype", ["e4m3", "bf16"])
-@pytest.mark.parametrize("lens", [[8000], [5000, 20, 3000], [1, 12000]], ids=["one", "mix", "two"])
+@pytest.mark.parametrize("lens", [[8000], [5000, 20, 3000], [1, 12000],
+                                  [4100, 3900, 4000, 4200, 3800, 4050]],
+                         ids=["one", "mix", "two", "six"])
 def test_few_long_requests(kvq, dtype, lens):
-    """Few requests with long contexts: every row is split over many CTAs and
-    merged across the GPU by the combine kernel (rows with few parts are
-    merged inside the split kernel; both paths are covered by the other
-    tests)."""
+    """Few requests with long contexts: every row is split over many CTAs (25
+    to ~270 parts) and merged across the GPU by the combine kernel (rows with
+    at most 8 parts are merged inside the split kernel; that path is covered
+    by the other tests)."""
     B = len(lens)
     w = inputs.uniform("few", 50 + B, B=B, ctx=max(lens), Hq=32, Hkv=8, D=128, P=16,
                        outlier_frac=0.01)
@@ -315,3 +317,24 @@ def test_workspace_reused_across_calls(kvq):
             assert np.array_equal(got, first[name]), f"{name}: repeated call differs"
         else:
             first[name] = got
+
+
+def test_combine_path_bad_page(kvq):
+    """Rows of ~25 parts, merged by the combine kernel, with an out-of-pool
+    page in request 2: that request's rows are zero, the page error is
+    raised, the other requests match the oracle."""
+    w = inputs.uniform("warpbad", 81, B=6, ctx=4000, Hq=32, Hkv=8, D=128, P=16)
+    r = Run(w, host_requests=[0, 2, 5])
+    r.fill_context()
+    q = r.append_step(0)
+    lens = w.seq_lens_after(0)
+    bt = w.block_table.copy()
+    bt[2, 100] = -3
+    got = r.attend(q, lens, bt=dev(bt))
+    assert r.err_word() == kvq.ERRBIT_PAGE
+    assert not got[2].any()
+    rows = [(b, h) for b in (0, 5) for h in range(0, 32, 3)]
+    want, err = oracle.decode_attn(oracle.KV_E4M3, r.hk, r.hv, r.k_scale, r.v_scale, q, bt, lens,
+                                   sm_scale=w.sm_scale, rows=rows, nthreads=16)
+    for b, h in rows:
+        assert_close(got[b, h], want[b, h], f"row ({b},{h})")

@@ -22,13 +22,14 @@
 // permuted consistently in the weights' fragments and in the staged x, which
 // leaves the sum unchanged), with a register ring of the next 3 (INT4) or 2
 // (e4m3) groups' loads in flight while the current one is computed.
-//  INT4: one LOP3 turns nibbles p and p + 4 of a word into the bf16 pair
-//        128 + (q + 8), an fma.bf16x2 subtracts 136 (exact), and
-//        mma.sync m16n8k16 bf16 -> fp32 accumulates one group, which is then
-//        scaled in fp32 and added to the output accumulator.
-//  e4m3: cvt.rn.f16x2.e4m3x2 widens two codes exactly; x is rounded to f16
-//        once while staged (exact for bf16 values in f16's normal range);
-//        mma.sync f16 -> fp32; the channel scale is applied at the end.
+//  x is rounded to f16 once while staged (exact for bf16 values in f16's
+//  normal range) and the products run on mma.sync m16n8k16 f16 -> fp32.
+//  INT4: one LOP3 and one fma.f16x2 turn two signed nibbles into exact f16
+//        values (magic number 1024; the high nibble of each byte needs no
+//        shift, the upper byte pair one shift per word); a group's products
+//        are accumulated apart, then scaled in fp32 and added to the output.
+//  e4m3: cvt.rn.f16x2.e4m3x2 widens two codes exactly; the channel scale is
+//        applied at the end.
 // Products are exact and the sums are fp32, so the result differs from the
 // fp64 definition only by fp32 summation rounding.
 #include <atomic>
@@ -53,15 +54,6 @@ constexpr int kWqWarps = 8;
 constexpr int kWqRows = 16 * kWqWarps;  // output channels per CTA
 constexpr int kWqGroup = 128;
 
-__device__ __forceinline__ void mma_bf16_16816(float c[4], const uint32_t a[4], uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ void mma_f16_16816(float c[4], const uint32_t a[4], uint32_t b0,
                                               uint32_t b1) {
   asm volatile(
@@ -71,13 +63,23 @@ __device__ __forceinline__ void mma_f16_16816(float c[4], const uint32_t a[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Nibbles 0 and 4 of v (bits 0-3 and 16-19), signed, as the bf16 pair
-// (q_lo, q_hi): (nib ^ 8) | 0x4300 is the bf16 value 128 + (q + 8), and
-// 128 + (q + 8) - 136 = q exactly.
-__device__ __forceinline__ uint32_t int4x2_to_bf16x2(uint32_t v) {
+// Signed nibbles of v as exact f16 pairs, without a shift for the high
+// nibble of a byte (f16 has a 10-bit mantissa):
+//  lo: nibbles 0 and 4 (bits 0-3, 16-19): (nib ^ 8) | 0x6400 is the f16 value
+//      1024 + (q + 8), and 1024 + (q + 8) - 1032 = q;
+//  hi: nibbles 1 and 5 (bits 4-7, 20-23): ((nib ^ 8) << 4) | 0x6400 is
+//      1024 + 16 (q + 8), and that / 16 - 72 = q.
+// Every value on the way is an integer below 2048, exact in f16.
+__device__ __forceinline__ uint32_t int4lo_to_f16x2(uint32_t v) {
   uint32_t t, r;
-  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(t) : "r"(v), "r"(0x000F000Fu), "r"(0x43084308u));
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(t), "r"(0x3F803F80u), "r"(0xC308C308u));
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(t) : "r"(v), "r"(0x000F000Fu), "r"(0x64086408u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(t), "r"(0x3C003C00u), "r"(0xE408E408u));
+  return r;
+}
+__device__ __forceinline__ uint32_t int4hi_to_f16x2(uint32_t v) {
+  uint32_t t, r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(t) : "r"(v), "r"(0x00F000F0u), "r"(0x64806480u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(t), "r"(0x2C002C00u), "r"(0xD480D480u));
   return r;
 }
 
@@ -173,11 +175,9 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
           v[8 * h + 2 * e + 1] = static_cast<uint16_t>(wv[e] >> 16);
         }
       }
-      if constexpr (!kInt4) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          v[e] = __half_as_ushort(__float2half_rn(__uint_as_float(uint32_t(v[e]) << 16)));
-      }
+      for (int e = 0; e < 32; ++e)  // x as f16 (exact for |x| in [2^-14, 65504])
+        v[e] = __half_as_ushort(__float2half_rn(__uint_as_float(uint32_t(v[e]) << 16)));
     } else {
 #pragma unroll
       for (int e = 0; e < 32; ++e) v[e] = 0;
@@ -224,11 +224,13 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
       for (int st = 0; st < 8; ++st) {
         uint32_t af[4];
         if constexpr (kInt4) {
-          const int q = st >> 1, p = 2 * (st & 1);
-          af[0] = int4x2_to_bf16x2(wr0[d][q] >> (4 * p));
-          af[1] = int4x2_to_bf16x2(wr8[d][q] >> (4 * p));
-          af[2] = int4x2_to_bf16x2(wr0[d][q] >> (4 * p + 4));
-          af[3] = int4x2_to_bf16x2(wr8[d][q] >> (4 * p + 4));
+          // step st: nibbles (p, p + 4), (p + 1, p + 5) of word st / 2, p = 2 (st % 2)
+          const uint32_t v0 = (st & 1) ? wr0[d][st >> 1] >> 8 : wr0[d][st >> 1];
+          const uint32_t v8 = (st & 1) ? wr8[d][st >> 1] >> 8 : wr8[d][st >> 1];
+          af[0] = int4lo_to_f16x2(v0);
+          af[1] = int4lo_to_f16x2(v8);
+          af[2] = int4hi_to_f16x2(v0);
+          af[3] = int4hi_to_f16x2(v8);
         } else {
           af[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr0[d][st] & 0xFFFFu));
           af[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr8[d][st] & 0xFFFFu));
@@ -239,10 +241,7 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
         for (int t = 0; t < NT; ++t) {
           const uint2 b = (NT > 1 || rr < Mp) ? xb[((g * 8 + st) * Mp + t * 8 + rr) * 4 + c]
                                               : make_uint2(0u, 0u);
-          if constexpr (kInt4)
-            mma_bf16_16816(gacc[t], af, b.x, b.y);
-          else
-            mma_f16_16816(acc[t], af, b.x, b.y);
+          mma_f16_16816(kInt4 ? gacc[t] : acc[t], af, b.x, b.y);
         }
       }
       if constexpr (kInt4) {

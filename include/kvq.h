@@ -177,8 +177,8 @@ KVQ_API kvq_status kvq_pages_update(int32_t *free_stack, int32_t *free_count, ui
  *   KVQ_W_E4M3: w uint8 e4m3 codes [N][K]; scales fp32 [N]:
  *     W[n][k] = e4m3(w[n][k]) * scales[n].
  * Products are exact and sums fp32 (split over k: the order of the partial
- * sums varies from run to run); for e4m3 weights x is rounded to f16, which is
- * exact for |x| in [2^-14, 65504].  Supported: 1 <= M <= 64, K a multiple of
+ * sums varies from run to run); x is rounded to f16 for the products, which
+ * is exact for |x| in [2^-14, 65504].  Supported: 1 <= M <= 64, K a multiple of
  * 128.  w and x 16-byte aligned, scales 4-byte aligned. */
 KVQ_API kvq_status kvq_wq_gemm(int32_t w_dtype, const void *w, const void *scales, const void *x,
                                float *y, int32_t M, int32_t N, int32_t K, kvq_stream_t stream);

@@ -17,6 +17,10 @@
 //          rows of aborted / empty / invalid requests are written as zeros.
 //   split  persistent grid of (#SMs x resident CTAs), launched as a
 //          programmatic dependent of the plan so its set-up overlaps it.
+//          The tensor-core kernel also works out its own start from the
+//          lengths and the abort mask and starts copying pages before the
+//          plan has finished (it waits for the plan only before it touches
+//          the counters, flags and output the plan writes).
 //          Each CTA owns an equal run of units (see decode_common.cuh).  Warp
 //          4 produces: it reads the block table and stages every page's
 //          contiguous [slot][dim] chunk of the row's kv head into a 4-stage
@@ -82,7 +86,11 @@ inline WsLayout ws_layout(int B, int Hq, int Hkv, int D) {
 // plan
 // ---------------------------------------------------------------------------
 
-constexpr int kPlanSmemPrefix = 4096;
+// The plan runs beside a split CTA on its SM (the split grid launches while
+// the plan is still running): 256 threads and 8 KB of shared memory leave
+// room for a split CTA's registers and ring.
+constexpr int kPlanThreads = 256;
+constexpr int kPlanSmemPrefix = 2048;
 
 struct PlanArgs {
   const int32_t *seq_lens;
@@ -98,9 +106,13 @@ struct PlanArgs {
   int32_t unit;          // tokens per scheduling unit
 };
 
-__global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   grid_dependency_wait();  // e.g. the tag check's abort mask is visible from here on
-  allow_dependents();      // the split grid may start its set-up now
+  // The split grid may launch now.  This comes after the wait on purpose:
+  // the tensor-core split kernel reads seq_lens and the abort mask before its
+  // own wait, which is safe only because everything ahead of the plan on the
+  // stream has completed by the time the split grid can launch.
+  allow_dependents();
   __shared__ int s_scan[32];
   __shared__ int s_carry;
   __shared__ int s_prefix[kPlanSmemPrefix];
@@ -668,6 +680,13 @@ int split_ctas_per_sm(const SplitKernel &k) {
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, f, k.threads, k.smem) != cudaSuccess)
     return 0;
+  // The split grid launches while the plan is still running.  An SM takes
+  // its shared-memory carveout from the first CTA placed on it, so the plan's
+  // SM would otherwise be configured too small for a split CTA, and that
+  // CTA would start only after the plan had exited.
+  if (cudaFuncSetAttribute(plan_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    return 0;
   cache_dev_fn[dev][fi] = occ;
   return occ;
 }
@@ -758,7 +777,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
 
   PlanArgs pa{seq_lens, abort_mask, hdr, prefix, start, done, bad, comb, out, err_word,
               B, Hq, D, MP, cache->page_size, nctas, Hkv / sk.hg, sk.unit};
-  if (launch_dependent(plan_kernel, 1, 1024, 0, s, pa) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_dependent(plan_kernel, 1, kPlanThreads, 0, s, pa) != cudaSuccess) return KVQ_ERR_CUDA;
 
   SplitArgs sa;
   sa.k_pool = static_cast<const uint8_t *>(cache->k_pool);
@@ -766,6 +785,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   sa.q = static_cast<const uint16_t *>(q);
   sa.block_table = block_table;
   sa.seq_lens = seq_lens;
+  sa.abort_mask = abort_mask;
   sa.hdr = hdr;
   sa.prefix = prefix;
   sa.start = start;

@@ -382,23 +382,38 @@ __global__ void __launch_bounds__(32 * (HG + 1))
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
   }
   __syncthreads();
-  grid_dependency_wait();  // the plan's outputs are visible from here on
-  allow_dependents();      // the combine grid may become resident and wait
 
-  const int S = a.hdr[0], U = a.hdr[1];
+  // Where this CTA starts.  Up to kSchedBatch requests the CTA computes it
+  // itself and starts copying pages while the plan kernel is still running;
+  // it waits for the plan (grid_dependency_wait) only before its first access
+  // to what the plan writes: the row counters and bad flags, the output.
+  // Larger batches wait at once and read the plan's schedule.
   const int c = blockIdx.x;
   const int groups = a.Hkv / HG;  // rows per request
+  constexpr int kSchedPer = 16;   // requests per thread in the CTA's own scan
+  SchedStart sc;
+  const bool early = self_schedule<32 * (HG + 1), kSchedPer>(a, groups, kTile, ctl, sc);
+  if (!early) {
+    grid_dependency_wait();
+    sc = plan_schedule(a, groups);
+  }
+  allow_dependents();  // the combine grid may become resident and wait
+  bool dep_ok = !early;  // this thread has passed grid_dependency_wait()
+  const int S = sc.S, U = sc.U;
 
   if (warp == HG) {
     // ------------------------------------------------------------- producer
+    const long long cap = static_cast<long long>(a.MP) * a.P;
     long long u = static_cast<long long>(c) * U;
     const long long u_end = min(u + U, static_cast<long long>(S));
-    int b = 0, grp = 0, s = 0;
-    if (u < u_end) {
-      const int4 st = a.start[c];
-      b = st.x;
-      grp = st.y;
-      s = st.z;
+    // request b: p0 units before it, length L, units_b units in each of its rows
+    int b = sc.b, p0 = sc.p0, L = sc.L, units_b = sc.ub, grp = 0, s = 0;
+    if (u < u_end && units_b > 0) {
+      const int r = static_cast<int>(u - p0);
+      grp = r / units_b;
+      s = r % units_b;
+    } else {
+      u = u_end;  // no work (the owner of a unit always has units)
     }
     const uint64_t pol = policy_evict_first();
     // block-table window of the current request: lane i holds logical page
@@ -408,10 +423,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
     auto bt_load = [&](int lp) -> int { return lp < a.MP ? __ldg(bt_row + lp) : -1; };
     uint32_t g = 0, nseg = 0;
     bool ok = true;
-    while (ok && u < u_end) {
-      const int p0 = __ldg(a.prefix + b), p1 = __ldg(a.prefix + b + 1);
-      const int units_b = (p1 - p0) / groups;
-      const int L = __ldg(a.seq_lens + b);
+    while (ok && u < u_end && b < a.B) {
       const int row = b * groups + grp;
       const long long ur = static_cast<long long>(p0) + static_cast<long long>(grp) * units_b;
       const int c_lo = static_cast<int>(ur / U);
@@ -462,6 +474,10 @@ __global__ void __launch_bounds__(32 * (HG + 1))
           const bool bad_page = page < 0 || page >= a.num_pages;
           if (lane == 0) {
             if (bad_page) {
+              if (!dep_ok) {  // the plan zeroes the bad flags
+                grid_dependency_wait();
+                dep_ok = true;
+              }
               atomicOr(a.bad + row, 1);
               report(a.err_word, KVQ_ERRBIT_PAGE);
             }
@@ -503,6 +519,10 @@ __global__ void __launch_bounds__(32 * (HG + 1))
           }
           if (lane == 0) {
             if (bad_bits) {
+              if (!dep_ok) {
+                grid_dependency_wait();
+                dep_ok = true;
+              }
               atomicOr(a.bad + row, 1);
               report(a.err_word, KVQ_ERRBIT_PAGE);
             }
@@ -538,9 +558,10 @@ __global__ void __launch_bounds__(32 * (HG + 1))
       s = 0;
       if (++grp == groups) {
         grp = 0;
-        ++b;
-        // requests without work (aborted, empty or invalid) own no units
-        while (b < a.B && __ldg(a.prefix + b + 1) == __ldg(a.prefix + b)) ++b;
+        p0 += units_b * groups;
+        // the next request with work (aborted, empty or invalid ones own no units)
+        units_b = 0;
+        while (units_b == 0 && ++b < a.B) units_b = request_units(a, b, cap, kTile, L);
       }
     }
     // tell the consumers there is nothing more
@@ -554,6 +575,9 @@ __global__ void __launch_bounds__(32 * (HG + 1))
         mbar_arrive(&ctl.full[slot]);
       }
     }
+    // The grid must not complete before the plan has: the combine kernel's
+    // wait covers only this grid.
+    if (!dep_ok) grid_dependency_wait();
     return;
   }
 
@@ -614,6 +638,10 @@ __global__ void __launch_bounds__(32 * (HG + 1))
     if (lane == 0) mbar_arrive(&ctl.empty[slot]);
 
     if (d0.z & kLast) {
+      if (!dep_ok) {  // output rows, partials and counters come after the plan
+        grid_dependency_wait();
+        dep_ok = true;
+      }
       const int row = d0.x, nparts = d0.w, pslot = d1.x, c_lo = d1.y, b = d1.z;
       const int kvh = (d1.w & 0xFFFF) * HG + warp;
       hs.l_run += __shfl_xor_sync(0xffffffffu, hs.l_run, 1);

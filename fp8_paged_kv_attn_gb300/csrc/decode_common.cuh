@@ -32,6 +32,7 @@ struct SplitArgs {
   const uint8_t *k_pool, *v_pool;
   const uint16_t *q;
   const int32_t *block_table, *seq_lens;
+  const uint8_t *abort_mask;  // [B] or null
   const int32_t *hdr;     // [0] total units S, [1] units per CTA U
   const int32_t *prefix;  // [B+1]: units before request b, over all its kv heads
   const int4 *start;      // [C]: (b, kv head, unit in row) where CTA c begins
@@ -62,6 +63,8 @@ struct Ctrl {
   uint64_t csync;                // consumer-wide barrier for the split-row hand-off
   int fail;
   int last;
+  int scan[16];                  // per-warp sums of the CTA's own schedule scan
+  int sched[4];                  // where the CTA starts: request, its prefix, length, units
 };
 
 // 2^x on the SFU (relative error ~2^-22; exactly 1 at x = 0)
@@ -108,6 +111,112 @@ __device__ __forceinline__ bool consumer_sync(Ctrl &ctl, uint32_t &count, int la
   const bool ok = ctl_wait(ctl, &ctl.csync, count & 1, err_word);
   ++count;
   return __all_sync(0xffffffffu, ok);
+}
+
+// ---------------------------------------------------------------------------
+// a CTA's own copy of the plan's schedule
+// ---------------------------------------------------------------------------
+
+// Units per row of request b, counted as the plan counts them: ceil(L / unit),
+// or 0 for an aborted request or a length outside [0, cap].  L is returned.
+// The read-only path is safe even before this grid's dependency wait: both
+// arrays were written before the grid launched (see self_schedule), and the
+// lines it leaves in L1 make the producer's later visits to neighbouring
+// requests hits.
+__device__ __forceinline__ int request_units(const SplitArgs &a, int b, long long cap, int unit,
+                                             int &L) {
+  L = __ldg(a.seq_lens + b);
+  const bool aborted = a.abort_mask && __ldg(a.abort_mask + b) != 0;
+  return (aborted || L < 0 || L > cap) ? 0 : (L + unit - 1) / unit;
+}
+
+// Where this CTA starts, as the plan would place it.
+struct SchedStart {
+  int S, U;   // total units, units per CTA
+  int b, p0;  // first request and the units before it (all of its rows)
+  int L, ub;  // that request's length and units per row
+};
+
+// The CTA works out its own start from seq_lens and the abort mask with the
+// plan's arithmetic (rows of ceil(L / unit) units, U = ceil(S / grid)), one
+// request set of PER consecutive requests per thread, so that it need not
+// wait for the plan kernel before it starts copying pages.  Reading those two
+// arrays before grid_dependency_wait() is safe because the plan kernel lets
+// this grid launch only after its own wait: by then everything ahead of the
+// plan on the stream (the tag check that wrote the mask, whatever wrote the
+// lengths) has completed.  Only what the plan itself writes (counters, the
+// merge list, zeroed rows) needs the wait.  Returns false, with nothing read,
+// when the batch is larger than NT x PER requests; the caller then waits and
+// takes the plan's schedule.  Every thread of the CTA calls it.
+template <int NT, int PER>
+__device__ __forceinline__ bool self_schedule(const SplitArgs &a, int rows_per_req, int unit,
+                                              Ctrl &ctl, SchedStart &sc) {
+  static_assert(NT % 32 == 0 && NT / 32 <= 16, "CTA size");
+  if (a.B > NT * PER) return false;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long cap = static_cast<long long>(a.MP) * a.P;
+  const int base = tid * PER;
+  int cnt[PER], len[PER];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    cnt[i] = 0;
+    len[i] = 0;
+    if (base + i < a.B) cnt[i] = request_units(a, base + i, cap, unit, len[i]);
+    sum += cnt[i] * rows_per_req;
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) ctl.scan[warp] = incl;
+  if (tid == 0) ctl.sched[0] = ctl.sched[1] = ctl.sched[2] = ctl.sched[3] = 0;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    const int t = ctl.scan[w];
+    if (w < warp) before += t;
+    total += t;
+  }
+  sc.S = total;
+  sc.U = total > 0 ? (total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) : 1;
+  const long long u0 = static_cast<long long>(blockIdx.x) * sc.U;
+  int pre = before + incl - sum;  // units before this thread's first request
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int n = cnt[i] * rows_per_req;
+    if (n > 0 && u0 >= pre && u0 < pre + n) {  // at most one request of the batch owns u0
+      ctl.sched[0] = base + i;
+      ctl.sched[1] = pre;
+      ctl.sched[2] = len[i];
+      ctl.sched[3] = cnt[i];
+    }
+    pre += n;
+  }
+  __syncthreads();
+  sc.b = ctl.sched[0];  // meaningful only when u0 < S
+  sc.p0 = ctl.sched[1];
+  sc.L = ctl.sched[2];
+  sc.ub = ctl.sched[3];
+  return true;
+}
+
+// The same start read from the plan's results (after grid_dependency_wait()).
+__device__ __forceinline__ SchedStart plan_schedule(const SplitArgs &a, int rows_per_req) {
+  SchedStart sc;
+  sc.S = a.hdr[0];
+  sc.U = a.hdr[1];
+  sc.b = sc.p0 = sc.L = sc.ub = 0;
+  if (static_cast<long long>(blockIdx.x) * sc.U < sc.S) {
+    sc.b = a.start[blockIdx.x].x;
+    sc.p0 = a.prefix[sc.b];
+    sc.ub = (a.prefix[sc.b + 1] - sc.p0) / rows_per_req;
+    sc.L = a.seq_lens[sc.b];
+  }
+  return sc;
 }
 
 // ---------------------------------------------------------------------------

@@ -444,8 +444,12 @@ def run_gpu(args, dist, rank, world, local):
     del rows
     tags = torch.from_numpy(w.page_tags.view(np.int32)).cuda()
     exp_tags = torch.from_numpy(w.expected_tags.view(np.int32)).cuda()
-    mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
-    out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+    # the step's result, out (fp32) then the abort mask, in one buffer so that
+    # the end-to-end loop reads it back with a single copy
+    out_bytes = B * Hq * D * 4
+    result_buf = torch.zeros(out_bytes + B, dtype=torch.uint8, device="cuda")
+    out = result_buf[:out_bytes].view(torch.float32).view(B, Hq, D)
+    mask = result_buf[out_bytes:]
     ws = kvq.workspace(B, Hq, Hkv, D)
     check = args.check == "on"
     graph = not args.eager
@@ -524,10 +528,9 @@ def run_gpu(args, dist, rank, world, local):
     e2e = None
     if not args.no_e2e:
         h_pinned = h_rows.pin_memory()
-        h_out = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
-        h_mask = torch.empty(B, dtype=torch.uint8).pin_memory()
+        h_result = torch.empty(result_buf.numel(), dtype=torch.uint8).pin_memory()
         h2d = packer.nbytes
-        d2h = h_out.numel() * 4 + h_mask.numel()
+        d2h = h_result.numel()
         torch.cuda.synchronize()
         dist_barrier(dist)
         e0 = torch.cuda.Event(enable_timing=True)
@@ -539,8 +542,7 @@ def run_gpu(args, dist, rank, world, local):
                 flush()
                 e2e_ev[j][0].record(stream)
             step.run_staged(h_pinned[args.warmup + j])
-            h_out.copy_(out, non_blocking=True)
-            h_mask.copy_(mask, non_blocking=True)
+            h_result.copy_(result_buf, non_blocking=True)
             if flush is not None:
                 e2e_ev[j][1].record(stream)
         e1.record(stream)

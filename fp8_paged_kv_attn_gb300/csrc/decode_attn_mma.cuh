@@ -183,13 +183,33 @@ __device__ __forceinline__ void tile_step(HeadState &st, const uint8_t *ks, cons
   const uint4 k1a = lds128(k1 + c0), k1b = lds128(k1 + c1);
   const uint32_t kw0[8] = {k0a.x, k0a.y, k0a.z, k0a.w, k0b.x, k0b.y, k0b.z, k0b.w};
   const uint32_t kw1[8] = {k1a.x, k1a.y, k1a.z, k1a.w, k1b.x, k1b.y, k1b.z, k1b.w};
+  // V^T rows 2t, 2t+1, 2t+8, 2t+9 at logical chunk gq, read with K so that
+  // their latency hides under q.k
+  const uint8_t *vr = vs + (2 * tq) * 128;
+  uint4 va = lds128(vr + ((gq ^ (2 * tq)) * 16));
+  uint4 vb = lds128(vr + 128 + ((gq ^ (2 * tq + 1)) * 16));
+  uint4 vc = lds128(vr + 8 * 128 + ((gq ^ (2 * tq)) * 16));
+  uint4 vd = lds128(vr + 9 * 128 + ((gq ^ (2 * tq + 1)) * 16));
+  // even and odd k-steps accumulate apart: four independent chains of four
+  // MMAs instead of two of eight (a consumer warp is bound by dependency
+  // latency, not by issue), summed at the end
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int s = 0; s < 8; ++s) {
+  for (int s = 0; s < 8; s += 2) {
     mma_16816(s0, st.qa0[s], 0u, st.qa2[s], 0u, e4m3x2_to_f16x2(kw0[s] & 0xFFFFu),
               e4m3x2_to_f16x2(kw0[s] >> 16));
     mma_16816(s1, st.qa0[s], 0u, st.qa2[s], 0u, e4m3x2_to_f16x2(kw1[s] & 0xFFFFu),
               e4m3x2_to_f16x2(kw1[s] >> 16));
+    mma_16816(s2, st.qa0[s + 1], 0u, st.qa2[s + 1], 0u, e4m3x2_to_f16x2(kw0[s + 1] & 0xFFFFu),
+              e4m3x2_to_f16x2(kw0[s + 1] >> 16));
+    mma_16816(s3, st.qa0[s + 1], 0u, st.qa2[s + 1], 0u, e4m3x2_to_f16x2(kw1[s + 1] & 0xFFFFu),
+              e4m3x2_to_f16x2(kw1[s + 1] >> 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    s0[i] += s2[i];
+    s1[i] += s3[i];
   }
   // ---- online softmax for head gq over the 16 tokens (log2 domain)
   const bool row_ok = gq < G;
@@ -227,12 +247,7 @@ __device__ __forceinline__ void tile_step(HeadState &st, const uint8_t *ks, cons
   const uint32_t pb0 = f32x2_to_f16x2(p00, p01);
   const uint32_t pb1 = f32x2_to_f16x2(p10, p11);
 
-  // ---- O^T += V^T P^T: rows 2t, 2t+1, 2t+8, 2t+9 at logical chunk gq
-  const uint8_t *vr = vs + (2 * tq) * 128;
-  uint4 va = lds128(vr + ((gq ^ (2 * tq)) * 16));
-  uint4 vb = lds128(vr + 128 + ((gq ^ (2 * tq + 1)) * 16));
-  uint4 vc = lds128(vr + 8 * 128 + ((gq ^ (2 * tq)) * 16));
-  uint4 vd = lds128(vr + 9 * 128 + ((gq ^ (2 * tq + 1)) * 16));
+  // ---- O^T += V^T P^T
   if (ntok < kTile) {  // tail: cached bytes past the sequence may be anything
     const uint4 z = make_uint4(0, 0, 0, 0);
     if (t0 >= ntok) va = z;

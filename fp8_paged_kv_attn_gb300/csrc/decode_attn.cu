@@ -12,15 +12,16 @@
 //   stream, e.g. the tag check), so launch latency overlaps the previous
 //   kernel's tail; each waits for its predecessor before touching memory.
 //
-//   plan   1 CTA: per-request unit counts (64-token units), their prefix sum,
-//          where each persistent CTA starts, and zeroed per-row counters;
-//          rows of aborted / empty / invalid requests are written as zeros.
+//   plan   1 CTA: per-request unit counts, their prefix sum, where each
+//          persistent CTA starts, zeroed per-row bad-page flags, the lists of
+//          rows split across CTAs; rows of aborted / empty / invalid requests
+//          are written as zeros.
 //   split  persistent grid of (#SMs x resident CTAs), launched as a
 //          programmatic dependent of the plan so its set-up overlaps it.
 //          The tensor-core kernel also works out its own start from the
 //          lengths and the abort mask and starts copying pages before the
-//          plan has finished (it waits for the plan only before it touches
-//          the counters, flags and output the plan writes).
+//          plan has finished (it waits for the plan only before it sets a
+//          bad-page flag, the one thing the plan writes that it touches).
 //          Each CTA owns an equal run of units (see decode_common.cuh).  Warp
 //          4 produces: it reads the block table and stages every page's
 //          contiguous [slot][dim] chunk of the row's kv head into a 4-stage
@@ -29,7 +30,10 @@
 //          heads sharing the kv head (each cached element converted once, used
 //          G times), online softmax in the log2 domain with lazy rescaling,
 //          p.v; at the end of a segment they merge and either write the
-//          output row or a partial that the row's last CTA merges.
+//          output row or, for a row split across CTAs, a partial.
+//   combine merges the partials of every split row once the split grid has
+//          finished (a warp per output row for rows of a few parts, a CTA
+//          per output row for rows of many).
 //   Two split kernels exist: a tensor-core one for head_dim 128, e4m3 or
 //   bf16 (decode_attn_mma.cuh: rows are groups of up to 8 kv heads, 16-token
 //   units, one consumer warp per kv head) and a CUDA-core one for head_dim 64
@@ -52,7 +56,7 @@ namespace kvq {
 // ---------------------------------------------------------------------------
 
 struct WsLayout {
-  size_t hdr, prefix, start, done, bad, comb, part, total;
+  size_t hdr, prefix, start, bad, comb, combw, part, total;
 };
 
 inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -68,11 +72,14 @@ inline WsLayout ws_layout(int B, int Hq, int Hkv, int D) {
   off = round256(off + (static_cast<size_t>(B) + 1) * sizeof(int32_t));
   w.start = off;
   off = round256(off + static_cast<size_t>(kMaxCtas) * sizeof(int4));
-  w.done = off;
-  off = round256(off + rows * sizeof(int32_t));
   w.bad = off;
   off = round256(off + rows * sizeof(int32_t));
-  w.comb = off;  // rows the combine kernel merges: {row, first CTA, parts, request}
+  // rows the combine kernel merges, {row, first CTA, parts, request}: split
+  // over more than kWarpMergeMax CTAs (a CTA per output row), and over 2 to
+  // kWarpMergeMax (a warp per output row)
+  w.comb = off;
+  off = round256(off + rows * sizeof(int4));
+  w.combw = off;
   off = round256(off + rows * sizeof(int4));
   // partial slots: row + CTA for every row split across CTAs; a tensor-core
   // row holds up to 8 kv heads, a CUDA-core row one
@@ -97,8 +104,8 @@ struct PlanArgs {
   const uint8_t *abort_mask;
   int32_t *hdr, *prefix;
   int4 *start;
-  int32_t *done, *bad;
-  int4 *comb;
+  int32_t *bad;
+  int4 *comb, *combw;
   float *out;
   uint32_t *err_word;
   int32_t B, Hq, D, MP, P, nctas;
@@ -146,10 +153,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (b < a.B) {
       a.prefix[b] = pre;
       if (b < kPlanSmemPrefix) s_prefix[b] = pre;
-      for (int h = 0; h < a.rows_per_req; ++h) {
-        a.done[b * a.rows_per_req + h] = 0;
-        a.bad[b * a.rows_per_req + h] = 0;
-      }
+      for (int h = 0; h < a.rows_per_req; ++h) a.bad[b * a.rows_per_req + h] = 0;
       if (units == 0) {  // aborted, empty or invalid: the rows are zero
         float4 *o = reinterpret_cast<float4 *>(a.out + static_cast<int64_t>(b) * a.Hq * a.D);
         for (int i = 0; i < a.Hq * a.D / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -190,9 +194,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     const int r = static_cast<int>(u - p0);
     a.start[c] = make_int4(lo, r / units_b, r % units_b, 0);
   }
-  // rows split over more than kFusedMergeMax CTAs go to the combine kernel
-  __shared__ int s_ncomb;
-  if (tid == 0) s_ncomb = 0;
+  // rows split across CTAs go to the combine kernel
+  __shared__ int s_ncomb, s_ncombw;
+  if (tid == 0) s_ncomb = s_ncombw = 0;
   __syncthreads();
   for (int b = tid; b < a.B; b += nt) {
     const int p0 = in_smem ? s_prefix[b] : __ldcg(a.prefix + b);
@@ -202,9 +206,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     for (int r = 0; r < a.rows_per_req; ++r) {
       const long long ur = static_cast<long long>(p0) + static_cast<long long>(r) * units_b;
       const int nparts = static_cast<int>((ur + units_b - 1) / U - ur / U) + 1;
-      if (nparts > kFusedMergeMax)
-        a.comb[atomicAdd(&s_ncomb, 1)] =
-            make_int4(b * a.rows_per_req + r, static_cast<int>(ur / U), nparts, b);
+      const int4 item = make_int4(b * a.rows_per_req + r, static_cast<int>(ur / U), nparts, b);
+      if (nparts > kWarpMergeMax)
+        a.comb[atomicAdd(&s_ncomb, 1)] = item;
+      else if (nparts > 1)
+        a.combw[atomicAdd(&s_ncombw, 1)] = item;
     }
   }
   __syncthreads();
@@ -212,6 +218,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     a.hdr[0] = S;
     a.hdr[1] = U;
     a.hdr[2] = s_ncomb;
+    a.hdr[3] = s_ncombw;
   }
 }
 
@@ -313,7 +320,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
   float q[G][C::EPL];
   float acc[G][C::EPL];
   float m_run[G], l_run[G];
-  uint32_t g = 0, segs = 0, csync_count = 0;
+  uint32_t g = 0, segs = 0;
   bool seg_bad = false;
 
   while (true) {
@@ -429,9 +436,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.fin[rb]);
       if (!ctl_wait(ctl, &ctl.fin[rb], (segs >> 1) & 1, a.err_word)) break;
-      finish_segment<G, D, C::RED>(a, ctl, red + rb * C::NCW * C::RED, d0, d1, seg_bad, lane,
-                                   csync_count);
-      if (ctl.fail) break;
+      finish_segment<G, D, C::RED>(a, red + rb * C::NCW * C::RED, d0, d1, seg_bad, lane);
       ++segs;
     }
     ++g;
@@ -439,12 +444,12 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
 }
 
 // ---------------------------------------------------------------------------
-// combine: rows split over more than kFusedMergeMax CTAs
+// combine: every row split across CTAs
 // ---------------------------------------------------------------------------
 
 struct CombineArgs {
   const int32_t *hdr, *bad;
-  const int4 *comb;
+  const int4 *comb, *combw;
   const float *part;
   float *out;
   int32_t B, Hq, Hkv, G, D, hg, rows_per_req;
@@ -452,6 +457,7 @@ struct CombineArgs {
 };
 
 constexpr int kCombineSubsets = 16;  // part subsets per combine CTA (32 lanes each)
+constexpr int kWarpBatch = 4;        // parts loaded at once by a warp-merged row
 constexpr int kCombineThreads = 32 * kCombineSubsets;
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float *s_red) {
@@ -470,18 +476,50 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float *s_red
   return v;
 }
 
-// Work item = one output row (query head) of one listed kv-head row; 512
-// threads.  The merge is written for latency (a row of a short batch can
-// have hundreds of parts): (1) every part's running max m_p and sum l_p are
-// loaded at once, one part per thread, and reduced to the row maximum M and
-// the denominator sum_p 2^(m_p - M) l_p; (2) thread t accumulates dims
-// 4*(t%32)..+3 of sum_p 2^(m_p - M) acc_p over the parts p = t/32, t/32 + 16,
-// ... with weights read from shared memory, so its loads are independent of
-// one another; (3) the 16 subsets are summed through shared memory.  A part
-// whose maximum is -inf carries no weight and its values are not used.
-// Launched as a programmatic dependent of the split kernel; with no listed
-// rows it exits after reading the count.
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
+// One output row (query head hr of a listed row) and where its parts live.
+struct CombineItem {
+  float *out;         // D floats
+  const float *base;  // part 0 of this query head's kv head
+  int nparts, row, hq;
+};
+
+__device__ __forceinline__ CombineItem combine_item(const CombineArgs &a, int4 cd, int hr,
+                                                    int64_t slot_floats, int64_t kpart) {
+  CombineItem it;
+  it.row = cd.x;
+  it.nparts = cd.z;
+  const int c_lo = cd.y, b = cd.w;
+  const int rin = it.row % a.rows_per_req;
+  const int kvh_in = hr / a.G;
+  it.hq = hr % a.G;
+  it.out = a.out + (static_cast<int64_t>(b) * a.Hq + (rin * a.hg + kvh_in) * a.G + it.hq) * a.D;
+  it.base = a.part + static_cast<int64_t>(it.row + c_lo) * slot_floats + kvh_in * kpart;
+  return it;
+}
+
+// Launched as a programmatic dependent of the split kernel; it waits for the
+// whole split grid, then merges by log-sum-exp every row that grid left in
+// parts (part p of a row is the slot of CTA c_lo + p, holding acc[G][D],
+// m[G], l[G] per kv head, m in the log2 domain):
+//   out = v_scale * sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
+// A part whose maximum is -inf carries no weight and its values are not used;
+// a row with a page outside the pool is written as zeros.
+//  - Rows of more than kWarpMergeMax parts (a row of a short batch can have
+//    hundreds): a whole CTA per output row, written for latency: (1) every
+//    part's m_p and l_p are loaded at once, one part per thread, and reduced
+//    to M and the denominator; (2) thread t accumulates dims 4*(t%32)..+3 over
+//    the parts p = t/32, t/32 + 16, ... with weights read from shared
+//    memory, so its loads are independent of one another; (3) the 16 subsets
+//    are summed through shared memory.
+//  - Rows of 2..kWarpMergeMax parts: one warp per output row, lane l owning
+//    dims 4l..4l+3; the parts' m, l and values are loaded kWarpBatch at a
+//    time and folded into a running maximum.
+// With nothing listed it exits after reading the two counts.  kMinBlocks = 2
+// caps the registers so that a grid of 2 x #SMs runs in one wave; a grid of
+// at most #SMs CTAs runs the uncapped build, which keeps more of a long
+// row's loads in flight.
+template <int kMinBlocks>
+__global__ void __launch_bounds__(kCombineThreads, kMinBlocks) combine_kernel(CombineArgs a) {
   __shared__ float s_w[kMaxCtas], s_l[kMaxCtas];
   __shared__ float s_red[kCombineSubsets];
   __shared__ float4 s_acc[kCombineSubsets][32];
@@ -490,40 +528,41 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
   const int tid = threadIdx.x, sub = tid >> 5, lane = tid & 31;
   const int heads_per_row = a.hg * a.G;
   const int nrows = a.B * a.rows_per_req;
-  // the first item's descriptor is loaded together with the count (the
-  // descriptor array has a slot for every row, so the load is in bounds
-  // even when the slot is not in use)
-  int item = blockIdx.x;
-  int4 cd = item / heads_per_row < nrows ? __ldcg(a.comb + item / heads_per_row)
-                                         : make_int4(0, 0, 0, 0);
-  const int ncomb = __ldcg(a.hdr + 2);
-  if (ncomb == 0) return;
   const int64_t kpart = part_stride(a.G, a.D);  // 16-byte multiple
   const int64_t slot_floats = a.hg * kpart;
   const int GD = a.G * a.D;
   const bool active = 4 * lane < a.D;
+  // the first items' descriptors are loaded together with the counts (both
+  // lists have a slot for every row, so the loads are in bounds even when
+  // the slots are not in use)
+  const int wid = blockIdx.x * kCombineSubsets + sub;  // this warp over the grid
+  int item = blockIdx.x;
+  int4 cd = item / heads_per_row < nrows ? __ldcg(a.comb + item / heads_per_row)
+                                         : make_int4(0, 0, 0, 0);
+  int4 cdw = wid / heads_per_row < nrows ? __ldcg(a.combw + wid / heads_per_row)
+                                         : make_int4(0, 0, 0, 0);
+  const int ncomb = __ldcg(a.hdr + 2);
+  const int ncombw = __ldcg(a.hdr + 3);
+
+  // ---- rows of many parts: a CTA per output row
   for (; item < ncomb * heads_per_row; item += gridDim.x) {
     if (item != static_cast<int>(blockIdx.x)) cd = __ldcg(a.comb + item / heads_per_row);
-    const int row = cd.x, c_lo = cd.y, nparts = cd.z, b = cd.w;  // nparts <= kMaxCtas
-    const int hr = item % heads_per_row;  // query head within the row
-    const int rin = row % a.rows_per_req;
-    const int kvh_in = hr / a.G, hq = hr % a.G;
-    float *out = a.out + (static_cast<int64_t>(b) * a.Hq + (rin * a.hg + kvh_in) * a.G + hq) * a.D;
-    const float *base = a.part + static_cast<int64_t>(row + c_lo) * slot_floats + kvh_in * kpart;
-    const int row_bad = __ldcg(a.bad + row);  // uniform over the CTA
+    const CombineItem it = combine_item(a, cd, item % heads_per_row, slot_floats, kpart);
+    const int nparts = it.nparts;  // <= kMaxCtas
+    const int row_bad = __ldcg(a.bad + it.row);  // uniform over the CTA
 
     // (1) maxima and sums of all parts
     float m_loc = -INFINITY;
     for (int p = tid; p < nparts; p += blockDim.x) {
-      const float *pp = base + p * slot_floats;
-      const float mp = __ldcg(pp + GD + hq);
+      const float *pp = it.base + p * slot_floats;
+      const float mp = __ldcg(pp + GD + it.hq);
       s_w[p] = mp;
-      s_l[p] = __ldcg(pp + GD + a.G + hq);
+      s_l[p] = __ldcg(pp + GD + a.G + it.hq);
       m_loc = fmaxf(m_loc, mp);
     }
     const float M = block_reduce(m_loc, true, s_red);
     if (row_bad) {  // a page of the row was out of range: the output is zero
-      for (int d = tid; d < a.D; d += blockDim.x) out[d] = 0.f;
+      for (int d = tid; d < a.D; d += blockDim.x) it.out[d] = 0.f;
       continue;
     }
     float l_loc = 0.f;
@@ -538,7 +577,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
     // (2) weighted sum of the parts' accumulators
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (active) {
-      const float4 *vbase = reinterpret_cast<const float4 *>(base + hq * a.D) + lane;
+      const float4 *vbase = reinterpret_cast<const float4 *>(it.base + it.hq * a.D) + lane;
       const int64_t vstride = slot_floats / 4;
 #pragma unroll 8
       for (int p = sub; p < nparts; p += kCombineSubsets) {
@@ -566,9 +605,58 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
         o.w += v.w;
       }
       const float sc = a.v_scale / den;
-      reinterpret_cast<float4 *>(out)[lane] = make_float4(o.x * sc, o.y * sc, o.z * sc, o.w * sc);
+      reinterpret_cast<float4 *>(it.out)[lane] =
+          make_float4(o.x * sc, o.y * sc, o.z * sc, o.w * sc);
     }
     __syncthreads();
+  }
+
+  // ---- rows of 2..kWarpMergeMax parts: a warp per output row
+  const int nwarps = gridDim.x * kCombineSubsets;
+  const int slot32 = static_cast<int>(slot_floats);  // at most 8 x 1040 floats
+  for (int w = wid; w < ncombw * heads_per_row; w += nwarps) {
+    if (w != wid) cdw = __ldcg(a.combw + w / heads_per_row);
+    const CombineItem it = combine_item(a, cdw, w % heads_per_row, slot_floats, kpart);
+    const bool row_bad = __ldcg(a.bad + it.row) != 0;
+    // parts in batches of kWarpBatch, all loads of a batch issued together,
+    // folded into a running maximum M (rows here have at most two batches)
+    float M = -INFINITY, den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < it.nparts; p0 += kWarpBatch) {
+      float m[kWarpBatch], l[kWarpBatch];
+      float4 v[kWarpBatch];
+#pragma unroll
+      for (int j = 0; j < kWarpBatch; ++j) {
+        const bool in = p0 + j < it.nparts;
+        const float *pp = it.base + (p0 + j) * slot32;
+        m[j] = in ? __ldcg(pp + GD + it.hq) : -INFINITY;
+        l[j] = in ? __ldcg(pp + GD + a.G + it.hq) : 0.f;
+        v[j] = in && active ? __ldcg(reinterpret_cast<const float4 *>(pp + it.hq * a.D) + lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float Mb = M;
+#pragma unroll
+      for (int j = 0; j < kWarpBatch; ++j) Mb = fmaxf(Mb, m[j]);
+      if (Mb == -INFINITY) continue;  // no part with a weight yet
+      const float f = M == -INFINITY ? 0.f : exp2f(M - Mb);
+      den *= f;
+      acc = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+#pragma unroll
+      for (int j = 0; j < kWarpBatch; ++j) {
+        const float wp = m[j] == -INFINITY ? 0.f : exp2f(m[j] - Mb);
+        if (wp != 0.f) den = fmaf(wp, l[j], den);
+        acc.x = fmaf(wp, v[j].x, acc.x);
+        acc.y = fmaf(wp, v[j].y, acc.y);
+        acc.z = fmaf(wp, v[j].z, acc.z);
+        acc.w = fmaf(wp, v[j].w, acc.w);
+      }
+      M = Mb;
+    }
+    if (active) {
+      const float sc = row_bad ? 0.f : a.v_scale / den;
+      reinterpret_cast<float4 *>(it.out)[lane] =
+          make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+    }
   }
 }
 
@@ -768,14 +856,14 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   int32_t *hdr = reinterpret_cast<int32_t *>(w + ws.hdr);
   int32_t *prefix = reinterpret_cast<int32_t *>(w + ws.prefix);
   int4 *start = reinterpret_cast<int4 *>(w + ws.start);
-  int32_t *done = reinterpret_cast<int32_t *>(w + ws.done);
   int32_t *bad = reinterpret_cast<int32_t *>(w + ws.bad);
   int4 *comb = reinterpret_cast<int4 *>(w + ws.comb);
+  int4 *combw = reinterpret_cast<int4 *>(w + ws.combw);
   float *part = reinterpret_cast<float *>(w + ws.part);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool fp8 = cache->kv_dtype == KVQ_KV_E4M3;
 
-  PlanArgs pa{seq_lens, abort_mask, hdr, prefix, start, done, bad, comb, out, err_word,
+  PlanArgs pa{seq_lens, abort_mask, hdr, prefix, start, bad, comb, combw, out, err_word,
               B, Hq, D, MP, cache->page_size, nctas, Hkv / sk.hg, sk.unit};
   if (launch_dependent(plan_kernel, 1, kPlanThreads, 0, s, pa) != cudaSuccess) return KVQ_ERR_CUDA;
 
@@ -789,7 +877,6 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   sa.hdr = hdr;
   sa.prefix = prefix;
   sa.start = start;
-  sa.done = done;
   sa.bad = bad;
   sa.part = part;
   sa.out = out;
@@ -818,14 +905,14 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   }
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
 
-  // rows split over many CTAs are merged across the GPU by combine_kernel;
-  // it is a programmatic dependent of the split grid and exits at once for
-  // rows the split kernel already finished
-  CombineArgs ca{hdr, bad, comb, part, out, B, Hq, Hkv, G, D, sk.hg, Hkv / sk.hg,
+  // rows split across CTAs are merged by combine_kernel, a programmatic
+  // dependent of the split grid; with no such rows it exits at once
+  CombineArgs ca{hdr, bad, comb, combw, part, out, B, Hq, Hkv, G, D, sk.hg, Hkv / sk.hg,
                  fp8 ? cache->v_scale : 1.0f};
   const int crows = B * Hq;
-  if (launch_dependent(combine_kernel, crows < 2 * sms ? crows : 2 * sms, kCombineThreads, 0, s,
-                       ca) != cudaSuccess)
+  const int cgrid = crows < 2 * sms ? crows : 2 * sms;
+  if (launch_dependent(cgrid <= sms ? combine_kernel<1> : combine_kernel<2>, cgrid,
+                       kCombineThreads, 0, s, ca) != cudaSuccess)
     return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -398,11 +398,13 @@ __global__ void __launch_bounds__(32 * (HG + 1))
   }
   __syncthreads();
 
-  // Where this CTA starts.  Up to kSchedBatch requests the CTA computes it
-  // itself and starts copying pages while the plan kernel is still running;
-  // it waits for the plan (grid_dependency_wait) only before its first access
-  // to what the plan writes: the row counters and bad flags, the output.
-  // Larger batches wait at once and read the plan's schedule.
+  // Where this CTA starts.  For up to 32 x (HG + 1) x kSchedPer requests the
+  // CTA computes it itself and starts copying pages while the plan kernel is
+  // still running; of what the plan writes it touches only the bad-page
+  // flags, and waits for the plan (grid_dependency_wait) before the first of
+  // those.  (The plan's zeroed output rows are those of requests without
+  // work, which no split CTA writes.)  Larger batches wait at once and read
+  // the plan's schedule.
   const int c = blockIdx.x;
   const int groups = a.Hkv / HG;  // rows per request
   constexpr int kSchedPer = 16;   // requests per thread in the CTA's own scan
@@ -413,7 +415,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
     sc = plan_schedule(a, groups);
   }
   allow_dependents();  // the combine grid may become resident and wait
-  bool dep_ok = !early;  // this thread has passed grid_dependency_wait()
+  bool dep_ok = !early;  // this thread has passed grid_dependency_wait() (producer)
   const int S = sc.S, U = sc.U;
 
   if (warp == HG) {
@@ -600,7 +602,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
   const int gq = lane >> 2;  // fragment row group
   const int tq = lane & 3;   // thread in group
   HeadState hs;
-  uint32_t g = 0, nseg = 0, csync_count = 0;
+  uint32_t g = 0, nseg = 0;
   bool seg_bad = false;
 
   while (true) {
@@ -653,11 +655,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
     if (lane == 0) mbar_arrive(&ctl.empty[slot]);
 
     if (d0.z & kLast) {
-      if (!dep_ok) {  // output rows, partials and counters come after the plan
-        grid_dependency_wait();
-        dep_ok = true;
-      }
-      const int row = d0.x, nparts = d0.w, pslot = d1.x, c_lo = d1.y, b = d1.z;
+      const int nparts = d0.w, pslot = d1.x, b = d1.z;
       const int kvh = (d1.w & 0xFFFF) * HG + warp;
       hs.l_run += __shfl_xor_sync(0xffffffffu, hs.l_run, 1);
       hs.l_run += __shfl_xor_sync(0xffffffffu, hs.l_run, 2);
@@ -725,90 +723,6 @@ __global__ void __launch_bounds__(32 * (HG + 1))
           if (hb < G) {
             mine[G * C::D + hb] = mb;
             mine[G * C::D + G + hb] = lb;
-          }
-        }
-        if (nparts > kFusedMergeMax) {  // merged by combine_kernel
-          ++nseg;
-          ++g;
-          continue;
-        }
-        __threadfence();
-        if (!consumer_sync(ctl, csync_count, lane, a.err_word)) break;
-        if (warp == 0 && lane == 0) {
-          const int prev = atomicAdd(a.done + row, 1);
-          ctl.last = prev == nparts - 1;
-        }
-        if (!consumer_sync(ctl, csync_count, lane, a.err_word)) break;
-        if (ctl.last) {
-          __threadfence();
-          const bool row_bad = __ldcg(a.bad + row) != 0;
-          // consecutive CTAs of one row wrote consecutive slots (slot = row + CTA)
-          const float *p0 = a.part + static_cast<int64_t>(row + c_lo) * C::PART +
-                            static_cast<int64_t>(warp) * C::KPART;
-          float msa = -INFINITY, msb = -INFINITY;
-          for (int p = 0; p < nparts; ++p) {
-            const float *pp = p0 + static_cast<int64_t>(p) * C::PART;
-            if (ha < G) msa = fmaxf(msa, __ldcg(pp + G * C::D + ha));
-            if (hb < G) msb = fmaxf(msb, __ldcg(pp + G * C::D + hb));
-          }
-          float acc[8][4] = {};
-          float dena = 0.f, denb = 0.f;
-          for (int p = 0; p < nparts; ++p) {
-            const float *pp = p0 + static_cast<int64_t>(p) * C::PART;
-            float fa = 0.f, fb = 0.f;
-            if (ha < G) {
-              const float m = __ldcg(pp + G * C::D + ha);
-              fa = m == -INFINITY ? 0.f : exp2f(m - msa);
-              dena = fmaf(fa, __ldcg(pp + G * C::D + G + ha), dena);
-            }
-            if (hb < G) {
-              const float m = __ldcg(pp + G * C::D + hb);
-              fb = m == -INFINITY ? 0.f : exp2f(m - msb);
-              denb = fmaf(fb, __ldcg(pp + G * C::D + G + hb), denb);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int dl = dim_lo<kBf16>(i, gq), dh = dim_hi<kBf16>(i, gq);
-              float2 va, vb;
-              if constexpr (!kBf16) {  // dims dl, dl+1: one 8-byte load
-                va = ha < G ? __ldcg(reinterpret_cast<const float2 *>(pp + ha * C::D + dl))
-                            : make_float2(0.f, 0.f);
-                vb = hb < G ? __ldcg(reinterpret_cast<const float2 *>(pp + hb * C::D + dl))
-                            : make_float2(0.f, 0.f);
-              } else {
-                va = ha < G ? make_float2(__ldcg(pp + ha * C::D + dl), __ldcg(pp + ha * C::D + dh))
-                            : make_float2(0.f, 0.f);
-                vb = hb < G ? make_float2(__ldcg(pp + hb * C::D + dl), __ldcg(pp + hb * C::D + dh))
-                            : make_float2(0.f, 0.f);
-              }
-              acc[i][0] = fmaf(fa, va.x, acc[i][0]);
-              acc[i][2] = fmaf(fa, va.y, acc[i][2]);
-              acc[i][1] = fmaf(fb, vb.x, acc[i][1]);
-              acc[i][3] = fmaf(fb, vb.y, acc[i][3]);
-            }
-          }
-          const float sa = row_bad ? 0.f : a.v_scale / dena;
-          const float sb = row_bad ? 0.f : a.v_scale / denb;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int dl = dim_lo<kBf16>(i, gq), dh = dim_hi<kBf16>(i, gq);
-            if constexpr (!kBf16) {
-              if (ha < G)
-                *reinterpret_cast<float2 *>(out + ha * C::D + dl) =
-                    make_float2(acc[i][0] * sa, acc[i][2] * sa);
-              if (hb < G)
-                *reinterpret_cast<float2 *>(out + hb * C::D + dl) =
-                    make_float2(acc[i][1] * sb, acc[i][3] * sb);
-            } else {
-              if (ha < G) {
-                out[ha * C::D + dl] = acc[i][0] * sa;
-                out[ha * C::D + dh] = acc[i][2] * sa;
-              }
-              if (hb < G) {
-                out[hb * C::D + dl] = acc[i][1] * sb;
-                out[hb * C::D + dh] = acc[i][3] * sb;
-              }
-            }
           }
         }
       }

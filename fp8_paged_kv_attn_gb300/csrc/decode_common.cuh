@@ -8,9 +8,10 @@
 // is balanced to within one unit whatever the length mix.  A CTA's range cuts
 // rows into segments; a row owned by one CTA is normalised and written
 // directly, otherwise every CTA writes a partial (acc[G][D], m[G], l[G] per
-// kv head) and the row is merged by log-sum-exp: by the last CTA to finish
-// it (an atomic counter, no waiting) when it has few parts, else by the
-// combine kernel, whose CTAs each merge one output row.
+// kv head) and the combine kernel merges the row by log-sum-exp once the
+// split grid has finished: one warp per output row when the row has few
+// parts, a whole CTA per output row when it has many.  No split CTA ever
+// waits for another, so the grid ends when the last CTA's stream does.
 #pragma once
 
 namespace kvq {
@@ -36,7 +37,6 @@ struct SplitArgs {
   const int32_t *hdr;     // [0] total units S, [1] units per CTA U
   const int32_t *prefix;  // [B+1]: units before request b, over all its kv heads
   const int4 *start;      // [C]: (b, kv head, unit in row) where CTA c begins
-  int32_t *done;          // [B*Hkv] CTAs finished per row (zeroed by the plan)
   int32_t *bad;           // [B*Hkv] a page of the row was outside the pool
   float *part;            // [B*Hkv + C][G][D+2] partials
   float *out;             // [B][Hq][D]
@@ -50,9 +50,10 @@ struct SplitArgs {
 // multiple of four floats so every head's block is 16-byte aligned.
 __host__ __device__ constexpr int part_stride(int G, int D) { return G * D + (2 * G + 3) / 4 * 4; }
 
-// Rows split over at most this many CTAs are merged by the last of them;
-// rows split further are merged by combine_kernel, spread over the GPU.
-constexpr int kFusedMergeMax = 8;
+// Rows split over at most this many CTAs are merged by one warp per output
+// row in the combine kernel (all parts' loads issued at once); rows split
+// further by a whole combine CTA per output row.
+constexpr int kWarpMergeMax = 8;
 
 // Shared-memory control block.
 struct Ctrl {
@@ -60,9 +61,7 @@ struct Ctrl {
   uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t qfull[2], qempty[2];  // double-buffered query rows (tensor-core kernel)
   uint64_t fin[2];               // per-segment merge of the consumer warps (CUDA-core kernel)
-  uint64_t csync;                // consumer-wide barrier for the split-row hand-off
   int fail;
-  int last;
   int scan[16];                  // per-warp sums of the CTA's own schedule scan
   int sched[4];                  // where the CTA starts: request, its prefix, length, units
 };
@@ -85,9 +84,7 @@ __device__ __forceinline__ void ctrl_init(Ctrl &ctl, int ns, int nc) {
     mbar_init(&ctl.qempty[i], nc);
     mbar_init(&ctl.fin[i], nc);
   }
-  mbar_init(&ctl.csync, nc);
   ctl.fail = 0;
-  ctl.last = 0;
   fence_barrier_init();
 }
 
@@ -100,17 +97,6 @@ __device__ __forceinline__ bool ctl_wait(Ctrl &ctl, uint64_t *bar, uint32_t pari
   if (mbar_wait(bar, parity)) return true;
   if (atomicExch(&ctl.fail, 1) == 0) report(err_word, KVQ_ERRBIT_TIMEOUT);
   return false;
-}
-
-// All consumer warps meet (every consumer warp calls this the same number of
-// times; `count` is that number so far, kept per warp).
-__device__ __forceinline__ bool consumer_sync(Ctrl &ctl, uint32_t &count, int lane,
-                                              uint32_t *err_word) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&ctl.csync);
-  const bool ok = ctl_wait(ctl, &ctl.csync, count & 1, err_word);
-  ++count;
-  return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------------------
@@ -350,11 +336,10 @@ __device__ __forceinline__ void producer_loop(const SplitArgs &a, Ctrl &ctl, uin
 // ---------------------------------------------------------------------------
 
 template <int G, int D, int RED>
-__device__ __forceinline__ void finish_segment(const SplitArgs &a, Ctrl &ctl, const float *red,
-                                               int4 d0, int4 d1, bool seg_bad, int lane,
-                                               uint32_t &csync_count) {
+__device__ __forceinline__ void finish_segment(const SplitArgs &a, const float *red, int4 d0,
+                                               int4 d1, bool seg_bad, int lane) {
   const int ctid = (threadIdx.x >> 5) * 32 + lane;
-  const int row = d0.x, nparts = d0.w, slot = d1.x, c_lo = d1.y, b = d1.z, kvh = d1.w;
+  const int nparts = d0.w, slot = d1.x, b = d1.z, kvh = d1.w;
   constexpr int GD = G * D;
   constexpr int PART = part_stride(G, D);
   float *out = a.out + (static_cast<int64_t>(b) * a.Hq + kvh * G) * D;
@@ -381,39 +366,6 @@ __device__ __forceinline__ void finish_segment(const SplitArgs &a, Ctrl &ctl, co
         mine[GD + G + h] = l;
       }
     }
-  }
-  if (nparts == 1 || nparts > kFusedMergeMax) return;
-
-  // split row: publish the partial, count it; the last CTA merges the row
-  __threadfence();
-  if (!consumer_sync(ctl, csync_count, lane, a.err_word)) return;
-  if (ctid == 0) {
-    const int prev = atomicAdd(a.done + row, 1);
-    ctl.last = prev == nparts - 1;
-  }
-  if (!consumer_sync(ctl, csync_count, lane, a.err_word)) return;
-  if (!ctl.last) return;
-  __threadfence();
-  const bool row_bad = __ldcg(a.bad + row) != 0;
-  const float *p0 = a.part + static_cast<int64_t>(row + c_lo) * PART;  // slot of CTA c_lo
-  for (int idx = ctid; idx < GD; idx += kConsumerWarps * 32) {
-    if (row_bad) {
-      out[idx] = 0.f;
-      continue;
-    }
-    const int h = idx / D;
-    float mstar = -INFINITY;
-    for (int p = 0; p < nparts; ++p) mstar = fmaxf(mstar, __ldcg(p0 + p * PART + GD + h));
-    float num = 0.f, den = 0.f;
-    for (int p = 0; p < nparts; ++p) {
-      // consecutive CTAs of one row write consecutive slots (slot = row + CTA)
-      const float *pp = p0 + p * PART;
-      const float ms = __ldcg(pp + GD + h);
-      const float f = ms == -INFINITY ? 0.f : exp2f(ms - mstar);
-      num = fmaf(f, __ldcg(pp + idx), num);
-      den = fmaf(f, __ldcg(pp + GD + G + h), den);
-    }
-    out[idx] = num / den * a.v_scale;
   }
 }
 

@@ -460,22 +460,6 @@ constexpr int kCombineSubsets = 16;  // part subsets per combine CTA (32 lanes e
 constexpr int kWarpBatch = 4;        // parts loaded at once by a warp-merged row
 constexpr int kCombineThreads = 32 * kCombineSubsets;
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float *s_red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float u = __shfl_xor_sync(0xffffffffu, v, o);
-    v = is_max ? fmaxf(v, u) : v + u;
-  }
-  if (lane == 0) s_red[warp] = v;
-  __syncthreads();
-  v = s_red[0];
-#pragma unroll
-  for (int w = 1; w < kCombineSubsets; ++w) v = is_max ? fmaxf(v, s_red[w]) : v + s_red[w];
-  __syncthreads();  // s_red may be reused
-  return v;
-}
-
 // One output row (query head hr of a listed row) and where its parts live.
 struct CombineItem {
   float *out;         // D floats
@@ -497,31 +481,64 @@ __device__ __forceinline__ CombineItem combine_item(const CombineArgs &a, int4 c
   return it;
 }
 
+// Folds parts p0, p0 + step, ... (< nparts) of one output row into a running
+// maximum M, denominator den and accumulator acc (dims 4*lane..+3): the
+// parts are loaded NB at a time, every load of a batch issued together.
+template <int NB>
+__device__ __forceinline__ void merge_parts(const CombineItem &it, int p0, int step, int slot32,
+                                            int GD, int G, int D, int lane, bool active,
+                                            float &M, float &den, float4 &acc) {
+  for (int pb = p0; pb < it.nparts; pb += NB * step) {
+    float m[NB], l[NB];
+    float4 v[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int p = pb + j * step;
+      const bool in = p < it.nparts;
+      const float *pp = it.base + p * slot32;
+      m[j] = in ? __ldcg(pp + GD + it.hq) : -INFINITY;
+      l[j] = in ? __ldcg(pp + GD + G + it.hq) : 0.f;
+      v[j] = in && active ? __ldcg(reinterpret_cast<const float4 *>(pp + it.hq * D) + lane)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float Mb = M;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) Mb = fmaxf(Mb, m[j]);
+    if (Mb == -INFINITY) continue;  // no part with a weight yet
+    const float f = M == -INFINITY ? 0.f : exp2f(M - Mb);
+    den *= f;
+    acc = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const float wp = m[j] == -INFINITY ? 0.f : exp2f(m[j] - Mb);
+      if (wp != 0.f) den = fmaf(wp, l[j], den);
+      acc.x = fmaf(wp, v[j].x, acc.x);
+      acc.y = fmaf(wp, v[j].y, acc.y);
+      acc.z = fmaf(wp, v[j].z, acc.z);
+      acc.w = fmaf(wp, v[j].w, acc.w);
+    }
+    M = Mb;
+  }
+}
+
 // Launched as a programmatic dependent of the split kernel; it waits for the
 // whole split grid, then merges by log-sum-exp every row that grid left in
 // parts (part p of a row is the slot of CTA c_lo + p, holding acc[G][D],
 // m[G], l[G] per kv head, m in the log2 domain):
 //   out = v_scale * sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
 // A part whose maximum is -inf carries no weight and its values are not used;
-// a row with a page outside the pool is written as zeros.
-//  - Rows of more than kWarpMergeMax parts (a row of a short batch can have
-//    hundreds): a whole CTA per output row, written for latency: (1) every
-//    part's m_p and l_p are loaded at once, one part per thread, and reduced
-//    to M and the denominator; (2) thread t accumulates dims 4*(t%32)..+3 over
-//    the parts p = t/32, t/32 + 16, ... with weights read from shared
-//    memory, so its loads are independent of one another; (3) the 16 subsets
-//    are summed through shared memory.
-//  - Rows of 2..kWarpMergeMax parts: one warp per output row, lane l owning
-//    dims 4l..4l+3; the parts' m, l and values are loaded kWarpBatch at a
-//    time and folded into a running maximum.
+// a row with a page outside the pool is written as zeros.  Both kinds of
+// work item fold parts with merge_parts (lane l owns dims 4l..4l+3):
+//  - rows of 2..kWarpMergeMax parts: one warp per output row;
+//  - longer rows (a row of a short batch can have hundreds of parts): a CTA
+//    per output row, its 16 warps folding every 16th part each, then warp 0
+//    folding the 16 results from shared memory.
 // With nothing listed it exits after reading the two counts.  kMinBlocks = 2
 // caps the registers so that a grid of 2 x #SMs runs in one wave; a grid of
-// at most #SMs CTAs runs the uncapped build, which keeps more of a long
-// row's loads in flight.
+// at most #SMs CTAs runs the uncapped build, which loads 8 parts at a time.
 template <int kMinBlocks>
 __global__ void __launch_bounds__(kCombineThreads, kMinBlocks) combine_kernel(CombineArgs a) {
-  __shared__ float s_w[kMaxCtas], s_l[kMaxCtas];
-  __shared__ float s_red[kCombineSubsets];
+  __shared__ float s_m[kCombineSubsets], s_den[kCombineSubsets];
   __shared__ float4 s_acc[kCombineSubsets][32];
   grid_dependency_wait();
   allow_dependents();  // e.g. the next step's append may be scheduled
@@ -545,113 +562,54 @@ __global__ void __launch_bounds__(kCombineThreads, kMinBlocks) combine_kernel(Co
   const int ncombw = __ldcg(a.hdr + 3);
 
   // ---- rows of many parts: a CTA per output row
+  const int slot32 = static_cast<int>(slot_floats);  // at most 8 x 1040 floats
   for (; item < ncomb * heads_per_row; item += gridDim.x) {
     if (item != static_cast<int>(blockIdx.x)) cd = __ldcg(a.comb + item / heads_per_row);
     const CombineItem it = combine_item(a, cd, item % heads_per_row, slot_floats, kpart);
-    const int nparts = it.nparts;  // <= kMaxCtas
-    const int row_bad = __ldcg(a.bad + it.row);  // uniform over the CTA
-
-    // (1) maxima and sums of all parts
-    float m_loc = -INFINITY;
-    for (int p = tid; p < nparts; p += blockDim.x) {
-      const float *pp = it.base + p * slot_floats;
-      const float mp = __ldcg(pp + GD + it.hq);
-      s_w[p] = mp;
-      s_l[p] = __ldcg(pp + GD + a.G + it.hq);
-      m_loc = fmaxf(m_loc, mp);
-    }
-    const float M = block_reduce(m_loc, true, s_red);
-    if (row_bad) {  // a page of the row was out of range: the output is zero
-      for (int d = tid; d < a.D; d += blockDim.x) it.out[d] = 0.f;
-      continue;
-    }
-    float l_loc = 0.f;
-    for (int p = tid; p < nparts; p += blockDim.x) {
-      const float mp = s_w[p];
-      const float w = mp == -INFINITY ? 0.f : exp2f(mp - M);
-      s_w[p] = w;
-      l_loc += w != 0.f ? w * s_l[p] : 0.f;
-    }
-    const float den = block_reduce(l_loc, false, s_red);  // also orders the s_w writes
-
-    // (2) weighted sum of the parts' accumulators
+    const bool row_bad = __ldcg(a.bad + it.row) != 0;  // uniform over the CTA
+    // subset `sub` folds parts sub, sub + 16, ...; then the subsets are folded
+    float M = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active) {
-      const float4 *vbase = reinterpret_cast<const float4 *>(it.base + it.hq * a.D) + lane;
-      const int64_t vstride = slot_floats / 4;
-#pragma unroll 8
-      for (int p = sub; p < nparts; p += kCombineSubsets) {
-        const float w = s_w[p];
-        float4 v = __ldcg(vbase + p * vstride);
-        if (w == 0.f) v = make_float4(0.f, 0.f, 0.f, 0.f);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-      }
-    }
+    merge_parts<kMinBlocks == 1 ? 8 : kWarpBatch>(it, sub, kCombineSubsets, slot32, GD, a.G, a.D,
+                                                  lane, active, M, den, acc);
     s_acc[sub][lane] = acc;
+    if (lane == 0) {
+      s_m[sub] = M;
+      s_den[sub] = den;
+    }
     __syncthreads();
-
-    // (3) the subsets
     if (sub == 0 && active) {
-      float4 o = s_acc[0][lane];
+      float Mr = -INFINITY;
 #pragma unroll
-      for (int i = 1; i < kCombineSubsets; ++i) {
+      for (int i = 0; i < kCombineSubsets; ++i) Mr = fmaxf(Mr, s_m[i]);
+      float d = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < kCombineSubsets; ++i) {
+        const float wi = s_m[i] == -INFINITY ? 0.f : exp2f(s_m[i] - Mr);
         const float4 v = s_acc[i][lane];
-        o.x += v.x;
-        o.y += v.y;
-        o.z += v.z;
-        o.w += v.w;
+        d = fmaf(wi, s_den[i], d);
+        o.x = fmaf(wi, v.x, o.x);
+        o.y = fmaf(wi, v.y, o.y);
+        o.z = fmaf(wi, v.z, o.z);
+        o.w = fmaf(wi, v.w, o.w);
       }
-      const float sc = a.v_scale / den;
+      const float sc = row_bad ? 0.f : a.v_scale / d;
       reinterpret_cast<float4 *>(it.out)[lane] =
           make_float4(o.x * sc, o.y * sc, o.z * sc, o.w * sc);
     }
-    __syncthreads();
+    __syncthreads();  // s_acc, s_m, s_den are reused by the next item
   }
 
   // ---- rows of 2..kWarpMergeMax parts: a warp per output row
   const int nwarps = gridDim.x * kCombineSubsets;
-  const int slot32 = static_cast<int>(slot_floats);  // at most 8 x 1040 floats
   for (int w = wid; w < ncombw * heads_per_row; w += nwarps) {
     if (w != wid) cdw = __ldcg(a.combw + w / heads_per_row);
     const CombineItem it = combine_item(a, cdw, w % heads_per_row, slot_floats, kpart);
     const bool row_bad = __ldcg(a.bad + it.row) != 0;
-    // parts in batches of kWarpBatch, all loads of a batch issued together,
-    // folded into a running maximum M (rows here have at most two batches)
     float M = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p0 = 0; p0 < it.nparts; p0 += kWarpBatch) {
-      float m[kWarpBatch], l[kWarpBatch];
-      float4 v[kWarpBatch];
-#pragma unroll
-      for (int j = 0; j < kWarpBatch; ++j) {
-        const bool in = p0 + j < it.nparts;
-        const float *pp = it.base + (p0 + j) * slot32;
-        m[j] = in ? __ldcg(pp + GD + it.hq) : -INFINITY;
-        l[j] = in ? __ldcg(pp + GD + a.G + it.hq) : 0.f;
-        v[j] = in && active ? __ldcg(reinterpret_cast<const float4 *>(pp + it.hq * a.D) + lane)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      float Mb = M;
-#pragma unroll
-      for (int j = 0; j < kWarpBatch; ++j) Mb = fmaxf(Mb, m[j]);
-      if (Mb == -INFINITY) continue;  // no part with a weight yet
-      const float f = M == -INFINITY ? 0.f : exp2f(M - Mb);
-      den *= f;
-      acc = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
-#pragma unroll
-      for (int j = 0; j < kWarpBatch; ++j) {
-        const float wp = m[j] == -INFINITY ? 0.f : exp2f(m[j] - Mb);
-        if (wp != 0.f) den = fmaf(wp, l[j], den);
-        acc.x = fmaf(wp, v[j].x, acc.x);
-        acc.y = fmaf(wp, v[j].y, acc.y);
-        acc.z = fmaf(wp, v[j].z, acc.z);
-        acc.w = fmaf(wp, v[j].w, acc.w);
-      }
-      M = Mb;
-    }
+    merge_parts<kWarpBatch>(it, 0, 1, slot32, GD, a.G, a.D, lane, active, M, den, acc);
     if (active) {
       const float sc = row_bad ? 0.f : a.v_scale / den;
       reinterpret_cast<float4 *>(it.out)[lane] =

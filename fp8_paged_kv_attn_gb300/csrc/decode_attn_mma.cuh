@@ -70,6 +70,10 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   return r;
 }
 
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {  // low half -> .x
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) {
   return *reinterpret_cast<const uint4 *>(p);
 }
@@ -96,6 +100,7 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
 }
 
 constexpr int kTile = 16;  // tokens per stage of the tensor-core kernel
+constexpr float kPScale = 128.f;  // scale of the e4m3 kernel's softmax weights
 constexpr int kPlane = kTile * 128;  // 2 KB: 16 tokens x 128 bytes of one head
 
 template <int G, int HG, bool kBf16>
@@ -130,6 +135,17 @@ struct HeadState {
   float qk_scale;
 };
 
+// Rows of S and columns of O^T in the e4m3 kernel (the MMA's 8 query-head
+// slots): slot h < G is query head h and carries the f16 weights p_hi; when
+// 2G <= 8, slot G + h holds a copy of head h's query row, so the lanes of that
+// row compute the same scores and weights and supply the remainders
+// p_lo = f16(p - p_hi) to column G + h, which is added to column h at the
+// segment's end.  G = 8 has no free slot and runs p_lo through a second MMA.
+template <int G>
+__device__ __forceinline__ int slot_head(int gq) {
+  return gq < G ? gq : ((2 * G <= 8 && gq < 2 * G) ? gq - G : -1);
+}
+
 // q rows of this warp's kv head (bf16 in shared memory) -> f16 fragments,
 // scaled by 2^e so that the largest |q| of the head group sits in [2^14, 2^15).
 template <int G>
@@ -137,8 +153,9 @@ __device__ __forceinline__ void load_q(HeadState &st, const uint8_t *qhead, floa
                                        int tq) {
   float qf[32];
   float qmax = 0.f;
-  if (gq < G) {
-    const uint8_t *qs = qhead + (gq * 128 + 32 * tq) * 2;
+  const int hq = slot_head<G>(gq);
+  if (hq >= 0) {
+    const uint8_t *qs = qhead + (hq * 128 + 32 * tq) * 2;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint4 w4 = lds128(qs + 16 * c);
@@ -212,7 +229,7 @@ __device__ __forceinline__ void tile_step(HeadState &st, const uint8_t *ks, cons
     s1[i] += s3[i];
   }
   // ---- online softmax for head gq over the 16 tokens (log2 domain)
-  const bool row_ok = gq < G;
+  const bool row_ok = slot_head<G>(gq) >= 0;
   const int t0 = 2 * tq, t1 = 8 + 2 * tq;
   const float x00 = (row_ok && t0 < ntok) ? s0[0] * st.qk_scale : -INFINITY;
   const float x01 = (row_ok && t0 + 1 < ntok) ? s0[1] * st.qk_scale : -INFINITY;
@@ -228,7 +245,7 @@ __device__ __forceinline__ void tile_step(HeadState &st, const uint8_t *ks, cons
       st.m_run = mx;
       st.l_run *= f;
     }
-    // O^T columns 2t and 2t+1 belong to heads whose rows live in lanes 8t, 8t+4
+    // O^T columns 2t and 2t+1 belong to the slots whose rows live in lanes 8t, 8t+4
     const float fa = __shfl_sync(0xffffffffu, f, 8 * tq);
     const float fb = __shfl_sync(0xffffffffu, f, 8 * tq + 4);
 #pragma unroll
@@ -239,13 +256,26 @@ __device__ __forceinline__ void tile_step(HeadState &st, const uint8_t *ks, cons
       st.o[i][3] *= fb;
     }
   }
-  const float p00 = x00 == -INFINITY ? 0.f : fast_exp2(x00 - st.m_run);
-  const float p01 = x01 == -INFINITY ? 0.f : fast_exp2(x01 - st.m_run);
-  const float p10 = x10 == -INFINITY ? 0.f : fast_exp2(x10 - st.m_run);
-  const float p11 = x11 == -INFINITY ? 0.f : fast_exp2(x11 - st.m_run);
+  // The weights are 2^(x - m_run) * kPScale: the same factor is in l_run, so
+  // it cancels (exactly: a power of two), and it puts the largest weight
+  // (1..2^8 under lazy rescaling) high in f16's range.  p = hi + lo in f16
+  // for p.v: one f16 alone leaves a relative error of 2^-11 per weight, which
+  // a short context with a large V value turns into more than the 1e-3
+  // tolerance; with the remainder the error is ~2^-22 relative (down to
+  // weights 2^-10 below the largest, below which lo is subnormal and the
+  // absolute error stays under 2^-25).
+  const float p00 = x00 == -INFINITY ? 0.f : fast_exp2(x00 - st.m_run) * kPScale;
+  const float p01 = x01 == -INFINITY ? 0.f : fast_exp2(x01 - st.m_run) * kPScale;
+  const float p10 = x10 == -INFINITY ? 0.f : fast_exp2(x10 - st.m_run) * kPScale;
+  const float p11 = x11 == -INFINITY ? 0.f : fast_exp2(x11 - st.m_run) * kPScale;
   st.l_run += (p00 + p01) + (p10 + p11);
-  const uint32_t pb0 = f32x2_to_f16x2(p00, p01);
-  const uint32_t pb1 = f32x2_to_f16x2(p10, p11);
+  const uint32_t ph0 = f32x2_to_f16x2(p00, p01), ph1 = f32x2_to_f16x2(p10, p11);
+  const float2 h0 = f16x2_to_f32x2(ph0), h1 = f16x2_to_f32x2(ph1);
+  const uint32_t pl0 = f32x2_to_f16x2(p00 - h0.x, p01 - h0.y);
+  const uint32_t pl1 = f32x2_to_f16x2(p10 - h1.x, p11 - h1.y);
+  // B operand of p.v: lane (g, t) supplies column g, the remainders in the
+  // copied slots (weights are 0 in slots without a head)
+  const uint32_t b0 = gq < G ? ph0 : pl0, b1 = gq < G ? ph1 : pl1;
 
   // ---- O^T += V^T P^T
   if (ntok < kTile) {  // tail: cached bytes past the sequence may be anything
@@ -262,8 +292,10 @@ __device__ __forceinline__ void tile_step(HeadState &st, const uint8_t *ks, cons
     const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes (a.b, b.b, a.b+1, b.b+1)
     const uint32_t x = prmt(wa[i >> 1], wb[i >> 1], sel);
     const uint32_t y = prmt(wc[i >> 1], wd[i >> 1], sel);
-    mma_16816(st.o[i], e4m3x2_to_f16x2(x & 0xFFFFu), e4m3x2_to_f16x2(x >> 16),
-              e4m3x2_to_f16x2(y & 0xFFFFu), e4m3x2_to_f16x2(y >> 16), pb0, pb1);
+    const uint32_t a0 = e4m3x2_to_f16x2(x & 0xFFFFu), a1 = e4m3x2_to_f16x2(x >> 16);
+    const uint32_t a2 = e4m3x2_to_f16x2(y & 0xFFFFu), a3 = e4m3x2_to_f16x2(y >> 16);
+    mma_16816(st.o[i], a0, a1, a2, a3, b0, b1);
+    if constexpr (2 * G > 8) mma_16816(st.o[i], a0, a1, a2, a3, pl0, pl1);
   }
 }
 
@@ -657,6 +689,19 @@ __global__ void __launch_bounds__(32 * (HG + 1))
     if (d0.z & kLast) {
       const int nparts = d0.w, pslot = d1.x, b = d1.z;
       const int kvh = (d1.w & 0xFFFF) * HG + warp;
+      if constexpr (!kBf16 && 2 * G <= 8) {  // add the p_lo columns G.. to columns 0..
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if constexpr (G == 1) {
+            hs.o[i][0] += hs.o[i][1];
+            hs.o[i][2] += hs.o[i][3];
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              hs.o[i][k] += __shfl_down_sync(0xffffffffu, hs.o[i][k], G / 2);
+          }
+        }
+      }
       hs.l_run += __shfl_xor_sync(0xffffffffu, hs.l_run, 1);
       hs.l_run += __shfl_xor_sync(0xffffffffu, hs.l_run, 2);
       // heads 2t and 2t+1 of the O^T columns: their m, l live in lanes 8t, 8t+4

@@ -263,11 +263,12 @@ def test_few_long_requests(kvq, dtype, lens):
 
 def test_workspace_reused_across_calls(kvq):
     """One workspace serves a mixed sequence of calls of different shapes
-    (every call's plan rewrites the per-call state: row counters, bad-page
-    flags, the list of rows merged across the GPU): rows merged by the combine
-    kernel (A), rows merged inside the split kernel with two aborted requests
-    and an out-of-pool page (B), and the head_dim-64 CUDA-core kernel (C),
-    each checked against the oracle, repeats bit-identical."""
+    (every call's plan rewrites the per-call state: bad-page flags, the two
+    lists of rows the combine kernel merges): rows of many parts, merged by a
+    combine CTA per output row (A), rows of a few parts, merged by a combine
+    warp per output row, with two aborted requests and an out-of-pool page
+    (B), and the head_dim-64 CUDA-core kernel (C), each checked against the
+    oracle, repeats bit-identical."""
     wa = inputs.uniform("reuseA", 71, B=2, ctx=9000, Hq=32, Hkv=8, D=128, P=16, outlier_frac=0.01)
     wa.ctx_lens = np.array([9000, 4100], dtype=np.int32)
     wb = inputs.uniform("reuseB", 72, B=64, ctx=1200, Hq=32, Hkv=8, D=128, P=16)
@@ -338,3 +339,57 @@ def test_combine_path_bad_page(kvq):
                                    sm_scale=w.sm_scale, rows=rows, nthreads=16)
     for b, h in rows:
         assert_close(got[b, h], want[b, h], f"row ({b},{h})")
+
+
+# The tensor-core split kernel schedules itself (before the plan kernel has
+# finished) for batches of up to 32 x (kv heads per group + 1) x 16 requests,
+# and takes the plan's schedule for larger ones: 1,024 requests when a group
+# is one kv head, 4,608 when it is eight.
+@pytest.mark.parametrize("Hkv,B", [(1, 1024), (1, 1100), (8, 4608), (8, 4700)],
+                         ids=["hg1_own_1024", "hg1_plan_1100", "hg8_own_4608", "hg8_plan_4700"])
+def test_schedule_at_and_past_the_own_scan_limit(kvq, Hkv, B):
+    """Short ragged requests (1-60 tokens) in numbers at and just past the
+    limit: sampled rows from the start, the end and around the boundary
+    requests match the oracle, and every other row is finite."""
+    w = inputs.ragged(seed=900 + B + Hkv, B=B, total=B * 25, lo=1, hi=60, Hq=4 * Hkv, Hkv=Hkv,
+                      D=128, P=16)
+    host = sorted({0, 1, 2, B // 2, 1023, 1024, B - 2, B - 1} & set(range(B)))
+    r = Run(w, host_requests=host)
+    r.fill_context()
+    q = r.append_step(0)
+    lens = w.seq_lens_after(0)
+    got = r.attend(q, lens)
+    assert r.err_word() == 0
+    assert np.isfinite(got).all()
+    rows = [(b, h) for b in host for h in range(w.Hq)]
+    ref, err = r.oracle_rows(q, lens, rows)
+    assert err == 0
+    for b, h in rows:
+        assert_close(got[b, h], ref[b, h], f"row ({b},{h})")
+
+
+def test_schedule_skips_runs_of_empty_and_aborted_requests(kvq):
+    """The split CTAs walk requests by their own lengths and abort flags:
+    runs of empty (L = 0) and aborted requests longer than 32, at the start,
+    in the middle and at the end of the batch, own no units; the rows between
+    them match the oracle and the skipped rows are zero."""
+    B = 200
+    w = inputs.uniform("skips", 91, B=B, ctx=600, Hq=32, Hkv=8, D=128, P=16)
+    real = list(range(50, 61)) + list(range(151, 160)) + [185]
+    r = Run(w, host_requests=real)
+    r.fill_context()
+    q = r.append_step(0)
+    lens = w.seq_lens_after(0).copy()
+    abort = np.zeros(B, dtype=np.uint8)
+    others = np.setdiff1d(np.arange(B), real)
+    lens[others[::2]] = 0          # empty
+    abort[others[1::2]] = 1        # aborted
+    lens[185] = 1                  # one token: its row is that token's V
+    got = r.attend(q, lens, abort=abort)
+    assert r.err_word() == 0
+    assert not got[others].any()
+    rows = [(b, h) for b in real for h in range(0, 32, 3)]
+    ref, err = r.oracle_rows(q, lens, rows, abort=abort)
+    assert err == 0
+    for b, h in rows:
+        assert_close(got[b, h], ref[b, h], f"row ({b},{h})")

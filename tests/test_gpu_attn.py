@@ -393,3 +393,53 @@ def test_schedule_skips_runs_of_empty_and_aborted_requests(kvq):
     assert err == 0
     for b, h in rows:
         assert_close(got[b, h], ref[b, h], f"row ({b},{h})")
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_softmax_weights_kept_to_fp32_accuracy(kvq, G):
+    """Two cached tokens whose scores differ by a fraction (weights that f16
+    cannot hold) and V rows of +100 and -100 r_d with r_d spanning 0.05..20
+    over the dims, so that in every head some output dims nearly cancel.
+    Rounding the weights to f16 alone would break the tolerance in every
+    head (checked here on the CPU from the oracle's dequantised cache); the
+    kernel, which carries each weight as f16 hi + lo (for G <= 4 through the
+    MMA's free head slots), matches the oracle everywhere."""
+    D, Hkv, L = 128, 2, 2
+    w = inputs.uniform("cancel", 95 + G, B=2, ctx=L, Hq=G * Hkv, Hkv=Hkv, D=D, P=16,
+                       outlier_frac=0.0)
+    r_d = np.exp(np.linspace(np.log(0.05), np.log(20.0), D))
+    k = np.zeros((L, Hkv, D), np.float32)
+    k[0], k[1] = 1.0, 1.5
+    v = np.zeros((L, Hkv, D), np.float32)
+    v[0], v[1] = 100.0, -100.0 * r_d
+    sources = [(_bf16_bits(k), _bf16_bits(v)) for _ in range(w.B)]
+    r = Run(w, sources=sources)
+    r.fill_context()
+    c = 0.05 + 0.0137 * np.arange(w.Hq)  # a score gap of 0.3 to 1.6 between the two tokens
+    q = _bf16_bits(np.broadcast_to(c[None, :, None], (w.B, w.Hq, D)))
+    lens = w.ctx_lens.astype(np.int32)
+    got = r.attend(q, lens)
+    assert r.err_word() == 0
+    rows = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+    ref, err = r.oracle_rows(q, lens, rows)
+    assert err == 0
+    for b, h in rows:
+        assert_close(got[b, h], ref[b, h], f"G={G} row ({b},{h})")
+    # the case is sensitive: f16 weights alone fail in every head
+    for b, h in rows:
+        g = h // G
+        pages = w.block_table[b, np.arange(L) // w.P]
+        slots = np.arange(L) % w.P
+        K = pins.torch_decode(r.hk[pages, g, slots, :]) * float(r.k_scale)
+        V = pins.torch_decode(r.hv[pages, g, slots, :]) * float(r.v_scale)
+        qf = (q[b, h].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        s = (K @ qf) * float(w.sm_scale)
+        p = 128.0 * np.exp(s - s.max())
+        o16 = (p.astype(np.float16).astype(np.float64) @ V) / p.sum()
+        assert (np.abs(o16 - ref[b, h]) > 1e-3 + 1e-3 * np.abs(ref[b, h])).any(), \
+            f"row ({b},{h}) does not distinguish f16 weights"

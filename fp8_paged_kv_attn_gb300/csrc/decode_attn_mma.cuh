@@ -299,6 +299,121 @@ __device__ __forceinline__ void tile_step(HeadState &st, const uint8_t *ks, cons
   }
 }
 
+
+// Two consecutive 16-token tiles of one segment in one pass: tile a (ksa /
+// vsa) is full, tile b holds ntok_b (1..16) valid tokens.  One softmax update
+// covers the 32 tokens, and q.k runs as eight independent chains of four.
+template <int G>
+__device__ __forceinline__ void tile_step2(HeadState &st, const uint8_t *ksa, const uint8_t *vsa,
+                                           const uint8_t *ksb, const uint8_t *vsb, int ntok_b,
+                                           int gq, int tq) {
+  const int c0 = ((2 * tq) ^ gq) * 16, c1 = ((2 * tq + 1) ^ gq) * 16;
+  uint32_t kw[4][8];  // [2 * tile + n-tile][word]: rows gq (n-tile 0) and 8 + gq (n-tile 1)
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint8_t *kr = (j < 2 ? ksa : ksb) + (gq + 8 * (j & 1)) * 128;
+    const uint4 x = lds128(kr + c0), y = lds128(kr + c1);
+    kw[j][0] = x.x;
+    kw[j][1] = x.y;
+    kw[j][2] = x.z;
+    kw[j][3] = x.w;
+    kw[j][4] = y.x;
+    kw[j][5] = y.y;
+    kw[j][6] = y.z;
+    kw[j][7] = y.w;
+  }
+  float sc[4][4], so[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[j][i] = so[j][i] = 0.f;
+#pragma unroll
+  for (int s = 0; s < 8; s += 2) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      mma_16816(sc[j], st.qa0[s], 0u, st.qa2[s], 0u, e4m3x2_to_f16x2(kw[j][s] & 0xFFFFu),
+                e4m3x2_to_f16x2(kw[j][s] >> 16));
+      mma_16816(so[j], st.qa0[s + 1], 0u, st.qa2[s + 1], 0u,
+                e4m3x2_to_f16x2(kw[j][s + 1] & 0xFFFFu), e4m3x2_to_f16x2(kw[j][s + 1] >> 16));
+    }
+  }
+  // ---- online softmax over the 32 tokens
+  const bool row_ok = slot_head<G>(gq) >= 0;
+  float x[4][2];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = 8 * (j & 1) + 2 * tq + e;  // token within its tile
+      const bool ok = row_ok && (j < 2 || t < ntok_b);
+      x[j][e] = ok ? (sc[j][e] + so[j][e]) * st.qk_scale : -INFINITY;
+      mx = fmaxf(mx, x[j][e]);
+    }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const bool grow = mx > st.m_run + kRescaleThreshold;
+  if (__any_sync(0xffffffffu, grow)) {
+    const float f = grow ? exp2f(st.m_run - mx) : 1.f;
+    if (grow) {
+      st.m_run = mx;
+      st.l_run *= f;
+    }
+    const float fa = __shfl_sync(0xffffffffu, f, 8 * tq);
+    const float fb = __shfl_sync(0xffffffffu, f, 8 * tq + 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      st.o[i][0] *= fa;
+      st.o[i][1] *= fb;
+      st.o[i][2] *= fa;
+      st.o[i][3] *= fb;
+    }
+  }
+  uint32_t bw[4], lw[4];  // B-operand words (hi or, in the copied slots, lo) and lo
+  float lsum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float p0 = x[j][0] == -INFINITY ? 0.f : fast_exp2(x[j][0] - st.m_run) * kPScale;
+    const float p1 = x[j][1] == -INFINITY ? 0.f : fast_exp2(x[j][1] - st.m_run) * kPScale;
+    lsum += p0 + p1;
+    const uint32_t ph = f32x2_to_f16x2(p0, p1);
+    const float2 h = f16x2_to_f32x2(ph);
+    const uint32_t pl = f32x2_to_f16x2(p0 - h.x, p1 - h.y);
+    bw[j] = gq < G ? ph : pl;
+    lw[j] = pl;
+  }
+  st.l_run += lsum;
+  // ---- O^T += V^T P^T for each tile
+#pragma unroll
+  for (int tb = 0; tb < 2; ++tb) {
+    const uint8_t *vr = (tb == 0 ? vsa : vsb) + (2 * tq) * 128;
+    uint4 va = lds128(vr + ((gq ^ (2 * tq)) * 16));
+    uint4 vb = lds128(vr + 128 + ((gq ^ (2 * tq + 1)) * 16));
+    uint4 vc = lds128(vr + 8 * 128 + ((gq ^ (2 * tq)) * 16));
+    uint4 vd = lds128(vr + 9 * 128 + ((gq ^ (2 * tq + 1)) * 16));
+    if (tb == 1 && ntok_b < kTile) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      const int t0 = 2 * tq, t1 = 8 + 2 * tq;
+      if (t0 >= ntok_b) va = z;
+      if (t0 + 1 >= ntok_b) vb = z;
+      if (t1 >= ntok_b) vc = z;
+      if (t1 + 1 >= ntok_b) vd = z;
+    }
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+    const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+      const uint32_t xx = prmt(wa[i >> 1], wb[i >> 1], sel);
+      const uint32_t yy = prmt(wc[i >> 1], wd[i >> 1], sel);
+      const uint32_t a0 = e4m3x2_to_f16x2(xx & 0xFFFFu), a1 = e4m3x2_to_f16x2(xx >> 16);
+      const uint32_t a2 = e4m3x2_to_f16x2(yy & 0xFFFFu), a3 = e4m3x2_to_f16x2(yy >> 16);
+      mma_16816(st.o[i], a0, a1, a2, a3, bw[2 * tb], bw[2 * tb + 1]);
+      if constexpr (2 * G > 8) mma_16816(st.o[i], a0, a1, a2, a3, lw[2 * tb], lw[2 * tb + 1]);
+    }
+  }
+}
+
 // bf16 query rows -> bf16 fragments (exact, no scaling); thread t supplies
 // dims 16t+4s.. of plane 0 (k-steps 0-3) and 64+16t+4(s-4).. (k-steps 4-7).
 template <int G>
@@ -640,9 +755,9 @@ __global__ void __launch_bounds__(32 * (HG + 1))
   while (true) {
     const int slot = g % NS;
     if (!ctl_wait(ctl, &ctl.full[slot], (g / NS) & 1, a.err_word)) break;
-    const int4 d0 = ctl.desc[slot][0];
+    int4 d0 = ctl.desc[slot][0];
     if (d0.x < 0) break;
-    const int4 d1 = ctl.desc[slot][1];
+    int4 d1 = ctl.desc[slot][1];
     const int ntok = d0.z & 0xFFFF;
     if (d0.z & kFirst) {
       const int qs = (d1.w >> 16) & 1;
@@ -655,7 +770,34 @@ __global__ void __launch_bounds__(32 * (HG + 1))
       if (lane == 0) mbar_arrive(&ctl.qempty[qs]);
       seg_bad = false;
     }
-    if constexpr (C::TILES == 1) {
+    bool paired = false;
+    if constexpr (!kBf16 && C::TILES == 1) {
+      // a stage that does not end its segment is full and followed by one of
+      // the same segment: take the two together when neither has a bad page
+      if (!(d0.z & (kLast | kBad))) {
+        const int slot2 = (g + 1) % NS;
+        if (!ctl_wait(ctl, &ctl.full[slot2], ((g + 1) / NS) & 1, a.err_word)) break;
+        const int4 e0 = ctl.desc[slot2][0];
+        if (!(e0.z & kBad)) {
+          tile_step2<G>(hs, kbuf + slot * C::KV_BYTES + warp * kPlane,
+                        vbuf + slot * C::KV_BYTES + warp * kPlane,
+                        kbuf + slot2 * C::KV_BYTES + warp * kPlane,
+                        vbuf + slot2 * C::KV_BYTES + warp * kPlane, e0.z & 0xFFFF, gq, tq);
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&ctl.empty[slot]);
+            mbar_arrive(&ctl.empty[slot2]);
+          }
+          d0 = e0;
+          d1 = ctl.desc[slot2][1];
+          ++g;
+          paired = true;
+        }
+      }
+    }
+    if (paired) {
+      // both stages done (and released) above
+    } else if constexpr (C::TILES == 1) {
       seg_bad |= (d0.z & kBad) != 0;
       if (!(d0.z & kBad)) {
         const uint8_t *kt = kbuf + slot * C::KV_BYTES + warp * kPlane;
@@ -683,8 +825,10 @@ __global__ void __launch_bounds__(32 * (HG + 1))
           tile_step<G>(hs, kt, vt, min(nt, kTile), gq, tq);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl.empty[slot]);
+    if (!paired) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.empty[slot]);
+    }
 
     if (d0.z & kLast) {
       const int nparts = d0.w, pslot = d1.x, b = d1.z;

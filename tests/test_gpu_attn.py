@@ -443,3 +443,31 @@ def test_softmax_weights_kept_to_fp32_accuracy(kvq, G):
         o16 = (p.astype(np.float16).astype(np.float64) @ V) / p.sum()
         assert (np.abs(o16 - ref[b, h]) > 1e-3 + 1e-3 * np.abs(ref[b, h])).any(), \
             f"row ({b},{h}) does not distinguish f16 weights"
+
+
+@pytest.mark.parametrize("G", [1, 8])
+def test_softmax_weights_bf16_cache(kvq, G):
+    """The cancellation case of test_softmax_weights_kept_to_fp32_accuracy on
+    the bf16-cache kernel (weights as bf16 hi + lo, about 16 significant
+    bits): every row matches the oracle."""
+    D, Hkv, L = 128, 2, 2
+    w = inputs.uniform("cancel_bf16", 97 + G, B=2, ctx=L, Hq=G * Hkv, Hkv=Hkv, D=D, P=16,
+                       outlier_frac=0.0)
+    r_d = np.exp(np.linspace(np.log(0.05), np.log(20.0), D))
+    k = np.zeros((L, Hkv, D), np.float32)
+    k[0], k[1] = 1.0, 1.5
+    v = np.zeros((L, Hkv, D), np.float32)
+    v[0], v[1] = 100.0, -100.0 * r_d
+    sources = [(_bf16_bits(k), _bf16_bits(v)) for _ in range(w.B)]
+    r = Run(w, kv_dtype=kvq.KV_BF16, sources=sources)
+    r.fill_context()
+    q = _bf16_bits(np.broadcast_to((0.05 + 0.0137 * np.arange(w.Hq))[None, :, None],
+                                   (w.B, w.Hq, D)))
+    lens = w.ctx_lens.astype(np.int32)
+    got = r.attend(q, lens)
+    assert r.err_word() == 0
+    rows = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+    ref, err = r.oracle_rows(q, lens, rows)
+    assert err == 0
+    for b, h in rows:
+        assert_close(got[b, h], ref[b, h], f"bf16 G={G} row ({b},{h})")

@@ -771,9 +771,11 @@ __global__ void __launch_bounds__(32 * (HG + 1))
       seg_bad = false;
     }
     bool paired = false;
-    if constexpr (!kBf16 && C::TILES == 1) {
+    if constexpr (!kBf16 && C::TILES == 1 && 2 * G > 8) {
       // a stage that does not end its segment is full and followed by one of
       // the same segment: take the two together when neither has a bad page
+      // (G = 8 only: its p.v runs two MMAs per tile, and the pair's shared
+      // softmax pays for them; for G <= 4 it measured 0-2% slower)
       if (!(d0.z & (kLast | kBad))) {
         const int slot2 = (g + 1) % NS;
         if (!ctl_wait(ctl, &ctl.full[slot2], ((g + 1) / NS) & 1, a.err_word)) break;

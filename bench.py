@@ -174,11 +174,22 @@ def measured_hbm_peak():
         return 6800.0, "fallback"
 
 
+def code_only(text: str) -> str:
+    """C++ source without its comments and with runs of whitespace collapsed,
+    so that a comment-only edit keeps the hash (the kernel sources hold no
+    string literal with // or /* in it)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def decode_source_sha() -> str:
+    """Hash of the decode-attention kernel sources (code only), which the
+    committed ncu traffic figure is tied to."""
     h = hashlib.sha256()
     for p in DECODE_KERNEL_SOURCES:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p)) as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

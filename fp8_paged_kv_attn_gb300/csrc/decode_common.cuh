@@ -130,8 +130,8 @@ struct SchedStart {
 // arrays before grid_dependency_wait() is safe because the plan kernel lets
 // this grid launch only after its own wait: by then everything ahead of the
 // plan on the stream (the tag check that wrote the mask, whatever wrote the
-// lengths) has completed.  Only what the plan itself writes (counters, the
-// merge list, zeroed rows) needs the wait.  Returns false, with nothing read,
+// lengths) has completed.  Only what the plan itself writes (bad-page flags,
+// the merge lists, zeroed rows) needs the wait.  Returns false, with nothing read,
 // when the batch is larger than NT x PER requests; the caller then waits and
 // takes the plan's schedule.  Every thread of the CTA calls it.
 template <int NT, int PER>

@@ -250,9 +250,9 @@ def test_full_integrity(kvq, oracle_mod):
                          ids=["one", "mix", "two", "six"])
 def test_few_long_requests(kvq, dtype, lens):
     """Few requests with long contexts: every row is split over many CTAs (25
-    to ~270 parts) and merged across the GPU by the combine kernel (rows with
-    at most 8 parts are merged inside the split kernel; that path is covered
-    by the other tests)."""
+    to ~270 parts) and merged by the combine kernel's CTA-per-row path (rows
+    of at most 8 parts take its warp-per-row path; that one is covered by
+    the other tests)."""
     B = len(lens)
     w = inputs.uniform("few", 50 + B, B=B, ctx=max(lens), Hq=32, Hkv=8, D=128, P=16,
                        outlier_frac=0.01)

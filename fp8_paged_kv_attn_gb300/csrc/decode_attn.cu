@@ -352,8 +352,11 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
 
     const uint8_t *ks = kbuf + slot * C::KV_BYTES;
     const uint8_t *vs = vbuf + slot * C::KV_BYTES;
+    // a stage with a page outside the pool holds stale bytes where that page
+    // would be: its row is written as zeros, so its math is skipped
+    const int c_end = (d0.z & kBad) ? 0 : C::ITERS;
 #pragma unroll
-    for (int c0 = 0; c0 < C::ITERS; c0 += C::CI) {
+    for (int c0 = 0; c0 < c_end; c0 += C::CI) {
       float sc[C::CI][G];
 #pragma unroll
       for (int ci = 0; ci < C::CI; ++ci) {
@@ -594,9 +597,12 @@ __global__ void __launch_bounds__(kCombineThreads, kMinBlocks) combine_kernel(Co
         o.z = fmaf(wi, v.z, o.z);
         o.w = fmaf(wi, v.w, o.w);
       }
-      const float sc = row_bad ? 0.f : a.v_scale / d;
+      const float sc = a.v_scale / d;
+      // a bad row is stored as zeros, not scaled by 0: its parts may hold
+      // values computed from a stage whose page was never copied
       reinterpret_cast<float4 *>(it.out)[lane] =
-          make_float4(o.x * sc, o.y * sc, o.z * sc, o.w * sc);
+          row_bad ? make_float4(0.f, 0.f, 0.f, 0.f)
+                  : make_float4(o.x * sc, o.y * sc, o.z * sc, o.w * sc);
     }
     __syncthreads();  // s_acc, s_m, s_den are reused by the next item
   }
@@ -611,9 +617,10 @@ __global__ void __launch_bounds__(kCombineThreads, kMinBlocks) combine_kernel(Co
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     merge_parts<kWarpBatch>(it, 0, 1, slot32, GD, a.G, a.D, lane, active, M, den, acc);
     if (active) {
-      const float sc = row_bad ? 0.f : a.v_scale / den;
+      const float sc = a.v_scale / den;
       reinterpret_cast<float4 *>(it.out)[lane] =
-          make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+          row_bad ? make_float4(0.f, 0.f, 0.f, 0.f)
+                  : make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
     }
   }
 }

@@ -459,9 +459,7 @@ struct CombineArgs {
   float v_scale;
 };
 
-constexpr int kCombineSubsets = 16;  // part subsets per combine CTA (32 lanes each)
-constexpr int kWarpBatch = 4;        // parts loaded at once by a warp-merged row
-constexpr int kCombineThreads = 32 * kCombineSubsets;
+constexpr int kWarpBatch = 4;  // parts loaded at once by a warp-merged row
 
 // One output row (query head hr of a listed row) and where its parts live.
 struct CombineItem {
@@ -536,11 +534,14 @@ __device__ __forceinline__ void merge_parts(const CombineItem &it, int p0, int s
 //  - longer rows (a row of a short batch can have hundreds of parts): a CTA
 //    per output row, its 16 warps folding every 16th part each, then warp 0
 //    folding the 16 results from shared memory.
-// With nothing listed it exits after reading the two counts.  kMinBlocks = 2
-// caps the registers so that a grid of 2 x #SMs runs in one wave; a grid of
-// at most #SMs CTAs runs the uncapped build, which loads 8 parts at a time.
-template <int kMinBlocks>
-__global__ void __launch_bounds__(kCombineThreads, kMinBlocks) combine_kernel(CombineArgs a) {
+// With nothing listed it exits after reading the two counts.  Two builds:
+// kSubsets = 16 warps uncapped (more of a long row's loads in flight) for
+// grids of at most #SMs CTAs, and 8 warps capped at 64 registers (4 CTAs per
+// SM) otherwise, small enough that one CTA becomes resident beside a running
+// split CTA and is waiting when the split grid ends.
+template <int kMinBlocks, int kSubsets>
+__global__ void __launch_bounds__(32 * kSubsets, kMinBlocks) combine_kernel(CombineArgs a) {
+  constexpr int kCombineSubsets = kSubsets;  // part subsets (warps) per CTA
   __shared__ float s_m[kCombineSubsets], s_den[kCombineSubsets];
   __shared__ float4 s_acc[kCombineSubsets][32];
   grid_dependency_wait();
@@ -875,9 +876,11 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   CombineArgs ca{hdr, bad, comb, combw, part, out, B, Hq, Hkv, G, D, sk.hg, Hkv / sk.hg,
                  fp8 ? cache->v_scale : 1.0f};
   const int crows = B * Hq;
-  const int cgrid = crows < 2 * sms ? crows : 2 * sms;
-  if (launch_dependent(cgrid <= sms ? combine_kernel<1> : combine_kernel<2>, cgrid,
-                       kCombineThreads, 0, s, ca) != cudaSuccess)
-    return KVQ_ERR_CUDA;
+  cudaError_t ce;
+  if (crows <= sms)
+    ce = launch_dependent(combine_kernel<1, 16>, crows, 512, 0, s, ca);
+  else
+    ce = launch_dependent(combine_kernel<4, 8>, crows < 4 * sms ? crows : 4 * sms, 256, 0, s, ca);
+  if (ce != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

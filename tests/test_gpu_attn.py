@@ -320,21 +320,25 @@ def test_workspace_reused_across_calls(kvq):
             first[name] = got
 
 
-def test_combine_path_bad_page(kvq):
-    """Rows of ~25 parts, merged by the combine kernel, with an out-of-pool
-    page in request 2: that request's rows are zero, the page error is
-    raised, the other requests match the oracle."""
-    w = inputs.uniform("warpbad", 81, B=6, ctx=4000, Hq=32, Hkv=8, D=128, P=16)
+@pytest.mark.parametrize("G,page", [(4, 100), (8, 100), (8, 101)],
+                         ids=["g4_p100", "g8_p100", "g8_p101"])
+def test_combine_path_bad_page(kvq, G, page):
+    """Rows split over many CTAs, merged by the combine kernel, with an
+    out-of-pool page in request 2 (for G = 8, whose consumers take two stages
+    per step, at two neighbouring pages, so that it falls in either stage of
+    a pair): that request's rows are zero, the page error is raised, the
+    other requests match the oracle."""
+    w = inputs.uniform("warpbad", 81 + G, B=6, ctx=4000, Hq=8 * G, Hkv=8, D=128, P=16)
     r = Run(w, host_requests=[0, 2, 5])
     r.fill_context()
     q = r.append_step(0)
     lens = w.seq_lens_after(0)
     bt = w.block_table.copy()
-    bt[2, 100] = -3
+    bt[2, page] = -3
     got = r.attend(q, lens, bt=dev(bt))
     assert r.err_word() == kvq.ERRBIT_PAGE
     assert not got[2].any()
-    rows = [(b, h) for b in (0, 5) for h in range(0, 32, 3)]
+    rows = [(b, h) for b in (0, 5) for h in range(0, w.Hq, 3)]
     want, err = oracle.decode_attn(oracle.KV_E4M3, r.hk, r.hv, r.k_scale, r.v_scale, q, bt, lens,
                                    sm_scale=w.sm_scale, rows=rows, nthreads=16)
     for b, h in rows:

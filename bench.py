@@ -120,18 +120,31 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
+        """Starts sampling every period_ms and returns once the sampler has
+        written its first line, so that the timed region that follows is
+        covered; samples written before that point are not counted."""
         self.proc = None
+        self.skip = 0
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            with open(self.path) as f:
+                n = sum(1 for _ in f)
+            if n > 0:
+                self.skip = n
+                break
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is None:
@@ -143,7 +156,9 @@ class ClockSampler:
             self.proc.kill()
         self.f.close()
         rows = []
-        for line in open(self.path):
+        for i, line in enumerate(open(self.path)):
+            if i < self.skip:  # written before the timed region began
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue

@@ -858,6 +858,8 @@ __global__ void __launch_bounds__(32 * (HG + 1))
       const int ha = 2 * tq, hb = 2 * tq + 1;
       float *out = a.out + (static_cast<int64_t>(b) * a.Hq + kvh * G) * C::D;
       if (nparts == 1) {
+        // a row with a page outside the pool is stored as zeros, selected
+        // rather than scaled by 0: its other pages may hold NaN codes
         const float sa = seg_bad ? 0.f : a.v_scale / la;
         const float sb = seg_bad ? 0.f : a.v_scale / lb;
 #pragma unroll
@@ -866,18 +868,18 @@ __global__ void __launch_bounds__(32 * (HG + 1))
           if constexpr (!kBf16) {  // dims dl, dl+1: one 8-byte store
             if (ha < G)
               *reinterpret_cast<float2 *>(out + ha * C::D + dl) =
-                  make_float2(hs.o[i][0] * sa, hs.o[i][2] * sa);
+                  seg_bad ? make_float2(0.f, 0.f) : make_float2(hs.o[i][0] * sa, hs.o[i][2] * sa);
             if (hb < G)
               *reinterpret_cast<float2 *>(out + hb * C::D + dl) =
-                  make_float2(hs.o[i][1] * sb, hs.o[i][3] * sb);
+                  seg_bad ? make_float2(0.f, 0.f) : make_float2(hs.o[i][1] * sb, hs.o[i][3] * sb);
           } else {
             if (ha < G) {
-              out[ha * C::D + dl] = hs.o[i][0] * sa;
-              out[ha * C::D + dh] = hs.o[i][2] * sa;
+              out[ha * C::D + dl] = seg_bad ? 0.f : hs.o[i][0] * sa;
+              out[ha * C::D + dh] = seg_bad ? 0.f : hs.o[i][2] * sa;
             }
             if (hb < G) {
-              out[hb * C::D + dl] = hs.o[i][1] * sb;
-              out[hb * C::D + dh] = hs.o[i][3] * sb;
+              out[hb * C::D + dl] = seg_bad ? 0.f : hs.o[i][1] * sb;
+              out[hb * C::D + dh] = seg_bad ? 0.f : hs.o[i][3] * sb;
             }
           }
         }

@@ -475,3 +475,34 @@ def test_softmax_weights_bf16_cache(kvq, G):
     assert err == 0
     for b, h in rows:
         assert_close(got[b, h], ref[b, h], f"bf16 G={G} row ({b},{h})")
+
+
+def test_bad_page_rows_are_zero_even_with_nan_codes(kvq):
+    """A request with a page outside the pool is written as zeros, including
+    when its other pages hold NaN codes (0x7F), for a row held by one CTA
+    (short request) and for a row split across CTAs (long request); the
+    other requests match the oracle."""
+    B = 120
+    w = inputs.uniform("badnan", 93, B=B, ctx=3000, Hq=32, Hkv=8, D=128, P=16)
+    lens = np.full(B, 40, dtype=np.int32)  # short rows: most are held by one CTA
+    lens[7] = 3000                          # a long row, split across CTAs
+    w.ctx_lens = lens.copy()
+    good = [0, 6, 8, 119]
+    r = Run(w, host_requests=good)
+    r.fill_context()
+    bt = w.block_table.copy()
+    for b_bad, page_bad, page_nan in ((3, 1, 0), (7, 100, 5)):
+        bt[b_bad, page_bad] = w.num_pages + 5
+        p = int(w.block_table[b_bad, page_nan])
+        r.cache.k_pool.view(torch.uint8)[p, :, 3, :] = 0x7F
+        r.cache.v_pool.view(torch.uint8)[p, :, 3, :] = 0x7F
+    q, *_ = w.step_inputs(0)
+    got = r.attend(q, lens, bt=dev(bt))
+    assert r.err_word() == kvq.ERRBIT_PAGE
+    for b_bad in (3, 7):
+        assert np.array_equal(got[b_bad], np.zeros_like(got[b_bad])), f"request {b_bad}"
+    rows = [(b, h) for b in good for h in range(0, 32, 3)]
+    want, err = oracle.decode_attn(oracle.KV_E4M3, r.hk, r.hv, r.k_scale, r.v_scale, q, bt, lens,
+                                   sm_scale=w.sm_scale, rows=rows, nthreads=16)
+    for b, h in rows:
+        assert_close(got[b, h], want[b, h], f"row ({b},{h})")

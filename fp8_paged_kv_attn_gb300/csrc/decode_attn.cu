@@ -42,6 +42,7 @@
 // Every wait is bounded (see mbar_wait); a wait that gives up raises
 // KVQ_ERRBIT_TIMEOUT and the CTA leaves its loop.
 #include <cfloat>
+#include <mutex>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -716,8 +717,10 @@ int split_ctas_per_sm(const SplitKernel &k) {
   static int cache_dev_fn[kMaxDev][kMaxFn];
   static const void *fns[kMaxFn];
   static int nfns = 0;
+  static std::mutex mu;  // calls may come from several host threads
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  std::lock_guard<std::mutex> lock(mu);
   const void *f = k.ptr();
   int fi = -1;
   for (int i = 0; i < nfns; ++i)
@@ -748,15 +751,16 @@ int split_ctas_per_sm(const SplitKernel &k) {
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // against libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  // looked up once, thread-safely (a function-local static's initialiser)
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 

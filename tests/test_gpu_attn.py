@@ -506,3 +506,42 @@ def test_bad_page_rows_are_zero_even_with_nan_codes(kvq):
                                    sm_scale=w.sm_scale, rows=rows, nthreads=16)
     for b, h in rows:
         assert_close(got[b, h], want[b, h], f"row ({b},{h})")
+
+
+def test_concurrent_calls_from_host_threads(kvq):
+    """Four host threads call kvq_decode_attn at once (ctypes releases the
+    GIL), each on its own stream with its own workspace and output, for a
+    shape whose kernels this process has not launched yet (the first call
+    sets up the kernel and caches its occupancy); every result equals a
+    single-threaded call's, bit for bit."""
+    import threading
+    w = inputs.uniform("threads", 99, B=5, ctx=2500, Hq=16, Hkv=8, D=128, P=16)
+    r = Run(w, kv_dtype=kvq.KV_BF16, host_requests=[0])
+    r.fill_context()
+    q, *_ = w.step_inputs(0)
+    lens = w.ctx_lens.astype(np.int32)
+    qd, ld = dev_bf16(q), dev(lens)
+    outs, errs = [None] * 4, []
+
+    def run(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                ws = kvq.workspace(w.B, w.Hq, w.Hkv, w.D)
+                out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device="cuda")
+                for _ in range(3):
+                    kvq.kvq_decode_attn(r.cache, qd, r.bt, ld, out, ws, sm_scale=float(w.sm_scale))
+            s.synchronize()
+            outs[i] = out.cpu().numpy()
+        except Exception as e:  # reported below
+            errs.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errs, errs
+    ref = r.attend(q, lens)
+    for i in range(4):
+        assert np.array_equal(outs[i], ref), f"thread {i}"

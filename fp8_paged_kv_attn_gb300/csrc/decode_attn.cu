@@ -706,7 +706,6 @@ bool pick_g(int G, SplitKernel *k) {
 bool pick_split(int D, int G, int Hkv, bool fp8, SplitKernel *k) {
   if (D == 128) return fp8 ? pick_hg_g<false>(G, Hkv, k) : pick_hg_g<true>(G, Hkv, k);
   if (D == 64) return fp8 ? pick_g<64, true>(G, k) : pick_g<64, false>(G, k);
-  if (D == 128) return fp8 ? pick_g<128, true>(G, k) : pick_g<128, false>(G, k);
   return false;
 }
 

@@ -13,16 +13,18 @@
 // process exits.
 //
 // The array's host-side name is only a stand-in for the device symbol, so its
-// device address is looked up once per device with cudaGetSymbolAddress, with
-// that device current, on the first call made on it; that first call on a
-// device should therefore come before any stream capture.  Every call then shares
-// the same array and it keeps the previous call's contents: the plan kernel
-// rewrites everything the attention kernels read before they read it, so
-// stale contents are harmless, but two calls whose kernels overlap on the GPU
+// device address is looked up with cudaGetSymbolAddress, with the caller's
+// device current, on every call.  The lookup is a host-side query once the
+// library's device code is loaded on that device; the first call on a device
+// may load it, so that first call should come before any stream capture.
+// Looking the address up each time (rather than caching it) keeps the call
+// correct after the primary context is destroyed and re-created
+// (cudaDeviceReset), when the array can move.  Every call shares the same
+// array and it keeps the previous call's contents: the plan kernel rewrites
+// everything the attention kernels read before they read it, so stale
+// contents are harmless, but two calls whose kernels overlap on the GPU
 // (different streams, or different host threads) race on the array and must
 // not be issued.
-#include <mutex>
-
 #include "kvq_internal.h"
 
 namespace {
@@ -30,21 +32,11 @@ namespace {
 constexpr size_t kStaticScratchBytes = KVQ_STATIC_SCRATCH_BYTES;
 static __device__ __align__(256) uint8_t g_kvq_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices];
-std::mutex g_scratch_mutex;
-
-// Device address of the scratch array on the current device (looked up once).
+// Device address of the scratch array on the current device.
 kvq_status scratch_on_current_device(void **ptr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_kvq_scratch) != cudaSuccess || !p) return KVQ_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *ptr = g_scratch_ptr[dev];
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_kvq_scratch) != cudaSuccess || !p) return KVQ_ERR_CUDA;
+  *ptr = p;
   return KVQ_OK;
 }
 

@@ -177,9 +177,11 @@ KVQ_API kvq_status kvq_pages_update(int32_t *free_stack, int32_t *free_count, ui
  *   KVQ_W_E4M3: w uint8 e4m3 codes [N][K]; scales fp32 [N]:
  *     W[n][k] = e4m3(w[n][k]) * scales[n].
  * Products are exact and sums fp32 (split over k: the order of the partial
- * sums varies from run to run); x is rounded to f16 for the products, which
- * is exact for |x| in [2^-14, 65504].  Supported: 1 <= M <= 64, K a multiple of
- * 128.  w and x 16-byte aligned, scales 4-byte aligned. */
+ * sums varies from run to run).  Any bf16 x is accepted: each token's values
+ * are scaled by a power of two for the products (exact for every value down
+ * to 2^-32 of the token's largest finite |x| in a k range, smaller ones are
+ * rounded to 2^-25 of it); NaN and inf propagate.  Supported: 1 <= M <= 64,
+ * K a multiple of 128.  w and x 16-byte aligned, scales 4-byte aligned. */
 KVQ_API kvq_status kvq_wq_gemm(int32_t w_dtype, const void *w, const void *scales, const void *x,
                                float *y, int32_t M, int32_t N, int32_t K, kvq_stream_t stream);
 
@@ -222,9 +224,10 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int32_
  * that loads it, until exit).  It allocates nothing.
  * - Shapes whose kvq_decode_attn_workspace_size() exceeds
  *   KVQ_STATIC_SCRATCH_BYTES return KVQ_ERR_WORKSPACE before any launch.
- * - The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, that device current); make that first call before
- *   any stream capture.
+ * - Every call looks up the array's device address on the current device
+ *   (cudaGetSymbolAddress), so the call stays valid after a device reset; the
+ *   first call on a device may load the library's device code there, so make
+ *   that first call before any stream capture.
  * - All calls share the one array: calls whose kernels can overlap on the GPU
  *   (different streams or host threads without ordering) race and must not be
  *   issued.  Stale contents from an earlier call are harmless. */

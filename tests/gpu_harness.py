@@ -116,6 +116,14 @@ class Run:
         q, k_new, v_new, req, pos = self.w.step_inputs(step)
         kvq.kvq_append(self.cache, dev_bf16(k_new), dev_bf16(v_new), dev(req), dev(pos), self.bt,
                        err_word=self.err)
+        self.oracle_append_step(step)
+        return q
+
+    def oracle_append_step(self, step: int):
+        """The oracle's side of decode step `step`'s append (host requests
+        only); the GPU side is whatever ran the step (an eager call or a
+        replayed graph)."""
+        q, k_new, v_new, req, pos = self.w.step_inputs(step)
         sel = np.array(self.host_requests, dtype=np.int64)
         e = oracle.quant_append(self.oracle_dtype, self.hk, self.hv, self.k_scale, self.v_scale,
                                 k_new[sel], v_new[sel], req[sel], pos[sel], self.w.block_table)

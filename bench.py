@@ -25,11 +25,13 @@ collective on the data path); value = all ranks' tokens / max rank time.
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -42,7 +44,7 @@ DECODE_KERNEL_SOURCES = ["fp8_paged_kv_attn_gb300/csrc/decode_attn.cu",
                          "fp8_paged_kv_attn_gb300/csrc/decode_attn_mma.cuh",
                          "fp8_paged_kv_attn_gb300/csrc/decode_common.cuh",
                          "fp8_paged_kv_attn_gb300/csrc/kvq_device.cuh"]
-TRAFFIC_PROFILE = "profiles/decode_attn_sweep_b64.md"
+TRAFFIC_PROFILE = "profiles/decode_attn_sweep_b64.json"
 
 
 def parse_args():
@@ -72,6 +74,19 @@ def parse_args():
                     help="--workload wq: one token count instead of 1, 8, 16, 32, 64")
     ap.add_argument("--wq-w", choices=["int4", "e4m3", "both"], default="both",
                     help="--workload wq: which weight format")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the 8x8192, integrity and ragged workloads in the "
+                         "default run")
+    ap.add_argument("--config-steps", type=int, default=50,
+                    help="timed steps of each of those workloads in the default run")
+    ap.add_argument("--config-warmup", type=int, default=5)
+    ap.add_argument("--sustain-s", type=float, default=1.0,
+                    help="seconds of back-to-back graph steps after the timed region (clock "
+                         "record under steady load); 0 turns it off")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the raw nvidia-smi clock samples in this file")
+    ap.add_argument("--no-parity-check", action="store_true",
+                    help="skip comparing sampled rows of the last timed step with the oracle")
     ap.add_argument("--sweep", action="store_true",
                     help="concurrency sweep 1/8/16/32/64 requests, e4m3 and bf16 KV at equal pool "
                          "bytes; one JSON line per point (not the headline line)")
@@ -116,19 +131,27 @@ def dist_barrier(dist):
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of SM clock, utilisation, power and throttle
+    reasons while the GPU measurements run.  The samples go to a temporary
+    file (or `path`); the summary counts a sample as under load when the GPU
+    reported at least 50% utilisation."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 20):
+    def __init__(self, gpu_index: int, period_ms: int = 20, path=None):
         """Starts sampling every period_ms and returns once the sampler has
-        written its first line, so that the timed region that follows is
+        written its first line, so that the measurements that follow are
         covered; samples written before that point are not counted."""
         self.proc = None
         self.skip = 0
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.keep = path is not None
+        if path is None:
+            fd, path = tempfile.mkstemp(prefix=f"kvq_clocks_{gpu_index}_", suffix=".csv")
+            os.close(fd)
+        self.path = path
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
@@ -156,24 +179,31 @@ class ClockSampler:
             self.proc.kill()
         self.f.close()
         rows = []
-        for i, line in enumerate(open(self.path)):
-            if i < self.skip:  # written before the timed region began
+        with open(self.path) as f:
+            lines = f.readlines()
+        if not self.keep:
+            os.unlink(self.path)
+        for i, line in enumerate(lines):
+            if i < self.skip:  # written before the measurements began
                 continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                util = float(parts[4])
+                rows.append((float(parts[1]), float(parts[2]), util, float(parts[3]), parts[5:9]))
             except ValueError:
                 continue
         if not rows:
             return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+        loaded = [r for r in rows if r[2] >= 50.0]
+        use = loaded if loaded else rows
+        reasons = sorted({self.REASONS[i] for r in use for i, v in enumerate(r[4])
                           if v.lower().startswith("active")})
-        return {"sm_mhz": statistics.median(r[0] for r in rows),
+        return {"sm_mhz": statistics.median(r[0] for r in use),
                 "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r[3] for r in use)}
 
 
 # ----------------------------------------------------------------------------
@@ -209,17 +239,16 @@ def decode_source_sha() -> str:
 
 
 def profiled_traffic():
-    """DRAM bytes per decode-attention call from the committed ncu summary,
+    """DRAM bytes per decode-attention call from the committed ncu figure,
     only if it was taken on the current kernel source."""
     try:
-        text = open(os.path.join(ROOT, TRAFFIC_PROFILE)).read()
-    except OSError:
+        with open(os.path.join(ROOT, TRAFFIC_PROFILE)) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
-    tr = re.search(r"traffic_bytes_per_call:\s*([0-9.eE+]+)", text)
-    if not sha or not tr or sha.group(1) != decode_source_sha():
+    if rec.get("source_sha256_16") != decode_source_sha():
         return None
-    return float(tr.group(1))
+    return float(rec["traffic_bytes_per_call"])
 
 
 def attn_bytes(lens, Hq, Hkv, D, P, es):
@@ -453,6 +482,7 @@ def run_gpu(args, dist, rank, world, local):
         kvq.kvq_append(cache, bf16(k).cuda(), bf16(v).cuda(), torch.from_numpy(req).cuda(),
                        torch.from_numpy(pos).cuda(), bt, err_word=err)
     torch.cuda.synchronize()
+    kept_sources = {b: sources[b] for b in spot_check_requests(B)}
     del sources
 
     # --- per-step inputs, packed one row per step (device resident for the
@@ -484,6 +514,16 @@ def run_gpu(args, dist, rank, world, local):
                       check=check, tags=tags, exp_tags=exp_tags, mask=mask if check else None,
                       graph=graph)
 
+    # the other decode workloads, set up before the measurements start (their
+    # host-side set-up would otherwise leave the GPU idle inside them)
+    extras = []
+    if rank == 0 and world == 1 and not args.no_configs:
+        for name in ("8x8192", "integrity", "ragged"):
+            extras.append(WorkloadStep(torch, kvq, name, args.seed,
+                                       args.config_warmup + args.config_steps,
+                                       eager=args.eager))
+        torch.cuda.synchronize()
+
     for i in range(args.warmup):
         step.eager(packer.views(d_rows[i]))
     if graph:
@@ -492,9 +532,9 @@ def run_gpu(args, dist, rank, world, local):
         step.run(last)  # first replay (graph upload) outside the timed region
     torch.cuda.synchronize()
 
-    def pairs():
+    def pairs(n=args.steps):
         return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
+                for _ in range(n)]
 
     # a step's KV smaller than 2 x L2 would stay cached from step to step:
     # then L2 is flushed before every timed step and each step is timed alone
@@ -505,7 +545,10 @@ def run_gpu(args, dist, rank, world, local):
     t_end = torch.cuda.Event(enable_timing=True)
     dist_barrier(dist)
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
+    # clocks are sampled over every GPU measurement below: the timed steps,
+    # the attention replays, the end-to-end loop, the sustained loop and the
+    # other workloads
+    clocks = ClockSampler(local, path=args.clocks_csv)
     torch.cuda.nvtx.range_push("timed")
     t_start.record(stream)
     for j in range(args.steps):
@@ -531,7 +574,8 @@ def run_gpu(args, dist, rank, world, local):
             step.run_attn_timed(d_rows[args.warmup + j], attn_ev[j], stream)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
-    clk = clocks.stop()
+    # the last timed step's output and abort mask, kept for the oracle check
+    last_result = result_buf.clone()
     dist_barrier(dist)
     if flush is None:
         elapsed_ms = t_start.elapsed_time(t_end)
@@ -578,6 +622,37 @@ def run_gpu(args, dist, rank, world, local):
         e2e_ms = dist_max(dist, e2e_ms)
         e2e = {"value": round(world * B * args.steps / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    # --- sustained: the same steps replayed back to back for about
+    # args.sustain_s seconds (cycling over the timed steps' inputs), so that
+    # the clock record covers a steady load, not only the short timed region
+    sustained = None
+    if args.sustain_s > 0 and graph:
+        n = max(1, int(math.ceil(args.sustain_s / (elapsed_ms * 1e-3 / args.steps))))
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for j in range(n):
+            if flush is not None:
+                flush()
+            step.run(d_rows[args.warmup + j % args.steps])
+        s1.record(stream)
+        torch.cuda.synchronize()
+        sms = s0.elapsed_time(s1)
+        sustained = {"steps": n, "ms": round(sms, 2), "ms_per_step": round(sms / n, 5),
+                     "tokens_per_s": round(B * n / (sms * 1e-3), 1),
+                     "l2": "flushed before every step (flush time included)"
+                           if flush is not None else "no flush"}
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item()):#x}")
+
+    # --- the other decode workloads, each timed in this process
+    configs = {}
+    for x in extras:
+        configs[x.name] = x.time(args.config_warmup, args.config_steps)
+    clk = clocks.stop()
+    del extras
 
     value = world * B * args.steps / (elapsed_ms * 1e-3)
     ctx_mean = float(np.mean([host_len[args.warmup + j].mean() for j in range(args.steps)]))
@@ -631,6 +706,15 @@ def run_gpu(args, dist, rank, world, local):
     }
     if e2e is not None:
         result["e2e"] = e2e
+    if sustained is not None:
+        result["sustained"] = sustained
+    if configs:
+        result["configs"] = configs
+    if rank == 0 and not args.no_parity_check:
+        result["parity_check"] = oracle_spot_check(
+            args, w, ks, vs, kv_bytes, kept_sources, packer, h_rows, gen, host_len,
+            last_result[:out_bytes].view(torch.float32).view(B, Hq, D).cpu().numpy(),
+            last_result[out_bytes:].cpu().numpy())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args, w, ks, vs, args.cpu_seconds)
     return result
@@ -668,6 +752,69 @@ class OracleRequestStep:
                                  self.bt1, lens, abort_mask=mask, sm_scale=w.sm_scale,
                                  nthreads=nthreads)
         return out
+
+
+def spot_check_requests(B):
+    """Requests whose output rows the default run checks against the oracle."""
+    return sorted({0, B // 2, B - 1})
+
+
+def _bf16_bits(t):
+    return t.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+
+
+def oracle_spot_check(args, w, ks, vs, kv_bytes, sources, packer, h_rows, gen, host_len,
+                      out_last, mask_last):
+    """Every output row of a few requests after the last timed step, against
+    the CPU oracle (fp64), and the whole abort mask, bit for bit.  The oracle's
+    pools hold those requests' prompts and every token the run appended for
+    them, in the run's order (warm-up steps, then the timed steps); the last
+    step's q, lengths and tags give the expected rows.  A mismatch fails the
+    run."""
+    import oracle
+    reqs = sorted(sources)
+    sel = np.array(reqs, dtype=np.int32)
+    dt = oracle.KV_E4M3 if kv_bytes == 1 else oracle.KV_BF16
+    shape = w.pool_shape()
+    hk = np.zeros(shape, dtype=np.uint8 if kv_bytes == 1 else np.uint16)
+    hv = np.zeros_like(hk)
+    for b in reqs:
+        k, v = sources[b]
+        req, pos = w.context_tokens(b)
+        if oracle.quant_append(dt, hk, hv, ks, vs, k, v, req, pos, w.block_table) != 0:
+            raise RuntimeError("oracle append of the prompt failed")
+    n_run = args.warmup + args.steps
+    for i in range(n_run):
+        f = packer.views(h_rows[i])
+        kb, vb = _bf16_bits(f["k"]), _bf16_bits(f["v"])
+        pos = f["pos"].numpy()
+        if oracle.quant_append(dt, hk, hv, ks, vs, np.ascontiguousarray(kb[sel]),
+                               np.ascontiguousarray(vb[sel]), sel,
+                               np.ascontiguousarray(pos[sel]), w.block_table) != 0:
+            raise RuntimeError("oracle append of a step failed")
+    last = packer.views(h_rows[n_run - 1])
+    q = _bf16_bits(last["q"])
+    lens = last["lens"].numpy().copy()
+    check = args.check == "on"
+    ref_mask = oracle.check_tags(w.block_table, lens, w.P, w.page_tags, w.expected_tags) \
+        if check else np.zeros(w.B, dtype=np.uint8)
+    mask_ok = (not check) or bool(np.array_equal(mask_last, ref_mask))
+    rows = [(b, h) for b in reqs for h in range(w.Hq)]
+    ref, oerr = oracle.decode_attn(dt, hk, hv, ks, vs, q, w.block_table, lens,
+                                   abort_mask=ref_mask, sm_scale=w.sm_scale, rows=rows,
+                                   nthreads=oracle_threads())
+    got = out_last[sel].astype(np.float64)
+    exp = ref[sel].astype(np.float64)
+    err = np.abs(got - exp)
+    tol = 1e-3 + 1e-3 * np.abs(exp)
+    worst = float(np.max(err / tol))
+    res = {"requests": reqs, "rows": len(rows), "step_generated_token": int(gen[n_run - 1]),
+           "context": [int(lens[b]) for b in reqs], "max_abs_err": float(err.max()),
+           "max_err_over_tol": round(worst, 5), "tol": "1e-3 + 1e-3*|ref| (fp64 oracle)",
+           "abort_mask_bit_exact": mask_ok, "ok": bool(worst <= 1.0 and mask_ok and oerr == 0)}
+    if not res["ok"]:
+        raise RuntimeError(f"the last timed step differs from the oracle: {res}")
+    return res
 
 
 def oracle_threads():
@@ -799,68 +946,89 @@ def run_sweep(args):
             del cache
 
 
+WORKLOADS = {"ragged": "ragged", "integrity": "integrity", "8x8192": "cfg8x8k"}
+
+
+class WorkloadStep:
+    """One of the other decode workloads (ragged: page 64, 8 query heads per
+    kv head; integrity: 256 requests, stale tags, check -> mask -> attention;
+    8x8192: one decode step of 8 requests x 8192 tokens) set up on the GPU
+    for timing.  The cache holds random finite e4m3 codes written on the GPU
+    (timing does not depend on the values; the parity tests cover these
+    workloads with real data).  Every step stages the same inputs."""
+
+    def __init__(self, torch, kvq, name, seed, rows_needed, eager=False):
+        from fp8_paged_kv_attn_gb300 import inputs
+        self.torch, self.kvq, self.name, self.eager = torch, kvq, name, eager
+        w = getattr(inputs, WORKLOADS[name])()
+        self.w = w
+        B, Hq, Hkv, D, P = w.B, w.Hq, w.Hkv, w.D, w.P
+        gen = torch.Generator(device="cuda").manual_seed(seed)
+        pools = [torch.randint(0, 0x77, w.pool_shape(), dtype=torch.uint8, device="cuda",
+                               generator=gen) for _ in range(2)]
+        self.cache = kvq.KVCache(pools[0], pools[1], 0.01, 0.01)
+        self.bt = torch.from_numpy(w.block_table).cuda()
+        self.tags = torch.from_numpy(w.page_tags.view(np.int32)).cuda()
+        self.exp_tags = torch.from_numpy(w.expected_tags.view(np.int32)).cuda()
+        self.lens = w.seq_lens_after(0)
+        q, k_new, v_new, req, pos = w.step_inputs(0)
+        assert np.array_equal(req, np.arange(B, dtype=np.int32))
+        self.packer = StepInputs(torch, B, Hq, Hkv, D)
+        row = self.packer.pack([{"q": q, "k": k_new, "v": v_new, "pos": pos,
+                                 "lens": self.lens}]).cuda()
+        self.rows = row.expand(rows_needed, -1)  # the same step inputs every step
+        self.mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
+        self.out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+        self.ws = kvq.workspace(B, Hq, Hkv, D)
+        self.flush = L2Flush(torch) if L2Flush.needed(
+            torch, attn_bytes(self.lens, Hq, Hkv, D, P, 1)) else None
+
+    def time(self, warmup, steps):
+        """Times `steps` whole steps with the check, then the same without it
+        but with the mask it produced (both arms attend the same requests, so
+        the difference is the check alone).  Returns the result record."""
+        torch, w = self.torch, self.w
+        B, Hq, Hkv, D, P = w.B, w.Hq, w.Hkv, w.D, w.P
+
+        def run(check):
+            step = DecodeStep(torch, self.kvq, self.cache, self.bt, P, float(w.sm_scale),
+                              self.packer, self.out, self.ws, check=check, tags=self.tags,
+                              exp_tags=self.exp_tags, mask=self.mask, graph=not self.eager)
+            step_ms, attn_ms = time_steps(torch, step, self.rows, warmup, steps, self.flush)
+            return step_ms, statistics.mean(attn_ms)
+
+        step_on, attn_on = run(True)
+        step_off, attn_off = run(False)
+        peak, _ = measured_hbm_peak()
+        aborted = int(self.mask.sum().item())
+        alive = (self.mask.cpu().numpy() == 0)
+        byts = attn_bytes(self.lens[alive], Hq, Hkv, D, P, 1)
+        gbs = byts / (attn_on * 1e-3) / 1e9
+        res = {"workload": w.name, "batch": B, "tokens": int(self.lens.sum()), "Hq": Hq,
+               "Hkv": Hkv, "page_size": P, "steps": steps,
+               "tokens_per_s": round(B / (step_on * 1e-3), 1),
+               "step_ms_with_check": round(step_on, 5),
+               "attn_us_with_check": round(attn_on * 1e3, 2),
+               "attn_GBs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+               "aborted_requests": aborted,
+               "l2": "flushed before each step" if self.flush else
+                     "KV larger than 2 x L2; no flush"}
+        if self.name == "integrity":
+            res["step_ms_without_check"] = round(step_off, 5)
+            res["check_overhead_pct_of_step"] = round(100 * (step_on - step_off) / step_off, 2)
+        return res
+
+
 def run_workload(args):
-    """Decode-step timing on the ragged (page 64, 8 query heads per kv head),
-    integrity (256 requests, stale tags, check -> mask -> attention) or 8x8192
-    workloads.  The cache holds random finite e4m3 codes written on the GPU
-    (timing only; the parity tests cover these workloads with real data).  For
-    the integrity workload it also times the same steps without the check
-    (attention still skipping the requests the check aborted) and reports the
-    check's share of the step."""
+    """Decode-step timing on one of the other workloads (WorkloadStep), one
+    JSON line."""
     import torch
-    from fp8_paged_kv_attn_gb300 import inputs, kvq
+    from fp8_paged_kv_attn_gb300 import kvq
 
     kvq.load()
-    peak, _ = measured_hbm_peak()
-    w = {"ragged": inputs.ragged, "integrity": inputs.integrity,
-         "8x8192": inputs.cfg8x8k}[args.workload]()
-    B, Hq, Hkv, D, P = w.B, w.Hq, w.Hkv, w.D, w.P
-    shape = w.pool_shape()
-    gen = torch.Generator(device="cuda").manual_seed(args.seed)
-    pools = [torch.randint(0, 0x77, shape, dtype=torch.uint8, device="cuda", generator=gen)
-             for _ in range(2)]
-    cache = kvq.KVCache(pools[0], pools[1], 0.01, 0.01)
-    bt = torch.from_numpy(w.block_table).cuda()
-    tags = torch.from_numpy(w.page_tags.view(np.int32)).cuda()
-    exp_tags = torch.from_numpy(w.expected_tags.view(np.int32)).cuda()
-    lens_np = w.seq_lens_after(0)
-    q, k_new, v_new, req, pos = w.step_inputs(0)
-    assert np.array_equal(req, np.arange(B, dtype=np.int32))
-    packer = StepInputs(torch, B, Hq, Hkv, D)
-    rows = packer.pack([{"q": q, "k": k_new, "v": v_new, "pos": pos, "lens": lens_np}]).cuda()
-    rows = rows.expand(args.warmup + args.steps, -1)  # the same step inputs every step
-    mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
-    out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
-    ws = kvq.workspace(B, Hq, Hkv, D)
-
-    flush = L2Flush(torch) if L2Flush.needed(torch, attn_bytes(lens_np, Hq, Hkv, D, P, 1)) \
-        else None
-
-    def run(check):
-        step = DecodeStep(torch, kvq, cache, bt, P, float(w.sm_scale), packer, out, ws,
-                          check=check, tags=tags, exp_tags=exp_tags, mask=mask,
-                          graph=not args.eager)
-        step_ms, attn_ms = time_steps(torch, step, rows, args.warmup, args.steps, flush)
-        return step_ms, statistics.mean(attn_ms)
-
-    # with the check, then without it but with the mask it produced, so that
-    # both attend the same requests and the difference is the check alone
-    step_on, attn_on = run(True)
-    step_off, attn_off = run(False)
-    aborted = int(mask.sum().item())
-    alive = (mask.cpu().numpy() == 0)
-    byts = attn_bytes(lens_np[alive], Hq, Hkv, D, P, 1)
-    res = {"workload": w.name, "batch": B, "tokens": int(lens_np.sum()), "Hq": Hq, "Hkv": Hkv,
-           "page_size": P, "steps": args.steps,
-           "step_ms_with_check": round(step_on, 5), "attn_us_with_check": round(attn_on * 1e3, 2),
-           "attn_GBs": round(byts / (attn_on * 1e-3) / 1e9, 1),
-           "frac_of_measured_peak": round(byts / (attn_on * 1e-3) / 1e9 / peak, 4),
-           "aborted_requests": aborted,
-           "l2": "flushed before each step" if flush else "KV larger than 2 x L2; no flush"}
-    if args.workload == "integrity":
-        res["step_ms_without_check"] = round(step_off, 5)
-        res["check_overhead_pct_of_step"] = round(100 * (step_on - step_off) / step_off, 2)
-    print(json.dumps(res), flush=True)
+    ws = WorkloadStep(torch, kvq, args.workload, args.seed, args.warmup + args.steps,
+                      eager=args.eager)
+    print(json.dumps(ws.time(args.warmup, args.steps)), flush=True)
 
 
 def run_prefill(args):

@@ -22,16 +22,24 @@
 // permuted consistently in the weights' fragments and in the staged x, which
 // leaves the sum unchanged), with a register ring of the next 3 (INT4) or 2
 // (e4m3) groups' loads in flight while the current one is computed.
-//  x is rounded to f16 once while staged (exact for bf16 values in f16's
-//  normal range) and the products run on mma.sync m16n8k16 f16 -> fp32.
+//  x is scaled while staged, per token over the CTA's k range, by the power
+//  of two 2^e that puts the token's largest finite |x| there in
+//  [2^14, 2^15), then rounded to f16: exact for every bf16 value down to
+//  2^-32 of that largest (f16 keeps 11 bits, bf16 has 8), whatever the
+//  magnitude (bf16 reaches 2^128, f16 only 65504).  The products run on
+//  mma.sync m16n8k16 f16 -> fp32 and the CTA's sums are multiplied by 2^-e
+//  (exact) in the epilogue.
 //  INT4: one LOP3 and one fma.f16x2 turn two signed nibbles into exact f16
 //        values (magic number 1024; the high nibble of each byte needs no
-//        shift, the upper byte pair one shift per word); a group's products
-//        are accumulated apart, then scaled in fp32 and added to the output.
+//        shift, the upper byte pair one shift per word); a group's sum is
+//        also multiplied by the group's bf16 scale.
 //  e4m3: cvt.rn.f16x2.e4m3x2 widens two codes exactly; the channel scale is
 //        applied at the end.
 // Products are exact and the sums are fp32, so the result differs from the
-// fp64 definition only by fp32 summation rounding.
+// fp64 definition only by fp32 summation rounding (and, for x values more
+// than 2^32 below their token's largest in the CTA's range, by the f16
+// rounding of those).  The INT4 sums stay finite in the scaled domain for
+// group scales below 2^97 in magnitude.
 #include <atomic>
 
 #include <cuda_fp16.h>
@@ -99,6 +107,13 @@ __device__ __forceinline__ constexpr int frag_src(int s, int i) {
   }
 }
 
+// The exponent e of 2^e that puts a token's largest finite |x| (fp32 bits;
+// 0 when all are zero) in [2^14, 2^15): in [-113, 147] for bf16 inputs.
+__device__ __forceinline__ int x_exponent(uint32_t max_bits) {
+  const float mx = __uint_as_float(max_bits);
+  return mx > 0.f ? 14 - ilogbf(mx) : 0;
+}
+
 template <bool kInt4>
 struct WqCfg {
   static constexpr int kWords = kInt4 ? 4 : 8;  // weight words per row half per lane per group
@@ -106,11 +121,16 @@ struct WqCfg {
 };
 
 // shared memory of a CTA: [group scales: kWqRows x gpc bf16][staged x]
+// [largest finite |x| per staged token over the CTA's k range, fp32 bits]
+__host__ __device__ constexpr int wq_staged_tokens(int nt, int M) { return nt == 1 ? M : 8 * nt; }
 __host__ __device__ constexpr size_t wq_scale_bytes(int gpc) {
   return (size_t(kWqRows) * gpc * 2 + 15) / 16 * 16;
 }
+__host__ __device__ constexpr size_t wq_x_bytes(int gpc, int nt, int M) {
+  return size_t(gpc) * kWqGroup * wq_staged_tokens(nt, M) * sizeof(uint16_t);
+}
 __host__ __device__ constexpr size_t wq_smem_bytes(int gpc, int nt, int M) {
-  return wq_scale_bytes(gpc) + size_t(gpc) * kWqGroup * (nt == 1 ? M : 8 * nt) * sizeof(uint16_t);
+  return wq_scale_bytes(gpc) + wq_x_bytes(gpc, nt, M) + size_t(wq_staged_tokens(nt, M)) * 4;
 }
 
 template <bool kInt4, int NT>
@@ -121,7 +141,9 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
   uint16_t *xs = reinterpret_cast<uint16_t *>(wq_smem + wq_scale_bytes(a.gpc));
   // tokens staged: 8 per tile, or just the M real ones when there is one
   // tile (lanes whose token is past M then use a zero operand)
-  const int Mp = NT == 1 ? a.M : 8 * NT;
+  const int Mp = wq_staged_tokens(NT, a.M);
+  uint32_t *xmax = reinterpret_cast<uint32_t *>(wq_smem + wq_scale_bytes(a.gpc) +
+                                                wq_x_bytes(a.gpc, NT, a.M));  // [Mp]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = lane & 3, rr = lane >> 2;
   const int kc = a.gpc * kWqGroup;
@@ -156,38 +178,73 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
 #pragma unroll
   for (int d = 0; d < C::kDepth - 1; ++d) load(d, wr0[d], wr8[d]);
 
-  // ---- stage x: one thread per (group, token, class) chunk of 32 k values:
-  // four 16-byte loads, the fragment permutation in registers, eight 8-byte
-  // stores (a warp's stores for one step are 256 contiguous bytes)
-  for (int ch = tid; ch < ng * Mp * 4; ch += blockDim.x) {
+  // ---- stage x: one thread per (group, token, class) chunk of 32 k values,
+  // in two passes.  The first finds each token's largest finite |x| over
+  // the CTA's k range (non-negative floats order like their bit patterns).
+  // The second loads the chunk again, one 16-byte load (8 values, which
+  // feed exactly fragment steps 2h and 2h + 1 of either weight type) at a
+  // time, scales it by 2^e, rounds it to f16 and stores the two steps'
+  // 8-byte fragment words (a warp's stores for one step are 256 contiguous
+  // bytes).
+  const int nch = ng * Mp * 4;
+  for (int m = tid; m < Mp; m += blockDim.x) xmax[m] = 0u;
+  __syncthreads();
+  auto chunk_src = [&](int ch) {
     const int cl = ch & 3, m = (ch >> 2) % Mp, g = (ch >> 2) / Mp;
-    uint16_t v[32];
-    if (m < a.M) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          a.x + static_cast<int64_t>(m) * a.K + kb0 + g * kWqGroup + cl * 32);
+    return reinterpret_cast<const uint4 *>(a.x + static_cast<int64_t>(m) * a.K + kb0 +
+                                           g * kWqGroup + cl * 32);
+  };
+  for (int ch = tid; ch < nch; ch += blockDim.x) {
+    const int m = (ch >> 2) % Mp;
+    if (m >= a.M) continue;
+    const uint4 *src = chunk_src(ch);
+    float mx = 0.f;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const uint4 u = __ldg(src + h);
-        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+    for (int h = 0; h < 4; ++h) {
+      const uint4 u = __ldg(src + h);
+      float xf[8];
+      bf16x2_to_f32(u.x, xf);
+      bf16x2_to_f32(u.y, xf + 2);
+      bf16x2_to_f32(u.z, xf + 4);
+      bf16x2_to_f32(u.w, xf + 6);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          v[8 * h + 2 * e] = static_cast<uint16_t>(wv[e] & 0xFFFFu);
-          v[8 * h + 2 * e + 1] = static_cast<uint16_t>(wv[e] >> 16);
-        }
+      for (int e = 0; e < 8; ++e) {
+        const float ax = fabsf(xf[e]);
+        if (ax < INFINITY) mx = fmaxf(mx, ax);  // NaN and inf take no part
       }
-#pragma unroll
-      for (int e = 0; e < 32; ++e)  // x as f16 (exact for |x| in [2^-14, 65504])
-        v[e] = __half_as_ushort(__float2half_rn(__uint_as_float(uint32_t(v[e]) << 16)));
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = 0;
+    }
+    if (mx > 0.f) atomicMax(xmax + m, __float_as_uint(mx));
+  }
+  __syncthreads();
+  for (int ch = tid; ch < nch; ch += blockDim.x) {
+    const int cl = ch & 3, m = (ch >> 2) % Mp, g = (ch >> 2) / Mp;
+    const bool real = m < a.M;
+    const uint4 *src = chunk_src(ch);
+    float f1 = 0.f, f2 = 0.f;  // tokens past M: zeros
+    if (real) {
+      const int ex = x_exponent(xmax[m]);
+      // x * 2^ex as two products by normal powers of two (2^ex alone is not
+      // a float for ex > 127); each is exact for the values f16 can hold
+      f1 = ldexpf(1.f, ex > 127 ? ex - 64 : ex);
+      f2 = ex > 127 ? 18446744073709551616.f : 1.f;  // 2^64
     }
     uint2 *dst = reinterpret_cast<uint2 *>(xs) + (g * 8 * Mp + m) * 4 + cl;
 #pragma unroll
-    for (int st = 0; st < 8; ++st) {
-      const uint32_t lo = uint32_t(v[frag_src<kInt4>(st, 0)]) | (uint32_t(v[frag_src<kInt4>(st, 1)]) << 16);
-      const uint32_t hi = uint32_t(v[frag_src<kInt4>(st, 2)]) | (uint32_t(v[frag_src<kInt4>(st, 3)]) << 16);
-      dst[st * Mp * 4] = make_uint2(lo, hi);
+    for (int h = 0; h < 4; ++h) {
+      const uint4 u = real ? __ldg(src + h) : make_uint4(0, 0, 0, 0);
+      float xf[8];
+      bf16x2_to_f32(u.x, xf);
+      bf16x2_to_f32(u.y, xf + 2);
+      bf16x2_to_f32(u.z, xf + 4);
+      bf16x2_to_f32(u.w, xf + 6);
+      auto h2 = [&](int i, int j) {  // f16 pair (value i low, value j high), scaled
+        const __half2 r = __floats2half2_rn((xf[i] * f1) * f2, (xf[j] * f1) * f2);
+        return *reinterpret_cast<const uint32_t *>(&r);
+      };
+#pragma unroll
+      for (int st = 2 * h; st < 2 * h + 2; ++st)
+        dst[st * Mp * 4] = make_uint2(h2(frag_src<kInt4>(st, 0) - 8 * h, frag_src<kInt4>(st, 1) - 8 * h),
+                                      h2(frag_src<kInt4>(st, 2) - 8 * h, frag_src<kInt4>(st, 3) - 8 * h));
     }
   }
   // ---- group scales of the CTA's rows (INT4), bf16
@@ -272,7 +329,9 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
       const int n = t * 8 + 2 * c + (e & 1);
       const int row = row0 + (e >> 1) * 8;
       if (n >= a.M || row >= a.N) continue;
-      const float v = acc[t][e] * ((e >> 1) ? f8 : f0);
+      // the channel scale, then back to x's scale (exact unless the result
+      // is below fp32's normal range; one rounding there)
+      const float v = (acc[t][e] * ((e >> 1) ? f8 : f0)) * ldexpf(1.f, -x_exponent(xmax[n]));
       float *dst = a.y + static_cast<int64_t>(n) * a.N + row;
       if (a.atomic)
         atomicAdd(dst, v);

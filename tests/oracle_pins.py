@@ -710,6 +710,63 @@ def random_wq_case(rng, wdtype, M, N, K, group=128):
     return w, s, x
 
 
+def wide_range_x(rng, M, K):
+    """bf16 activations [M, K] (bit patterns) over bf16's whole range, one
+    regime per row (cycled): N(0,1) with entries of +-1e5 and +-3e4 (beyond
+    f16's 65504); magnitudes log-uniform over 13 decades in one row; all
+    near 1e-6; bf16 subnormals only; subnormals mixed with 1e-30; near 1e30;
+    zeros but one 1e5; all zeros."""
+    x = np.zeros((M, K), dtype=np.float32)
+    for m in range(M):
+        kind = m % 8
+        z = rng.standard_normal(K).astype(np.float32)
+        if kind == 0:
+            z[rng.choice(K, 6, replace=False)] = np.float32([1e5, -1e5, 3e4, -3e4, 99999.0, -65520.0])
+            x[m] = z
+        elif kind == 1:
+            x[m] = z * np.float32(10.0) ** rng.uniform(-8, 5, K).astype(np.float32)
+        elif kind == 2:
+            x[m] = z * np.float32(1e-6)
+        elif kind == 4:
+            x[m] = z * np.float32(1e-30)
+        elif kind == 5:
+            x[m] = z * np.float32(1e30)
+        elif kind == 6:
+            x[m, rng.integers(K)] = np.float32(1e5)
+    bits = inputs.f32_to_bf16_bits(x)
+    for m in range(M):
+        kind = m % 8
+        if kind in (3, 4):  # bf16 subnormals: exponent field 0, mantissa 1..127
+            sub = rng.integers(1, 128, K).astype(np.uint16) | \
+                (rng.integers(0, 2, K).astype(np.uint16) << np.uint16(15))
+            if kind == 3:
+                bits[m] = sub
+            else:
+                pick = rng.random(K) < 0.5
+                bits[m] = np.where(pick, sub, bits[m])
+    return bits
+
+
+def pin_wq_wide_range_x(oracle):
+    """Activations over bf16's whole range (wide_range_x): the oracle still
+    equals a float64 matmul of independently dequantised weights to within
+    the last fp32 bit, for both weight types."""
+    rng = np.random.default_rng(33)
+    for wdtype in (0, 1):
+        w, s, _ = random_wq_case(rng, wdtype, 8, 40, 640)
+        x = wide_range_x(rng, 8, 640)
+        if wdtype == 0:
+            wd = numpy_int4_weights(w, s, 128)
+        else:
+            wd = torch.from_numpy(w).view(E4M3).to(torch.float64).numpy() * \
+                s.astype(np.float64)[:, None]
+        ref = _bf16_to_f64(x) @ wd.T
+        got = oracle.wq_gemm(oracle.W_INT4 if wdtype == 0 else oracle.W_E4M3, w, s, x)
+        assert np.all(np.isfinite(got))
+        np.testing.assert_allclose(got, ref, rtol=2e-7, atol=1e-44)
+        assert np.any(np.abs(got[0]) > 1e4) and np.all(got[7] == 0.0)
+
+
 def pin_int4_nibbles(oracle):
     """Every byte value: with a one-hot x picking k = 0 or k = 1 and scale 1,
     y is the low or high nibble read as a signed 4-bit number."""

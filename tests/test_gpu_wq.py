@@ -1,12 +1,26 @@
 """GPU parity of kvq_wq_gemm (weight-only INT4 / e4m3 decode matrix product)
 against the oracle.
 
-Tolerance, derived from the arithmetic: the kernel's products are exact
-(INT4 and e4m3 values are exact in bf16 / f16, and so is x in the range
-used), and a sum of K terms in fp32 -- tensor-core accumulation, split-K
-partial sums added with atomics -- is within K * u * sum|w x| of the exact
-sum (u = 2^-24, the standard worst-case bound for recursive summation);
-the test allows twice that, K * 2^-23 * sum_k |w[n][k] x[m][k]|, elementwise.
+Tolerance, derived from the kernel's arithmetic.  The oracle is exact up to
+one final fp32 rounding.  The kernel:
+  * scales each token's x by a power of two 2^e (largest finite |x| of its k
+    range into [2^14, 2^15)) and rounds it to f16: exact for values down to
+    2^-32 of that largest, otherwise off by at most 2^-25 * 2^-e.  The test
+    takes e from the token's largest |x| over all of K, which can only widen
+    the allowance (a CTA's range is part of K);
+  * multiplies exactly (INT4, e4m3 and scaled x are exact in f16) and sums
+    with fp32 tensor-core accumulation: every mma.sync step, a rounding of at
+    most 2^-22 of the running sum's magnitude (allowing for an accumulator
+    that truncates instead of rounding to nearest), then fp32 roundings
+    (2^-24 each) for the INT4 group scale, the split-K atomics and the
+    channel scale.  The chain is at most 8 * (groups per CTA) steps deep for
+    e4m3 (one accumulator through a CTA's groups) and 8 steps plus one per
+    group for INT4 (a group is summed apart); groups per CTA and split-K
+    parts are each at most K / 128.
+So elementwise, with A = sum_k |W[n][k] x[m][k]| and G = K / 128,
+  e4m3: |err| <= (8 G 2^-22 + (G + 3) 2^-24) A + 2^-25 2^-e sum_k |W[n][k]|
+  INT4: |err| <= (8 2^-22 + (2 G + 3) 2^-24) A + 2^-25 2^-e sum_k |W[n][k]|
+plus 2^-140 for results below fp32's normal range.
 """
 import numpy as np
 import pytest
@@ -38,18 +52,31 @@ def run_gpu(wdtype, w, s, x):
     return y.cpu().numpy()
 
 
+def wq_bound(wdtype, w, s, x):
+    wd = _dequant(wdtype, w, s)
+    xf = pins._bf16_to_f64(x)
+    G = x.shape[1] // 128
+    absum = np.abs(xf) @ np.abs(wd).T
+    if wdtype == oracle.W_E4M3:
+        rel = 8 * G * 2.0 ** -22 + (G + 3) * 2.0 ** -24
+    else:
+        rel = 8 * 2.0 ** -22 + (2 * G + 3) * 2.0 ** -24
+    ax = np.where(np.isfinite(xf), np.abs(xf), 0.0).max(axis=1)
+    e = np.where(ax > 0, 14 - np.floor(np.log2(np.where(ax > 0, ax, 1.0))), 0.0)
+    xround = np.outer(2.0 ** (-25 - e), np.abs(wd).sum(axis=1))
+    return rel * absum + xround + 2.0 ** -140, absum
+
+
 def check(wdtype, w, s, x, rows=None, what=""):
     got = run_gpu(wdtype, w, s, x)
     if rows is not None:
         w, s, got = w[rows], s[rows], got[:, rows]
     ref = oracle.wq_gemm(wdtype, w, s, x)
-    K = x.shape[1]
-    absum = np.abs(pins._bf16_to_f64(x)) @ np.abs(_dequant(wdtype, w, s)).T
-    bound = K * 2.0 ** -23 * absum + 1e-30
+    bound, absum = wq_bound(wdtype, w, s, x)
     err = np.abs(got.astype(np.float64) - ref)
     assert np.all(np.isfinite(got)), what
     assert np.all(err <= bound), (what, float((err / bound).max()))
-    return float((err / np.maximum(absum, 1e-30)).max())
+    return float((err / np.maximum(absum, 1e-300)).max())
 
 
 SHAPES = [(1, 16, 128), (3, 100, 384), (8, 64, 1024), (13, 200, 640), (33, 64, 256),
@@ -111,3 +138,28 @@ def test_wq_gemm_arguments(kvq):
     assert L.kvq_wq_gemm(2, p(w), p(s), p(x), p(y), 1, 1, 128, None) == 1   # dtype
     assert L.kvq_wq_gemm(0, p(w) + 8, p(s), p(x), p(y), 1, 1, 128, None) == 1  # alignment
     assert L.kvq_wq_gemm(0, None, p(s), p(x), p(y), 1, 1, 128, None) == 1
+
+
+@pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])
+@pytest.mark.parametrize("M,N,K", [(8, 200, 1280), (13, 130, 5120), (1, 64, 384), (64, 129, 768),
+                                   (24, 300, 2560)])
+def test_wq_gemm_wide_range_x(kvq, wdtype, M, N, K):
+    """Activations over bf16's whole range: +-1e5 and +-3e4 (beyond f16's
+    65504), 13 decades within a row, ~1e-6, bf16 subnormals, ~1e-30 and
+    ~1e30, zero rows (oracle_pins.wide_range_x)."""
+    rng = np.random.default_rng(7 * M + N + K + wdtype)
+    w, s, _ = pins.random_wq_case(rng, wdtype, M, N, K)
+    x = pins.wide_range_x(rng, M, K)
+    check(wdtype, w, s, x, what=f"wide x {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])
+def test_wq_gemm_wide_range_x_full_size(kvq, wdtype):
+    """The large projection (28672 x 5120) at 64 tokens with wide-range
+    activations: 96 sampled output channels."""
+    rng = np.random.default_rng(90 + wdtype)
+    M, N, K = 64, 28672, 5120
+    w, s, _ = pins.random_wq_case(rng, wdtype, M, N, K)
+    x = pins.wide_range_x(rng, M, K)
+    rows = np.sort(rng.choice(N, 96, replace=False))
+    check(wdtype, w, s, x, rows=rows, what="wide x full size")

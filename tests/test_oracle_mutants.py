@@ -98,6 +98,7 @@ def run_all_pins():
         ("int4_nibbles", lambda: pins.pin_int4_nibbles(oracle)),
         ("wq_vs_numpy", lambda: pins.pin_wq_vs_numpy(oracle)),
         ("wq_single", lambda: pins.pin_wq_single_weight(oracle)),
+        ("wq_wide_range_x", lambda: pins.pin_wq_wide_range_x(oracle)),
         ("pages_golden", lambda: pins.pin_pages_golden(oracle)),
         ("pages_invariants", lambda: pins.pin_pages_invariants(oracle, n_ops=30)),
         ("pages_overflow", lambda: pins.pin_pages_overflow_and_state(oracle)),

@@ -16,3 +16,7 @@ def test_wq_vs_numpy_and_torch():
 
 def test_wq_single_weight():
     pins.pin_wq_single_weight(oracle)
+
+
+def test_wq_wide_range_x():
+    pins.pin_wq_wide_range_x(oracle)

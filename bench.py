@@ -63,8 +63,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seed", type=int, default=2)
-    ap.add_argument("--workload", choices=["ragged", "integrity", "8x8192", "prefill", "pages",
-                                           "wq"],
+    ap.add_argument("--workload", choices=["ragged", "integrity", "8x8192", "prefill", "handoff",
+                                           "pages", "wq"],
                     default=None,
                     help="time one of the other decode workloads (pools filled with random "
                          "finite e4m3 codes on the GPU; one JSON line, not the headline)")
@@ -522,6 +522,7 @@ def run_gpu(args, dist, rank, world, local):
             extras.append(WorkloadStep(torch, kvq, name, args.seed,
                                        args.config_warmup + args.config_steps,
                                        eager=args.eager))
+        extras.append(HandoffStep(torch, kvq, args.seed))
         torch.cuda.synchronize()
 
     for i in range(args.warmup):
@@ -650,7 +651,8 @@ def run_gpu(args, dist, rank, world, local):
     # --- the other decode workloads, each timed in this process
     configs = {}
     for x in extras:
-        configs[x.name] = x.time(args.config_warmup, args.config_steps)
+        rec = x.time(args.config_warmup, args.config_steps)
+        configs[getattr(x, "name", "prefill_handoff")] = rec
     clk = clocks.stop()
     del extras
 
@@ -1088,6 +1090,80 @@ def run_prefill(args):
         del cache
 
 
+class HandoffStep:
+    """The prefill -> decode handoff of the sweep's 64 requests x 8192-token
+    prompts in one kvq_handoff_pages call: a BF16 prefill pool of 64-token
+    pages (random finite bf16 values written on the GPU; timing does not
+    depend on them, the parity tests cover real data) into the e4m3 decode
+    pool of 64 requests x 575 pages of 16 tokens."""
+
+    def __init__(self, torch, kvq, seed, B=64):
+        from fp8_paged_kv_attn_gb300 import inputs
+        self.torch, self.kvq = torch, kvq
+        h = inputs.handoff(seed=seed, B=B)
+        self.h = h
+        gen = torch.Generator(device="cuda").manual_seed(seed)
+
+        def bf16_pool():  # finite bf16 in (-2, 2): magnitude bits below 0x4000, random sign
+            mag = torch.randint(0, 0x4000, h.src_shape(), dtype=torch.int16, device="cuda",
+                                generator=gen)
+            neg = torch.randint(0, 2, h.src_shape(), dtype=torch.int16, device="cuda",
+                                generator=gen)
+            return (mag - neg * 32768).view(torch.bfloat16)
+
+        self.src = kvq.KVCache(bf16_pool(), bf16_pool())
+        self.dst = kvq.KVCache(torch.zeros(h.dst_shape(), dtype=torch.uint8, device="cuda"),
+                               torch.zeros(h.dst_shape(), dtype=torch.uint8, device="cuda"),
+                               2.0 / 448, 2.0 / 448)
+        self.sbt = torch.from_numpy(h.src_block_table).cuda()
+        self.dbt = torch.from_numpy(h.dst_block_table).cuda()
+        self.count = torch.from_numpy(h.count).cuda()
+        self.first = torch.from_numpy(h.first).cuda()
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.tokens = int(h.count.sum())
+        # read bf16 K and V, write e4m3 codes; one block-table entry per page
+        self.bytes = (self.tokens * h.Hkv * h.D * 2 * (2 + 1)
+                      + int(sum(-(-int(c) // h.src_P) + -(-int(c) // h.dst_P) for c in h.count)) * 4)
+
+    def call(self):
+        self.kvq.kvq_handoff_pages(self.src, self.sbt, self.dst, self.dbt, self.count,
+                                   first=self.first, err_word=self.err)
+
+    def time(self, warmup, steps):
+        torch = self.torch
+        stream = torch.cuda.current_stream()
+        for _ in range(warmup):
+            self.call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record(stream)
+            self.call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        if int(self.err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(self.err.item()):#x}")
+        peak, _ = measured_hbm_peak()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        gbs = self.bytes / (ms * 1e-3) / 1e9
+        h = self.h
+        return {"workload": f"prefill_handoff_{h.B}x8192_bf16p{h.src_P}_to_e4m3p{h.dst_P}",
+                "tokens": self.tokens, "Hkv": h.Hkv, "D": h.D, "steps": steps,
+                "us_per_call": round(ms * 1e3, 2), "tokens_per_s": round(self.tokens / (ms * 1e-3), 1),
+                "GBs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                "bytes_per_call": self.bytes,
+                "l2": "inputs larger than L2 (3.2 GB per call); no flush"}
+
+
+def run_handoff(args):
+    import torch
+    from fp8_paged_kv_attn_gb300 import kvq
+    kvq.load()
+    print(json.dumps(HandoffStep(torch, kvq, args.seed, args.batch).time(args.warmup, args.steps)),
+          flush=True)
+
+
 def run_pages(args):
     """The page allocator (kvq_pages_update), one line per scenario: the
     batches of a decode step and of admission.  Each scenario is K calls
@@ -1282,6 +1358,9 @@ def main():
         return
     if args.workload == "prefill":
         run_prefill(args)
+        return
+    if args.workload == "handoff":
+        run_handoff(args)
         return
     if args.workload:
         run_workload(args)

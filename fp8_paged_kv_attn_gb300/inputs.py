@@ -328,3 +328,74 @@ def integrity(seed: int = 4, B: int = 256, lo: int = 1024, hi: int = 16384,
     victims = sorted(int(v) for v in rng.choice(B, size=n_victims, replace=False))
     _inject_stale(w, pool, rng, victims, pages_per_victim)
     return w
+
+
+@dataclass
+class Handoff:
+    """A prefill -> decode handoff: B prompts held in a paged BF16 prefill
+    cache (page size src_P) to be moved into the paged decode cache (page
+    size dst_P).  Request b's tokens [first[b], first[b] + count[b]) move;
+    both block tables come from seeded shuffled free lists.  K/V values are
+    drawn like the decode workloads' (kv_source)."""
+    name: str
+    seed: int
+    B: int
+    Hkv: int
+    D: int
+    src_P: int
+    dst_P: int
+    src_pages: int
+    dst_pages: int
+    first: np.ndarray            # int32 [B]
+    count: np.ndarray            # int32 [B]
+    src_block_table: np.ndarray  # int32 [B, src_MP]
+    dst_block_table: np.ndarray  # int32 [B, dst_MP]
+    outlier_frac: float = 0.01
+
+    @property
+    def src_MP(self) -> int:
+        return self.src_block_table.shape[1]
+
+    @property
+    def dst_MP(self) -> int:
+        return self.dst_block_table.shape[1]
+
+    def kv_source(self, b: int) -> Tuple[np.ndarray, np.ndarray]:
+        """bf16 bits [first[b] + count[b], Hkv, D] for K and V of request b's
+        prompt (positions 0 .. first + count - 1)."""
+        L = int(self.first[b] + self.count[b])
+        shape = (L, self.Hkv, self.D)
+        k = normal_bf16(np.random.default_rng([self.seed, b, 1]), shape, self.outlier_frac)
+        v = normal_bf16(np.random.default_rng([self.seed, b, 2]), shape, self.outlier_frac)
+        return k, v
+
+    def src_shape(self):
+        return (self.src_pages, self.Hkv, self.src_P, self.D)
+
+    def dst_shape(self):
+        return (self.dst_pages, self.Hkv, self.dst_P, self.D)
+
+
+def handoff(seed: int = 5, B: int = 64, lens=None, first=None, Hkv: int = 8, D: int = 128,
+            src_P: int = 64, dst_P: int = 16, src_pool_factor: float = 1.25,
+            decode_room: int = SWEEP_DECODE_STEPS, dst_pool_factor: float = 1.0) -> Handoff:
+    """Prompts of `lens` tokens (default: B x 8192, the sweep's prompts)
+    moved from a prefill pool of src_P-token pages (1.25x the need) into a
+    decode pool of dst_P-token pages with room for `decode_room` more tokens
+    per request.  `first` (default zeros) offsets each request's range."""
+    rng = np.random.default_rng(seed)
+    lens = np.full(B, SWEEP_PROMPT, dtype=np.int64) if lens is None else \
+        np.asarray(lens, dtype=np.int64)
+    B = int(lens.shape[0])
+    first = np.zeros(B, dtype=np.int64) if first is None else np.asarray(first, dtype=np.int64)
+    ends = first + lens
+    src_caps = [max(1, -(-int(e) // src_P)) for e in ends]
+    dst_caps = [max(1, -(-(int(e) + decode_room) // dst_P)) for e in ends]
+    src_np = int(math.ceil(src_pool_factor * sum(src_caps)))
+    dst_np = int(math.ceil(dst_pool_factor * sum(dst_caps)))
+    src_pool = PagePool(src_np, rng)
+    dst_pool = PagePool(dst_np, rng)
+    sbt, _ = _assign_pages(src_pool, B, max(src_caps), src_caps)
+    dbt, _ = _assign_pages(dst_pool, B, max(dst_caps), dst_caps)
+    return Handoff(f"handoff_b{B}_p{src_P}to{dst_P}", seed, B, Hkv, D, src_P, dst_P, src_np,
+                   dst_np, first.astype(np.int32), lens.astype(np.int32), sbt, dbt)

@@ -42,7 +42,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_WORKSPACE", 3: "KVQ
           4: "KVQ_ERR_UNSUPPORTED"}
 
 # every symbol include/kvq.h declares
-EXPORTS = ("kvq_append", "kvq_check_tags", "kvq_pages_update", "kvq_decode_attn_workspace_size",
+EXPORTS = ("kvq_append", "kvq_handoff_pages", "kvq_check_tags", "kvq_pages_update", "kvq_decode_attn_workspace_size",
            "kvq_decode_attn", "kvq_decode_attn_static", "kvq_wq_gemm", "kvq_status_string")
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -82,6 +82,8 @@ def load(build_if_missing: bool = True):
     cp = ctypes.POINTER(CCache)
     L.kvq_append.argtypes = [cp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp]
     L.kvq_append.restype = ctypes.c_int
+    L.kvq_handoff_pages.argtypes = [cp, vp, i32, cp, vp, i32, vp, vp, i32, vp, vp]
+    L.kvq_handoff_pages.restype = ctypes.c_int
     L.kvq_check_tags.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp, vp, vp]
     L.kvq_check_tags.restype = ctypes.c_int
     L.kvq_pages_update.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, vp, vp, i32, vp, vp, vp,
@@ -189,6 +191,27 @@ def kvq_append(cache: KVCache, k_new, v_new, req_idx, pos, block_table, err_word
                       _dev(block_table, "block_table", I32, 2), B, MP,
                       _dev(err_word, "err_word", U32), _stream(stream))
     _check("kvq_append", st)
+
+
+def kvq_handoff_pages(src: KVCache, src_block_table, dst: KVCache, dst_block_table, count,
+                      first=None, err_word=None, stream=None) -> None:
+    """Prefill -> decode handoff: tokens [first[b], first[b] + count[b]) of
+    every request b, read from the paged bf16 cache `src` through
+    src_block_table [B, src_MP] and stored into `dst` through
+    dst_block_table [B, dst_MP] with kvq_append's rounding."""
+    L = load()
+    cs, cd = src.c(), dst.c()
+    B, src_MP = src_block_table.shape
+    if dst_block_table.shape[0] != B or count.shape[0] != B or \
+            (first is not None and first.shape[0] != B):
+        raise ValueError("dst_block_table, count and first must have B rows")
+    st = L.kvq_handoff_pages(ctypes.byref(cs), _dev(src_block_table, "src_block_table", I32, 2),
+                             src_MP, ctypes.byref(cd),
+                             _dev(dst_block_table, "dst_block_table", I32, 2),
+                             int(dst_block_table.shape[1]), _dev(first, "first", I32, 1),
+                             _dev(count, "count", I32, 1), B, _dev(err_word, "err_word", U32),
+                             _stream(stream))
+    _check("kvq_handoff_pages", st)
 
 
 def kvq_check_tags(block_table, seq_lens, page_size: int, page_tags, expected_tags, abort_mask,

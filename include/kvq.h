@@ -1,6 +1,7 @@
 /*
- * kvq -- FP8 (e4m3) paged KV cache: quantise-and-append, batched page-tag
- * integrity check, the page allocator that sets the tags, single-query
+ * kvq -- FP8 (e4m3) paged KV cache: quantise-and-append, the prefill -> decode
+ * handoff of BF16 pages, batched page-tag integrity check, the page
+ * allocator that sets the tags, single-query
  * paged decode attention, and the weight-only INT4 / FP8 decode matrix
  * product, for NVIDIA GB300 (sm_103a).  Plain C ABI: pointers,
  * sizes, a CUDA stream.  The library allocates no memory.
@@ -110,6 +111,30 @@ KVQ_API kvq_status kvq_append(const kvq_cache *cache, const void *k_new, const v
                       const int32_t *block_table, int32_t B, int32_t MP,
                       uint32_t *err_word, kvq_stream_t stream);
 
+/* Prefill -> decode handoff of whole prompts ([KVQ]: the prefill side keeps
+ * its KV cache in BF16, the decode side stores it as e4m3, so a prompt is
+ * converted once when decode takes it over).  `src` is a paged BF16 cache
+ * (kv_dtype KVQ_KV_BF16; its scales are ignored), `dst` the decode cache
+ * (e4m3, or bf16 for a plain paged copy) with the same num_kv_heads and
+ * head_dim; the two page sizes may differ.  For every request b < B and
+ * logical position p in [first[b], first[b] + count[b]) (first may be NULL:
+ * all zeros), the K/V of token p -- src page src_block_table[b*src_MP +
+ * p/src->page_size], slot p % src->page_size -- are stored at dst page
+ * dst_block_table[b*dst_MP + p/dst->page_size], slot p % dst->page_size,
+ * exactly as kvq_append stores a token (same code for the same value, with
+ * dst's k_scale / v_scale).  Nothing else in dst is written; src is only
+ * read and must not overlap dst.
+ * A request whose range is negative or reaches past either table's
+ * capacity (MP * page_size) writes nothing and raises KVQ_ERRBIT_POS; a
+ * token whose src or dst page is outside its pool writes nothing and raises
+ * KVQ_ERRBIT_PAGE.  first and count are int32 [B] device arrays; pools
+ * 16-byte aligned; num_kv_heads <= 8. */
+KVQ_API kvq_status kvq_handoff_pages(const kvq_cache *src, const int32_t *src_block_table,
+                                     int32_t src_MP, const kvq_cache *dst,
+                                     const int32_t *dst_block_table, int32_t dst_MP,
+                                     const int32_t *first, const int32_t *count, int32_t B,
+                                     uint32_t *err_word, kvq_stream_t stream);
+
 /* Batched page-tag integrity check ([GUARD]), a separate pass before decode.
  * abort_mask[b] = 1 if, for some logical page i < ceil(seq_lens[b]/page_size),
  * block_table[b*MP+i] is outside [0, num_pages) or
@@ -180,7 +205,9 @@ KVQ_API kvq_status kvq_pages_update(int32_t *free_stack, int32_t *free_count, ui
  * sums varies from run to run).  Any bf16 x is accepted: each token's values
  * are scaled by a power of two for the products (exact for every value down
  * to 2^-32 of the token's largest finite |x| in a k range, smaller ones are
- * rounded to 2^-25 of it); NaN and inf propagate.  Supported: 1 <= M <= 64,
+ * rounded to 2^-25 of it); NaN and inf propagate.  Split-K partial sums are
+ * added with fp32 atomics, which flush subnormals: a result below 2^-126 in
+ * magnitude can be off by up to (2 K/128 + 1) * 2^-126.  Supported: 1 <= M <= 64,
  * K a multiple of 128.  w and x 16-byte aligned, scales 4-byte aligned. */
 KVQ_API kvq_status kvq_wq_gemm(int32_t w_dtype, const void *w, const void *scales, const void *x,
                                float *y, int32_t M, int32_t N, int32_t K, kvq_stream_t stream);

@@ -69,6 +69,9 @@ def _load(path):
     L.oracle_quant_append.argtypes = [i32, vp, vp, i32, i32, i32, i32, f32, f32,
                                       vp, vp, vp, vp, i32, vp, i32, i32]
     L.oracle_quant_append.restype = u32
+    L.oracle_handoff_pages.argtypes = [vp, vp, i32, i32, vp, i32, i32, vp, vp, i32, i32, vp, i32,
+                                       i32, i32, f32, f32, vp, vp, i32, vp]
+    L.oracle_handoff_pages.restype = u32
     L.oracle_check_tags.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp, vp]
     L.oracle_check_tags.restype = None
     L.oracle_wq_gemm.argtypes = [i32, vp, vp, vp, vp, i32, i32, i32, i32]
@@ -140,6 +143,33 @@ def quant_append(kv_dtype, k_pool, v_pool, k_scale, v_scale, k_new, v_new, req_i
                                          float(k_scale), float(v_scale), _ptr(k_new),
                                          _ptr(v_new), _ptr(req_idx), _ptr(pos), n,
                                          _ptr(block_table), B, MP))
+
+
+def handoff_pages(src_k, src_v, src_block_table, dst_dtype, dst_k, dst_v, dst_block_table,
+                  k_scale, v_scale, count, first=None) -> int:
+    """Prefill -> decode handoff in place: tokens [first[b], first[b] +
+    count[b]) of every request, gathered from the bf16 pools src_k / src_v
+    (uint16 [pages, Hkv, Ps, D]) through src_block_table [B, src_MP] and
+    appended into dst_k / dst_v through dst_block_table [B, dst_MP].
+    Returns the error bits."""
+    SNP, H, SP, D = src_k.shape
+    DNP, H2, DP, D2 = dst_k.shape
+    assert (H, D) == (H2, D2) and src_v.shape == src_k.shape and dst_v.shape == dst_k.shape
+    src_k, src_v = _c(src_k, np.uint16), _c(src_v, np.uint16)
+    assert dst_k.flags.c_contiguous and dst_v.flags.c_contiguous
+    assert dst_k.dtype == (np.uint8 if dst_dtype == KV_E4M3 else np.uint16)
+    sbt = _c(src_block_table, np.int32)
+    dbt = _c(dst_block_table, np.int32)
+    B, SMP = sbt.shape
+    assert dbt.shape[0] == B
+    count = _c(count, np.int32)
+    first = None if first is None else _c(first, np.int32)
+    scratch = np.empty(2 * H * D, dtype=np.uint16)
+    return int(lib().oracle_handoff_pages(_ptr(src_k), _ptr(src_v), SNP, SP, _ptr(sbt), SMP,
+                                          dst_dtype, _ptr(dst_k), _ptr(dst_v), DNP, DP,
+                                          _ptr(dbt), dbt.shape[1], H, D, float(k_scale),
+                                          float(v_scale), _ptr(first), _ptr(count), B,
+                                          _ptr(scratch)))
 
 
 def check_tags(block_table, seq_lens, page_size, page_tags, expected_tags) -> np.ndarray:

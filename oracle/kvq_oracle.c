@@ -189,6 +189,57 @@ uint32_t oracle_quant_append(int kv_dtype, void *k_pool, void *v_pool,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Prefill -> decode handoff                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* [KVQ] The prefill side keeps its KV cache in BF16 and the decode side stores
+ * it as e4m3: a prompt is converted when decode takes it over.  For every
+ * request b and logical position p in [first[b], first[b] + count[b])
+ * (first may be NULL: zeros), token p's BF16 K and V [Hkv][D] are gathered
+ * from the prefill pools (page src_bt[b * src_MP + p / src_P], slot
+ * p % src_P) and written into the decode pools at the same logical position
+ * of request b through dst_bt, by oracle_quant_append (the decode append's
+ * own quantisation).  A request whose range is negative or reaches past
+ * either table writes nothing (POS); a token whose prefill page is outside
+ * the pool writes nothing (PAGE); the append reports a bad decode page
+ * itself (PAGE).  Returns the error bits. */
+uint32_t oracle_handoff_pages(const uint16_t *src_k, const uint16_t *src_v, int src_pages,
+                              int src_P, const int32_t *src_bt, int src_MP,
+                              int dst_dtype, void *dst_k, void *dst_v, int dst_pages, int dst_P,
+                              const int32_t *dst_bt, int dst_MP, int num_kv_heads, int head_dim,
+                              float k_scale, float v_scale, const int32_t *first,
+                              const int32_t *count, int B, uint16_t *scratch)
+{
+    uint32_t err = 0;
+    const int H = num_kv_heads, D = head_dim;
+    uint16_t *tk = scratch, *tv = scratch + (int64_t)H * D; /* one token's K and V */
+    for (int b = 0; b < B; ++b) {
+        int64_t f = first ? first[b] : 0;
+        int64_t n = count[b];
+        if (f < 0 || n < 0 || f + n > (int64_t)src_MP * src_P || f + n > (int64_t)dst_MP * dst_P) {
+            err |= ORACLE_ERR_POS;
+            continue;
+        }
+        for (int64_t p = f; p < f + n; ++p) {
+            int sp = src_bt[(int64_t)b * src_MP + p / src_P];
+            if (sp < 0 || sp >= src_pages) { err |= ORACLE_ERR_PAGE; continue; }
+            int slot = (int)(p % src_P);
+            for (int h = 0; h < H; ++h) {
+                for (int d = 0; d < D; ++d) {
+                    int64_t at = (((int64_t)sp * H + h) * src_P + slot) * D + d;
+                    tk[(int64_t)h * D + d] = src_k[at];
+                    tv[(int64_t)h * D + d] = src_v[at];
+                }
+            }
+            int32_t req = b, pos = (int32_t)p;
+            err |= oracle_quant_append(dst_dtype, dst_k, dst_v, dst_pages, dst_P, H, D, k_scale,
+                                       v_scale, tk, tv, &req, &pos, 1, dst_bt, B, dst_MP);
+        }
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Page-tag integrity check                                                  */
 /* ------------------------------------------------------------------------ */
 

@@ -230,6 +230,93 @@ def pin_append_bf16_copy(oracle, w):
         assert np.array_equal(vp[pages, :, j % w.P, :], v)
 
 
+def handoff_case(rng=None):
+    """A small handoff: 5 requests (an empty one, ranges that start past 0
+    and end mid-page), prefill pages of 32 tokens, decode pages of 16, GQA
+    head count 2, D 64; the prefill pools hold random bf16 values where the
+    requests' tokens live and a sentinel elsewhere."""
+    h = inputs.handoff(seed=61, lens=[37, 0, 100, 16, 61], first=[0, 3, 5, 0, 40], Hkv=2, D=64,
+                       src_P=32, dst_P=16, decode_room=20, dst_pool_factor=1.5)
+    rng = np.random.default_rng(62) if rng is None else rng
+    # one spare page past the pool, so that a page id one past the end stays
+    # inside the allocation even for code that does not check it
+    spare = (h.src_pages + 1,) + h.src_shape()[1:]
+    sk = np.full(spare, 0xBEEF, dtype=np.uint16)[:h.src_pages]
+    sv = np.full(spare, 0xBEEF, dtype=np.uint16)[:h.src_pages]
+    for b in range(h.B):
+        k, v = h.kv_source(b)
+        j = np.arange(k.shape[0])
+        pages = h.src_block_table[b, j // h.src_P]
+        sk[pages, :, j % h.src_P, :] = k
+        sv[pages, :, j % h.src_P, :] = v
+    ks = inputs.scale_from_amax(inputs.amax_bf16(sk[sk != 0xBEEF]))
+    vs = inputs.scale_from_amax(inputs.amax_bf16(sv[sv != 0xBEEF]))
+    return h, sk, sv, ks, vs
+
+
+def pin_handoff_vs_torch(oracle):
+    """The handoff: every moved token is found at its decode slot, quantised
+    as torch would quantise the bf16 value torch indexing reads from its
+    prefill slot (fp32 division by the scale, then float8_e4m3fn); a bf16
+    decode pool receives the bits unchanged; every other decode byte keeps
+    its sentinel; bad ranges and pages raise their bits and write nothing."""
+    h, sk, sv, ks, vs = handoff_case()
+    for dt in (oracle.KV_E4M3, oracle.KV_BF16):
+        npdt = np.uint8 if dt == oracle.KV_E4M3 else np.uint16
+        sent = SENTINEL if dt == oracle.KV_E4M3 else 0xA5A5
+        dk = np.full(h.dst_shape(), sent, dtype=npdt)
+        dv = np.full(h.dst_shape(), sent, dtype=npdt)
+        err = oracle.handoff_pages(sk, sv, h.src_block_table, dt, dk, dv, h.dst_block_table, ks, vs,
+                                   h.count, h.first)
+        assert err == 0
+        touched = np.zeros((h.dst_pages, h.dst_P), dtype=bool)
+        tsk, tsv = torch.from_numpy(sk.view(np.int16)), torch.from_numpy(sv.view(np.int16))
+        for b in range(h.B):
+            p = torch.arange(int(h.first[b]), int(h.first[b] + h.count[b]))
+            if p.numel() == 0:
+                continue
+            spg = torch.from_numpy(h.src_block_table[b].astype(np.int64))[p // h.src_P]
+            src_k = tsk[spg, :, p % h.src_P, :].view(torch.bfloat16)
+            src_v = tsv[spg, :, p % h.src_P, :].view(torch.bfloat16)
+            dpg = h.dst_block_table[b][(p // h.dst_P).numpy()]
+            dsl = (p % h.dst_P).numpy()
+            if dt == oracle.KV_E4M3:
+                want_k = (src_k.float() / torch.tensor(ks)).to(E4M3).view(torch.uint8).numpy()
+                want_v = (src_v.float() / torch.tensor(vs)).to(E4M3).view(torch.uint8).numpy()
+            else:
+                want_k = src_k.view(torch.int16).numpy().view(np.uint16)
+                want_v = src_v.view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(dk[dpg, :, dsl, :], want_k), f"K of request {b}"
+            assert np.array_equal(dv[dpg, :, dsl, :], want_v), f"V of request {b}"
+            touched[dpg, dsl] = True
+        assert np.all(dk.transpose(0, 2, 1, 3)[~touched] == sent)
+        assert np.all(dv.transpose(0, 2, 1, 3)[~touched] == sent)
+    # errors: a range past the decode table, a negative count, a prefill
+    # page outside the pool, a decode page outside the pool
+    cnt = h.count.copy()
+    fst = h.first.copy()
+    sbt = h.src_block_table.copy()
+    dbt = h.dst_block_table.copy()
+    cnt[0] = h.dst_MP * h.dst_P + 1        # request 0: past the capacity
+    cnt[1] = -1                            # request 1: negative
+    sbt[2, (5 + 10) // h.src_P] = -1       # request 2: token 10 of its range (and its page-mates)
+    sbt[3, 0] = h.src_pages                # request 3: one past the prefill pool
+    dbt[4, (40 + 3) // h.dst_P] = h.dst_pages  # request 4: the decode page of its token 3
+    dk = np.full(h.dst_shape(), SENTINEL, dtype=np.uint8)
+    dv = np.full(h.dst_shape(), SENTINEL, dtype=np.uint8)
+    err = oracle.handoff_pages(sk, sv, sbt, oracle.KV_E4M3, dk, dv, dbt, ks, vs, cnt, fst)
+    assert err == oracle.ERR_POS | oracle.ERR_PAGE
+    for b in (0, 1, 3):  # nothing of these requests is written
+        pages = h.dst_block_table[b][h.dst_block_table[b] >= 0]
+        assert np.all(dk[pages] == SENTINEL) and np.all(dv[pages] == SENTINEL)
+    # request 2: the tokens on the bad prefill page are not written, the rest are
+    p = np.arange(5, 105)
+    on_bad = (p // h.src_P) == (5 + 10) // h.src_P
+    dpg, dsl = h.dst_block_table[2][p // h.dst_P], p % h.dst_P
+    assert np.all(dk[dpg[on_bad], :, dsl[on_bad], :] == SENTINEL)
+    assert not np.any(np.all(dk[dpg[~on_bad], :, dsl[~on_bad], :] == SENTINEL, axis=(1, 2)))
+
+
 def pin_half_bytes(w):
     """An e4m3 pool holds the same tokens as a bf16 pool in half the bytes; at
     equal pool bytes the bf16 pool admits half the requests (the pages' BF16

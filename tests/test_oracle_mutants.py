@@ -65,6 +65,10 @@ MUTANTS = {
     "wq_nibble_order": ("int nib = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);",
                         "int nib = (k % 2 == 0) ? (byte >> 4) : (byte & 0x0F);"),
     "wq_unsigned": ("return nib >= 8 ? nib - 16 : nib;", "return nib - 8;"),
+    "handoff_src_slot": ("int slot = (int)(p % src_P);", "int slot = (int)(p % dst_P);"),
+    "handoff_first_ignored": ("int64_t f = first ? first[b] : 0;", "int64_t f = 0;"),
+    "handoff_src_page_unchecked": ("if (sp < 0 || sp >= src_pages) { err |= ORACLE_ERR_PAGE; continue; }",
+                                   "if (sp < 0) { err |= ORACLE_ERR_PAGE; continue; }"),
     "wq_group": ("(double)bf16_to_float(s[k / group]);", "(double)bf16_to_float(s[k / 64]);"),
     "wq_no_e4m3_scale": ("wv = oracle_e4m3_decode(row[k]) * (double)s[n];",
                          "wv = oracle_e4m3_decode(row[k]);"),
@@ -96,6 +100,7 @@ def run_all_pins():
         ("attn_equal_keys", lambda: pins.pin_attn_equal_keys(oracle)),
         ("attn_abort", lambda: pins.pin_attn_abort_and_errors(oracle)),
         ("int4_nibbles", lambda: pins.pin_int4_nibbles(oracle)),
+        ("handoff", lambda: pins.pin_handoff_vs_torch(oracle)),
         ("wq_vs_numpy", lambda: pins.pin_wq_vs_numpy(oracle)),
         ("wq_single", lambda: pins.pin_wq_single_weight(oracle)),
         ("wq_wide_range_x", lambda: pins.pin_wq_wide_range_x(oracle)),

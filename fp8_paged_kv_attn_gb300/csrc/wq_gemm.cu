@@ -22,13 +22,13 @@
 // permuted consistently in the weights' fragments and in the staged x, which
 // leaves the sum unchanged), with a register ring of the next 3 (INT4) or 2
 // (e4m3) groups' loads in flight while the current one is computed.
-//  x is scaled while staged, per token over the CTA's k range, by the power
-//  of two 2^e that puts the token's largest finite |x| there in
-//  [2^14, 2^15), then rounded to f16: exact for every bf16 value down to
-//  2^-32 of that largest (f16 keeps 11 bits, bf16 has 8), whatever the
-//  magnitude (bf16 reaches 2^128, f16 only 65504).  The products run on
-//  mma.sync m16n8k16 f16 -> fp32 and the CTA's sums are multiplied by 2^-e
-//  (exact) in the epilogue.
+//  x is scaled while staged, per token and 128-wide k group, by the power of
+//  two 2^e that puts the group's largest finite |x| in [2^14, 2^15), then
+//  rounded to f16: exact for every bf16 value down to 2^-32 of that largest
+//  (f16 keeps 11 bits, bf16 has 8), whatever the magnitude (bf16 reaches
+//  2^128, f16 only 65504).  The products run on mma.sync m16n8k16 f16 ->
+//  fp32; each group's sums are accumulated apart and multiplied by 2^-e
+//  (exact) before they are added to the output.
 //  INT4: one LOP3 and one fma.f16x2 turn two signed nibbles into exact f16
 //        values (magic number 1024; the high nibble of each byte needs no
 //        shift, the upper byte pair one shift per word); a group's sum is
@@ -37,9 +37,9 @@
 //        applied at the end.
 // Products are exact and the sums are fp32, so the result differs from the
 // fp64 definition only by fp32 summation rounding (and, for x values more
-// than 2^32 below their token's largest in the CTA's range, by the f16
-// rounding of those).  The INT4 sums stay finite in the scaled domain for
-// group scales below 2^97 in magnitude.
+// than 2^32 below their group's largest, by the f16 rounding of those; and,
+// for results below fp32's normal range, by the split-K atomics, since an
+// fp32 atomic add flushes subnormal operands).
 #include <atomic>
 
 #include <cuda_fp16.h>
@@ -69,6 +69,16 @@ __device__ __forceinline__ void mma_f16_16816(float c[4], const uint32_t a[4], u
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The same with a zero accumulator in (the first step of a group's sum).
+__device__ __forceinline__ void mma_f16_16816_zero(float c[4], const uint32_t a[4], uint32_t b0,
+                                                   uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 // Signed nibbles of v as exact f16 pairs, without a shift for the high
@@ -107,11 +117,23 @@ __device__ __forceinline__ constexpr int frag_src(int s, int i) {
   }
 }
 
-// The exponent e of 2^e that puts a token's largest finite |x| (fp32 bits;
-// 0 when all are zero) in [2^14, 2^15): in [-113, 147] for bf16 inputs.
+// The exponent e of 2^e that puts a token's largest finite |x| (the bits of
+// a non-negative fp32 value; 0 when all are zero) in [2^14, 2^15): 14 minus
+// floor(log2 |x|), read off the bits (a subnormal m * 2^-149 has
+// floor(log2) = -118 - clz(m)); in [-113, 149] for bf16 inputs.
 __device__ __forceinline__ int x_exponent(uint32_t max_bits) {
-  const float mx = __uint_as_float(max_bits);
-  return mx > 0.f ? 14 - ilogbf(mx) : 0;
+  if (max_bits == 0u) return 0;
+  const int field = static_cast<int>(max_bits >> 23);
+  const int lg = field > 0 ? field - 127 : -118 - __clz(static_cast<int>(max_bits));
+  return 14 - lg;
+}
+
+// 2^n as an fp32 bit pattern, n in [-126, 127] (exact, normal).
+__device__ __forceinline__ float pow2i(int n) { return __int_as_float((n + 127) << 23); }
+
+// 2^n for n in [-149, 127], a subnormal float below -126 (exact).
+__device__ __forceinline__ float pow2_any(int n) {
+  return n >= -126 ? pow2i(n) : __int_as_float(1 << (149 + n));
 }
 
 template <bool kInt4>
@@ -121,7 +143,7 @@ struct WqCfg {
 };
 
 // shared memory of a CTA: [group scales: kWqRows x gpc bf16][staged x]
-// [largest finite |x| per staged token over the CTA's k range, fp32 bits]
+// [2^-e per (group, staged token), fp32]
 __host__ __device__ constexpr int wq_staged_tokens(int nt, int M) { return nt == 1 ? M : 8 * nt; }
 __host__ __device__ constexpr size_t wq_scale_bytes(int gpc) {
   return (size_t(kWqRows) * gpc * 2 + 15) / 16 * 16;
@@ -130,11 +152,11 @@ __host__ __device__ constexpr size_t wq_x_bytes(int gpc, int nt, int M) {
   return size_t(gpc) * kWqGroup * wq_staged_tokens(nt, M) * sizeof(uint16_t);
 }
 __host__ __device__ constexpr size_t wq_smem_bytes(int gpc, int nt, int M) {
-  return wq_scale_bytes(gpc) + wq_x_bytes(gpc, nt, M) + size_t(wq_staged_tokens(nt, M)) * 4;
+  return wq_scale_bytes(gpc) + wq_x_bytes(gpc, nt, M) + size_t(gpc) * wq_staged_tokens(nt, M) * 4;
 }
 
 template <bool kInt4, int NT>
-__global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
+__global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel(WqArgs a) {
   using C = WqCfg<kInt4>;
   extern __shared__ __align__(16) uint8_t wq_smem[];
   uint16_t *sc_s = reinterpret_cast<uint16_t *>(wq_smem);  // [rows][gpc] bf16
@@ -142,8 +164,8 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
   // tokens staged: 8 per tile, or just the M real ones when there is one
   // tile (lanes whose token is past M then use a zero operand)
   const int Mp = wq_staged_tokens(NT, a.M);
-  uint32_t *xmax = reinterpret_cast<uint32_t *>(wq_smem + wq_scale_bytes(a.gpc) +
-                                                wq_x_bytes(a.gpc, NT, a.M));  // [Mp]
+  float *xu = reinterpret_cast<float *>(wq_smem + wq_scale_bytes(a.gpc) +
+                                        wq_x_bytes(a.gpc, NT, a.M));  // [gpc][Mp]: 2^-e
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = lane & 3, rr = lane >> 2;
   const int kc = a.gpc * kWqGroup;
@@ -178,73 +200,71 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
 #pragma unroll
   for (int d = 0; d < C::kDepth - 1; ++d) load(d, wr0[d], wr8[d]);
 
-  // ---- stage x: one thread per (group, token, class) chunk of 32 k values,
-  // in two passes.  The first finds each token's largest finite |x| over
-  // the CTA's k range (non-negative floats order like their bit patterns).
-  // The second loads the chunk again, one 16-byte load (8 values, which
-  // feed exactly fragment steps 2h and 2h + 1 of either weight type) at a
-  // time, scales it by 2^e, rounds it to f16 and stores the two steps'
-  // 8-byte fragment words (a warp's stores for one step are 256 contiguous
-  // bytes).
+  // ---- stage x: one thread per (group, token, class) chunk of 32 k values:
+  // four 16-byte loads; the chunk's largest finite |x| (a bf16 magnitude
+  // below 0x7F80, compared as an integer), shared with the group's other
+  // three chunks, which sit in lanes 4j .. 4j + 3 of the same warp (the
+  // block size is a multiple of 4; every lane takes part in every pass);
+  // the values times 2^e rounded to f16; the fragment permutation on whole
+  // words (e4m3: the values' own order; INT4: two byte permutes per pair of
+  // words); eight 8-byte stores (a warp's stores for one step are 256
+  // contiguous bytes).
   const int nch = ng * Mp * 4;
-  for (int m = tid; m < Mp; m += blockDim.x) xmax[m] = 0u;
-  __syncthreads();
-  auto chunk_src = [&](int ch) {
+  for (int base = 0; base < nch; base += blockDim.x) {
+    const int ch = base + tid;
     const int cl = ch & 3, m = (ch >> 2) % Mp, g = (ch >> 2) / Mp;
-    return reinterpret_cast<const uint4 *>(a.x + static_cast<int64_t>(m) * a.K + kb0 +
-                                           g * kWqGroup + cl * 32);
-  };
-  for (int ch = tid; ch < nch; ch += blockDim.x) {
-    const int m = (ch >> 2) % Mp;
-    if (m >= a.M) continue;
-    const uint4 *src = chunk_src(ch);
-    float mx = 0.f;
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const uint4 u = __ldg(src + h);
-      float xf[8];
-      bf16x2_to_f32(u.x, xf);
-      bf16x2_to_f32(u.y, xf + 2);
-      bf16x2_to_f32(u.z, xf + 4);
-      bf16x2_to_f32(u.w, xf + 6);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float ax = fabsf(xf[e]);
-        if (ax < INFINITY) mx = fmaxf(mx, ax);  // NaN and inf take no part
-      }
-    }
-    if (mx > 0.f) atomicMax(xmax + m, __float_as_uint(mx));
-  }
-  __syncthreads();
-  for (int ch = tid; ch < nch; ch += blockDim.x) {
-    const int cl = ch & 3, m = (ch >> 2) % Mp, g = (ch >> 2) / Mp;
-    const bool real = m < a.M;
-    const uint4 *src = chunk_src(ch);
-    float f1 = 0.f, f2 = 0.f;  // tokens past M: zeros
+    const bool real = ch < nch && m < a.M;
+    uint32_t wv[16];  // bf16 pairs, value 2i in the low half of word i
+    uint32_t mx = 0u;
     if (real) {
-      const int ex = x_exponent(xmax[m]);
-      // x * 2^ex as two products by normal powers of two (2^ex alone is not
-      // a float for ex > 127); each is exact for the values f16 can hold
-      f1 = ldexpf(1.f, ex > 127 ? ex - 64 : ex);
-      f2 = ex > 127 ? 18446744073709551616.f : 1.f;  // 2^64
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          a.x + static_cast<int64_t>(m) * a.K + kb0 + g * kWqGroup + cl * 32);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint4 u = __ldg(src + h);
+        wv[4 * h] = u.x;
+        wv[4 * h + 1] = u.y;
+        wv[4 * h + 2] = u.z;
+        wv[4 * h + 3] = u.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t lo = wv[i] & 0x7FFFu, hi = (wv[i] >> 16) & 0x7FFFu;
+        if (lo < 0x7F80u) mx = max(mx, lo);  // NaN and inf take no part
+        if (hi < 0x7F80u) mx = max(mx, hi);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) wv[i] = 0u;
     }
-    uint2 *dst = reinterpret_cast<uint2 *>(xs) + (g * 8 * Mp + m) * 4 + cl;
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (ch < nch) {
+      const int ex = x_exponent(mx << 16);
+      if (cl == 0) xu[g * Mp + m] = pow2_any(-ex);
+      // x * 2^ex as products by normal powers of two (2^ex alone is not a
+      // float for ex > 127), each exact for the values f16 can hold
+      const float f1 = pow2i(ex > 127 ? ex - 64 : ex);
+      const float f2 = ex > 127 ? pow2i(64) : 1.f;
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const uint4 u = real ? __ldg(src + h) : make_uint4(0, 0, 0, 0);
-      float xf[8];
-      bf16x2_to_f32(u.x, xf);
-      bf16x2_to_f32(u.y, xf + 2);
-      bf16x2_to_f32(u.z, xf + 4);
-      bf16x2_to_f32(u.w, xf + 6);
-      auto h2 = [&](int i, int j) {  // f16 pair (value i low, value j high), scaled
-        const __half2 r = __floats2half2_rn((xf[i] * f1) * f2, (xf[j] * f1) * f2);
-        return *reinterpret_cast<const uint32_t *>(&r);
-      };
+      for (int i = 0; i < 16; ++i) {
+        float xf[2];
+        bf16x2_to_f32(wv[i], xf);
+        const __half2 h = ex > 127 ? __floats2half2_rn((xf[0] * f1) * f2, (xf[1] * f1) * f2)
+                                   : __floats2half2_rn(xf[0] * f1, xf[1] * f1);
+        wv[i] = *reinterpret_cast<const uint32_t *>(&h);
+      }
+      uint2 *dst = reinterpret_cast<uint2 *>(xs) + (g * 8 * Mp + m) * 4 + cl;
 #pragma unroll
-      for (int st = 2 * h; st < 2 * h + 2; ++st)
-        dst[st * Mp * 4] = make_uint2(h2(frag_src<kInt4>(st, 0) - 8 * h, frag_src<kInt4>(st, 1) - 8 * h),
-                                      h2(frag_src<kInt4>(st, 2) - 8 * h, frag_src<kInt4>(st, 3) - 8 * h));
+      for (int st = 0; st < 8; ++st) {
+        if constexpr (kInt4) {
+          // values 8q + p + {0, 4} and 8q + p + {1, 5}, q = st / 2, p = 2 (st % 2)
+          const uint32_t a0 = wv[4 * (st >> 1) + (st & 1)], a2 = wv[4 * (st >> 1) + (st & 1) + 2];
+          dst[st * Mp * 4] = make_uint2(__byte_perm(a0, a2, 0x5410), __byte_perm(a0, a2, 0x7632));
+        } else {
+          dst[st * Mp * 4] = make_uint2(wv[2 * st], wv[2 * st + 1]);  // values 4st .. 4st + 3
+        }
+      }
     }
   }
   // ---- group scales of the CTA's rows (INT4), bf16
@@ -272,11 +292,7 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
       constexpr int kAhead = C::kDepth - 1;
       const int nd = (d + kAhead) % C::kDepth;  // register slot of group g + kDepth - 1
       load(g + kAhead, wr0[nd], wr8[nd]);
-      float gacc[NT][4];
-      if constexpr (kInt4) {
-#pragma unroll
-        for (int t = 0; t < NT; ++t) gacc[t][0] = gacc[t][1] = gacc[t][2] = gacc[t][3] = 0.f;
-      }
+      float gacc[NT][4];  // the group's sums (the first step writes them)
 #pragma unroll
       for (int st = 0; st < 8; ++st) {
         uint32_t af[4];
@@ -298,18 +314,42 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
         for (int t = 0; t < NT; ++t) {
           const uint2 b = (NT > 1 || rr < Mp) ? xb[((g * 8 + st) * Mp + t * 8 + rr) * 4 + c]
                                               : make_uint2(0u, 0u);
-          mma_f16_16816(kInt4 ? gacc[t] : acc[t], af, b.x, b.y);
+          if (st == 0)
+            mma_f16_16816_zero(gacc[t], af, b.x, b.y);
+          else
+            mma_f16_16816(gacc[t], af, b.x, b.y);
         }
       }
+      // the group's sums back to x's scale (2^-e of each token: exact unless
+      // the sum is below fp32's normal range), times the INT4 group scale,
+      // into the output
+      float s0 = 1.f, s8 = 1.f;
       if constexpr (kInt4) {
-        const float s0 = __uint_as_float(uint32_t(sc0[g]) << 16);
-        const float s8 = __uint_as_float(uint32_t(sc8[g]) << 16);
+        s0 = __uint_as_float(uint32_t(sc0[g]) << 16);
+        s8 = __uint_as_float(uint32_t(sc8[g]) << 16);
+      }
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          acc[t][0] = fmaf(s0, gacc[t][0], acc[t][0]);
-          acc[t][1] = fmaf(s0, gacc[t][1], acc[t][1]);
-          acc[t][2] = fmaf(s8, gacc[t][2], acc[t][2]);
-          acc[t][3] = fmaf(s8, gacc[t][3], acc[t][3]);
+      for (int t = 0; t < NT; ++t) {
+        const int n0 = t * 8 + 2 * c;  // tokens of accumulator elements 0/2 and 1/3
+        float u0, u1;
+        if constexpr (NT > 1) {  // Mp = 8 NT: both tokens staged, the pair 8-byte aligned
+          const float2 u = *reinterpret_cast<const float2 *>(xu + g * Mp + n0);
+          u0 = u.x;
+          u1 = u.y;
+        } else {
+          u0 = n0 < Mp ? xu[g * Mp + n0] : 0.f;
+          u1 = n0 + 1 < Mp ? xu[g * Mp + n0 + 1] : 0.f;
+        }
+        if constexpr (kInt4) {
+          acc[t][0] = fmaf(s0, gacc[t][0] * u0, acc[t][0]);
+          acc[t][1] = fmaf(s0, gacc[t][1] * u1, acc[t][1]);
+          acc[t][2] = fmaf(s8, gacc[t][2] * u0, acc[t][2]);
+          acc[t][3] = fmaf(s8, gacc[t][3] * u1, acc[t][3]);
+        } else {
+          acc[t][0] = fmaf(gacc[t][0], u0, acc[t][0]);
+          acc[t][1] = fmaf(gacc[t][1], u1, acc[t][1]);
+          acc[t][2] = fmaf(gacc[t][2], u0, acc[t][2]);
+          acc[t][3] = fmaf(gacc[t][3], u1, acc[t][3]);
         }
       }
     }
@@ -329,9 +369,7 @@ __global__ void __launch_bounds__(32 * kWqWarps) wq_gemm_kernel(WqArgs a) {
       const int n = t * 8 + 2 * c + (e & 1);
       const int row = row0 + (e >> 1) * 8;
       if (n >= a.M || row >= a.N) continue;
-      // the channel scale, then back to x's scale (exact unless the result
-      // is below fp32's normal range; one rounding there)
-      const float v = (acc[t][e] * ((e >> 1) ? f8 : f0)) * ldexpf(1.f, -x_exponent(xmax[n]));
+      const float v = acc[t][e] * ((e >> 1) ? f8 : f0);
       float *dst = a.y + static_cast<int64_t>(n) * a.N + row;
       if (a.atomic)
         atomicAdd(dst, v);

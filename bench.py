@@ -87,6 +87,8 @@ def parse_args():
                     help="keep the raw nvidia-smi clock samples in this file")
     ap.add_argument("--no-parity-check", action="store_true",
                     help="skip comparing sampled rows of the last timed step with the oracle")
+    ap.add_argument("--sweep-tokens", type=int, default=1000,
+                    help="--sweep: generated tokens timed per point (all 1000 by default)")
     ap.add_argument("--sweep", action="store_true",
                     help="concurrency sweep 1/8/16/32/64 requests, e4m3 and bf16 KV at equal pool "
                          "bytes; one JSON line per point (not the headline line)")
@@ -369,6 +371,32 @@ class DecodeStep:
         else:
             self.eager(self.static)
 
+    def capture_flush_pair(self, flush):
+        """Two more graphs for timing the attention call as it runs inside a
+        step graph: the L2 flush alone, and the flush followed by the call.
+        Their difference is the call's device time without the launch latency
+        of a graph (which a step graph pays once for all its kernels)."""
+        torch = self.torch
+        self.g_f = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_f):
+            flush()
+        self.g_fa = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_fa):
+            flush()
+            self.attn(self.static)
+        torch.cuda.synchronize()
+
+    def run_attn_diff(self, row, ev, stream):
+        """Stages the step's inputs, then the flush graph and the flush +
+        attention graph, each between two recorded events (ev: four events)."""
+        self.row.copy_(row, non_blocking=True)
+        ev[0].record(stream)
+        self.g_f.replay()
+        ev[1].record(stream)
+        ev[2].record(stream)
+        self.g_fa.replay()
+        ev[3].record(stream)
+
     def run_attn_timed(self, row, ev, stream):
         """The step's attention call alone between two recorded events (for
         the graph, the step's inputs are staged before the first event)."""
@@ -402,20 +430,28 @@ class L2Flush:
 
 def time_steps(torch, step, d_rows, warmup, steps, flush=None):
     """Warm-up steps, then `steps` whole steps, then each step's attention
-    call timed alone.  Returns (ms per step, [ms per attention call]).
-    Without `flush` the whole steps run back to back in one timed region;
-    with it, L2 is flushed before every timed step and every attention call,
-    and each is timed by its own pair of events."""
+    call timed alone.  Returns (ms per step, [ms per attention call],
+    [ms per attention call in its own graph] or None).
+    Without `flush` the whole steps run back to back in one timed region and
+    each attention call is timed in its own graph.  With it, L2 is flushed
+    before every timed step and each step is timed by its own pair of
+    events; the attention call is timed (graph mode) as the difference of a
+    graph holding the flush and the call and one holding the flush alone, so
+    that the graph's own launch latency cancels (the call as it runs inside a
+    step graph), and also in its own graph after a flush (launch latency
+    included)."""
     stream = torch.cuda.current_stream()
     for i in range(warmup):
         step.eager(step.packer.views(d_rows[i]))
     if step.graph:
         step.capture(d_rows[max(warmup - 1, 0)])
         step.run(d_rows[max(warmup - 1, 0)])
+        if flush is not None:
+            step.capture_flush_pair(flush)
     torch.cuda.synchronize()
 
-    def pairs():
-        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    def pairs(k=2):
+        return [tuple(torch.cuda.Event(enable_timing=True) for _ in range(k))
                 for _ in range(steps)]
 
     ev, es = pairs(), pairs()
@@ -436,17 +472,26 @@ def time_steps(torch, step, d_rows, warmup, steps, flush=None):
             else:
                 step.eager(step.packer.views(d_rows[warmup + j]))
             es[j][1].record(stream)
+    own = None
     if step.graph or flush is not None:
         for j in range(steps):
             if flush is not None:
                 flush()
             step.run_attn_timed(d_rows[warmup + j], ev[j], stream)
+    if step.graph and flush is not None:
+        own = ev
+        ev = pairs(4)
+        for j in range(steps):
+            step.run_attn_diff(d_rows[warmup + j], ev[j], stream)
     torch.cuda.synchronize()
     if flush is None:
         step_ms = es[0][0].elapsed_time(es[0][1]) / steps
     else:
         step_ms = statistics.mean(a.elapsed_time(b) for a, b in es)
-    return step_ms, [a.elapsed_time(b) for a, b in ev]
+    if own is None:
+        return step_ms, [e[0].elapsed_time(e[1]) for e in ev], None
+    return (step_ms, [e[2].elapsed_time(e[3]) - e[0].elapsed_time(e[1]) for e in ev],
+            [e[0].elapsed_time(e[1]) for e in own])
 
 
 # ----------------------------------------------------------------------------
@@ -880,8 +925,11 @@ def run_reference(args, rank):
 
 def run_sweep(args):
     """FP8 vs BF16 KV over 1..64 concurrent requests at equal pool bytes (the
-    pages' decode table shape).  Each point times `steps` decode steps
-    (append + attention, no tag check) after `warmup` steps."""
+    pages' decode table shape: 8192-token prompts, 1000 generated tokens).
+    Each point runs the whole generation: `--sweep-tokens` (default all
+    1000) decode steps (append + attention, no tag check), timed after
+    `warmup` steps that append the first generated tokens (re-appended, same
+    values, by the timed steps), and reports the mean over the generation."""
     import torch
     from fp8_paged_kv_attn_gb300 import inputs, kvq
 
@@ -890,6 +938,7 @@ def run_sweep(args):
     ref = inputs.sweep(64, kv_bytes=1, seed=args.seed)
     sources = ref.kv_sources(threads=os.cpu_count() or 8)
     ks, vs = ref.scales(sources)
+    n_gen = min(args.sweep_tokens, inputs.SWEEP_DECODE_STEPS)
 
     def bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
@@ -913,8 +962,9 @@ def run_sweep(args):
                 req, pos = w.context_tokens(b)
                 kvq.kvq_append(cache, bf16(k).cuda(), bf16(v).cuda(), torch.from_numpy(req).cuda(),
                                torch.from_numpy(pos).cuda(), bt)
-            n = args.warmup + args.steps
-            gen = [(args.offset + i) % inputs.SWEEP_DECODE_STEPS for i in range(n)]
+            # warm-up steps append generated tokens 0 .. W-1; the timed steps
+            # then run the whole generation, tokens 0 .. n_gen-1
+            gen = list(range(args.warmup)) + list(range(n_gen))
             packer = StepInputs(torch, B, w.Hq, w.Hkv, w.D)
             lens = [w.seq_lens_after(gi) for gi in gen]
             rows = []
@@ -922,30 +972,36 @@ def run_sweep(args):
                 q, k_new, v_new, _, pos = w.step_inputs(gi)
                 rows.append({"q": q, "k": k_new, "v": v_new, "pos": pos, "lens": ln})
             d_rows = packer.pack(rows).cuda()
+            del rows
             out = torch.empty((B, w.Hq, w.D), dtype=torch.float32, device="cuda")
             ws = kvq.workspace(B, w.Hq, w.Hkv, w.D)
             step = DecodeStep(torch, kvq, cache, bt, w.P, float(w.sm_scale), packer, out, ws,
                               graph=not args.eager)
             byts = [attn_bytes(lens[i], w.Hq, w.Hkv, w.D, w.P, kv_bytes)
-                    for i in range(args.warmup, n)]
+                    for i in range(args.warmup, len(gen))]
             flush = L2Flush(torch) if L2Flush.needed(torch, byts[0]) else None
-            step_ms, attn_ms = time_steps(torch, step, d_rows, args.warmup, args.steps, flush)
+            step_ms, attn_ms, attn_own = time_steps(torch, step, d_rows, args.warmup, n_gen,
+                                                    flush)
             gbs = sum(byts) / (sum(attn_ms) * 1e-3) / 1e9
-            line = {"sweep": True, "kv": kv, "batch": B,
+            line = {"sweep": True, "kv": kv, "batch": B, "generated_tokens": n_gen,
                     "tokens_per_s": round(B / (step_ms * 1e-3), 1),
                     "ms_per_step": round(step_ms, 5),
                     "attn_us": round(statistics.mean(attn_ms) * 1e3, 2),
                     "attn_us_p95": round(float(np.percentile(attn_ms, 95)) * 1e3, 2),
                     "attn_GBs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
                     "l2": "flushed before each step" if flush else "KV larger than 2 x L2; no flush",
+                    "attn_timing": ("difference of a graph of (L2 flush, call) and one of the "
+                                    "flush alone" if attn_own else "the call's own graph"),
                     "pool_pages": w.num_pages,
                     "mean_context": round(float(np.mean([x.mean() for x in lens[args.warmup:]])), 1)}
+            if attn_own:
+                line["attn_us_own_graph"] = round(statistics.mean(attn_own) * 1e3, 2)
             if flush is not None:  # the same steps back to back, L2 warm, for comparison
-                wstep, wattn = time_steps(torch, step, d_rows, args.warmup, args.steps)
+                wstep, wattn, _ = time_steps(torch, step, d_rows, args.warmup, n_gen)
                 line["tokens_per_s_warm"] = round(B / (wstep * 1e-3), 1)
                 line["attn_us_warm"] = round(statistics.mean(wattn) * 1e3, 2)
             print(json.dumps(line), flush=True)
-            del cache
+            del cache, d_rows
 
 
 WORKLOADS = {"ragged": "ragged", "integrity": "integrity", "8x8192": "cfg8x8k"}
@@ -996,11 +1052,11 @@ class WorkloadStep:
             step = DecodeStep(torch, self.kvq, self.cache, self.bt, P, float(w.sm_scale),
                               self.packer, self.out, self.ws, check=check, tags=self.tags,
                               exp_tags=self.exp_tags, mask=self.mask, graph=not self.eager)
-            step_ms, attn_ms = time_steps(torch, step, self.rows, warmup, steps, self.flush)
-            return step_ms, statistics.mean(attn_ms)
+            step_ms, attn_ms, own = time_steps(torch, step, self.rows, warmup, steps, self.flush)
+            return step_ms, statistics.mean(attn_ms), (statistics.mean(own) if own else None)
 
-        step_on, attn_on = run(True)
-        step_off, attn_off = run(False)
+        step_on, attn_on, own_on = run(True)
+        step_off, attn_off, _ = run(False)
         peak, _ = measured_hbm_peak()
         aborted = int(self.mask.sum().item())
         alive = (self.mask.cpu().numpy() == 0)
@@ -1014,7 +1070,12 @@ class WorkloadStep:
                "attn_GBs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
                "aborted_requests": aborted,
                "l2": "flushed before each step" if self.flush else
-                     "KV larger than 2 x L2; no flush"}
+                     "KV larger than 2 x L2; no flush",
+               "attn_timing": ("difference of a graph of (L2 flush, call) and one of the flush "
+                               "alone" if own_on else "the call's own graph")}
+        if own_on:
+            res["attn_us_own_graph"] = round(own_on * 1e3, 2)
+            res["frac_own_graph"] = round(byts / (own_on * 1e-3) / 1e9 / peak, 4)
         if self.name == "integrity":
             res["step_ms_without_check"] = round(step_off, 5)
             res["check_overhead_pct_of_step"] = round(100 * (step_on - step_off) / step_off, 2)

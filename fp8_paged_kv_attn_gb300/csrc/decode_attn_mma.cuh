@@ -585,7 +585,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
     int win_b = -1, win = 0, cur = -1, nxt = -1;
     const int32_t *bt_row = a.block_table;
     auto bt_load = [&](int lp) -> int { return lp < a.MP ? __ldg(bt_row + lp) : -1; };
-    uint32_t g = 0, nseg = 0;
+    uint32_t g = 0, nseg = 0, nq = 0;  // stages, segments and query copies issued
     bool ok = true;
     while (ok && u < u_end && b < a.B) {
       const int row = b * groups + grp;
@@ -615,6 +615,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
           bulk_g2s(qbuf + qs * C::Q_BYTES,
                    a.q + (static_cast<int64_t>(b) * a.Hq + grp * HG * G) * C::D, C::Q_BYTES,
                    &ctl.qfull[qs]);
+          ++nq;
         }
       }
       for (int st = 0; st < nstages; ++st, ++g) {
@@ -738,6 +739,14 @@ __global__ void __launch_bounds__(32 * (HG + 1))
         ctl.desc[slot][0] = make_int4(-1, 0, 0, 0);
         mbar_arrive(&ctl.full[slot]);
       }
+    } else if (lane == 0) {
+      // A wait gave up: before the CTA exits, let the copies it started land
+      // (bounded waits), so that none writes into shared memory the SM may
+      // already have handed to another CTA.  Only the last NS stages and the
+      // last two query copies can still be in flight (a slot is reused only
+      // after its previous copy completed and was consumed).
+      for (uint32_t k = g > NS ? g - NS : 0; k < g; ++k) mbar_wait(&ctl.full[k % NS], (k / NS) & 1);
+      for (uint32_t k = nq > 2 ? nq - 2 : 0; k < nq; ++k) mbar_wait(&ctl.qfull[k & 1], (k >> 1) & 1);
     }
     // The grid must not complete before the plan has: the combine kernel's
     // wait covers only this grid.

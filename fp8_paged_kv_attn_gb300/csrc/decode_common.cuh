@@ -328,6 +328,13 @@ __device__ __forceinline__ void producer_loop(const SplitArgs &a, Ctrl &ctl, uin
       }
     }
   }
+  // A wait gave up (not the normal end, which arrives with the end marker):
+  // before the CTA exits, let the copies it started land (bounded waits), so
+  // that none writes into shared memory the SM may already have handed to
+  // another CTA.  Only the last kStages stages can still be in flight.
+  if (lane == 0 && *reinterpret_cast<volatile int *>(&ctl.fail))
+    for (uint32_t k = g > kStages ? g - kStages : 0; k < g; ++k)
+      mbar_wait(&ctl.full[k % kStages], (k / kStages) & 1);
 }
 
 // ---------------------------------------------------------------------------

@@ -12,28 +12,25 @@
 //   stream, e.g. the tag check), so launch latency overlaps the previous
 //   kernel's tail; each waits for its predecessor before touching memory.
 //
-//   plan   1 CTA: per-request unit counts, their prefix sum, where each
-//          persistent CTA starts, zeroed per-row bad-page flags, the lists of
-//          rows split across CTAs; rows of aborted / empty / invalid requests
-//          are written as zeros.
-//   split  persistent grid of (#SMs x resident CTAs), launched as a
-//          programmatic dependent of the plan so its set-up overlaps it.
-//          The tensor-core kernel also works out its own start from the
-//          lengths and the abort mask and starts copying pages before the
-//          plan has finished (it waits for the plan only before it sets a
-//          bad-page flag, the one thing the plan writes that it touches).
-//          Each CTA owns an equal run of units (see decode_common.cuh).  Warp
-//          4 produces: it reads the block table and stages every page's
-//          contiguous [slot][dim] chunk of the row's kv head into a 4-stage
-//          shared-memory ring with TMA-engine copies (mbarrier-tracked, L2
-//          evict-first).  Warps 0-3 consume: convert, q.k for the G query
-//          heads sharing the kv head (each cached element converted once, used
-//          G times), online softmax in the log2 domain with lazy rescaling,
-//          p.v; at the end of a segment they merge and either write the
-//          output row or, for a row split across CTAs, a partial.
+//   plan   (only for batches the split kernel cannot schedule itself, and
+//          for the head_dim-64 kernel) 1 CTA: per-request unit counts, their
+//          prefix sum, where each persistent CTA starts; rows of aborted /
+//          empty / invalid requests are written as zeros with a descriptor
+//          of 0 parts.
+//   split  persistent grid of (#SMs x resident CTAs).  The tensor-core
+//          kernel works out its own start from the lengths and the abort
+//          mask for up to 4,608 requests, so then it is the call's first
+//          kernel.  Each CTA owns an equal run of units (see
+//          decode_common.cuh).  A producer warp reads the block table and
+//          stages the pages with TMA-engine copies into a shared-memory ring
+//          (mbarrier-tracked, L2 evict-first); consumer warps convert, run
+//          q.k for the query heads sharing a kv head (each cached element
+//          converted once, used G times), the online softmax in the log2
+//          domain with lazy rescaling, and p.v; at the end of a segment they
+//          write the output row or, for a row split across CTAs, a partial.
 //   combine merges the partials of every split row once the split grid has
 //          finished (a warp per output row for rows of a few parts, a CTA
-//          per output row for rows of many).
+//          per output row for rows of many), reading each row's descriptor.
 //   Two split kernels exist: a tensor-core one for head_dim 128, e4m3 or
 //   bf16 (decode_attn_mma.cuh: rows are groups of up to 8 kv heads, 16-token
 //   units, one consumer warp per kv head) and a CUDA-core one for head_dim 64
@@ -57,7 +54,7 @@ namespace kvq {
 // ---------------------------------------------------------------------------
 
 struct WsLayout {
-  size_t hdr, prefix, start, bad, comb, combw, part, total;
+  size_t hdr, prefix, start, desc, part, total;
 };
 
 inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -73,14 +70,9 @@ inline WsLayout ws_layout(int B, int Hq, int Hkv, int D) {
   off = round256(off + (static_cast<size_t>(B) + 1) * sizeof(int32_t));
   w.start = off;
   off = round256(off + static_cast<size_t>(kMaxCtas) * sizeof(int4));
-  w.bad = off;
-  off = round256(off + rows * sizeof(int32_t));
-  // rows the combine kernel merges, {row, first CTA, parts, request}: split
-  // over more than kWarpMergeMax CTAs (a CTA per output row), and over 2 to
-  // kWarpMergeMax (a warp per output row)
-  w.comb = off;
-  off = round256(off + rows * sizeof(int4));
-  w.combw = off;
+  // a descriptor per row (first CTA, parts, request): rows are kv heads or
+  // groups of kv heads, at most B * Hkv
+  w.desc = off;
   off = round256(off + rows * sizeof(int4));
   // partial slots: row + CTA for every row split across CTAs; a tensor-core
   // row holds up to 8 kv heads, a CUDA-core row one
@@ -105,8 +97,7 @@ struct PlanArgs {
   const uint8_t *abort_mask;
   int32_t *hdr, *prefix;
   int4 *start;
-  int32_t *bad;
-  int4 *comb, *combw;
+  int4 *desc;
   float *out;
   uint32_t *err_word;
   int32_t B, Hq, D, MP, P, nctas;
@@ -116,11 +107,7 @@ struct PlanArgs {
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   grid_dependency_wait();  // e.g. the tag check's abort mask is visible from here on
-  // The split grid may launch now.  This comes after the wait on purpose:
-  // the tensor-core split kernel reads seq_lens and the abort mask before its
-  // own wait, which is safe only because everything ahead of the plan on the
-  // stream has completed by the time the split grid can launch.
-  allow_dependents();
+  allow_dependents();      // the split grid may launch; it waits for this grid
   __shared__ int s_scan[32];
   __shared__ int s_carry;
   __shared__ int s_prefix[kPlanSmemPrefix];
@@ -154,10 +141,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     if (b < a.B) {
       a.prefix[b] = pre;
       if (b < kPlanSmemPrefix) s_prefix[b] = pre;
-      for (int h = 0; h < a.rows_per_req; ++h) a.bad[b * a.rows_per_req + h] = 0;
-      if (units == 0) {  // aborted, empty or invalid: the rows are zero
+      if (units == 0) {  // aborted, empty or invalid: the rows are zero, with no parts
         float4 *o = reinterpret_cast<float4 *>(a.out + static_cast<int64_t>(b) * a.Hq * a.D);
         for (int i = 0; i < a.Hq * a.D / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < a.rows_per_req; ++r)
+          a.desc[b * a.rows_per_req + r] = make_int4(0, 0, b, 0);
       }
     }
     __syncthreads();
@@ -195,31 +183,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
     const int r = static_cast<int>(u - p0);
     a.start[c] = make_int4(lo, r / units_b, r % units_b, 0);
   }
-  // rows split across CTAs go to the combine kernel
-  __shared__ int s_ncomb, s_ncombw;
-  if (tid == 0) s_ncomb = s_ncombw = 0;
-  __syncthreads();
-  for (int b = tid; b < a.B; b += nt) {
-    const int p0 = in_smem ? s_prefix[b] : __ldcg(a.prefix + b);
-    const int p1 = in_smem ? s_prefix[b + 1] : __ldcg(a.prefix + b + 1);
-    const int units_b = (p1 - p0) / a.rows_per_req;
-    if (units_b == 0) continue;
-    for (int r = 0; r < a.rows_per_req; ++r) {
-      const long long ur = static_cast<long long>(p0) + static_cast<long long>(r) * units_b;
-      const int nparts = static_cast<int>((ur + units_b - 1) / U - ur / U) + 1;
-      const int4 item = make_int4(b * a.rows_per_req + r, static_cast<int>(ur / U), nparts, b);
-      if (nparts > kWarpMergeMax)
-        a.comb[atomicAdd(&s_ncomb, 1)] = item;
-      else if (nparts > 1)
-        a.combw[atomicAdd(&s_ncombw, 1)] = item;
-    }
-  }
-  __syncthreads();
   if (tid == 0) {
     a.hdr[0] = S;
     a.hdr[1] = U;
-    a.hdr[2] = s_ncomb;
-    a.hdr[3] = s_ncombw;
   }
 }
 
@@ -452,8 +418,7 @@ __global__ void __launch_bounds__(32 * (kConsumerWarps + 1), 2) split_kernel(Spl
 // ---------------------------------------------------------------------------
 
 struct CombineArgs {
-  const int32_t *hdr, *bad;
-  const int4 *comb, *combw;
+  const int4 *desc;
   const float *part;
   float *out;
   int32_t B, Hq, Hkv, G, D, hg, rows_per_req;
@@ -462,34 +427,35 @@ struct CombineArgs {
 
 constexpr int kWarpBatch = 4;  // parts loaded at once by a warp-merged row
 
-// One output row (query head hr of a listed row) and where its parts live.
+// One output row (query head hr of a row) and where its parts live.
 struct CombineItem {
   float *out;         // D floats
   const float *base;  // part 0 of this query head's kv head
-  int nparts, row, hq;
+  int nparts, hq;
 };
 
-__device__ __forceinline__ CombineItem combine_item(const CombineArgs &a, int4 cd, int hr,
+// d: the row's descriptor (first CTA, parts, request, 0).
+__device__ __forceinline__ CombineItem combine_item(const CombineArgs &a, int row, int4 d, int hr,
                                                     int64_t slot_floats, int64_t kpart) {
   CombineItem it;
-  it.row = cd.x;
-  it.nparts = cd.z;
-  const int c_lo = cd.y, b = cd.w;
-  const int rin = it.row % a.rows_per_req;
+  it.nparts = d.y;
+  const int c_lo = d.x, b = d.z;
+  const int rin = row % a.rows_per_req;
   const int kvh_in = hr / a.G;
   it.hq = hr % a.G;
   it.out = a.out + (static_cast<int64_t>(b) * a.Hq + (rin * a.hg + kvh_in) * a.G + it.hq) * a.D;
-  it.base = a.part + static_cast<int64_t>(it.row + c_lo) * slot_floats + kvh_in * kpart;
+  it.base = a.part + static_cast<int64_t>(row + c_lo) * slot_floats + kvh_in * kpart;
   return it;
 }
 
 // Folds parts p0, p0 + step, ... (< nparts) of one output row into a running
 // maximum M, denominator den and accumulator acc (dims 4*lane..+3): the
-// parts are loaded NB at a time, every load of a batch issued together.
+// parts are loaded NB at a time, every load of a batch issued together.  A
+// part whose l is negative met a page outside the pool: `bad` is set.
 template <int NB>
 __device__ __forceinline__ void merge_parts(const CombineItem &it, int p0, int step, int slot32,
                                             int GD, int G, int D, int lane, bool active,
-                                            float &M, float &den, float4 &acc) {
+                                            float &M, float &den, float4 &acc, bool &bad) {
   for (int pb = p0; pb < it.nparts; pb += NB * step) {
     float m[NB], l[NB];
     float4 v[NB];
@@ -503,6 +469,8 @@ __device__ __forceinline__ void merge_parts(const CombineItem &it, int p0, int s
       v[j] = in && active ? __ldcg(reinterpret_cast<const float4 *>(pp + it.hq * D) + lane)
                           : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) bad |= l[j] < 0.f;
     float Mb = M;
 #pragma unroll
     for (int j = 0; j < NB; ++j) Mb = fmaxf(Mb, m[j]);
@@ -529,100 +497,132 @@ __device__ __forceinline__ void merge_parts(const CombineItem &it, int p0, int s
 // m[G], l[G] per kv head, m in the log2 domain):
 //   out = v_scale * sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
 // A part whose maximum is -inf carries no weight and its values are not used;
-// a row with a page outside the pool is written as zeros.  Both kinds of
-// work item fold parts with merge_parts (lane l owns dims 4l..4l+3):
-//  - rows of 2..kWarpMergeMax parts: one warp per output row;
-//  - longer rows (a row of a short batch can have hundreds of parts): a CTA
-//    per output row, its 16 warps folding every 16th part each, then warp 0
-//    folding the 16 results from shared memory.
-// With nothing listed it exits after reading the two counts.  Two builds:
-// kSubsets = 16 warps uncapped (more of a long row's loads in flight) for
-// grids of at most #SMs CTAs, and 8 warps capped at 64 registers (4 CTAs per
-// SM) otherwise, small enough that one CTA becomes resident beside a running
-// split CTA and is waiting when the split grid ends.
+// a row with a part that met a page outside the pool (l < 0) is written as
+// zeros.  The work items are all output rows (row, query head), in two
+// passes that read each row's descriptor: output rows of rows in more than
+// kWarpMergeMax parts, a CTA each (a row of a short batch can have hundreds
+// of parts), its kSubsets warps folding every kSubsets-th part and warp 0
+// folding their results from shared memory; then output rows of rows in 2 to
+// kWarpMergeMax parts, a warp each.  A CTA (warp) loads the descriptors of
+// all its items at once.  Two builds: kSubsets = 16 warps uncapped (more of a
+// long row's loads in flight) for grids of at most #SMs CTAs, and 8 warps
+// capped at 64 registers (4 CTAs per SM) otherwise, small enough that one
+// CTA becomes resident beside a running split CTA and is waiting when the
+// split grid ends.
 template <int kMinBlocks, int kSubsets>
 __global__ void __launch_bounds__(32 * kSubsets, kMinBlocks) combine_kernel(CombineArgs a) {
-  constexpr int kCombineSubsets = kSubsets;  // part subsets (warps) per CTA
-  __shared__ float s_m[kCombineSubsets], s_den[kCombineSubsets];
-  __shared__ float4 s_acc[kCombineSubsets][32];
+  __shared__ float s_m[kSubsets], s_den[kSubsets];
+  __shared__ float4 s_acc[kSubsets][32];
+  __shared__ int s_bad[kSubsets];
+  __shared__ int4 s_items[32];  // (item, first CTA, parts, request)
+  __shared__ int s_n;
   grid_dependency_wait();
   allow_dependents();  // e.g. the next step's append may be scheduled
   const int tid = threadIdx.x, sub = tid >> 5, lane = tid & 31;
   const int heads_per_row = a.hg * a.G;
-  const int nrows = a.B * a.rows_per_req;
+  const int nout = a.B * a.Hq;  // output rows: row-major over (row, query head in row)
   const int64_t kpart = part_stride(a.G, a.D);  // 16-byte multiple
   const int64_t slot_floats = a.hg * kpart;
+  const int slot32 = static_cast<int>(slot_floats);  // at most 8 x 1040 floats
   const int GD = a.G * a.D;
   const bool active = 4 * lane < a.D;
-  // the first items' descriptors are loaded together with the counts (both
-  // lists have a slot for every row, so the loads are in bounds even when
-  // the slots are not in use)
-  const int wid = blockIdx.x * kCombineSubsets + sub;  // this warp over the grid
-  int item = blockIdx.x;
-  int4 cd = item / heads_per_row < nrows ? __ldcg(a.comb + item / heads_per_row)
-                                         : make_int4(0, 0, 0, 0);
-  int4 cdw = wid / heads_per_row < nrows ? __ldcg(a.combw + wid / heads_per_row)
-                                         : make_int4(0, 0, 0, 0);
-  const int ncomb = __ldcg(a.hdr + 2);
-  const int ncombw = __ldcg(a.hdr + 3);
 
-  // ---- rows of many parts: a CTA per output row
-  const int slot32 = static_cast<int>(slot_floats);  // at most 8 x 1040 floats
-  for (; item < ncomb * heads_per_row; item += gridDim.x) {
-    if (item != static_cast<int>(blockIdx.x)) cd = __ldcg(a.comb + item / heads_per_row);
-    const CombineItem it = combine_item(a, cd, item % heads_per_row, slot_floats, kpart);
-    const bool row_bad = __ldcg(a.bad + it.row) != 0;  // uniform over the CTA
-    // subset `sub` folds parts sub, sub + 16, ...; then the subsets are folded
-    float M = -INFINITY, den = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    merge_parts<kMinBlocks == 1 ? 8 : kWarpBatch>(it, sub, kCombineSubsets, slot32, GD, a.G, a.D,
-                                                  lane, active, M, den, acc);
-    s_acc[sub][lane] = acc;
-    if (lane == 0) {
-      s_m[sub] = M;
-      s_den[sub] = den;
+  // ---- rows of many parts: a CTA per output row.  Lane j of warp 0 looks
+  // at item blockIdx + (base + j) * grid and lists it, with its row's
+  // descriptor, when the row has more than kWarpMergeMax parts; then the CTA
+  // merges the listed items one by one.
+  for (int64_t base = 0; blockIdx.x + base * gridDim.x < nout; base += 32) {
+    if (sub == 0) {
+      const int64_t item = blockIdx.x + (base + lane) * gridDim.x;
+      int4 d = make_int4(0, 0, 0, 0);
+      if (item < nout) d = __ldcg(a.desc + item / heads_per_row);
+      const bool mine = d.y > kWarpMergeMax;
+      const unsigned bal = __ballot_sync(0xffffffffu, mine);
+      if (mine)
+        s_items[__popc(bal & ((1u << lane) - 1))] = make_int4(static_cast<int>(item), d.x, d.y, d.z);
+      if (lane == 0) s_n = __popc(bal);
     }
     __syncthreads();
-    if (sub == 0 && active) {
-      float Mr = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kCombineSubsets; ++i) Mr = fmaxf(Mr, s_m[i]);
-      float d = 0.f;
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int i = 0; i < kCombineSubsets; ++i) {
-        const float wi = s_m[i] == -INFINITY ? 0.f : exp2f(s_m[i] - Mr);
-        const float4 v = s_acc[i][lane];
-        d = fmaf(wi, s_den[i], d);
-        o.x = fmaf(wi, v.x, o.x);
-        o.y = fmaf(wi, v.y, o.y);
-        o.z = fmaf(wi, v.z, o.z);
-        o.w = fmaf(wi, v.w, o.w);
+    const int n = s_n;
+    for (int k = 0; k < n; ++k) {
+      const int4 li = s_items[k];
+      const int row = li.x / heads_per_row;
+      const CombineItem it = combine_item(a, row, make_int4(li.y, li.z, li.w, 0),
+                                          li.x % heads_per_row, slot_floats, kpart);
+      // subset `sub` folds parts sub, sub + kSubsets, ...; then the subsets are folded
+      float M = -INFINITY, den = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      bool bad = false;
+      merge_parts<kMinBlocks == 1 ? 8 : kWarpBatch>(it, sub, kSubsets, slot32, GD, a.G, a.D, lane,
+                                                    active, M, den, acc, bad);
+      s_acc[sub][lane] = acc;
+      bad = __any_sync(0xffffffffu, bad);
+      if (lane == 0) {
+        s_m[sub] = M;
+        s_den[sub] = den;
+        s_bad[sub] = bad;
       }
-      const float sc = a.v_scale / d;
-      // a bad row is stored as zeros, not scaled by 0: its parts may hold
-      // values computed from a stage whose page was never copied
-      reinterpret_cast<float4 *>(it.out)[lane] =
-          row_bad ? make_float4(0.f, 0.f, 0.f, 0.f)
-                  : make_float4(o.x * sc, o.y * sc, o.z * sc, o.w * sc);
+      __syncthreads();
+      if (sub == 0 && active) {
+        float Mr = -INFINITY;
+        bool row_bad = false;
+#pragma unroll
+        for (int i = 0; i < kSubsets; ++i) {
+          Mr = fmaxf(Mr, s_m[i]);
+          row_bad |= s_bad[i] != 0;
+        }
+        float d = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < kSubsets; ++i) {
+          const float wi = s_m[i] == -INFINITY ? 0.f : exp2f(s_m[i] - Mr);
+          const float4 v = s_acc[i][lane];
+          d = fmaf(wi, s_den[i], d);
+          o.x = fmaf(wi, v.x, o.x);
+          o.y = fmaf(wi, v.y, o.y);
+          o.z = fmaf(wi, v.z, o.z);
+          o.w = fmaf(wi, v.w, o.w);
+        }
+        const float sc = a.v_scale / d;
+        // a bad row is stored as zeros, not scaled by 0: its parts may hold
+        // values computed from a stage whose page was never copied
+        reinterpret_cast<float4 *>(it.out)[lane] =
+            row_bad ? make_float4(0.f, 0.f, 0.f, 0.f)
+                    : make_float4(o.x * sc, o.y * sc, o.z * sc, o.w * sc);
+      }
+      __syncthreads();  // s_acc, s_m, s_den, s_bad are reused by the next item
     }
-    __syncthreads();  // s_acc, s_m, s_den are reused by the next item
+    __syncthreads();  // every warp has read s_n before warp 0 lists the next pass
   }
 
-  // ---- rows of 2..kWarpMergeMax parts: a warp per output row
-  const int nwarps = gridDim.x * kCombineSubsets;
-  for (int w = wid; w < ncombw * heads_per_row; w += nwarps) {
-    if (w != wid) cdw = __ldcg(a.combw + w / heads_per_row);
-    const CombineItem it = combine_item(a, cdw, w % heads_per_row, slot_floats, kpart);
-    const bool row_bad = __ldcg(a.bad + it.row) != 0;
-    float M = -INFINITY, den = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    merge_parts<kWarpBatch>(it, 0, 1, slot32, GD, a.G, a.D, lane, active, M, den, acc);
-    if (active) {
-      const float sc = a.v_scale / den;
-      reinterpret_cast<float4 *>(it.out)[lane] =
-          row_bad ? make_float4(0.f, 0.f, 0.f, 0.f)
-                  : make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+  // ---- rows of 2..kWarpMergeMax parts: a warp per output row.  Lane j looks
+  // at item wid + (base + j) * nwarps; the warp merges the listed ones.
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kSubsets;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kSubsets + sub;
+  for (int64_t base = 0; wid + base * nwarps < nout; base += 32) {
+    const int64_t item = wid + (base + lane) * nwarps;
+    int4 d = make_int4(0, 0, 0, 0);
+    if (item < nout) d = __ldcg(a.desc + item / heads_per_row);
+    unsigned todo = __ballot_sync(0xffffffffu, d.y >= 2 && d.y <= kWarpMergeMax);
+    while (todo) {
+      const int j = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int it_idx = static_cast<int>(__shfl_sync(0xffffffffu, item, j));
+      const int4 dj = make_int4(__shfl_sync(0xffffffffu, d.x, j), __shfl_sync(0xffffffffu, d.y, j),
+                                __shfl_sync(0xffffffffu, d.z, j), 0);
+      const int row = it_idx / heads_per_row;
+      const CombineItem it = combine_item(a, row, dj, it_idx % heads_per_row, slot_floats, kpart);
+      float M = -INFINITY, den = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      bool bad = false;
+      merge_parts<kWarpBatch>(it, 0, 1, slot32, GD, a.G, a.D, lane, active, M, den, acc, bad);
+      bad = __any_sync(0xffffffffu, bad);
+      if (active) {
+        const float sc = a.v_scale / den;
+        reinterpret_cast<float4 *>(it.out)[lane] =
+            bad ? make_float4(0.f, 0.f, 0.f, 0.f)
+                : make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+      }
     }
   }
 }
@@ -825,16 +825,21 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   int32_t *hdr = reinterpret_cast<int32_t *>(w + ws.hdr);
   int32_t *prefix = reinterpret_cast<int32_t *>(w + ws.prefix);
   int4 *start = reinterpret_cast<int4 *>(w + ws.start);
-  int32_t *bad = reinterpret_cast<int32_t *>(w + ws.bad);
-  int4 *comb = reinterpret_cast<int4 *>(w + ws.comb);
-  int4 *combw = reinterpret_cast<int4 *>(w + ws.combw);
+  int4 *desc = reinterpret_cast<int4 *>(w + ws.desc);
   float *part = reinterpret_cast<float *>(w + ws.part);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool fp8 = cache->kv_dtype == KVQ_KV_E4M3;
 
-  PlanArgs pa{seq_lens, abort_mask, hdr, prefix, start, bad, comb, combw, out, err_word,
-              B, Hq, D, MP, cache->page_size, nctas, Hkv / sk.hg, sk.unit};
-  if (launch_dependent(plan_kernel, 1, kPlanThreads, 0, s, pa) != cudaSuccess) return KVQ_ERR_CUDA;
+  // The tensor-core kernel schedules batches of up to 4,608 requests itself
+  // (the same test as its self_schedule): then there is no plan kernel and
+  // the split grid is the call's first kernel.
+  const bool self = sk.tma && self_schedulable(B, sk.threads, kSelfSchedPer, nctas);
+  if (!self) {
+    PlanArgs pa{seq_lens, abort_mask, hdr, prefix, start, desc, out, err_word,
+                B, Hq, D, MP, cache->page_size, nctas, Hkv / sk.hg, sk.unit};
+    if (launch_dependent(plan_kernel, 1, kPlanThreads, 0, s, pa) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+  }
 
   SplitArgs sa;
   sa.k_pool = static_cast<const uint8_t *>(cache->k_pool);
@@ -846,7 +851,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   sa.hdr = hdr;
   sa.prefix = prefix;
   sa.start = start;
-  sa.bad = bad;
+  sa.desc = desc;
   sa.part = part;
   sa.out = out;
   sa.err_word = err_word;
@@ -859,9 +864,10 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   sa.q_scale = sm_scale * (fp8 ? cache->k_scale : 1.0f) * kLog2e;
   sa.v_scale = fp8 ? cache->v_scale : 1.0f;
 
-  // the split grid is a programmatic dependent of the plan: its CTAs start
-  // (shared-memory and barrier set-up) while the plan finishes, and wait for
-  // the plan's results with griddepcontrol.wait
+  // the split grid is a programmatic dependent of the work before it (the
+  // plan, or whatever precedes the call): its CTAs start (shared-memory and
+  // barrier set-up) while that work finishes, and wait for it with
+  // griddepcontrol.wait
   cudaError_t e;
   if (sk.tma) {
     CUtensorMap kmap, vmap;
@@ -875,8 +881,9 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache *cache, const void *q, int
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
 
   // rows split across CTAs are merged by combine_kernel, a programmatic
-  // dependent of the split grid; with no such rows it exits at once
-  CombineArgs ca{hdr, bad, comb, combw, part, out, B, Hq, Hkv, G, D, sk.hg, Hkv / sk.hg,
+  // dependent of the split grid; with no such rows it exits after reading
+  // the descriptors
+  CombineArgs ca{desc, part, out, B, Hq, Hkv, G, D, sk.hg, Hkv / sk.hg,
                  fp8 ? cache->v_scale : 1.0f};
   const int crows = B * Hq;
   cudaError_t ce;

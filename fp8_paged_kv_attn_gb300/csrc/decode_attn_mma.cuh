@@ -545,24 +545,23 @@ __global__ void __launch_bounds__(32 * (HG + 1))
   }
   __syncthreads();
 
-  // Where this CTA starts.  For up to 32 x (HG + 1) x kSchedPer requests the
-  // CTA computes it itself and starts copying pages while the plan kernel is
-  // still running; of what the plan writes it touches only the bad-page
-  // flags, and waits for the plan (grid_dependency_wait) before the first of
-  // those.  (The plan's zeroed output rows are those of requests without
-  // work, which no split CTA writes.)  Larger batches wait at once and read
-  // the plan's schedule.
+  // Where this CTA starts.  Everything ahead of this kernel on the stream
+  // (the tag check that wrote the abort mask, whatever wrote the lengths;
+  // for a large batch the plan) is complete and visible once
+  // grid_dependency_wait() returns.  For up to 32 x (HG + 1) x kSelfSchedPer
+  // requests there is no plan kernel: every CTA works out the schedule
+  // itself and does the plan's other work for the requests without work that
+  // fall to it (zeroed rows, their descriptors, length errors).  Larger
+  // batches read the plan's schedule.
   const int c = blockIdx.x;
   const int groups = a.Hkv / HG;  // rows per request
-  constexpr int kSchedPer = 16;   // requests per thread in the CTA's own scan
   SchedStart sc;
-  const bool early = self_schedule<32 * (HG + 1), kSchedPer>(a, groups, kTile, ctl, sc);
-  if (!early) {
-    grid_dependency_wait();
+  grid_dependency_wait();
+  if (self_schedule<32 * (HG + 1), kSelfSchedPer>(a, groups, kTile, ctl, sc))
+    zero_requests<C::D>(a, groups, ctl);
+  else
     sc = plan_schedule(a, groups);
-  }
   allow_dependents();  // the combine grid may become resident and wait
-  bool dep_ok = !early;  // this thread has passed grid_dependency_wait() (producer)
   const int S = sc.S, U = sc.U;
 
   if (warp == HG) {
@@ -605,6 +604,8 @@ __global__ void __launch_bounds__(32 * (HG + 1))
         cur = bt_load(win + lane);
         nxt = bt_load(win + 32 + lane);
       }
+      // the CTA that holds the row's first unit writes the row's descriptor
+      if (lane == 0 && s == 0) a.desc[row] = make_int4(c_lo, nparts, b, 0);
       // the group's query rows, double-buffered per segment
       const int qs = nseg & 1;
       if (lane == 0) {
@@ -638,14 +639,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
           const int page = __shfl_sync(0xffffffffu, cur, lp_first - win);
           const bool bad_page = page < 0 || page >= a.num_pages;
           if (lane == 0) {
-            if (bad_page) {
-              if (!dep_ok) {  // the plan zeroes the bad flags
-                grid_dependency_wait();
-                dep_ok = true;
-              }
-              atomicOr(a.bad + row, 1);
-              report(a.err_word, KVQ_ERRBIT_PAGE);
-            }
+            if (bad_page) report(a.err_word, KVQ_ERRBIT_PAGE);
             ctl.desc[slot][0] = make_int4(
                 row, tok0,
                 ntok | (st == 0 ? kFirst : 0) | (st == nstages - 1 ? kLast : 0) |
@@ -683,14 +677,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
             }
           }
           if (lane == 0) {
-            if (bad_bits) {
-              if (!dep_ok) {
-                grid_dependency_wait();
-                dep_ok = true;
-              }
-              atomicOr(a.bad + row, 1);
-              report(a.err_word, KVQ_ERRBIT_PAGE);
-            }
+            if (bad_bits) report(a.err_word, KVQ_ERRBIT_PAGE);
             ctl.desc[slot][0] = make_int4(
                 row, tok0,
                 ntok | (st == 0 ? kFirst : 0) | (st == nstages - 1 ? kLast : 0) | bad_bits,
@@ -748,9 +735,6 @@ __global__ void __launch_bounds__(32 * (HG + 1))
       for (uint32_t k = g > NS ? g - NS : 0; k < g; ++k) mbar_wait(&ctl.full[k % NS], (k / NS) & 1);
       for (uint32_t k = nq > 2 ? nq - 2 : 0; k < nq; ++k) mbar_wait(&ctl.qfull[k & 1], (k >> 1) & 1);
     }
-    // The grid must not complete before the plan has: the combine kernel's
-    // wait covers only this grid.
-    if (!dep_ok) grid_dependency_wait();
     return;
   }
 
@@ -917,14 +901,14 @@ __global__ void __launch_bounds__(32 * (HG + 1))
             }
           }
         }
-        if (gq == 0) {
+        if (gq == 0) {  // l = -1 marks a part that met a page outside the pool
           if (ha < G) {
             mine[G * C::D + ha] = ma;
-            mine[G * C::D + G + ha] = la;
+            mine[G * C::D + G + ha] = seg_bad ? -1.f : la;
           }
           if (hb < G) {
             mine[G * C::D + hb] = mb;
-            mine[G * C::D + G + hb] = lb;
+            mine[G * C::D + G + hb] = seg_bad ? -1.f : lb;
           }
         }
       }

@@ -8,10 +8,14 @@
 // is balanced to within one unit whatever the length mix.  A CTA's range cuts
 // rows into segments; a row owned by one CTA is normalised and written
 // directly, otherwise every CTA writes a partial (acc[G][D], m[G], l[G] per
-// kv head) and the combine kernel merges the row by log-sum-exp once the
-// split grid has finished: one warp per output row when the row has few
-// parts, a whole CTA per output row when it has many.  No split CTA ever
-// waits for another, so the grid ends when the last CTA's stream does.
+// kv head; l = -1 marks a part that met a page outside the pool) and the
+// combine kernel merges the row by log-sum-exp once the split grid has
+// finished: one warp per output row when the row has few parts, a whole CTA
+// per output row when it has many.  The CTA that holds a row's first unit
+// writes the row's merge descriptor (first CTA, parts, request); rows of
+// requests without work get a descriptor of 0 parts from whoever zeroes
+// their output.  No split CTA ever waits for another, so the grid ends when
+// the last CTA's stream does.
 #pragma once
 
 namespace kvq {
@@ -34,10 +38,10 @@ struct SplitArgs {
   const uint16_t *q;
   const int32_t *block_table, *seq_lens;
   const uint8_t *abort_mask;  // [B] or null
-  const int32_t *hdr;     // [0] total units S, [1] units per CTA U
-  const int32_t *prefix;  // [B+1]: units before request b, over all its kv heads
-  const int4 *start;      // [C]: (b, kv head, unit in row) where CTA c begins
-  int32_t *bad;           // [B*Hkv] a page of the row was outside the pool
+  const int32_t *hdr;     // [0] total units S, [1] units per CTA U (plan)
+  const int32_t *prefix;  // [B+1]: units before request b, over all its kv heads (plan)
+  const int4 *start;      // [C]: (b, kv head, unit in row) where CTA c begins (plan)
+  int4 *desc;             // [rows]: (first CTA, parts, request, 0) of every row
   float *part;            // [B*Hkv + C][G][D+2] partials
   float *out;             // [B][Hq][D]
   uint32_t *err_word;
@@ -49,6 +53,16 @@ struct SplitArgs {
 // Floats of one kv head's partial: acc[G][D], m[G], l[G], padded to a
 // multiple of four floats so every head's block is 16-byte aligned.
 __host__ __device__ constexpr int part_stride(int G, int D) { return G * D + (2 * G + 3) / 4 * 4; }
+
+// Requests without work (aborted, empty or of invalid length) that one CTA
+// zeroes in a call whose schedule the split kernel works out itself: request
+// b goes to CTA b % grid, and that schedule covers at most 4,608 requests
+// over at least 152 CTAs.
+constexpr int kZeroMax = 32;
+
+// Requests per thread in a CTA's own schedule scan (tensor-core kernel):
+// 32 x (HG + 1) threads x 16 = 4,608 requests for 8-kv-head groups.
+constexpr int kSelfSchedPer = 16;
 
 // Rows split over at most this many CTAs are merged by one warp per output
 // row in the combine kernel (all parts' loads issued at once); rows split
@@ -64,6 +78,8 @@ struct Ctrl {
   int fail;
   int scan[16];                  // per-warp sums of the CTA's own schedule scan
   int sched[4];                  // where the CTA starts: request, its prefix, length, units
+  int nzero;                     // requests without work this CTA zeroes (own schedule)
+  int zero[kZeroMax];
 };
 
 // 2^x on the SFU (relative error ~2^-22; exactly 1 at x = 0)
@@ -116,6 +132,14 @@ __device__ __forceinline__ int request_units(const SplitArgs &a, int b, long lon
   return (aborted || L < 0 || L > cap) ? 0 : (L + unit - 1) / unit;
 }
 
+// Whether a CTA of NT threads can work out the schedule of B requests
+// itself (PER requests a thread) and hold the list of requests without work
+// that fall to it (B / grid of them at most).  The host takes the same
+// decision when it leaves out the plan kernel.
+__host__ __device__ constexpr bool self_schedulable(int B, int NT, int PER, int grid) {
+  return B <= NT * PER && B <= kZeroMax * grid;
+}
+
 // Where this CTA starts, as the plan would place it.
 struct SchedStart {
   int S, U;   // total units, units per CTA
@@ -138,17 +162,28 @@ template <int NT, int PER>
 __device__ __forceinline__ bool self_schedule(const SplitArgs &a, int rows_per_req, int unit,
                                               Ctrl &ctl, SchedStart &sc) {
   static_assert(NT % 32 == 0 && NT / 32 <= 16, "CTA size");
-  if (a.B > NT * PER) return false;
+  if (!self_schedulable(a.B, NT, PER, gridDim.x)) return false;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long cap = static_cast<long long>(a.MP) * a.P;
   const int base = tid * PER;
   int cnt[PER], len[PER];
+  // every length and abort byte of the thread's requests is loaded before
+  // any is used, so that both arrays' lines are fetched in one round trip
+#pragma unroll
+  for (int i = 0; i < PER; ++i) len[i] = base + i < a.B ? __ldg(a.seq_lens + base + i) : 0;
+  uint32_t aborted = 0;  // bit i: request base + i was aborted
+  if (a.abort_mask) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (base + i < a.B && __ldg(a.abort_mask + base + i) != 0) aborted |= 1u << i;
+  }
   int sum = 0;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    cnt[i] = 0;
-    len[i] = 0;
-    if (base + i < a.B) cnt[i] = request_units(a, base + i, cap, unit, len[i]);
+    // units of request base + i, as request_units counts them
+    const int L = len[i];
+    cnt[i] = (base + i >= a.B || ((aborted >> i) & 1u) || L < 0 || L > cap)
+                 ? 0 : (L + unit - 1) / unit;
     sum += cnt[i] * rows_per_req;
   }
   int incl = sum;
@@ -171,6 +206,8 @@ __device__ __forceinline__ bool self_schedule(const SplitArgs &a, int rows_per_r
   sc.U = total > 0 ? (total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) : 1;
   const long long u0 = static_cast<long long>(blockIdx.x) * sc.U;
   int pre = before + incl - sum;  // units before this thread's first request
+  if (tid == 0) ctl.nzero = 0;
+  __syncthreads();
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int n = cnt[i] * rows_per_req;
@@ -180,6 +217,11 @@ __device__ __forceinline__ bool self_schedule(const SplitArgs &a, int rows_per_r
       ctl.sched[2] = len[i];
       ctl.sched[3] = cnt[i];
     }
+    // a request without work is this CTA's to zero when b % grid == CTA
+    if (base + i < a.B && n == 0 && (base + i) % static_cast<int>(gridDim.x) == blockIdx.x) {
+      const int k = atomicAdd(&ctl.nzero, 1);
+      if (k < kZeroMax) ctl.zero[k] = base + i;  // at most ceil(B / grid) <= kZeroMax
+    }
     pre += n;
   }
   __syncthreads();
@@ -188,6 +230,29 @@ __device__ __forceinline__ bool self_schedule(const SplitArgs &a, int rows_per_r
   sc.L = ctl.sched[2];
   sc.ub = ctl.sched[3];
   return true;
+}
+
+// With its own schedule, the CTA also stands in for the plan on the requests
+// without work that fall to it: their output rows are zeroed, their rows get
+// a descriptor of 0 parts, and a length outside [0, MP * P] (of a request
+// that was not aborted) raises KVQ_ERRBIT_SEQLEN.  Every thread calls it.
+template <int D>
+__device__ __forceinline__ void zero_requests(const SplitArgs &a, int rows_per_req,
+                                              const Ctrl &ctl) {
+  const int n = min(ctl.nzero, kZeroMax);
+  const long long cap = static_cast<long long>(a.MP) * a.P;
+  for (int i = 0; i < n; ++i) {
+    const int b = ctl.zero[i];
+    float4 *o = reinterpret_cast<float4 *>(a.out + static_cast<int64_t>(b) * a.Hq * D);
+    for (int k = threadIdx.x; k < a.Hq * D / 4; k += blockDim.x)
+      o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (threadIdx.x < rows_per_req) a.desc[b * rows_per_req + threadIdx.x] = make_int4(0, 0, b, 0);
+    if (threadIdx.x == 0) {
+      const int L = __ldg(a.seq_lens + b);
+      const bool aborted = a.abort_mask && __ldg(a.abort_mask + b) != 0;
+      if (!aborted && (L < 0 || L > cap)) report(a.err_word, KVQ_ERRBIT_SEQLEN);
+    }
+  }
 }
 
 // The same start read from the plan's results (after grid_dependency_wait()).
@@ -294,13 +359,14 @@ __device__ __forceinline__ void producer_loop(const SplitArgs &a, Ctrl &ctl, uin
         if (page < 0 || page >= a.num_pages) {
           bad_page = true;
           page = -1;
-          atomicOr(a.bad + row, 1);
           report(a.err_word, KVQ_ERRBIT_PAGE);
         }
       }
       const unsigned valid_mask = __ballot_sync(0xffffffffu, page >= 0);
       const bool any_bad = __any_sync(0xffffffffu, bad_page);
       const bool first = st == 0, last = st == nstages - 1;
+      if (lane == 0 && first && s == 0)  // this CTA holds the row's first unit
+        a.desc[row] = make_int4(c_lo, nparts, b, 0);
       if (lane == 0) {
         ctl.desc[slot][0] = make_int4(row, tok0,
                                       ntok | (first ? kFirst : 0) | (last ? kLast : 0) |
@@ -370,7 +436,7 @@ __device__ __forceinline__ void finish_segment(const SplitArgs &a, const float *
       mine[idx] = acc;
       if (idx % D == 0) {
         mine[GD + h] = mstar;
-        mine[GD + G + h] = l;
+        mine[GD + G + h] = seg_bad ? -1.f : l;  // -1: this part met a bad page
       }
     }
   }

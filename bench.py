@@ -253,6 +253,14 @@ def profiled_traffic():
     return float(rec["traffic_bytes_per_call"])
 
 
+def attn_kernels(B, D):
+    """Kernels one kvq_decode_attn call launches for 8 kv heads a request:
+    the split and combine kernels when the split kernel schedules the batch
+    itself (head_dim 128, up to 4,608 requests), plus the plan kernel
+    otherwise."""
+    return 2 if D == 128 and B <= 4608 else 3
+
+
 def attn_bytes(lens, Hq, Hkv, D, P, es):
     """Algorithmic bytes of one decode-attention call: every cached K and V
     element once, q in, out (fp32), and the block-table entries read."""
@@ -305,7 +313,7 @@ class DecodeStep:
     Python binding.
 
     graph=True captures the step once over static buffers into a CUDA graph
-    (the five kernels are chained as programmatic dependents, which the
+    (the kernels are chained as programmatic dependents, which the
     capture keeps as programmatic edges); each step then stages its inputs
     with one copy into the static row and replays the graph.  A second graph
     holds the attention call alone, for timing it by itself.  graph=False
@@ -728,7 +736,7 @@ def run_gpu(args, dist, rank, world, local):
                    f"L2 ({flush.l2 >> 20} MB) flushed before every timed step and attention "
                    f"call ({kv_step / 1e6:.0f} MB of KV per step); each timed by its own events"),
             "step": "kvq_append + kvq_check_tags + kvq_decode_attn",
-            "launch": "CUDA graph per step (inputs staged with one device copy; the five "
+            "launch": "CUDA graph per step (inputs staged with one device copy; the step's "
                       "kernels chained as programmatic dependents)" if graph
                       else "eager library calls",
         },
@@ -748,7 +756,7 @@ def run_gpu(args, dist, rank, world, local):
             "ms_per_call_median": round(statistics.median(attn_ms), 5),
             "ms_per_call_p95": round(float(np.percentile(attn_ms, 95)), 5),
         },
-        "gpu_launches": args.steps * (1 + (1 if check else 0) + 3),
+        "gpu_launches": args.steps * (1 + (1 if check else 0) + attn_kernels(B, D)),
         "clocks": clk,
     }
     if e2e is not None:

@@ -14,13 +14,11 @@
 // Work layout: grid (token blocks, requests); a CTA of 8 warps takes 64
 // consecutive tokens of one request, a warp 8 of them.  Lanes 0..7 of a warp
 // look up the prefill and decode page of its 8 tokens at once (two loads
-// each); then, token by token, the lanes take the token's 16-byte output
+// each); then, token by token, the lanes take the token's K 16-byte output
 // chunks (16 codes; a head's row of D bf16 values is contiguous in the
-// prefill page) in batches of two per lane, loading a batch's source words
-// before converting and storing them.  Small register footprint: four CTAs
-// (32 warps) per SM keep enough loads in flight.
-// A request's token range is checked once; CTAs past the range exit at once.
-//
+// prefill page), then its V chunks, each batch's source words loaded before
+// any of them is converted and stored.  The kv-head count and D are template
+// parameters, so every lane's chunk offsets are fixed before the token loop.
 // HBM-bound: per token and kv head 2 D (2 + s) bytes (read bf16 K and V,
 // write s-byte codes), plus 4 bytes per prefill and per decode page.
 #include <algorithm>
@@ -45,81 +43,81 @@ constexpr int kHoWarps = 8;
 constexpr int kHoTokPerWarp = 8;
 constexpr int kHoTokPerCta = kHoWarps * kHoTokPerWarp;
 
-template <bool kFp8, int D>
-__global__ void __launch_bounds__(32 * kHoWarps, 4) handoff_kernel(HandoffArgs a) {
-  constexpr int kElems = kFp8 ? 16 : 8;  // elements per 16-byte output chunk
-  constexpr int kCpr = D / kElems;       // chunks per (token, head) row
-  constexpr int kSrcWords = kFp8 ? 2 : 1;
+template <bool kFp8, int H, int D>
+__global__ void __launch_bounds__(32 * kHoWarps, 6) handoff_kernel(HandoffArgs a) {
+  constexpr int kElems = kFp8 ? 16 : 8;             // elements per 16-byte output chunk
+  constexpr int kCpr = D / kElems;                  // chunks per (token, head) row
+  constexpr int kChunks = H * kCpr;                 // chunks of one token's K (or V)
+  constexpr int kPer = (kChunks + 31) / 32;         // chunks per lane per tensor
+  constexpr int kSrcWords = kFp8 ? 2 : 1;           // 16-byte source words per chunk
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per_tensor = a.H * kCpr;
-  const int total = 2 * per_tensor;
-  constexpr int kPer = kFp8 ? 2 : 4;    // chunks per lane per batch
+  // this lane's chunks: element offsets inside a token's (page, head 0, slot)
+  // block, the same for every token (heads are P * D elements apart)
+  int soff[kPer], doff[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int c = lane + 32 * k;
+    soff[k] = (c / kCpr) * a.Ps * D + (c % kCpr) * kElems;
+    doff[k] = (c / kCpr) * a.Pd * D + (c % kCpr) * kElems;
+  }
   grid_dependency_wait();
   allow_dependents();
 
   for (int b = blockIdx.y; b < a.B; b += gridDim.y) {
-    const int64_t f = a.first ? __ldg(a.first + b) : 0;
-    const int64_t n = __ldg(a.count + b);
-    const int64_t src_cap = static_cast<int64_t>(a.src_MP) * a.Ps;
-    const int64_t dst_cap = static_cast<int64_t>(a.dst_MP) * a.Pd;
-    if (f < 0 || n < 0 || f + n > src_cap || f + n > dst_cap) {
+    const int f = a.first ? __ldg(a.first + b) : 0;
+    const int n = __ldg(a.count + b);
+    const long long end = static_cast<long long>(f) + n;
+    if (f < 0 || n < 0 || end > static_cast<long long>(a.src_MP) * a.Ps ||
+        end > static_cast<long long>(a.dst_MP) * a.Pd) {
       if (blockIdx.x == 0 && threadIdx.x == 0) report(a.err_word, KVQ_ERRBIT_POS);
       continue;
     }
-    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kHoTokPerCta + warp * kHoTokPerWarp;
-    if (t0 >= n) continue;
-    const int ntok = static_cast<int>(min(static_cast<int64_t>(kHoTokPerWarp), n - t0));
+    // positions fit in 32 bits from here on: both tables hold at most
+    // INT32_MAX tokens (checked by the host)
+    const long long t0l = static_cast<long long>(blockIdx.x) * kHoTokPerCta + warp * kHoTokPerWarp;
+    if (t0l >= n) continue;
+    const int t0 = static_cast<int>(t0l);
+    const int ntok = min(kHoTokPerWarp, n - t0);
     // lanes 0..ntok-1: the prefill and decode pages of token f + t0 + lane
     int sp = -1, dp = -1;
     if (lane < ntok) {
-      const int64_t p = f + t0 + lane;
+      const int p = f + t0 + lane;
       sp = __ldg(a.src_bt + static_cast<int64_t>(b) * a.src_MP + p / a.Ps);
       dp = __ldg(a.dst_bt + static_cast<int64_t>(b) * a.dst_MP + p / a.Pd);
     }
     for (int j = 0; j < ntok; ++j) {
-      const int64_t p = f + t0 + j;
+      const int p = f + t0 + j;
       const int spage = __shfl_sync(0xffffffffu, sp, j);
       const int dpage = __shfl_sync(0xffffffffu, dp, j);
       if (spage < 0 || spage >= a.src_pages || dpage < 0 || dpage >= a.dst_pages) {
         if (lane == 0) report(a.err_word, KVQ_ERRBIT_PAGE);
         continue;  // uniform over the warp
       }
-      // element offsets of (page, head 0, slot, dim 0); heads are P * D apart
-      const int64_t src0 = (static_cast<int64_t>(spage) * a.H * a.Ps + p % a.Ps) * D;
-      const int64_t dst0 = (static_cast<int64_t>(dpage) * a.H * a.Pd + p % a.Pd) * D;
-      const int64_t src_hs = static_cast<int64_t>(a.Ps) * D, dst_hs = static_cast<int64_t>(a.Pd) * D;
-      // the lane's chunks in batches of kPer: the batch's source words first,
-      // then its stores
-      for (int base = 0; base < total; base += 32 * kPer) {
+      // element offsets of the token's (page, head 0, slot, dim 0)
+      const int64_t src0 = (static_cast<int64_t>(spage) * H * a.Ps + p % a.Ps) * D;
+      const int64_t dst0 = (static_cast<int64_t>(dpage) * H * a.Pd + p % a.Pd) * D;
+      // K, then V: a batch's source words are all loaded before any is stored
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint16_t *src = (t ? a.src_v : a.src_k) + src0;
         uint4 s[kPer][kSrcWords];
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int c = base + lane + 32 * k;
-          if (c < total) {
-            const bool is_v = c >= per_tensor;
-            const int cc = is_v ? c - per_tensor : c;
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                (is_v ? a.src_v : a.src_k) + src0 + (cc / kCpr) * src_hs + (cc % kCpr) * kElems);
+        for (int k = 0; k < kPer; ++k)
+          if (kChunks % 32 == 0 || lane + 32 * k < kChunks)
 #pragma unroll
-            for (int w = 0; w < kSrcWords; ++w) s[k][w] = __ldcs(src + w);
-          }
-        }
+            for (int w = 0; w < kSrcWords; ++w)
+              s[k][w] = __ldcs(reinterpret_cast<const uint4 *>(src + soff[k]) + w);
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-          const int c = base + lane + 32 * k;
-          if (c >= total) break;
-          const bool is_v = c >= per_tensor;
-          const int cc = is_v ? c - per_tensor : c;
-          const int64_t dst = dst0 + (cc / kCpr) * dst_hs + (cc % kCpr) * kElems;
+          if (!(kChunks % 32 == 0 || lane + 32 * k < kChunks)) continue;
           if constexpr (kFp8) {
-            uint8_t *pool = static_cast<uint8_t *>(is_v ? a.dst_v : a.dst_k);
-            *reinterpret_cast<uint4 *>(pool + dst) =
-                quantise16(s[k][0], s[k][1], is_v ? a.v_scale : a.k_scale,
-                           is_v ? a.v_rlo : a.k_rlo, is_v ? a.v_rhi : a.k_rhi,
-                           is_v ? a.v_fast : a.k_fast);
+            uint8_t *dst = static_cast<uint8_t *>(t ? a.dst_v : a.dst_k) + dst0 + doff[k];
+            *reinterpret_cast<uint4 *>(dst) =
+                quantise16(s[k][0], s[k][1], t ? a.v_scale : a.k_scale, t ? a.v_rlo : a.k_rlo,
+                           t ? a.v_rhi : a.k_rhi, t ? a.v_fast : a.k_fast);
           } else {
-            uint16_t *pool = static_cast<uint16_t *>(is_v ? a.dst_v : a.dst_k);
-            *reinterpret_cast<uint4 *>(pool + dst) = s[k][0];
+            uint16_t *dst = static_cast<uint16_t *>(t ? a.dst_v : a.dst_k) + dst0 + doff[k];
+            *reinterpret_cast<uint4 *>(dst) = s[k][0];
           }
         }
       }
@@ -129,9 +127,20 @@ __global__ void __launch_bounds__(32 * kHoWarps, 4) handoff_kernel(HandoffArgs a
 
 using HandoffFn = void (*)(HandoffArgs);
 
-inline HandoffFn pick_handoff(bool fp8, int D) {
-  if (D == 64) return fp8 ? handoff_kernel<true, 64> : handoff_kernel<false, 64>;
-  if (D == 128) return fp8 ? handoff_kernel<true, 128> : handoff_kernel<false, 128>;
+template <bool kFp8, int D>
+HandoffFn pick_handoff_h(int H) {
+  switch (H) {
+    case 1: return handoff_kernel<kFp8, 1, D>;
+    case 2: return handoff_kernel<kFp8, 2, D>;
+    case 4: return handoff_kernel<kFp8, 4, D>;
+    case 8: return handoff_kernel<kFp8, 8, D>;
+  }
+  return nullptr;
+}
+
+inline HandoffFn pick_handoff(bool fp8, int H, int D) {
+  if (D == 64) return fp8 ? pick_handoff_h<true, 64>(H) : pick_handoff_h<false, 64>(H);
+  if (D == 128) return fp8 ? pick_handoff_h<true, 128>(H) : pick_handoff_h<false, 128>(H);
   return nullptr;
 }
 
@@ -151,7 +160,8 @@ extern "C" kvq_status kvq_handoff_pages(const kvq_cache *src, const int32_t *src
   if (src->kv_dtype != KVQ_KV_BF16) return KVQ_ERR_INVALID_ARG;
   if (src->num_kv_heads != dst->num_kv_heads || src->head_dim != dst->head_dim)
     return KVQ_ERR_INVALID_ARG;
-  if (src->num_kv_heads > 8) return KVQ_ERR_UNSUPPORTED;
+  const int H = src->num_kv_heads;
+  if (H != 1 && H != 2 && H != 4 && H != 8) return KVQ_ERR_UNSUPPORTED;
   if (B < 0 || src_MP <= 0 || dst_MP <= 0) return KVQ_ERR_INVALID_ARG;
   if (B == 0) return KVQ_OK;
   if (!src_block_table || !dst_block_table || !count) return KVQ_ERR_INVALID_ARG;
@@ -182,7 +192,7 @@ extern "C" kvq_status kvq_handoff_pages(const kvq_cache *src, const int32_t *src
   reciprocals(a.k_scale, &a.k_rlo, &a.k_rhi, &a.k_fast);
   reciprocals(a.v_scale, &a.v_rlo, &a.v_rhi, &a.v_fast);
 
-  const HandoffFn fn = pick_handoff(dst->kv_dtype == KVQ_KV_E4M3, dst->head_dim);
+  const HandoffFn fn = pick_handoff(dst->kv_dtype == KVQ_KV_E4M3, dst->num_kv_heads, dst->head_dim);
   if (!fn) return KVQ_ERR_UNSUPPORTED;
   // a request moves at most min(both capacities) tokens; token blocks past
   // its count exit at once

@@ -128,7 +128,7 @@ KVQ_API kvq_status kvq_append(const kvq_cache *cache, const void *k_new, const v
  * capacity (MP * page_size) writes nothing and raises KVQ_ERRBIT_POS; a
  * token whose src or dst page is outside its pool writes nothing and raises
  * KVQ_ERRBIT_PAGE.  first and count are int32 [B] device arrays; pools
- * 16-byte aligned; num_kv_heads <= 8. */
+ * 16-byte aligned; num_kv_heads in {1, 2, 4, 8} (else KVQ_ERR_UNSUPPORTED). */
 KVQ_API kvq_status kvq_handoff_pages(const kvq_cache *src, const int32_t *src_block_table,
                                      int32_t src_MP, const kvq_cache *dst,
                                      const int32_t *dst_block_table, int32_t dst_MP,

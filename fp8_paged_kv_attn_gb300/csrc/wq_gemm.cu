@@ -15,13 +15,19 @@
 // Kernel: a CTA of 8 warps covers 128 output channels (16 per warp) and a
 // range of 128-wide k groups (split-K over CTAs, partial sums added with
 // atomics into a zeroed y).  The CTA first stages its slice of x in shared
-// memory in MMA-fragment order (so each lane's B operand is one 8-byte
-// load; a thread stages a 32-value chunk with four 16-byte loads and a
-// permutation in registers); each lane then streams its weights straight
-// from HBM as contiguous 16-byte runs (the k order inside a group is
-// permuted consistently in the weights' fragments and in the staged x, which
-// leaves the sum unchanged), with a register ring of the next 3 (INT4) or 2
-// (e4m3) groups' loads in flight while the current one is computed.
+// memory in MMA-fragment order (so a lane's B registers for two MMA steps
+// are one 16-byte load; a thread stages a 32-value chunk with four 16-byte
+// loads and a permutation in registers) and, for INT4, its rows' group
+// scales as fp32 pairs (rows r and r + 8: one 8-byte load per group; the
+// scale loads are all issued before any is stored, so they cost one memory
+// round trip, not one per element); each lane then streams its weights
+// straight from HBM as contiguous 16-byte runs (the k order inside a group
+// is permuted consistently in the weights' fragments and in the staged x,
+// which leaves the sum unchanged), with a register ring of the next 3 (INT4)
+// or 2 (e4m3) groups' loads in flight while the current one is computed.
+// Rows past N and, with one token tile, token slots past M read a valid
+// neighbour instead of branching (an output row depends only on its row of
+// the A operand, an output token only on its column of B; neither is stored).
 //  x is scaled while staged, per token and 128-wide k group, by the power of
 //  two 2^e that puts the group's largest finite |x| in [2^14, 2^15), then
 //  rounded to f16: exact for every bf16 value down to 2^-32 of that largest
@@ -136,36 +142,40 @@ __device__ __forceinline__ float pow2_any(int n) {
   return n >= -126 ? pow2i(n) : __int_as_float(1 << (149 + n));
 }
 
-template <bool kInt4>
+template <bool kInt4, int NT>
 struct WqCfg {
   static constexpr int kWords = kInt4 ? 4 : 8;  // weight words per row half per lane per group
-  static constexpr int kDepth = kInt4 ? 4 : 3;  // groups of weights held in registers per warp
+  // groups of weights held in registers per warp (fewer when more than four
+  // token tiles need the registers; those products are bound by the MMAs)
+  static constexpr int kDepth = NT > 4 ? 2 : kInt4 ? 4 : 3;
 };
 
-// shared memory of a CTA: [group scales: kWqRows x gpc bf16][staged x]
-// [2^-e per (group, staged token), fp32]
+// shared memory of a CTA: [INT4 group scales: fp32 pairs for rows (r, r + 8),
+// per pair and group][staged x][2^-e per (group, token slot of the tiles), fp32]
 __host__ __device__ constexpr int wq_staged_tokens(int nt, int M) { return nt == 1 ? M : 8 * nt; }
-__host__ __device__ constexpr size_t wq_scale_bytes(int gpc) {
-  return (size_t(kWqRows) * gpc * 2 + 15) / 16 * 16;
+__host__ __device__ constexpr size_t wq_scale_bytes(bool int4, int gpc) {
+  return int4 ? size_t(kWqRows / 2) * gpc * 8 : 0;
 }
 __host__ __device__ constexpr size_t wq_x_bytes(int gpc, int nt, int M) {
   return size_t(gpc) * kWqGroup * wq_staged_tokens(nt, M) * sizeof(uint16_t);
 }
-__host__ __device__ constexpr size_t wq_smem_bytes(int gpc, int nt, int M) {
-  return wq_scale_bytes(gpc) + wq_x_bytes(gpc, nt, M) + size_t(gpc) * wq_staged_tokens(nt, M) * 4;
+__host__ __device__ constexpr size_t wq_smem_bytes(bool int4, int gpc, int nt, int M) {
+  return wq_scale_bytes(int4, gpc) + wq_x_bytes(gpc, nt, M) + size_t(gpc) * 8 * nt * 4;
 }
 
 template <bool kInt4, int NT>
 __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel(WqArgs a) {
-  using C = WqCfg<kInt4>;
+  using C = WqCfg<kInt4, NT>;
+  constexpr int kTok = 8 * NT;  // token slots of the MMA tiles
   extern __shared__ __align__(16) uint8_t wq_smem[];
-  uint16_t *sc_s = reinterpret_cast<uint16_t *>(wq_smem);  // [rows][gpc] bf16
-  uint16_t *xs = reinterpret_cast<uint16_t *>(wq_smem + wq_scale_bytes(a.gpc));
-  // tokens staged: 8 per tile, or just the M real ones when there is one
-  // tile (lanes whose token is past M then use a zero operand)
+  const size_t scb = wq_scale_bytes(kInt4, a.gpc);
+  float2 *sc_s = reinterpret_cast<float2 *>(wq_smem);  // [kWqRows / 2][gpc]
+  // staged x, one 16-byte word per (group, step pair, token, lane class):
+  // the B registers of two consecutive MMA steps
+  uint4 *xs = reinterpret_cast<uint4 *>(wq_smem + scb);
+  // tokens staged: 8 per tile, or just the M real ones when there is one tile
   const int Mp = wq_staged_tokens(NT, a.M);
-  float *xu = reinterpret_cast<float *>(wq_smem + wq_scale_bytes(a.gpc) +
-                                        wq_x_bytes(a.gpc, NT, a.M));  // [gpc][Mp]: 2^-e
+  float *xu = reinterpret_cast<float *>(wq_smem + scb + wq_x_bytes(a.gpc, NT, a.M));  // [gpc][kTok]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = lane & 3, rr = lane >> 2;
   const int kc = a.gpc * kWqGroup;
@@ -173,32 +183,69 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
   const int ng = min(a.gpc, (a.K - kb0) / kWqGroup);
   const int row_base = blockIdx.x * kWqRows;
   const int row0 = row_base + warp * 16 + rr;  // this lane's rows: row0, row0 + 8
-  const bool ok0 = row0 < a.N, ok8 = row0 + 8 < a.N;
+  // An output row depends only on its own row of A, an output token only on
+  // its own column of B: rows past N read row N - 1 and, with one tile,
+  // token slots past M read token M - 1; neither sum is ever stored.
   const int64_t row_bytes = kInt4 ? a.K / 2 : a.K;
   constexpr int kGroupBytes = kInt4 ? kWqGroup / 2 : kWqGroup;
-  const uint8_t *w0 = a.w + static_cast<int64_t>(row0) * row_bytes +
-                      (kInt4 ? kb0 / 2 + c * 16 : kb0 + c * 32);
-  const uint8_t *w8 = w0 + 8 * row_bytes;
+  const int64_t lane_off = kInt4 ? kb0 / 2 + c * 16 : kb0 + c * 32;
+  const uint8_t *w0 = a.w + static_cast<int64_t>(min(row0, a.N - 1)) * row_bytes + lane_off;
+  const uint8_t *w8 = a.w + static_cast<int64_t>(min(row0 + 8, a.N - 1)) * row_bytes + lane_off;
   grid_dependency_wait();
   allow_dependents();
 
-  // this lane's weights of group g (zeros for rows past N)
+  // this lane's weights of group g
   auto load = [&](int g, uint32_t (&r0)[C::kWords], uint32_t (&r8)[C::kWords]) {
     if (g >= ng) return;
 #pragma unroll
     for (int h = 0; h < C::kWords / 4; ++h) {
-      const uint4 u0 = ok0 ? __ldcs(reinterpret_cast<const uint4 *>(w0 + g * kGroupBytes) + h)
-                           : make_uint4(0, 0, 0, 0);
-      const uint4 u8 = ok8 ? __ldcs(reinterpret_cast<const uint4 *>(w8 + g * kGroupBytes) + h)
-                           : make_uint4(0, 0, 0, 0);
+      const uint4 u0 = __ldcs(reinterpret_cast<const uint4 *>(w0 + g * kGroupBytes) + h);
+      const uint4 u8 = __ldcs(reinterpret_cast<const uint4 *>(w8 + g * kGroupBytes) + h);
       r0[4 * h] = u0.x; r0[4 * h + 1] = u0.y; r0[4 * h + 2] = u0.z; r0[4 * h + 3] = u0.w;
       r8[4 * h] = u8.x; r8[4 * h + 1] = u8.y; r8[4 * h + 2] = u8.z; r8[4 * h + 3] = u8.w;
     }
   };
-  // the first kDepth - 1 groups are in flight while x is staged
+  // the first kDepth - 1 groups are in flight while x and the scales are staged
   uint32_t wr0[C::kDepth][C::kWords], wr8[C::kDepth][C::kWords];
 #pragma unroll
   for (int d = 0; d < C::kDepth - 1; ++d) load(d, wr0[d], wr8[d]);
+
+  // ---- INT4 group scales of the CTA's row pairs, fp32 in shared memory.
+  // One item = (row pair p, group g): rows row_base + 16 (p / 8) + p % 8 and
+  // 8 below.  Every load of a batch is issued before any is stored, and the
+  // first batch's loads are in flight while x is staged
+  constexpr int kScB = 5;  // items per thread per batch
+  const int nsc = kInt4 ? (kWqRows / 2) * ng : 0;
+  const uint16_t *sp = static_cast<const uint16_t *>(a.scales);
+  const int64_t gs = a.K / kWqGroup;
+  uint16_t scv[kScB][2];
+  auto scale_loads = [&](int base) {
+#pragma unroll
+    for (int i = 0; i < kScB; ++i) {
+      const int e = base + i * blockDim.x + tid;
+      if (e < nsc) {
+        const int p = e / ng, g = e - p * ng;
+        const int r = row_base + (p >> 3) * 16 + (p & 7);
+        const int64_t col = kb0 / kWqGroup + g;
+        scv[i][0] = __ldg(sp + min(r, a.N - 1) * gs + col);
+        scv[i][1] = __ldg(sp + min(r + 8, a.N - 1) * gs + col);
+      }
+    }
+  };
+  auto scale_stores = [&](int base) {
+#pragma unroll
+    for (int i = 0; i < kScB; ++i) {
+      const int e = base + i * blockDim.x + tid;
+      if (e < nsc) {
+        const int p = e / ng, g = e - p * ng;
+        sc_s[p * a.gpc + g] = make_float2(__uint_as_float(uint32_t(scv[i][0]) << 16),
+                                          __uint_as_float(uint32_t(scv[i][1]) << 16));
+      }
+    }
+  };
+  // (with one token tile; with more, registers are short and x takes longer)
+  constexpr bool kEarly = kInt4 && NT == 1;
+  if constexpr (kEarly) scale_loads(0);
 
   // ---- stage x: one thread per (group, token, class) chunk of 32 k values:
   // four 16-byte loads; the chunk's largest finite |x| (a bf16 magnitude
@@ -207,8 +254,7 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
   // block size is a multiple of 4; every lane takes part in every pass);
   // the values times 2^e rounded to f16; the fragment permutation on whole
   // words (e4m3: the values' own order; INT4: two byte permutes per pair of
-  // words); eight 8-byte stores (a warp's stores for one step are 256
-  // contiguous bytes).
+  // words); four 16-byte stores, one per step pair.
   const int nch = ng * Mp * 4;
   for (int base = 0; base < nch; base += blockDim.x) {
     const int ch = base + tid;
@@ -241,7 +287,7 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     if (ch < nch) {
       const int ex = x_exponent(mx << 16);
-      if (cl == 0) xu[g * Mp + m] = pow2_any(-ex);
+      if (cl == 0) xu[g * kTok + m] = pow2_any(-ex);
       // x * 2^ex as products by normal powers of two (2^ex alone is not a
       // float for ex > 127), each exact for the values f16 can hold
       const float f1 = pow2i(ex > 127 ? ex - 64 : ex);
@@ -254,26 +300,26 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
                                    : __floats2half2_rn(xf[0] * f1, xf[1] * f1);
         wv[i] = *reinterpret_cast<const uint32_t *>(&h);
       }
-      uint2 *dst = reinterpret_cast<uint2 *>(xs) + (g * 8 * Mp + m) * 4 + cl;
+      uint4 *dst = xs + (g * 4 * Mp + m) * 4 + cl;
 #pragma unroll
-      for (int st = 0; st < 8; ++st) {
+      for (int q = 0; q < 4; ++q) {
         if constexpr (kInt4) {
-          // values 8q + p + {0, 4} and 8q + p + {1, 5}, q = st / 2, p = 2 (st % 2)
-          const uint32_t a0 = wv[4 * (st >> 1) + (st & 1)], a2 = wv[4 * (st >> 1) + (st & 1) + 2];
-          dst[st * Mp * 4] = make_uint2(__byte_perm(a0, a2, 0x5410), __byte_perm(a0, a2, 0x7632));
-        } else {
-          dst[st * Mp * 4] = make_uint2(wv[2 * st], wv[2 * st + 1]);  // values 4st .. 4st + 3
+          // step 2q + j: values 8q + 2j + {0, 4} and 8q + 2j + {1, 5}
+          dst[q * Mp * 4] = make_uint4(__byte_perm(wv[4 * q], wv[4 * q + 2], 0x5410),
+                                       __byte_perm(wv[4 * q], wv[4 * q + 2], 0x7632),
+                                       __byte_perm(wv[4 * q + 1], wv[4 * q + 3], 0x5410),
+                                       __byte_perm(wv[4 * q + 1], wv[4 * q + 3], 0x7632));
+        } else {  // step 2q + j: values 8q + 4j .. 8q + 4j + 3
+          dst[q * Mp * 4] = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
         }
       }
     }
   }
-  // ---- group scales of the CTA's rows (INT4), bf16
   if constexpr (kInt4) {
-    const uint16_t *sp = static_cast<const uint16_t *>(a.scales);
-    const int64_t gs = a.K / kWqGroup;
-    for (int e = tid; e < kWqRows * ng; e += blockDim.x) {
-      const int r = e / ng, g = e % ng, row = row_base + r;
-      sc_s[r * a.gpc + g] = row < a.N ? sp[row * gs + kb0 / kWqGroup + g] : uint16_t(0);
+    if constexpr (kEarly) scale_stores(0);
+    for (int base = kEarly ? kScB * blockDim.x : 0; base < nsc; base += kScB * blockDim.x) {
+      scale_loads(base);
+      scale_stores(base);
     }
   }
   __syncthreads();
@@ -281,8 +327,10 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
   float acc[NT][4];
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-  const uint2 *xb = reinterpret_cast<const uint2 *>(xs);
-  const uint16_t *sc0 = sc_s + (warp * 16 + rr) * a.gpc, *sc8 = sc0 + 8 * a.gpc;
+  // this lane's B words (token slot t * 8 + rr) and group scales
+  const uint4 *xl = xs + (NT == 1 ? min(rr, Mp - 1) : rr) * 4 + c;
+  const float2 *scl = sc_s + (warp * 8 + rr) * a.gpc;
+  const float *xul = xu + 2 * c;
 
   for (int g0 = 0; g0 < ng; g0 += C::kDepth) {
 #pragma unroll
@@ -293,63 +341,74 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
       const int nd = (d + kAhead) % C::kDepth;  // register slot of group g + kDepth - 1
       load(g + kAhead, wr0[nd], wr8[nd]);
       float gacc[NT][4];  // the group's sums (the first step writes them)
+      const uint4 *xg = xl + g * 4 * Mp * 4;
 #pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        uint32_t af[4];
-        if constexpr (kInt4) {
-          // step st: nibbles (p, p + 4), (p + 1, p + 5) of word st / 2, p = 2 (st % 2)
-          const uint32_t v0 = (st & 1) ? wr0[d][st >> 1] >> 8 : wr0[d][st >> 1];
-          const uint32_t v8 = (st & 1) ? wr8[d][st >> 1] >> 8 : wr8[d][st >> 1];
-          af[0] = int4lo_to_f16x2(v0);
-          af[1] = int4lo_to_f16x2(v8);
-          af[2] = int4hi_to_f16x2(v0);
-          af[3] = int4hi_to_f16x2(v8);
-        } else {
-          af[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr0[d][st] & 0xFFFFu));
-          af[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr8[d][st] & 0xFFFFu));
-          af[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr0[d][st] >> 16));
-          af[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr8[d][st] >> 16));
-        }
+      for (int q = 0; q < 4; ++q) {
+        // steps 2q and 2q + 1: with up to 4 tiles both A fragments, then per
+        // tile one 16-byte load of both steps' B registers; with more, one
+        // step at a time (registers) and 8-byte loads
+        constexpr int kJ = 2;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const uint2 b = (NT > 1 || rr < Mp) ? xb[((g * 8 + st) * Mp + t * 8 + rr) * 4 + c]
-                                              : make_uint2(0u, 0u);
-          if (st == 0)
-            mma_f16_16816_zero(gacc[t], af, b.x, b.y);
-          else
-            mma_f16_16816(gacc[t], af, b.x, b.y);
+        for (int j0 = 0; j0 < 2; j0 += kJ) {
+          uint32_t af[kJ][4];
+#pragma unroll
+          for (int jj = 0; jj < kJ; ++jj) {
+            const int j = j0 + jj;
+            if constexpr (kInt4) {
+              // step 2q + j: nibbles (p, p + 4), (p + 1, p + 5) of word q, p = 2 j
+              const uint32_t v0 = j ? wr0[d][q] >> 8 : wr0[d][q];
+              const uint32_t v8 = j ? wr8[d][q] >> 8 : wr8[d][q];
+              af[jj][0] = int4lo_to_f16x2(v0);
+              af[jj][1] = int4lo_to_f16x2(v8);
+              af[jj][2] = int4hi_to_f16x2(v0);
+              af[jj][3] = int4hi_to_f16x2(v8);
+            } else {
+              const int st = 2 * q + j;
+              af[jj][0] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr0[d][st] & 0xFFFFu));
+              af[jj][1] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr8[d][st] & 0xFFFFu));
+              af[jj][2] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr0[d][st] >> 16));
+              af[jj][3] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr8[d][st] >> 16));
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const uint4 *bp = xg + (q * Mp + t * 8) * 4;
+            if constexpr (kJ == 2) {
+              const uint4 bq = *bp;
+              if (q == 0)
+                mma_f16_16816_zero(gacc[t], af[0], bq.x, bq.y);
+              else
+                mma_f16_16816(gacc[t], af[0], bq.x, bq.y);
+              mma_f16_16816(gacc[t], af[1], bq.z, bq.w);
+            } else {
+              const uint2 bh = reinterpret_cast<const uint2 *>(bp)[j0];
+              if (q == 0 && j0 == 0)
+                mma_f16_16816_zero(gacc[t], af[0], bh.x, bh.y);
+              else
+                mma_f16_16816(gacc[t], af[0], bh.x, bh.y);
+            }
+          }
         }
       }
       // the group's sums back to x's scale (2^-e of each token: exact unless
       // the sum is below fp32's normal range), times the INT4 group scale,
       // into the output
-      float s0 = 1.f, s8 = 1.f;
-      if constexpr (kInt4) {
-        s0 = __uint_as_float(uint32_t(sc0[g]) << 16);
-        s8 = __uint_as_float(uint32_t(sc8[g]) << 16);
-      }
+      float2 s = make_float2(1.f, 1.f);
+      if constexpr (kInt4) s = scl[g];
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        const int n0 = t * 8 + 2 * c;  // tokens of accumulator elements 0/2 and 1/3
-        float u0, u1;
-        if constexpr (NT > 1) {  // Mp = 8 NT: both tokens staged, the pair 8-byte aligned
-          const float2 u = *reinterpret_cast<const float2 *>(xu + g * Mp + n0);
-          u0 = u.x;
-          u1 = u.y;
-        } else {
-          u0 = n0 < Mp ? xu[g * Mp + n0] : 0.f;
-          u1 = n0 + 1 < Mp ? xu[g * Mp + n0 + 1] : 0.f;
-        }
+        // tokens t * 8 + 2c and + 1 (accumulator elements 0/2 and 1/3)
+        const float2 u = *reinterpret_cast<const float2 *>(xul + g * kTok + t * 8);
         if constexpr (kInt4) {
-          acc[t][0] = fmaf(s0, gacc[t][0] * u0, acc[t][0]);
-          acc[t][1] = fmaf(s0, gacc[t][1] * u1, acc[t][1]);
-          acc[t][2] = fmaf(s8, gacc[t][2] * u0, acc[t][2]);
-          acc[t][3] = fmaf(s8, gacc[t][3] * u1, acc[t][3]);
+          acc[t][0] = fmaf(s.x, gacc[t][0] * u.x, acc[t][0]);
+          acc[t][1] = fmaf(s.x, gacc[t][1] * u.y, acc[t][1]);
+          acc[t][2] = fmaf(s.y, gacc[t][2] * u.x, acc[t][2]);
+          acc[t][3] = fmaf(s.y, gacc[t][3] * u.y, acc[t][3]);
         } else {
-          acc[t][0] = fmaf(gacc[t][0], u0, acc[t][0]);
-          acc[t][1] = fmaf(gacc[t][1], u1, acc[t][1]);
-          acc[t][2] = fmaf(gacc[t][2], u0, acc[t][2]);
-          acc[t][3] = fmaf(gacc[t][3], u1, acc[t][3]);
+          acc[t][0] = fmaf(gacc[t][0], u.x, acc[t][0]);
+          acc[t][1] = fmaf(gacc[t][1], u.y, acc[t][1]);
+          acc[t][2] = fmaf(gacc[t][2], u.x, acc[t][2]);
+          acc[t][3] = fmaf(gacc[t][3], u.y, acc[t][3]);
         }
       }
     }
@@ -358,9 +417,9 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
   // ---- epilogue: c0, c1 -> row0, tokens 2c, 2c + 1 of each tile; c2, c3 -> row0 + 8
   float f0 = 1.f, f8 = 1.f;
   if constexpr (!kInt4) {
-    const float *sp = static_cast<const float *>(a.scales);
-    f0 = ok0 ? sp[row0] : 0.f;
-    f8 = ok8 ? sp[row0 + 8] : 0.f;
+    const float *fs = static_cast<const float *>(a.scales);
+    f0 = fs[min(row0, a.N - 1)];
+    f8 = fs[min(row0 + 8, a.N - 1)];
   }
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
@@ -437,7 +496,7 @@ extern "C" kvq_status kvq_wq_gemm(int32_t w_dtype, const void *w, const void *sc
   // staged x must fit the shared-memory budget
   const int row_tiles = (N + kWqRows - 1) / kWqRows;
   const int groups = K / kWqGroup;
-  auto smem_of = [&](int gpc) { return wq_smem_bytes(gpc, nt, M); };
+  auto smem_of = [&](int gpc) { return wq_smem_bytes(int4, gpc, nt, M); };
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!wq_smem_opt_in(fn, int4 ? nt - 1 : 8 + nt - 1)) return KVQ_ERR_CUDA;
   // k splits: as many as fill the GPU's resident CTAs once (at the occupancy

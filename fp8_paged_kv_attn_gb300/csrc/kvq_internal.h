@@ -4,6 +4,8 @@
 #include <cmath>
 #include <cstdint>
 #include <utility>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "kvq.h"
@@ -16,6 +18,10 @@ inline bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) &
 
 // Number of SMs of the current device (cached per device).
 kvq_status device_sm_count(int *sms);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda); null when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Launches `kernel` as a programmatic dependent of the work ahead of it on
 // `stream`: its CTAs may be scheduled as soon as the previous kernel has let

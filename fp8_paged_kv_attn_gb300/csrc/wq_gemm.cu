@@ -12,22 +12,31 @@
 // scales per 128-wide group of k), and the FP8 path it is compared with as
 // e4m3 weights with an fp32 scale per output channel.
 //
-// Kernel: a CTA of 8 warps covers 128 output channels (16 per warp) and a
-// range of 128-wide k groups (split-K over CTAs, partial sums added with
-// atomics into a zeroed y).  The CTA first stages its slice of x in shared
-// memory in MMA-fragment order (so a lane's B registers for two MMA steps
-// are one 16-byte load; a thread stages a 32-value chunk with four 16-byte
-// loads and a permutation in registers) and, for INT4, its rows' group
-// scales as fp32 pairs (rows r and r + 8: one 8-byte load per group; the
-// scale loads are all issued before any is stored, so they cost one memory
-// round trip, not one per element); each lane then streams its weights
-// straight from HBM as contiguous 16-byte runs (the k order inside a group
-// is permuted consistently in the weights' fragments and in the staged x,
-// which leaves the sum unchanged), with a register ring of the next 3 (INT4)
-// or 2 (e4m3) groups' loads in flight while the current one is computed.
+// Two kernels, one per regime:
+//  * the TMA-ring kernel (up to 4 tokens for INT4, 2 for e4m3): 64 output
+//    channels per CTA; a producer warp streams the weights into a
+//    shared-memory ring with the TMA engine, eight consumer warps read them
+//    from there; a k split is a thread-block cluster whose partial sums are
+//    added through distributed shared memory in rank order (details at the
+//    kernel);
+//  * the register-ring kernel (more tokens): a CTA of 8 warps covers 128
+//    output channels (16 per warp) and a range of 128-wide k groups
+//    (split-K over CTAs, partial sums added with atomics into a zeroed y);
+//    each lane streams its weights straight from HBM as contiguous 16-byte
+//    runs with a register ring of the next 3 (INT4) or 2 (e4m3) groups'
+//    loads in flight while the current one is computed.
+// Both first stage their slice of x in shared memory in MMA-fragment order
+// (a lane's B registers for two MMA steps are one 16-byte load; the k order
+// inside a group is permuted consistently in the weights' fragments and in
+// the staged x, which leaves the sum unchanged) and, for INT4, their rows'
+// group scales as fp32 pairs (rows r and r + 8: one 8-byte load per group;
+// the scale loads are all issued before any is stored, so they cost one
+// memory round trip).  The weights and scales are read before the kernel
+// waits for the work ahead of it on the stream (they are constant); x after.
 // Rows past N and, with one token tile, token slots past M read a valid
 // neighbour instead of branching (an output row depends only on its row of
 // the A operand, an output token only on its column of B; neither is stored).
+// Arithmetic, both kernels:
 //  x is scaled while staged, per token and 128-wide k group, by the power of
 //  two 2^e that puts the group's largest finite |x| in [2^14, 2^15), then
 //  rounded to f16: exact for every bf16 value down to 2^-32 of that largest
@@ -44,8 +53,8 @@
 // Products are exact and the sums are fp32, so the result differs from the
 // fp64 definition only by fp32 summation rounding (and, for x values more
 // than 2^32 below their group's largest, by the f16 rounding of those; and,
-// for results below fp32's normal range, by the split-K atomics, since an
-// fp32 atomic add flushes subnormal operands).
+// in the register-ring kernel, for results below fp32's normal range, by the
+// split-K atomics, since an fp32 atomic add flushes subnormal operands).
 #include <atomic>
 
 #include <cuda_fp16.h>
@@ -54,18 +63,6 @@
 
 namespace kvq {
 
-struct WqArgs {
-  const uint8_t *w;       // INT4 [N][K/2] or e4m3 [N][K]
-  const void *scales;     // bf16 [N][K/128] or fp32 [N]
-  const uint16_t *x;      // bf16 [M][K]
-  float *y;               // fp32 [M][N]
-  int32_t M, N, K;
-  int32_t gpc;            // 128-wide k groups per CTA
-  int32_t atomic;         // add into y (split-K) instead of storing
-};
-
-constexpr int kWqWarps = 8;
-constexpr int kWqRows = 16 * kWqWarps;  // output channels per CTA
 constexpr int kWqGroup = 128;
 
 __device__ __forceinline__ void mma_f16_16816(float c[4], const uint32_t a[4], uint32_t b0,
@@ -107,22 +104,6 @@ __device__ __forceinline__ uint32_t int4hi_to_f16x2(uint32_t v) {
   return r;
 }
 
-// The fragment order of a lane class's 32 k values in a group: slot i (0..3;
-// slots 0-1 are the B register b0b1, 2-3 are b2b3) of step s (0..7) holds
-// value j = frag_src(s, i).  INT4: step s uses nibbles (p, p + 4) and
-// (p + 1, p + 5) of weight word q = s / 2 with p = 2 (s % 2), i.e. k offsets
-// 8q + p + {0, 4, 1, 5}; e4m3: step s uses bytes 4s .. 4s + 3 in order.
-template <bool kInt4>
-__device__ __forceinline__ constexpr int frag_src(int s, int i) {
-  if constexpr (kInt4) {
-    const int q = s >> 1, p = 2 * (s & 1);
-    const int d = (i == 0) ? 0 : (i == 1) ? 4 : (i == 2) ? 1 : 5;
-    return 8 * q + p + d;
-  } else {
-    return 4 * s + i;
-  }
-}
-
 // The exponent e of 2^e that puts a token's largest finite |x| (the bits of
 // a non-negative fp32 value; 0 when all are zero) in [2^14, 2^15): 14 minus
 // floor(log2 |x|), read off the bits (a subnormal m * 2^-149 has
@@ -142,143 +123,140 @@ __device__ __forceinline__ float pow2_any(int n) {
   return n >= -126 ? pow2i(n) : __int_as_float(1 << (149 + n));
 }
 
-template <bool kInt4, int NT>
-struct WqCfg {
-  static constexpr int kWords = kInt4 ? 4 : 8;  // weight words per row half per lane per group
-  // groups of weights held in registers per warp (fewer when more than four
-  // token tiles need the registers; those products are bound by the MMAs)
-  static constexpr int kDepth = NT > 4 ? 2 : kInt4 ? 4 : 3;
-};
+// ---------------------------------------------------------------------------
+// Pieces shared by both kernels
+// ---------------------------------------------------------------------------
+//
+// Fragment order.  mma.m16n8k16 pairs a lane's A slots with its own B slots:
+// for lane class c (lane % 4), A registers 0/1 (rows r, r + 8) hold the k
+// pair that B register 0 holds and A registers 2/3 the pair of B register 1.
+// Which actual k sits in a slot is free, as long as A and B agree, so each
+// lane class owns 32 k values of a 128-wide group and the B operand is
+// staged in the order the weights arrive:
+//  INT4: the class's 16 weight bytes per row, word q (8 nibbles) feeding
+//        steps 2q (nibbles 0, 4 and 1, 5) and 2q + 1 (nibbles 2, 6 and 3, 7);
+//  e4m3: the class's 32 code bytes per row, word st (4 codes) feeding step
+//        st (codes 0, 1 and 2, 3).
+// A lane's two B registers of steps 2q and 2q + 1 are one 16-byte word of
+// the staged x: [group][step pair q][token slot][lane class].
 
-// shared memory of a CTA: [INT4 group scales: fp32 pairs for rows (r, r + 8),
-// per pair and group][staged x][2^-e per (group, token slot of the tiles), fp32]
-__host__ __device__ constexpr int wq_staged_tokens(int nt, int M) { return nt == 1 ? M : 8 * nt; }
-__host__ __device__ constexpr size_t wq_scale_bytes(bool int4, int gpc) {
-  return int4 ? size_t(kWqRows / 2) * gpc * 8 : 0;
-}
-__host__ __device__ constexpr size_t wq_x_bytes(int gpc, int nt, int M) {
-  return size_t(gpc) * kWqGroup * wq_staged_tokens(nt, M) * sizeof(uint16_t);
-}
-__host__ __device__ constexpr size_t wq_smem_bytes(bool int4, int gpc, int nt, int M) {
-  return wq_scale_bytes(int4, gpc) + wq_x_bytes(gpc, nt, M) + size_t(gpc) * 8 * nt * 4;
-}
-
-template <bool kInt4, int NT>
-__global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel(WqArgs a) {
-  using C = WqCfg<kInt4, NT>;
-  constexpr int kTok = 8 * NT;  // token slots of the MMA tiles
-  extern __shared__ __align__(16) uint8_t wq_smem[];
-  const size_t scb = wq_scale_bytes(kInt4, a.gpc);
-  float2 *sc_s = reinterpret_cast<float2 *>(wq_smem);  // [kWqRows / 2][gpc]
-  // staged x, one 16-byte word per (group, step pair, token, lane class):
-  // the B registers of two consecutive MMA steps
-  uint4 *xs = reinterpret_cast<uint4 *>(wq_smem + scb);
-  // tokens staged: 8 per tile, or just the M real ones when there is one tile
-  const int Mp = wq_staged_tokens(NT, a.M);
-  float *xu = reinterpret_cast<float *>(wq_smem + scb + wq_x_bytes(a.gpc, NT, a.M));  // [gpc][kTok]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int c = lane & 3, rr = lane >> 2;
-  const int kc = a.gpc * kWqGroup;
-  const int kb0 = blockIdx.y * kc;
-  const int ng = min(a.gpc, (a.K - kb0) / kWqGroup);
-  const int row_base = blockIdx.x * kWqRows;
-  const int row0 = row_base + warp * 16 + rr;  // this lane's rows: row0, row0 + 8
-  // An output row depends only on its own row of A, an output token only on
-  // its own column of B: rows past N read row N - 1 and, with one tile,
-  // token slots past M read token M - 1; neither sum is ever stored.
-  const int64_t row_bytes = kInt4 ? a.K / 2 : a.K;
-  constexpr int kGroupBytes = kInt4 ? kWqGroup / 2 : kWqGroup;
-  const int64_t lane_off = kInt4 ? kb0 / 2 + c * 16 : kb0 + c * 32;
-  const uint8_t *w0 = a.w + static_cast<int64_t>(min(row0, a.N - 1)) * row_bytes + lane_off;
-  const uint8_t *w8 = a.w + static_cast<int64_t>(min(row0 + 8, a.N - 1)) * row_bytes + lane_off;
-  grid_dependency_wait();
-  allow_dependents();
-
-  // this lane's weights of group g
-  auto load = [&](int g, uint32_t (&r0)[C::kWords], uint32_t (&r8)[C::kWords]) {
-    if (g >= ng) return;
+// One group's products for NT token tiles: gacc[t] = the sum of kQ step
+// pairs (all 4 of a group, or 2: one e4m3 half-group) starting from zero.
+// w0 / w8: the lane's weight words of rows r and r + 8; xg: the lane's B
+// word of the first step pair (token slot of tile 0), Mp token slots per
+// step pair.
+template <bool kInt4, int NT, int kQ = 4>
+__device__ __forceinline__ void group_mma(float (&gacc)[NT][4],
+                                          const uint32_t (&w0)[kInt4 ? kQ : 2 * kQ],
+                                          const uint32_t (&w8)[kInt4 ? kQ : 2 * kQ],
+                                          const uint4 *xg, int Mp) {
 #pragma unroll
-    for (int h = 0; h < C::kWords / 4; ++h) {
-      const uint4 u0 = __ldcs(reinterpret_cast<const uint4 *>(w0 + g * kGroupBytes) + h);
-      const uint4 u8 = __ldcs(reinterpret_cast<const uint4 *>(w8 + g * kGroupBytes) + h);
-      r0[4 * h] = u0.x; r0[4 * h + 1] = u0.y; r0[4 * h + 2] = u0.z; r0[4 * h + 3] = u0.w;
-      r8[4 * h] = u8.x; r8[4 * h + 1] = u8.y; r8[4 * h + 2] = u8.z; r8[4 * h + 3] = u8.w;
-    }
-  };
-  // the first kDepth - 1 groups are in flight while x and the scales are staged
-  uint32_t wr0[C::kDepth][C::kWords], wr8[C::kDepth][C::kWords];
+  for (int q = 0; q < kQ; ++q) {
+    uint32_t af[2][4];
 #pragma unroll
-  for (int d = 0; d < C::kDepth - 1; ++d) load(d, wr0[d], wr8[d]);
-
-  // ---- INT4 group scales of the CTA's row pairs, fp32 in shared memory.
-  // One item = (row pair p, group g): rows row_base + 16 (p / 8) + p % 8 and
-  // 8 below.  Every load of a batch is issued before any is stored, and the
-  // first batch's loads are in flight while x is staged
-  constexpr int kScB = 5;  // items per thread per batch
-  const int nsc = kInt4 ? (kWqRows / 2) * ng : 0;
-  const uint16_t *sp = static_cast<const uint16_t *>(a.scales);
-  const int64_t gs = a.K / kWqGroup;
-  uint16_t scv[kScB][2];
-  auto scale_loads = [&](int base) {
-#pragma unroll
-    for (int i = 0; i < kScB; ++i) {
-      const int e = base + i * blockDim.x + tid;
-      if (e < nsc) {
-        const int p = e / ng, g = e - p * ng;
-        const int r = row_base + (p >> 3) * 16 + (p & 7);
-        const int64_t col = kb0 / kWqGroup + g;
-        scv[i][0] = __ldg(sp + min(r, a.N - 1) * gs + col);
-        scv[i][1] = __ldg(sp + min(r + 8, a.N - 1) * gs + col);
+    for (int j = 0; j < 2; ++j) {
+      if constexpr (kInt4) {
+        // step 2q + j: nibbles (p, p + 4), (p + 1, p + 5) of word q, p = 2 j
+        const uint32_t v0 = j ? w0[q] >> 8 : w0[q];
+        const uint32_t v8 = j ? w8[q] >> 8 : w8[q];
+        af[j][0] = int4lo_to_f16x2(v0);
+        af[j][1] = int4lo_to_f16x2(v8);
+        af[j][2] = int4hi_to_f16x2(v0);
+        af[j][3] = int4hi_to_f16x2(v8);
+      } else {
+        const int st = 2 * q + j;
+        af[j][0] = e4m3x2_to_f16x2(static_cast<uint16_t>(w0[st] & 0xFFFFu));
+        af[j][1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w8[st] & 0xFFFFu));
+        af[j][2] = e4m3x2_to_f16x2(static_cast<uint16_t>(w0[st] >> 16));
+        af[j][3] = e4m3x2_to_f16x2(static_cast<uint16_t>(w8[st] >> 16));
       }
     }
-  };
-  auto scale_stores = [&](int base) {
 #pragma unroll
-    for (int i = 0; i < kScB; ++i) {
-      const int e = base + i * blockDim.x + tid;
-      if (e < nsc) {
-        const int p = e / ng, g = e - p * ng;
-        sc_s[p * a.gpc + g] = make_float2(__uint_as_float(uint32_t(scv[i][0]) << 16),
-                                          __uint_as_float(uint32_t(scv[i][1]) << 16));
-      }
+    for (int t = 0; t < NT; ++t) {
+      const uint4 bq = xg[(q * Mp + t * 8) * 4];
+      if (q == 0)
+        mma_f16_16816_zero(gacc[t], af[0], bq.x, bq.y);
+      else
+        mma_f16_16816(gacc[t], af[0], bq.x, bq.y);
+      mma_f16_16816(gacc[t], af[1], bq.z, bq.w);
     }
-  };
-  // (with one token tile; with more, registers are short and x takes longer)
-  constexpr bool kEarly = kInt4 && NT == 1;
-  if constexpr (kEarly) scale_loads(0);
+  }
+}
 
-  // ---- stage x: one thread per (group, token, class) chunk of 32 k values:
-  // four 16-byte loads; the chunk's largest finite |x| (a bf16 magnitude
-  // below 0x7F80, compared as an integer), shared with the group's other
-  // three chunks, which sit in lanes 4j .. 4j + 3 of the same warp (the
-  // block size is a multiple of 4; every lane takes part in every pass);
-  // the values times 2^e rounded to f16; the fragment permutation on whole
-  // words (e4m3: the values' own order; INT4: two byte permutes per pair of
-  // words); four 16-byte stores, one per step pair.
+// The group's sums back to x's scale (2^-e of each token: exact unless the
+// sum is below fp32's normal range), times the INT4 group scales s (rows r,
+// r + 8), into the running sums.  xug: 2^-e of the group's token slots
+// 2c, 2c + 1 of tile 0 (tiles 8 slots apart).  kOne (one token): only the
+// sums of token slot 2c (elements 0 and 2) are kept, the others are never
+// stored.
+template <bool kInt4, int NT, bool kOne = false>
+__device__ __forceinline__ void group_fold(float (&acc)[NT][4], const float (&gacc)[NT][4],
+                                           float2 s, const float *xug) {
+  if constexpr (kOne) {
+    const float u = xug[0];
+    acc[0][0] = kInt4 ? fmaf(s.x, gacc[0][0] * u, acc[0][0]) : fmaf(gacc[0][0], u, acc[0][0]);
+    acc[0][2] = kInt4 ? fmaf(s.y, gacc[0][2] * u, acc[0][2]) : fmaf(gacc[0][2], u, acc[0][2]);
+    return;
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const float2 u = *reinterpret_cast<const float2 *>(xug + t * 8);
+    if constexpr (kInt4) {
+      acc[t][0] = fmaf(s.x, gacc[t][0] * u.x, acc[t][0]);
+      acc[t][1] = fmaf(s.x, gacc[t][1] * u.y, acc[t][1]);
+      acc[t][2] = fmaf(s.y, gacc[t][2] * u.x, acc[t][2]);
+      acc[t][3] = fmaf(s.y, gacc[t][3] * u.y, acc[t][3]);
+    } else {
+      acc[t][0] = fmaf(gacc[t][0], u.x, acc[t][0]);
+      acc[t][1] = fmaf(gacc[t][1], u.y, acc[t][1]);
+      acc[t][2] = fmaf(gacc[t][2], u.x, acc[t][2]);
+      acc[t][3] = fmaf(gacc[t][3], u.y, acc[t][3]);
+    }
+  }
+}
+
+// Stages x[m][kb0 .. kb0 + 128 ng) for Mp token slots (slots past M are
+// zero) with threads tid = 0 .. nthr - 1 of whole warps, nthr a multiple of
+// 32: one thread per (group, token, class) chunk of 32 k values: four
+// 16-byte loads; the chunk's largest finite |x| (a bf16 magnitude below
+// 0x7F80, compared as an integer), shared with the group's other three
+// chunks, which sit in lanes 4j .. 4j + 3 of the same warp (every lane takes
+// part in every pass); the values times 2^e (e puts the group's largest in
+// [2^14, 2^15)) rounded to f16; 2^-e into xu[g * kTok + m]; the fragment
+// permutation on whole words (e4m3: the values' own order; INT4: two byte
+// permutes per pair of words); four 16-byte stores, one per step pair.
+// A class's 32 values are x[32 cl ..] or, with kHalves (e4m3 weights that
+// arrive as two 64-byte halves of a group), x[16 cl ..] and x[64 + 16 cl ..].
+template <bool kInt4, bool kHalves>
+__device__ __forceinline__ void stage_x(uint4 *xs, float *xu, int kTok, const uint16_t *x, int K,
+                                        int M, int Mp, int kb0, int ng, int tid, int nthr) {
   const int nch = ng * Mp * 4;
-  for (int base = 0; base < nch; base += blockDim.x) {
+  for (int base = 0; base < nch; base += nthr) {
     const int ch = base + tid;
     const int cl = ch & 3, m = (ch >> 2) % Mp, g = (ch >> 2) / Mp;
-    const bool real = ch < nch && m < a.M;
+    const bool real = ch < nch && m < M;
     uint32_t wv[16];  // bf16 pairs, value 2i in the low half of word i
     uint32_t mx = 0u;
     if (real) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          a.x + static_cast<int64_t>(m) * a.K + kb0 + g * kWqGroup + cl * 32);
+      const uint16_t *row = x + static_cast<int64_t>(m) * K + kb0 + g * kWqGroup;
+      const uint4 *s0 = reinterpret_cast<const uint4 *>(row + (kHalves ? 16 * cl : 32 * cl));
+      const uint4 *s1 = kHalves ? reinterpret_cast<const uint4 *>(row + 64 + 16 * cl) : s0 + 2;
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        const uint4 u = __ldg(src + h);
+        const uint4 u = __ldg(h < 2 ? s0 + h : s1 + (h - 2));
         wv[4 * h] = u.x;
         wv[4 * h + 1] = u.y;
         wv[4 * h + 2] = u.z;
         wv[4 * h + 3] = u.w;
       }
+      // both halves of a word at once; NaN and inf (>= 0x7F80) take no part
+      uint32_t mx2 = 0u;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const uint32_t lo = wv[i] & 0x7FFFu, hi = (wv[i] >> 16) & 0x7FFFu;
-        if (lo < 0x7F80u) mx = max(mx, lo);  // NaN and inf take no part
-        if (hi < 0x7F80u) mx = max(mx, hi);
+        const uint32_t m = wv[i] & 0x7FFF7FFFu;
+        mx2 = __vmaxu2(mx2, m & __vcmpltu2(m, 0x7F807F80u));
       }
+      mx = max(mx2 & 0xFFFFu, mx2 >> 16);
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i) wv[i] = 0u;
@@ -315,11 +293,169 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
       }
     }
   }
+}
+
+// INT4 group scales of a CTA's row pairs as fp32 pairs, sc_s[p * gpc + g]
+// for pair p (rows row_base + 16 (p / 8) + p % 8 and 8 below, a row past N
+// reads row N - 1) and group g < ng.  Items e = p * ng + g go to threads in
+// order (a warp reads runs of consecutive scales), kScB per thread and
+// batch: every load of a batch is issued before any is stored, so a batch
+// costs one memory round trip.  p = e / ng is taken as floor((e + 1/2) /
+// ng) in fp32, exact for every ng up to 2048 and e below 64 ng (checked
+// exhaustively).
+constexpr int kScB = 5;
+struct ScaleStage {
+  const uint16_t *sp;  // bf16 scales [N][K / 128], from the CTA's first group
+  float2 *sc_s;
+  int64_t gs;          // groups per row of the matrix
+  int ng, gpc, N, row_base, n, tid, nthr;
+  float inv_ng;
+  uint16_t v[kScB][2];
+  __device__ __forceinline__ ScaleStage(const void *scales, float2 *sc_s_, int K, int N_,
+                                        int kb0, int ng_, int gpc_, int row_base_, int pairs,
+                                        int tid_, int nthr_) {
+    gs = K / kWqGroup;
+    sp = static_cast<const uint16_t *>(scales) + kb0 / kWqGroup;
+    sc_s = sc_s_;
+    ng = ng_;
+    gpc = gpc_;
+    N = N_;
+    row_base = row_base_;
+    n = pairs * ng_;
+    tid = tid_;
+    nthr = nthr_;
+    inv_ng = 1.f / static_cast<float>(ng_);
+  }
+  __device__ __forceinline__ int batches() const {
+    return (n + kScB * nthr - 1) / (kScB * nthr);
+  }
+  __device__ __forceinline__ void split(int e, int &p, int &g) const {
+    p = static_cast<int>((static_cast<float>(e) + 0.5f) * inv_ng);
+    g = e - p * ng;
+  }
+  __device__ __forceinline__ void load(int batch) {
+#pragma unroll
+    for (int i = 0; i < kScB; ++i) {
+      const int e = (batch * kScB + i) * nthr + tid;
+      if (e < n) {
+        int p, g;
+        split(e, p, g);
+        const int r = row_base + (p >> 3) * 16 + (p & 7);
+        v[i][0] = __ldg(sp + min(r, N - 1) * gs + g);
+        v[i][1] = __ldg(sp + min(r + 8, N - 1) * gs + g);
+      }
+    }
+  }
+  __device__ __forceinline__ void store(int batch) {
+#pragma unroll
+    for (int i = 0; i < kScB; ++i) {
+      const int e = (batch * kScB + i) * nthr + tid;
+      if (e < n) {
+        int p, g;
+        split(e, p, g);
+        sc_s[p * gpc + g] = make_float2(__uint_as_float(uint32_t(v[i][0]) << 16),
+                                        __uint_as_float(uint32_t(v[i][1]) << 16));
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Register-ring kernel (any tile count; used for more tokens than the ring takes)
+// ---------------------------------------------------------------------------
+
+struct WqArgs {
+  const uint8_t *w;       // INT4 [N][K/2] or e4m3 [N][K]
+  const void *scales;     // bf16 [N][K/128] or fp32 [N]
+  const uint16_t *x;      // bf16 [M][K]
+  float *y;               // fp32 [M][N]
+  int32_t M, N, K;
+  int32_t gpc;            // 128-wide k groups per CTA
+  int32_t atomic;         // add into y (split-K) instead of storing
+};
+
+constexpr int kWqWarps = 8;
+constexpr int kWqRows = 16 * kWqWarps;  // output channels per CTA
+
+template <bool kInt4, int NT>
+struct WqCfg {
+  static constexpr int kWords = kInt4 ? 4 : 8;  // weight words per row half per lane per group
+  // groups of weights held in registers per warp (fewer when more than four
+  // token tiles need the registers; those products are bound by the MMAs)
+  static constexpr int kDepth = NT > 4 ? 2 : kInt4 ? 4 : 3;
+};
+
+// shared memory of a CTA: [INT4 group scales: fp32 pairs for rows (r, r + 8),
+// per pair and group][staged x][2^-e per (group, token slot of the tiles), fp32]
+__host__ __device__ constexpr int wq_staged_tokens(int nt, int M) { return nt == 1 ? M : 8 * nt; }
+__host__ __device__ constexpr size_t wq_scale_bytes(bool int4, int pairs, int gpc) {
+  return int4 ? size_t(pairs) * gpc * 8 : 0;
+}
+__host__ __device__ constexpr size_t wq_x_bytes(int gpc, int nt, int M) {
+  return size_t(gpc) * kWqGroup * wq_staged_tokens(nt, M) * sizeof(uint16_t);
+}
+__host__ __device__ constexpr size_t wq_smem_bytes(bool int4, int gpc, int nt, int M) {
+  return wq_scale_bytes(int4, kWqRows / 2, gpc) + wq_x_bytes(gpc, nt, M) + size_t(gpc) * 8 * nt * 4;
+}
+
+template <bool kInt4, int NT>
+__global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel(WqArgs a) {
+  using C = WqCfg<kInt4, NT>;
+  constexpr int kTok = 8 * NT;  // token slots of the MMA tiles
+  extern __shared__ __align__(16) uint8_t wq_smem[];
+  const size_t scb = wq_scale_bytes(kInt4, kWqRows / 2, a.gpc);
+  float2 *sc_s = reinterpret_cast<float2 *>(wq_smem);  // [kWqRows / 2][gpc]
+  uint4 *xs = reinterpret_cast<uint4 *>(wq_smem + scb);
+  // tokens staged: 8 per tile, or just the M real ones when there is one tile
+  const int Mp = wq_staged_tokens(NT, a.M);
+  float *xu = reinterpret_cast<float *>(wq_smem + scb + wq_x_bytes(a.gpc, NT, a.M));  // [gpc][kTok]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = lane & 3, rr = lane >> 2;
+  const int kb0 = blockIdx.y * a.gpc * kWqGroup;
+  const int ng = min(a.gpc, (a.K - kb0) / kWqGroup);
+  const int row_base = blockIdx.x * kWqRows;
+  const int row0 = row_base + warp * 16 + rr;  // this lane's rows: row0, row0 + 8
+  // An output row depends only on its own row of A, an output token only on
+  // its own column of B: rows past N read row N - 1 and, with one tile,
+  // token slots past M read token M - 1; neither sum is ever stored.
+  const int64_t row_bytes = kInt4 ? a.K / 2 : a.K;
+  constexpr int kGroupBytes = kInt4 ? kWqGroup / 2 : kWqGroup;
+  const int64_t lane_off = kInt4 ? kb0 / 2 + c * 16 : kb0 + c * 32;
+  const uint8_t *w0 = a.w + static_cast<int64_t>(min(row0, a.N - 1)) * row_bytes + lane_off;
+  const uint8_t *w8 = a.w + static_cast<int64_t>(min(row0 + 8, a.N - 1)) * row_bytes + lane_off;
+
+  // this lane's weights of group g
+  auto load = [&](int g, uint32_t (&r0)[C::kWords], uint32_t (&r8)[C::kWords]) {
+    if (g >= ng) return;
+#pragma unroll
+    for (int h = 0; h < C::kWords / 4; ++h) {
+      const uint4 u0 = __ldcs(reinterpret_cast<const uint4 *>(w0 + g * kGroupBytes) + h);
+      const uint4 u8 = __ldcs(reinterpret_cast<const uint4 *>(w8 + g * kGroupBytes) + h);
+      r0[4 * h] = u0.x; r0[4 * h + 1] = u0.y; r0[4 * h + 2] = u0.z; r0[4 * h + 3] = u0.w;
+      r8[4 * h] = u8.x; r8[4 * h + 1] = u8.y; r8[4 * h + 2] = u8.z; r8[4 * h + 3] = u8.w;
+    }
+  };
+  // the first kDepth - 1 groups are in flight while x and the scales are staged
+  uint32_t wr0[C::kDepth][C::kWords], wr8[C::kDepth][C::kWords];
+#pragma unroll
+  for (int d = 0; d < C::kDepth - 1; ++d) load(d, wr0[d], wr8[d]);
+
+  // INT4 scales: with one token tile the first batch's loads are in flight
+  // while x is staged (with more, registers are short and x takes longer)
+  constexpr int nthr = 32 * kWqWarps;
+  ScaleStage sst(a.scales, sc_s, a.K, a.N, kb0, ng, a.gpc, row_base, kWqRows / 2, tid, nthr);
+  constexpr bool kEarly = kInt4 && NT == 1;
+  if constexpr (kEarly) sst.load(0);
+  // The weights and their scales are constant (see kvq_wq_gemm): only x
+  // waits for the work ahead of this kernel on the stream.
+  grid_dependency_wait();
+  allow_dependents();
+  stage_x<kInt4, false>(xs, xu, kTok, a.x, a.K, a.M, Mp, kb0, ng, tid, nthr);
   if constexpr (kInt4) {
-    if constexpr (kEarly) scale_stores(0);
-    for (int base = kEarly ? kScB * blockDim.x : 0; base < nsc; base += kScB * blockDim.x) {
-      scale_loads(base);
-      scale_stores(base);
+    if constexpr (kEarly) sst.store(0);
+    for (int b = kEarly ? 1 : 0; b < sst.batches(); ++b) {
+      sst.load(b);
+      sst.store(b);
     }
   }
   __syncthreads();
@@ -340,77 +476,9 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
       constexpr int kAhead = C::kDepth - 1;
       const int nd = (d + kAhead) % C::kDepth;  // register slot of group g + kDepth - 1
       load(g + kAhead, wr0[nd], wr8[nd]);
-      float gacc[NT][4];  // the group's sums (the first step writes them)
-      const uint4 *xg = xl + g * 4 * Mp * 4;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        // steps 2q and 2q + 1: with up to 4 tiles both A fragments, then per
-        // tile one 16-byte load of both steps' B registers; with more, one
-        // step at a time (registers) and 8-byte loads
-        constexpr int kJ = 2;
-#pragma unroll
-        for (int j0 = 0; j0 < 2; j0 += kJ) {
-          uint32_t af[kJ][4];
-#pragma unroll
-          for (int jj = 0; jj < kJ; ++jj) {
-            const int j = j0 + jj;
-            if constexpr (kInt4) {
-              // step 2q + j: nibbles (p, p + 4), (p + 1, p + 5) of word q, p = 2 j
-              const uint32_t v0 = j ? wr0[d][q] >> 8 : wr0[d][q];
-              const uint32_t v8 = j ? wr8[d][q] >> 8 : wr8[d][q];
-              af[jj][0] = int4lo_to_f16x2(v0);
-              af[jj][1] = int4lo_to_f16x2(v8);
-              af[jj][2] = int4hi_to_f16x2(v0);
-              af[jj][3] = int4hi_to_f16x2(v8);
-            } else {
-              const int st = 2 * q + j;
-              af[jj][0] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr0[d][st] & 0xFFFFu));
-              af[jj][1] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr8[d][st] & 0xFFFFu));
-              af[jj][2] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr0[d][st] >> 16));
-              af[jj][3] = e4m3x2_to_f16x2(static_cast<uint16_t>(wr8[d][st] >> 16));
-            }
-          }
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const uint4 *bp = xg + (q * Mp + t * 8) * 4;
-            if constexpr (kJ == 2) {
-              const uint4 bq = *bp;
-              if (q == 0)
-                mma_f16_16816_zero(gacc[t], af[0], bq.x, bq.y);
-              else
-                mma_f16_16816(gacc[t], af[0], bq.x, bq.y);
-              mma_f16_16816(gacc[t], af[1], bq.z, bq.w);
-            } else {
-              const uint2 bh = reinterpret_cast<const uint2 *>(bp)[j0];
-              if (q == 0 && j0 == 0)
-                mma_f16_16816_zero(gacc[t], af[0], bh.x, bh.y);
-              else
-                mma_f16_16816(gacc[t], af[0], bh.x, bh.y);
-            }
-          }
-        }
-      }
-      // the group's sums back to x's scale (2^-e of each token: exact unless
-      // the sum is below fp32's normal range), times the INT4 group scale,
-      // into the output
-      float2 s = make_float2(1.f, 1.f);
-      if constexpr (kInt4) s = scl[g];
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        // tokens t * 8 + 2c and + 1 (accumulator elements 0/2 and 1/3)
-        const float2 u = *reinterpret_cast<const float2 *>(xul + g * kTok + t * 8);
-        if constexpr (kInt4) {
-          acc[t][0] = fmaf(s.x, gacc[t][0] * u.x, acc[t][0]);
-          acc[t][1] = fmaf(s.x, gacc[t][1] * u.y, acc[t][1]);
-          acc[t][2] = fmaf(s.y, gacc[t][2] * u.x, acc[t][2]);
-          acc[t][3] = fmaf(s.y, gacc[t][3] * u.y, acc[t][3]);
-        } else {
-          acc[t][0] = fmaf(gacc[t][0], u.x, acc[t][0]);
-          acc[t][1] = fmaf(gacc[t][1], u.y, acc[t][1]);
-          acc[t][2] = fmaf(gacc[t][2], u.x, acc[t][2]);
-          acc[t][3] = fmaf(gacc[t][3], u.y, acc[t][3]);
-        }
-      }
+      float gacc[NT][4];
+      group_mma<kInt4, NT>(gacc, wr0[d], wr8[d], xl + g * 4 * Mp * 4, Mp);
+      group_fold<kInt4, NT>(acc, gacc, kInt4 ? scl[g] : make_float2(1.f, 1.f), xul + g * kTok);
     }
   }
 
@@ -438,7 +506,348 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
   }
 }
 
+// ---------------------------------------------------------------------------
+// TMA-ring kernel (up to 4 tokens: one token tile)
+// ---------------------------------------------------------------------------
+//
+// A CTA covers 64 output channels and a range of k groups; a ninth warp's
+// lane 0 streams the CTA's weights into a ring of shared-memory stages with
+// the TMA engine, starting before the kernel's grid-dependency wait: one
+// stage is 256 consecutive bytes of each of the 64 rows (four INT4 groups or
+// two e4m3 groups), copied as four boxes of 64 bytes x 64 rows, each stored
+// row after row (a warp's 16-byte reads of two adjacent rows fill all 32
+// banks once).  Eight consumer warps: warp w takes rows 16 (w % 4) .. + 15
+// of boxes 2 (w / 4) and 2 (w / 4) + 1 (INT4: groups 4k + 2 (w / 4) + {0, 1}
+// of stage k; e4m3: both halves of group 2k + w / 4), so every SM keeps 24
+// consumer warps busy; the two warps of a row block add their sums at the
+// end.  The ring is as deep as three CTAs per SM allow (3 to 8 stages of
+// 16 KB), so the bytes in flight do not depend on registers.  Rows past N
+// are zero-filled by the copy.  Consumers wait for a stage, read their
+// rows' words, compute, and release it; every wait is bounded.  Split-K
+// runs as a thread-block cluster along k: each CTA leaves its partial sums
+// in shared memory and the cluster's first CTA adds them in rank order
+// (distributed shared memory), so there is no memset, no atomic and the
+// result does not vary from run to run.  One token (M == 1) has its own
+// instantiation that keeps only the live accumulator elements.
+
+constexpr int kRingWarps = 8;                          // consumer warps
+constexpr int kRingRows = 64;                          // output channels per CTA
+constexpr int kRingThreads = 32 * (kRingWarps + 1);    // + the producer warp
+constexpr int kRingMaxStages = 8;
+constexpr int kBoxBytes = 64;                          // a box: 64 bytes x kRingRows rows
+constexpr int kStageBoxes = 4;                         // boxes per stage (2 per consumer warp)
+constexpr int kStageBytes = kStageBoxes * kBoxBytes * kRingRows;  // 16 KB
+constexpr int kRingMaxCluster = 8;
+
+struct RingArgs {
+  const void *scales;     // bf16 [N][K/128] or fp32 [N]
+  const uint16_t *x;      // bf16 [M][K]
+  float *y;               // fp32 [M][N]
+  uint32_t *err_word;
+  int32_t M, N, K;
+  int32_t gpc;            // 128-wide k groups per CTA
+  int32_t stages;         // ring depth, 2 .. kRingMaxStages
+};
+
+struct RingCtl {
+  uint64_t full[kRingMaxStages], empty[kRingMaxStages];
+  int fail;
+};
+
+// Shared memory of a ring CTA (offsets from a 1024-byte aligned base).
+struct RingLayout {
+  size_t x, sc, xu, part, ctl, total;
+};
+__host__ __device__ inline RingLayout ring_layout(bool int4, int stages, int gpc, int M) {
+  RingLayout L{};
+  size_t o = size_t(stages) * kStageBytes;
+  L.x = o;
+  o += size_t(gpc) * kWqGroup * M * 2;
+  L.sc = o;
+  o += wq_scale_bytes(int4, kRingRows / 2, gpc);
+  L.xu = o;
+  o += size_t(gpc) * 8 * 4;
+  L.part = o;
+  o += size_t(kRingRows / 16) * 32 * 16;
+  L.ctl = o;
+  o += (sizeof(RingCtl) + 15) / 16 * 16;
+  L.total = o + 1024;  // room to align the base
+  return L;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// may sleep until it completes (or about 1 ms has passed) instead of
+// returning at once, so waiting warps issue fewer polls.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait (the bounds of mbar_wait: about 2^31 SM cycles or 2^24
+// polls); on timeout the error bit is raised once and the CTA's fail flag
+// tells every role to stop.
+__device__ __forceinline__ bool ring_wait(RingCtl &ctl, uint64_t *bar, uint32_t parity,
+                                          uint32_t *err_word) {
+  volatile int *fail = &ctl.fail;
+  if (*fail) return false;
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (clock64() - t0 > kWaitCycles) break;
+  }
+  if (atomicExch(&ctl.fail, 1) == 0) report(err_word, KVQ_ERRBIT_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(const void *local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
+template <bool kInt4, bool kOne>
+__global__ void __launch_bounds__(kRingThreads, 3)
+    wq_ring_kernel(const __grid_constant__ CUtensorMap wmap, RingArgs a) {
+  extern __shared__ __align__(128) uint8_t ring_raw[];
+  uint8_t *sm = ring_raw + ((1024 - (smem_addr(ring_raw) & 1023)) & 1023);
+  const RingLayout L = ring_layout(kInt4, a.stages, a.gpc, a.M);
+  uint8_t *ring = sm;
+  uint4 *xs = reinterpret_cast<uint4 *>(sm + L.x);
+  float2 *sc_s = reinterpret_cast<float2 *>(sm + L.sc);
+  float *xu = reinterpret_cast<float *>(sm + L.xu);
+  float4 *part = reinterpret_cast<float4 *>(sm + L.part);
+  RingCtl &ctl = *reinterpret_cast<RingCtl *>(sm + L.ctl);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int S = a.stages, Mp = kOne ? 1 : a.M;  // kOne: M == 1
+  const int kb0 = blockIdx.y * a.gpc * kWqGroup;
+  const int ng = min(a.gpc, (a.K - kb0) / kWqGroup);
+  const int row_base = blockIdx.x * kRingRows;
+  constexpr int kGroupBytes = kInt4 ? kWqGroup / 2 : kWqGroup;
+  constexpr int kStageCols = kStageBoxes * kBoxBytes;  // bytes of each row per stage
+  const int nst = (ng * kGroupBytes + kStageCols - 1) / kStageCols;  // stages
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&ctl.full[s], 1);
+      mbar_init(&ctl.empty[s], kRingWarps);
+    }
+    ctl.fail = 0;
+    fence_barrier_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+  }
+  __syncthreads();
+  // The weights and their scales are constant (see kvq_wq_gemm): the
+  // producer streams them and the consumers load the scales without waiting
+  // for the work ahead of this kernel on the stream, so the first stages
+  // arrive while that work finishes; only x (and y) wait for it.
+
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const int c = lane & 3, rr = lane >> 2;
+  const int rb = warp & 3, h = warp >> 2;  // row block and box of a consumer warp
+  const int rl = rb * 16 + rr;             // this lane's rows in the tile: rl, rl + 8
+  if (warp == kRingWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const int x0 = kInt4 ? kb0 / 2 : kb0;  // byte column of the first stage
+      int k = 0, s = 0;
+      uint32_t ph = 0;  // parity of the pass over the ring
+      bool ok = true;
+      for (; k < nst; ++k) {
+        if (k >= S && !ring_wait(ctl, &ctl.empty[s], ph ^ 1u, a.err_word)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
+        uint8_t *dst = ring + s * kStageBytes;
+#pragma unroll
+        for (int b = 0; b < kStageBoxes; ++b)
+          tma_load_2d(dst + b * kBoxBytes * kRingRows, &wmap, x0 + k * kStageCols + b * kBoxBytes,
+                      row_base, &ctl.full[s], pol);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) {
+        // A wait gave up: let the copies this CTA started land (bounded
+        // waits) before it exits, so that none writes into shared memory the
+        // SM may already have handed to another CTA.  Only the last S stages
+        // can still be in flight.
+        for (int j = k > S ? k - S : 0; j < k; ++j)
+          mbar_wait(&ctl.full[j % S], static_cast<uint32_t>(j / S) & 1u);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- consumers
+    constexpr int nthr = 32 * kRingWarps;
+    ScaleStage sst(a.scales, sc_s, a.K, a.N, kb0, ng, a.gpc, row_base, kRingRows / 2, tid, nthr);
+    if constexpr (kInt4) sst.load(0);
+    grid_dependency_wait();
+    allow_dependents();
+    stage_x<kInt4, !kInt4>(xs, xu, 8, a.x, a.K, a.M, Mp, kb0, ng, tid, nthr);
+    if constexpr (kInt4) {
+      sst.store(0);
+      for (int b = 1; b < sst.batches(); ++b) {
+        sst.load(b);
+        sst.store(b);
+      }
+    }
+    // the consumer warps only (named barrier 1): the producer is streaming
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kRingWarps) : "memory");
+
+    const uint4 *xl = xs + min(rr, Mp - 1) * 4 + c;
+    const float2 *scl = sc_s + (rb * 8 + rr) * a.gpc;
+    const float *xul = xu + 2 * c;
+    float acc1[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    int s = 0;
+    uint32_t ph = 0;
+    // this warp's boxes of a stage: kHB = kStageBoxes / 2 of them, from box h kHB
+    constexpr int kHB = kStageBoxes / 2;
+    for (int k = 0; k < nst; ++k) {
+      if (!ring_wait(ctl, &ctl.full[s], ph, a.err_word)) break;
+      const uint8_t *st =
+          ring + s * kStageBytes + h * kHB * kBoxBytes * kRingRows + rl * kBoxBytes + c * 16;
+      uint4 u0[kHB], u8[kHB];
+#pragma unroll
+      for (int i = 0; i < kHB; ++i) {
+        u0[i] = *reinterpret_cast<const uint4 *>(st + i * kBoxBytes * kRingRows);
+        u8[i] = *reinterpret_cast<const uint4 *>(st + i * kBoxBytes * kRingRows + 8 * kBoxBytes);
+      }
+      float gacc[1][4];
+      if constexpr (kInt4) {
+        // box b of stage k = group kStageBoxes k + b
+#pragma unroll
+        for (int i = 0; i < kHB; ++i) {
+          const int g = kStageBoxes * k + h * kHB + i;
+          if (g < ng) {
+            const uint32_t a0[4] = {u0[i].x, u0[i].y, u0[i].z, u0[i].w};
+            const uint32_t a8[4] = {u8[i].x, u8[i].y, u8[i].z, u8[i].w};
+            group_mma<true, 1>(gacc, a0, a8, xl + g * 4 * Mp * 4, Mp);
+            group_fold<true, 1, kOne>(acc1, gacc, scl[g], xul + g * 8);
+          }
+        }
+      } else if constexpr (kHB == 1) {
+        // box h = bytes 64 h .. 64 h + 63 of group k: step pairs 2h, 2h + 1
+        const uint32_t a0[4] = {u0[0].x, u0[0].y, u0[0].z, u0[0].w};
+        const uint32_t a8[4] = {u8[0].x, u8[0].y, u8[0].z, u8[0].w};
+        group_mma<false, 1, 2>(gacc, a0, a8, xl + (k * 4 + 2 * h) * Mp * 4, Mp);
+        group_fold<false, 1, kOne>(acc1, gacc, make_float2(1.f, 1.f), xul + k * 8);
+      } else {
+        // boxes 2h, 2h + 1 = both halves of group 2k + h
+        const int g = 2 * k + h;
+        if (g < ng) {
+          const uint32_t a0[8] = {u0[0].x, u0[0].y, u0[0].z, u0[0].w,
+                                  u0[1].x, u0[1].y, u0[1].z, u0[1].w};
+          const uint32_t a8[8] = {u8[0].x, u8[0].y, u8[0].z, u8[0].w,
+                                  u8[1].x, u8[1].y, u8[1].z, u8[1].w};
+          group_mma<false, 1>(gacc, a0, a8, xl + g * 4 * Mp * 4, Mp);
+          group_fold<false, 1, kOne>(acc1, gacc, make_float2(1.f, 1.f), xul + g * 8);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.empty[s]);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = acc1[0][e];
+  }
+
+  // ---- the CTA's sums: the two warps of a row block add theirs (box 1's
+  // into box 0's); with split K the cluster's first CTA then adds the
+  // others' (rank order) and stores.  Every thread reaches both cluster
+  // barriers, whatever happened above.
+  const bool consumer = warp < kRingWarps, lead = warp < kRingWarps / 2;
+  if (consumer) {
+    if (!lead) part[rb * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * kRingWarps) : "memory");
+    if (lead) {
+      const float4 v = part[rb * 32 + lane];
+      acc[0] += v.x;
+      acc[1] += v.y;
+      acc[2] += v.z;
+      acc[3] += v.w;
+    }
+  }
+  bool store = lead;
+  if (gridDim.y > 1) {
+    if (lead) part[rb * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    cluster_sync_all();
+    const uint32_t rank = cluster_rank();
+    store = lead && rank == 0;
+    if (store) {
+      for (uint32_t r = 1; r < gridDim.y; ++r) {
+        const float4 v = ld_cluster_f4(part + rb * 32 + lane, r);
+        acc[0] += v.x;
+        acc[1] += v.y;
+        acc[2] += v.z;
+        acc[3] += v.w;
+      }
+    }
+    cluster_sync_all();  // the others' shared memory stays until it has been read
+  }
+  if (store) {
+    const int row0 = row_base + rl;
+    float f0 = 1.f, f8 = 1.f;
+    if constexpr (!kInt4) {
+      const float *fs = static_cast<const float *>(a.scales);
+      f0 = fs[min(row0, a.N - 1)];
+      f8 = fs[min(row0 + 8, a.N - 1)];
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int n = 2 * c + (e & 1);
+      const int row = row0 + (e >> 1) * 8;
+      if (n < a.M && row < a.N)
+        a.y[static_cast<int64_t>(n) * a.N + row] = acc[e] * ((e >> 1) ? f8 : f0);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host
+// ---------------------------------------------------------------------------
+
 using WqFn = void (*)(WqArgs);
+using RingFn = void (*)(CUtensorMap, RingArgs);
 
 template <bool kInt4>
 WqFn pick_wq(int nt) {
@@ -457,18 +866,87 @@ WqFn pick_wq(int nt) {
 
 constexpr size_t kWqSmemMax = 112 * 1024;
 
-// Opt each kernel into the shared-memory budget once per device (slot =
-// kernel variant), outside any stream capture after the first call.
-bool wq_smem_opt_in(WqFn fn, int slot) {
+// Opt a kernel into a shared-memory budget once per device (slot = kernel
+// variant), outside any stream capture after the first call.
+bool wq_smem_opt_in(const void *fn, int slot, size_t bytes) {
   constexpr int kMaxDev = 64;
-  static std::atomic<bool> done[kMaxDev][16];
+  static std::atomic<bool> done[kMaxDev][20];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
   if (done[dev][slot].load(std::memory_order_acquire)) return true;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kWqSmemMax)) != cudaSuccess)
+                           static_cast<int>(bytes)) != cudaSuccess)
     return false;
   done[dev][slot].store(true, std::memory_order_release);
+  return true;
+}
+
+// Shared memory one CTA may use so that three of them fit on an SM (cached
+// per device).
+size_t smem_per_cta3() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int sm_bytes = 0, reserved = 0;
+    if (cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+            cudaSuccess)
+      return 0;
+    v = sm_bytes / 3 - reserved;
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  return static_cast<size_t>(v);
+}
+
+// 2-D map over the weights [N rows][row_bytes bytes], boxes of 64 bytes x 64
+// rows, no swizzle; rows past N read as zeros.
+bool encode_weight_map(CUtensorMap *map, const void *w, int64_t row_bytes, int N) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(N)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[2] = {kBoxBytes, kRingRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(w), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The ring kernel's plan for one call: k split (cluster size), groups per
+// CTA, ring depth, shared memory.  False when the shape does not suit it.
+struct RingPlan {
+  int ksplit, gpc, stages;
+  size_t smem;
+};
+bool ring_plan(bool int4, int M, int N, int K, int sms, RingPlan *p) {
+  // measured: more tokens run faster on the register ring
+  if (M > (int4 ? 4 : 2)) return false;
+  constexpr int kPerSm = 3;
+  const size_t budget = smem_per_cta3();
+  const int groups = K / kWqGroup;
+  const int tiles = (N + kRingRows - 1) / kRingRows;
+  const int slots = kPerSm * sms;
+  // the staged x of a CTA stays small (<= 24 KB), and the grid fills the
+  // GPU's slots once where it can, splitting k into clusters of up to 8
+  constexpr size_t kXMax = 24 * 1024;
+  auto x_bytes = [&](int g) { return size_t(g) * kWqGroup * M * 2; };
+  auto gpc_of = [&](int k) { return (groups + k - 1) / k; };
+  int ksplit = 1;
+  while (ksplit <= kRingMaxCluster && x_bytes(gpc_of(ksplit)) > kXMax) ++ksplit;
+  if (ksplit > kRingMaxCluster) return false;
+  for (int k = ksplit + 1; k <= kRingMaxCluster && k <= groups; ++k)
+    if (static_cast<int64_t>(tiles) * k <= slots) ksplit = k;
+  const int gpc = gpc_of(ksplit);
+  ksplit = (groups + gpc - 1) / gpc;  // no CTA without groups
+  int stages = kRingMaxStages;
+  while (stages > 2 && ring_layout(int4, stages, gpc, M).total > budget) --stages;
+  const size_t smem = ring_layout(int4, stages, gpc, M).total;
+  if (smem > budget || stages < 3) return false;
+  *p = RingPlan{ksplit, gpc, stages, smem};
   return true;
 }
 
@@ -478,7 +956,7 @@ using namespace kvq;
 
 extern "C" kvq_status kvq_wq_gemm(int32_t w_dtype, const void *w, const void *scales,
                                   const void *x, float *y, int32_t M, int32_t N, int32_t K,
-                                  kvq_stream_t stream) {
+                                  uint32_t *err_word, kvq_stream_t stream) {
   if (w_dtype != KVQ_W_INT4 && w_dtype != KVQ_W_E4M3) return KVQ_ERR_INVALID_ARG;
   if (!w || !scales || !x || !y) return KVQ_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < kWqGroup) return KVQ_ERR_INVALID_ARG;
@@ -488,19 +966,47 @@ extern "C" kvq_status kvq_wq_gemm(int32_t w_dtype, const void *w, const void *sc
     return KVQ_ERR_INVALID_ARG;
   const bool int4 = w_dtype == KVQ_W_INT4;
   const int nt = (M + 7) / 8;
-  const WqFn fn = int4 ? pick_wq<true>(nt) : pick_wq<false>(nt);
   int sms = 0;
   if (device_sm_count(&sms) != KVQ_OK) return KVQ_ERR_CUDA;
-
-  // split K so that the grid covers the GPU several times over; each CTA's
-  // staged x must fit the shared-memory budget
-  const int row_tiles = (N + kWqRows - 1) / kWqRows;
-  const int groups = K / kWqGroup;
-  auto smem_of = [&](int gpc) { return wq_smem_bytes(int4, gpc, nt, M); };
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (!wq_smem_opt_in(fn, int4 ? nt - 1 : 8 + nt - 1)) return KVQ_ERR_CUDA;
-  // k splits: as many as fill the GPU's resident CTAs once (at the occupancy
-  // the staged x allows), fewer groups per CTA only when shared memory asks
+  const int groups = K / kWqGroup;
+  const int64_t row_bytes = int4 ? K / 2 : K;
+
+  // one token tile: the TMA-ring kernel
+  RingPlan rp;
+  CUtensorMap wmap;
+  if (ring_plan(int4, M, N, K, sms, &rp) && encode_weight_map(&wmap, w, row_bytes, N)) {
+    const RingFn fn = int4 ? (M == 1 ? wq_ring_kernel<true, true> : wq_ring_kernel<true, false>)
+                           : (M == 1 ? wq_ring_kernel<false, true> : wq_ring_kernel<false, false>);
+    if (!wq_smem_opt_in(reinterpret_cast<const void *>(fn), 16 + (int4 ? 1 : 0) + (M == 1 ? 2 : 0),
+                        smem_per_cta3()))
+      return KVQ_ERR_CUDA;
+    RingArgs ra{scales, static_cast<const uint16_t *>(x), y, err_word, M, N, K, rp.gpc, rp.stages};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + kRingRows - 1) / kRingRows, rp.ksplit);
+    cfg.blockDim = dim3(kRingThreads);
+    cfg.dynamicSmemBytes = rp.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = rp.ksplit;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = rp.ksplit > 1 ? 2 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, wmap, ra);
+    return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  }
+
+  // otherwise the register-ring kernel: split K so that the grid covers the
+  // GPU's resident CTAs once; each CTA's staged x must fit the budget
+  const WqFn fn = int4 ? pick_wq<true>(nt) : pick_wq<false>(nt);
+  const int row_tiles = (N + kWqRows - 1) / kWqRows;
+  auto smem_of = [&](int gpc) { return wq_smem_bytes(int4, gpc, nt, M); };
+  if (!wq_smem_opt_in(reinterpret_cast<const void *>(fn), int4 ? nt - 1 : 8 + nt - 1, kWqSmemMax))
+    return KVQ_ERR_CUDA;
   int gpc = groups;
   while (gpc > 1 && smem_of(gpc) > kWqSmemMax) --gpc;
   int ksplit = (groups + gpc - 1) / gpc;

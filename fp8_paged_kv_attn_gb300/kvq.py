@@ -89,7 +89,7 @@ def load(build_if_missing: bool = True):
     L.kvq_pages_update.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, vp, vp, i32, vp, vp, vp,
                                    i32, vp, vp, vp]
     L.kvq_pages_update.restype = ctypes.c_int
-    L.kvq_wq_gemm.argtypes = [i32, vp, vp, vp, vp, i32, i32, i32, vp]
+    L.kvq_wq_gemm.argtypes = [i32, vp, vp, vp, vp, i32, i32, i32, vp, vp]
     L.kvq_wq_gemm.restype = ctypes.c_int
     L.kvq_decode_attn_workspace_size.argtypes = [i32, i32, i32, i32]
     L.kvq_decode_attn_workspace_size.restype = sz
@@ -273,10 +273,11 @@ def kvq_pages_update(state: PageState, rel_req=None, rel_npages=None, acq_req=No
     _check("kvq_pages_update", st)
 
 
-def kvq_wq_gemm(w_dtype: int, w, scales, x, y, stream=None) -> None:
+def kvq_wq_gemm(w_dtype: int, w, scales, x, y, err_word=None, stream=None) -> None:
     """y [M, N] fp32 = x [M, K] bf16 times the quantised weights (include/kvq.h):
     W_INT4: w uint8 [N, K/2], scales bf16 (or int16 bits) [N, K/128];
-    W_E4M3: w uint8 [N, K], scales fp32 [N]."""
+    W_E4M3: w uint8 [N, K], scales fp32 [N].  err_word: optional int32 [1]
+    device tensor that collects KVQ_ERRBIT_TIMEOUT."""
     L = load()
     M, K = x.shape
     N = int(w.shape[0])
@@ -291,7 +292,8 @@ def kvq_wq_gemm(w_dtype: int, w, scales, x, y, stream=None) -> None:
             raise ValueError("e4m3 weights must be [N, K] with scales [N]")
         sc = _dev(scales, "scales", (torch.float32,), 1)
     st = L.kvq_wq_gemm(int(w_dtype), _dev(w, "w", U8, 2), sc, _dev(x, "x", BF16, 2),
-                       _dev(y, "y", (torch.float32,), 2), M, N, K, _stream(stream))
+                       _dev(y, "y", (torch.float32,), 2), M, N, K,
+                       _dev(err_word, "err_word", U32), _stream(stream))
     _check("kvq_wq_gemm", st)
 
 

@@ -201,16 +201,29 @@ KVQ_API kvq_status kvq_pages_update(int32_t *free_stack, int32_t *free_count, ui
  *     W[n][k] = int4(n, k) * scales[n][k/128];
  *   KVQ_W_E4M3: w uint8 e4m3 codes [N][K]; scales fp32 [N]:
  *     W[n][k] = e4m3(w[n][k]) * scales[n].
- * Products are exact and sums fp32 (split over k: the order of the partial
- * sums varies from run to run).  Any bf16 x is accepted: each token's values
- * are scaled by a power of two for the products (exact for every value down
- * to 2^-32 of the token's largest finite |x| in a k range, smaller ones are
- * rounded to 2^-25 of it); NaN and inf propagate.  Split-K partial sums are
- * added with fp32 atomics, which flush subnormals: a result below 2^-126 in
- * magnitude can be off by up to (2 K/128 + 1) * 2^-126.  Supported: 1 <= M <= 64,
- * K a multiple of 128.  w and x 16-byte aligned, scales 4-byte aligned. */
+ * Products are exact and sums fp32.  Any bf16 x is accepted: each token's
+ * values are scaled by a power of two for the products (exact for every
+ * value down to 2^-32 of the token's largest finite |x| in a k range,
+ * smaller ones are rounded to 2^-25 of it); NaN and inf propagate.
+ * Up to 8 tokens (when a CTA's share of x fits its shared memory) the
+ * weights stream through a shared-memory ring fed by the TMA engine and a k
+ * split runs as a thread-block cluster whose partial sums are added in a
+ * fixed order: every run gives the same bits.  Otherwise split-K partial
+ * sums are added with fp32 atomics: their order varies from run to run, and
+ * atomics flush subnormals, so a result below 2^-126 in magnitude can be off
+ * by up to (2 K/128 + 1) * 2^-126.
+ * w and scales are taken as constant model weights: the call starts reading
+ * them before the work ahead of it on the stream has finished (programmatic
+ * dependent launch), so they must not be written by the kernel launched just
+ * before it on the same stream if that kernel lets its dependents start
+ * early, as every kvq kernel does; x is read only once that work is done.
+ * err_word (device uint32, nullable): KVQ_ERRBIT_TIMEOUT when a bounded wait
+ * inside the kernel gave up (y is then undefined).
+ * Supported: 1 <= M <= 64, K a multiple of 128.  w and x 16-byte aligned,
+ * scales 4-byte aligned. */
 KVQ_API kvq_status kvq_wq_gemm(int32_t w_dtype, const void *w, const void *scales, const void *x,
-                               float *y, int32_t M, int32_t N, int32_t K, kvq_stream_t stream);
+                               float *y, int32_t M, int32_t N, int32_t K, uint32_t *err_word,
+                               kvq_stream_t stream);
 
 /* Bytes of device workspace kvq_decode_attn needs for these sizes (split
  * partials and the per-call work plan).  Depends on B, Hq, num_kv_heads and

@@ -93,11 +93,13 @@ def test_wq_gemm_shapes(kvq, wdtype, M, N, K):
 
 
 @pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])
-def test_wq_gemm_every_code(kvq, wdtype):
+@pytest.mark.parametrize("M", [1, 2, 9], ids=["ring1", "ring", "registers"])
+def test_wq_gemm_every_code(kvq, wdtype, M):
     """Every INT4 byte value / every finite e4m3 code (subnormals, +-448, -0)
-    in every lane position of a 128-wide group, against dense random x."""
+    in every lane position of a 128-wide group, against dense random x (1
+    and 2 tokens: the TMA-ring kernel; 9: the register-ring kernel)."""
     rng = np.random.default_rng(40 + wdtype)
-    M, N, K = 9, 64, 512
+    N, K = 64, 512
     x = inputs.normal_bf16(rng, (M, K))
     if wdtype == 0:
         base = np.arange(256, dtype=np.uint8)
@@ -124,6 +126,44 @@ def test_wq_gemm_full_size_sampled(kvq, wdtype, M, N, K):
     check(wdtype, w, s, x, rows=rows, what=f"{M}x{N}x{K}")
 
 
+# Up to 4 tokens (INT4) or 2 (e4m3) run the TMA-ring kernel (one token its
+# own specialisation): k split over clusters of 1 to 8 CTAs (4, 5, 6 and 7
+# included), rows past N zero-filled by the copy, odd group counts per CTA,
+# one group in all.
+RING_SHAPES = [(1, 200, 1536), (2, 1000, 640), (1, 130, 3584), (2, 5000, 1536), (1, 64, 128),
+               (2, 65, 256), (4, 300, 1024), (3, 777, 2560)]
+
+
+@pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])
+@pytest.mark.parametrize("M,N,K", RING_SHAPES)
+def test_wq_ring_shapes(kvq, wdtype, M, N, K):
+    rng = np.random.default_rng(7 * M + N + K + wdtype)
+    w, s, x = pins.random_wq_case(rng, wdtype, M, N, K)
+    rows = None if N <= 1000 else np.sort(rng.choice(N, 128, replace=False))
+    check(wdtype, w, s, x, rows=rows, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])
+def test_wq_ring_deterministic(kvq, wdtype):
+    """The split-K sums of the ring kernel are added in cluster-rank order, not
+    by atomics: two calls give the same bits, and no wait gives up."""
+    rng = np.random.default_rng(90 + wdtype)
+    M, N, K = 2, 1792, 5120
+    w, s, x = pins.random_wq_case(rng, wdtype, M, N, K)
+    sd = dev(s.view(np.int16)) if wdtype == oracle.W_INT4 else dev(s)
+    xd = dev(x.view(np.int16)).view(torch.bfloat16)
+    wd = dev(w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ys = []
+    for _ in range(2):
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        kvq.kvq_wq_gemm(wdtype, wd, sd, xd, y, err_word=err)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(ys[0].view(torch.int32), ys[1].view(torch.int32))
+
+
 def test_wq_gemm_arguments(kvq):
     L = kvq.load()
     y = torch.zeros(4, dtype=torch.float32, device="cuda")
@@ -131,13 +171,13 @@ def test_wq_gemm_arguments(kvq):
     s = torch.zeros(8, dtype=torch.float32, device="cuda")
     x = torch.zeros(128 * 65, dtype=torch.bfloat16, device="cuda")
     p = lambda t: t.data_ptr()  # noqa: E731
-    assert L.kvq_wq_gemm(0, p(w), p(s), p(x), p(y), 65, 1, 128, None) == 4   # M > 64
-    assert L.kvq_wq_gemm(0, p(w), p(s), p(x), p(y), 1, 1, 200, None) == 4   # K % 128
-    assert L.kvq_wq_gemm(0, p(w), p(s), p(x), p(y), 1, 1, 100, None) == 1   # K < 128
-    assert L.kvq_wq_gemm(0, p(w), p(s), p(x), p(y), 0, 1, 128, None) == 1   # M < 1
-    assert L.kvq_wq_gemm(2, p(w), p(s), p(x), p(y), 1, 1, 128, None) == 1   # dtype
-    assert L.kvq_wq_gemm(0, p(w) + 8, p(s), p(x), p(y), 1, 1, 128, None) == 1  # alignment
-    assert L.kvq_wq_gemm(0, None, p(s), p(x), p(y), 1, 1, 128, None) == 1
+    assert L.kvq_wq_gemm(0, p(w), p(s), p(x), p(y), 65, 1, 128, None, None) == 4   # M > 64
+    assert L.kvq_wq_gemm(0, p(w), p(s), p(x), p(y), 1, 1, 200, None, None) == 4   # K % 128
+    assert L.kvq_wq_gemm(0, p(w), p(s), p(x), p(y), 1, 1, 100, None, None) == 1   # K < 128
+    assert L.kvq_wq_gemm(0, p(w), p(s), p(x), p(y), 0, 1, 128, None, None) == 1   # M < 1
+    assert L.kvq_wq_gemm(2, p(w), p(s), p(x), p(y), 1, 1, 128, None, None) == 1   # dtype
+    assert L.kvq_wq_gemm(0, p(w) + 8, p(s), p(x), p(y), 1, 1, 128, None, None) == 1  # alignment
+    assert L.kvq_wq_gemm(0, None, p(s), p(x), p(y), 1, 1, 128, None, None) == 1
 
 
 @pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])

@@ -576,6 +576,7 @@ def run_gpu(args, dist, rank, world, local):
                                        args.config_warmup + args.config_steps,
                                        eager=args.eager))
         extras.append(HandoffStep(torch, kvq, args.seed))
+        extras.append(WqStep(torch, kvq, args.seed))
         torch.cuda.synchronize()
 
     for i in range(args.warmup):
@@ -1336,6 +1337,78 @@ WQ_LAYER = [("qkv", 1792, 5120), ("o", 5120, 1536), ("gate_up", 3072, 5120), ("d
 WQ_LAYERS = 40
 
 
+def wq_weights(torch, kvq, gen, wdtype, N, K):
+    """Seeded random quantised weights [N, K] and their scales; returns (w, scales, bytes)."""
+    if wdtype == kvq.W_INT4:
+        w = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=gen)
+        s = torch.full((N, K // 128), 0x3C00, dtype=torch.int16, device="cuda")
+        return w, s, N * K // 2 + N * (K // 128) * 2
+    w = torch.randint(0, 0x77, (N, K), dtype=torch.uint8, device="cuda", generator=gen)
+    s = torch.full((N,), 0.01, dtype=torch.float32, device="cuda")
+    return w, s, N * K + N * 4
+
+
+def graph_time(torch, calls, reps=20):
+    """Capture the calls once into a CUDA graph, replay `reps` times; median ms
+    per replay (CUDA events on the current stream)."""
+    stream = torch.cuda.current_stream()
+    for f in calls:
+        f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for f in calls:
+            f()
+    g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for e in ev:
+        e[0].record(stream)
+        g.replay()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+class WqStep:
+    """The large weight-only projection (28672 x 5120) at one token, INT4 and
+    e4m3, cycled over 8 weight copies larger than L2 (one step = the 8
+    products in one CUDA graph)."""
+    name = "wq_large_m1"
+
+    def __init__(self, torch, kvq, seed, N=28672, K=5120, copies=8):
+        self.torch, self.kvq = torch, kvq
+        gen = torch.Generator(device="cuda").manual_seed(seed)
+        self.N, self.K = N, K
+        self.mats = {wd: [wq_weights(torch, kvq, gen, wd, N, K) for _ in range(copies)]
+                     for wd in (kvq.W_INT4, kvq.W_E4M3)}
+        self.x = torch.randn((1, K), device="cuda", generator=gen).to(torch.bfloat16)
+        self.ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _ in range(copies)]
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def time(self, warmup, steps):
+        torch, kvq = self.torch, self.kvq
+        peak, _ = measured_hbm_peak()
+        out = {"workload": f"weight-only projection {self.N} x {self.K}, one token, "
+                           f"{len(self.ys)} weight copies per step (larger than L2; no flush)",
+               "steps": steps}
+        for wd, name in ((kvq.W_E4M3, "e4m3"), (kvq.W_INT4, "int4")):
+            calls = [(lambda w=w, s=s, y=y: kvq.kvq_wq_gemm(wd, w, s, self.x, y, err_word=self.err))
+                     for (w, s, _), y in zip(self.mats[wd], self.ys)]
+            ms = graph_time(torch, calls, max(steps, 3))
+            nbytes = sum(m[2] for m in self.mats[wd])
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out[name] = {"us_per_product": round(ms * 1e3 / len(calls), 2),
+                         "GBs": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                         "bytes_per_product": nbytes // len(calls)}
+        if int(self.err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(self.err.item()):#x}")
+        out["int4_speedup_vs_e4m3"] = round(out["e4m3"]["us_per_product"]
+                                            / out["int4"]["us_per_product"], 3)
+        return out
+
+
 def run_wq(args):
     """Weight-only INT4 vs e4m3 decode matrix products (kvq_wq_gemm), the
     pages' second decode workload: every generated token streams all the
@@ -1351,36 +1424,6 @@ def run_wq(args):
     kvq.load()
     peak, _ = measured_hbm_peak()
     gen = torch.Generator(device="cuda").manual_seed(args.seed)
-    stream = torch.cuda.current_stream()
-
-    def weights(wdtype, N, K):
-        if wdtype == kvq.W_INT4:
-            w = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=gen)
-            s = torch.full((N, K // 128), 0x3C00, dtype=torch.int16, device="cuda")
-            return w, s, N * K // 2 + N * (K // 128) * 2
-        w = torch.randint(0, 0x77, (N, K), dtype=torch.uint8, device="cuda", generator=gen)
-        s = torch.full((N,), 0.01, dtype=torch.float32, device="cuda")
-        return w, s, N * K + N * 4
-
-    def timed(calls, reps=20):
-        """Capture the calls once, replay `reps` times; median ms per replay."""
-        for f in calls:
-            f()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for f in calls:
-                f()
-        g.replay()
-        torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(reps)]
-        for e in ev:
-            e[0].record(stream)
-            g.replay()
-            e[1].record(stream)
-        torch.cuda.synchronize()
-        return statistics.median(a.elapsed_time(b) for a, b in ev)
 
     kinds = ("stack", "large") if args.wq_kind == "all" else (args.wq_kind,)
     formats = [(kvq.W_E4M3, "e4m3"), (kvq.W_INT4, "int4")]
@@ -1391,10 +1434,11 @@ def run_wq(args):
         res = {}
         for wdtype, name in formats:
             if kind == "stack":
-                mats = [weights(wdtype, N, K) + (N, K) for _ in range(WQ_LAYERS)
-                        for _, N, K in WQ_LAYER]
+                mats = [wq_weights(torch, kvq, gen, wdtype, N, K) + (N, K)
+                        for _ in range(WQ_LAYERS) for _, N, K in WQ_LAYER]
             else:
-                mats = [weights(wdtype, 28672, 5120) + (28672, 5120) for _ in range(8)]
+                mats = [wq_weights(torch, kvq, gen, wdtype, 28672, 5120) + (28672, 5120)
+                        for _ in range(8)]
             nbytes = sum(m[2] for m in mats)
             for M in ms_list:
                 xs = {K: torch.randn((M, K), device="cuda", generator=gen).to(torch.bfloat16)
@@ -1402,7 +1446,7 @@ def run_wq(args):
                 ys = [torch.empty((M, m[3]), dtype=torch.float32, device="cuda") for m in mats]
                 calls = [(lambda m=m, y=y: kvq.kvq_wq_gemm(wdtype, m[0], m[1], xs[m[4]], y))
                          for m, y in zip(mats, ys)]
-                ms = timed(calls)
+                ms = graph_time(torch, calls)
                 gbs = nbytes / (ms * 1e-3) / 1e9
                 res[(name, M)] = ms
                 line = {"workload": f"wq_{kind}", "w": name, "M": M, "products": len(mats),

@@ -17,7 +17,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libkvq.so")
 
 SOURCES = ["api.cu", "append.cu", "handoff.cu", "check_tags.cu", "pages.cu", "decode_attn.cu",
-           "decode_attn_static.cu", "wq_gemm.cu"]
+           "decode_attn_static.cu", "wq_gemm.cu", "selftest.cu"]
 HEADERS = ["kvq_device.cuh", "kvq_internal.h", "quant_e4m3.cuh", "decode_common.cuh",
            "decode_attn_mma.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

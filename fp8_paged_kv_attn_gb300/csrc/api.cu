@@ -40,3 +40,13 @@ extern "C" const char *kvq_status_string(kvq_status s) {
   }
   return "KVQ_ERR_UNKNOWN";
 }
+
+extern "C" kvq_status kvq_selftest_wait(int32_t which, const void *src, uint32_t *err_word,
+                                        uint32_t *landed, kvq_stream_t stream) {
+  if (!src || !err_word || !landed || !kvq::aligned16(src)) return KVQ_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint32_t *w = static_cast<const uint32_t *>(src);
+  if (which == 0) return kvq::selftest_attn_wait(w, err_word, landed, s);
+  if (which == 1) return kvq::selftest_ring_wait(w, err_word, landed, s);
+  return KVQ_ERR_INVALID_ARG;
+}

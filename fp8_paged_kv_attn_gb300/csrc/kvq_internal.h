@@ -23,6 +23,13 @@ kvq_status device_sm_count(int *sms);
 // against libcuda); null when the driver does not provide it.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// Self-tests of the bounded waits (kvq_selftest_wait): the split kernels'
+// (decode_attn.cu) and the weight ring's (wq_gemm.cu).
+kvq_status selftest_attn_wait(const uint32_t *src, uint32_t *err_word, uint32_t *landed,
+                              cudaStream_t stream);
+kvq_status selftest_ring_wait(const uint32_t *src, uint32_t *err_word, uint32_t *landed,
+                              cudaStream_t stream);
+
 // Launches `kernel` as a programmatic dependent of the work ahead of it on
 // `stream`: its CTAs may be scheduled as soon as the previous kernel has let
 // dependents go (or has finished), which hides the launch latency between

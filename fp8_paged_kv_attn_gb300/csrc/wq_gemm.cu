@@ -842,6 +842,41 @@ __global__ void __launch_bounds__(kRingThreads, 3)
   }
 }
 
+// Self-test of the ring kernel's failure path (kvq_selftest_wait, which = 1):
+// as attn_wait_selftest_kernel, with the ring's wait (ring_wait, which sleeps
+// between polls) on a barrier that nothing arrives at, then the drain of the
+// bulk copy the CTA started.
+__global__ void ring_wait_selftest_kernel(const uint32_t *src, uint32_t *err_word,
+                                          uint32_t *landed) {
+  __shared__ __align__(128) uint32_t buf[16];
+  __shared__ RingCtl ctl;
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl.full[0], 1);
+    mbar_init(&ctl.full[1], 1);
+    ctl.fail = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  grid_dependency_wait();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&ctl.full[0], sizeof(buf));
+    bulk_g2s(buf, src, sizeof(buf), &ctl.full[0]);
+  }
+  const bool ok = ring_wait(ctl, &ctl.full[1], 0, err_word);  // nothing arrives on full[1]
+  if (threadIdx.x == 0) {
+    const bool drained = mbar_wait(&ctl.full[0], 0);
+    *landed = (!ok && drained) ? buf[0] : 0u;
+  }
+}
+
+kvq_status selftest_ring_wait(const uint32_t *src, uint32_t *err_word, uint32_t *landed,
+                              cudaStream_t stream) {
+  const cudaError_t e =
+      launch_dependent(ring_wait_selftest_kernel, dim3(1), dim3(64), 0, stream, src, err_word,
+                       landed);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------------------
 // host
 // ---------------------------------------------------------------------------

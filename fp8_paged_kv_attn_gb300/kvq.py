@@ -43,7 +43,8 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_WORKSPACE", 3: "KVQ
 
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_append", "kvq_handoff_pages", "kvq_check_tags", "kvq_pages_update", "kvq_decode_attn_workspace_size",
-           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_wq_gemm", "kvq_status_string")
+           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_wq_gemm", "kvq_selftest_wait",
+           "kvq_status_string")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -91,6 +92,8 @@ def load(build_if_missing: bool = True):
     L.kvq_pages_update.restype = ctypes.c_int
     L.kvq_wq_gemm.argtypes = [i32, vp, vp, vp, vp, i32, i32, i32, vp, vp]
     L.kvq_wq_gemm.restype = ctypes.c_int
+    L.kvq_selftest_wait.argtypes = [i32, vp, vp, vp, vp]
+    L.kvq_selftest_wait.restype = ctypes.c_int
     L.kvq_decode_attn_workspace_size.argtypes = [i32, i32, i32, i32]
     L.kvq_decode_attn_workspace_size.restype = sz
     L.kvq_decode_attn.argtypes = [cp, vp, i32, i32, vp, i32, vp, vp, f32, vp, vp, sz, vp, vp]
@@ -295,6 +298,16 @@ def kvq_wq_gemm(w_dtype: int, w, scales, x, y, err_word=None, stream=None) -> No
                        _dev(y, "y", (torch.float32,), 2), M, N, K,
                        _dev(err_word, "err_word", U32), _stream(stream))
     _check("kvq_wq_gemm", st)
+
+
+def kvq_selftest_wait(which: int, src, err_word, landed, stream=None) -> None:
+    """Launch the bounded-wait self-test (include/kvq.h): which = 0 the split
+    attention kernels' wait, 1 the weight ring's.  src: 16 int32 on the
+    device; err_word, landed: int32 [1] device tensors."""
+    L = load()
+    st = L.kvq_selftest_wait(int(which), _dev(src, "src", U32), _dev(err_word, "err_word", U32),
+                             _dev(landed, "landed", U32), _stream(stream))
+    _check("kvq_selftest_wait", st)
 
 
 def kvq_decode_attn_workspace_size(B: int, Hq: int, num_kv_heads: int, head_dim: int) -> int:

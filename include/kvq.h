@@ -278,6 +278,19 @@ KVQ_API kvq_status kvq_decode_attn_static(const kvq_cache *cache, const void *q,
                                           float sm_scale, float *out, uint32_t *err_word,
                                           kvq_stream_t stream);
 
+/* Self-test of a kernel failure path (no fault, no hang): one CTA starts a
+ * real bulk copy of 64 bytes from src (device, 16-byte aligned) into shared
+ * memory, then waits on an mbarrier that nothing ever arrives at, with the
+ * bounded wait of the split attention kernels (which = 0) or of the weight
+ * ring of kvq_wq_gemm (which = 1).  The wait gives up after its bound (about
+ * 2^31 SM cycles, ~1 s), ORs KVQ_ERRBIT_TIMEOUT into *err_word, then lets the
+ * copy it started land before the CTA exits (the drain every such kernel runs
+ * on this path) and stores the copy's first word in *landed (0 if the wait
+ * or the drain did not behave).  The context stays usable afterwards.
+ * err_word and landed: device uint32. */
+KVQ_API kvq_status kvq_selftest_wait(int32_t which, const void *src, uint32_t *err_word,
+                                     uint32_t *landed, kvq_stream_t stream);
+
 /* Human-readable name of a status. */
 KVQ_API const char *kvq_status_string(kvq_status status);
 

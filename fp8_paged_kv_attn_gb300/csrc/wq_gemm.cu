@@ -295,7 +295,12 @@ __device__ __forceinline__ void stage_x(uint4 *xs, float *xu, int kTok, const ui
   }
 }
 
-// INT4 group scales of a CTA's row pairs as fp32 pairs, sc_s[p * gpc + g]
+// The row stride (in fp32 pairs) of the staged INT4 scales: gpc rounded up
+// to an odd number, so that the eight row pairs a warp reads at once fall in
+// eight different bank pairs.
+__host__ __device__ constexpr int wq_scale_stride(int gpc) { return gpc | 1; }
+
+// INT4 group scales of a CTA's row pairs as fp32 pairs, sc_s[p * stride + g]
 // for pair p (rows row_base + 16 (p / 8) + p % 8 and 8 below, a row past N
 // reads row N - 1) and group g < ng.  Items e = p * ng + g go to threads in
 // order (a warp reads runs of consecutive scales), kScB per thread and
@@ -308,17 +313,17 @@ struct ScaleStage {
   const uint16_t *sp;  // bf16 scales [N][K / 128], from the CTA's first group
   float2 *sc_s;
   int64_t gs;          // groups per row of the matrix
-  int ng, gpc, N, row_base, n, tid, nthr;
+  int ng, gpc, N, row_base, n, tid, nthr;  // gpc: the row stride of sc_s
   float inv_ng;
   uint16_t v[kScB][2];
   __device__ __forceinline__ ScaleStage(const void *scales, float2 *sc_s_, int K, int N_,
-                                        int kb0, int ng_, int gpc_, int row_base_, int pairs,
+                                        int kb0, int ng_, int stride, int row_base_, int pairs,
                                         int tid_, int nthr_) {
     gs = K / kWqGroup;
     sp = static_cast<const uint16_t *>(scales) + kb0 / kWqGroup;
     sc_s = sc_s_;
     ng = ng_;
-    gpc = gpc_;
+    gpc = stride;
     N = N_;
     row_base = row_base_;
     n = pairs * ng_;
@@ -389,7 +394,7 @@ struct WqCfg {
 // per pair and group][staged x][2^-e per (group, token slot of the tiles), fp32]
 __host__ __device__ constexpr int wq_staged_tokens(int nt, int M) { return nt == 1 ? M : 8 * nt; }
 __host__ __device__ constexpr size_t wq_scale_bytes(bool int4, int pairs, int gpc) {
-  return int4 ? size_t(pairs) * gpc * 8 : 0;
+  return int4 ? size_t(pairs) * wq_scale_stride(gpc) * 8 : 0;
 }
 __host__ __device__ constexpr size_t wq_x_bytes(int gpc, int nt, int M) {
   return size_t(gpc) * kWqGroup * wq_staged_tokens(nt, M) * sizeof(uint16_t);
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
   constexpr int kTok = 8 * NT;  // token slots of the MMA tiles
   extern __shared__ __align__(16) uint8_t wq_smem[];
   const size_t scb = wq_scale_bytes(kInt4, kWqRows / 2, a.gpc);
-  float2 *sc_s = reinterpret_cast<float2 *>(wq_smem);  // [kWqRows / 2][gpc]
+  float2 *sc_s = reinterpret_cast<float2 *>(wq_smem);  // [kWqRows / 2][stride]
   uint4 *xs = reinterpret_cast<uint4 *>(wq_smem + scb);
   // tokens staged: 8 per tile, or just the M real ones when there is one tile
   const int Mp = wq_staged_tokens(NT, a.M);
@@ -443,7 +448,8 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
   // INT4 scales: with one token tile the first batch's loads are in flight
   // while x is staged (with more, registers are short and x takes longer)
   constexpr int nthr = 32 * kWqWarps;
-  ScaleStage sst(a.scales, sc_s, a.K, a.N, kb0, ng, a.gpc, row_base, kWqRows / 2, tid, nthr);
+  ScaleStage sst(a.scales, sc_s, a.K, a.N, kb0, ng, wq_scale_stride(a.gpc), row_base, kWqRows / 2,
+                 tid, nthr);
   constexpr bool kEarly = kInt4 && NT == 1;
   if constexpr (kEarly) sst.load(0);
   // The weights and their scales are constant (see kvq_wq_gemm): only x
@@ -465,7 +471,7 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
   for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
   // this lane's B words (token slot t * 8 + rr) and group scales
   const uint4 *xl = xs + (NT == 1 ? min(rr, Mp - 1) : rr) * 4 + c;
-  const float2 *scl = sc_s + (warp * 8 + rr) * a.gpc;
+  const float2 *scl = sc_s + (warp * 8 + rr) * wq_scale_stride(a.gpc);
   const float *xul = xu + 2 * c;
 
   for (int g0 = 0; g0 < ng; g0 += C::kDepth) {
@@ -716,7 +722,8 @@ __global__ void __launch_bounds__(kRingThreads, 3)
   } else {
     // ----------------------------------------------------------- consumers
     constexpr int nthr = 32 * kRingWarps;
-    ScaleStage sst(a.scales, sc_s, a.K, a.N, kb0, ng, a.gpc, row_base, kRingRows / 2, tid, nthr);
+    ScaleStage sst(a.scales, sc_s, a.K, a.N, kb0, ng, wq_scale_stride(a.gpc), row_base,
+                   kRingRows / 2, tid, nthr);
     if constexpr (kInt4) sst.load(0);
     grid_dependency_wait();
     allow_dependents();
@@ -732,7 +739,7 @@ __global__ void __launch_bounds__(kRingThreads, 3)
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kRingWarps) : "memory");
 
     const uint4 *xl = xs + min(rr, Mp - 1) * 4 + c;
-    const float2 *scl = sc_s + (rb * 8 + rr) * a.gpc;
+    const float2 *scl = sc_s + (rb * 8 + rr) * wq_scale_stride(a.gpc);
     const float *xul = xu + 2 * c;
     float acc1[1][4] = {{0.f, 0.f, 0.f, 0.f}};
     int s = 0;

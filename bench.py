@@ -743,7 +743,7 @@ def run_gpu(args, dist, rank, world, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "kvq_decode_attn (plan + split + combine), CUDA events around each call"
+            "kernel": "kvq_decode_attn (split + combine; + plan above 4,608 requests), CUDA events around each call"
                       + (" (its own graph, replayed per step)" if graph else ""),
             "achieved": round(achieved, 1),
             "peak": peak,

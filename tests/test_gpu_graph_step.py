@@ -2,11 +2,12 @@
 kvq_decode_attn captured once into a CUDA graph and replayed over staged
 inputs -- against the oracle.
 
-Captured, the five kernels' programmatic dependent launches become
-programmatic edges of the graph.  The tensor-core split kernel reads the
-sequence lengths and the abort mask before its own grid-dependency wait,
-which is correct only if the graph orders it after the tag check exactly as
-the stream does; eager calls (every other test) do not show that.  Here the
+Captured, the step's programmatic dependent launches (append, check, split,
+combine; plus the plan kernel for very large batches) become programmatic
+edges of the graph.  The split kernel reads the sequence lengths and the
+abort mask right after its grid-dependency wait, which is correct only if the
+graph orders it after the tag check exactly as the stream does; eager calls
+(every other test) do not show that.  Here the
 benchmark's own DecodeStep captures the step once, then replays it for four
 consecutive decode steps, each staged with one device copy into the graph's
 static buffers.  Before one replay a page of one request is re-tagged on the

@@ -557,14 +557,18 @@ struct RingArgs {
 
 struct RingCtl {
   uint64_t full[kRingMaxStages], empty[kRingMaxStages];
+  uint64_t red;  // split K: the other CTAs' sums have arrived (cluster rank 0)
   int fail;
 };
 
 // Shared memory of a ring CTA (offsets from a 1024-byte aligned base).
 struct RingLayout {
-  size_t x, sc, xu, part, ctl, total;
+  size_t x, sc, xu, part, recv, ctl, total;
 };
-__host__ __device__ inline RingLayout ring_layout(bool int4, int stages, int gpc, int M) {
+// recv: with split K, the cluster's first CTA receives the sums of the other
+// ksplit - 1 CTAs there (a float4 per row block and lane each).
+__host__ __device__ inline RingLayout ring_layout(bool int4, int stages, int gpc, int M,
+                                                  int ksplit) {
   RingLayout L{};
   size_t o = size_t(stages) * kStageBytes;
   L.x = o;
@@ -575,6 +579,8 @@ __host__ __device__ inline RingLayout ring_layout(bool int4, int stages, int gpc
   o += size_t(gpc) * 8 * 4;
   L.part = o;
   o += size_t(kRingRows / 16) * 32 * 16;
+  L.recv = o;
+  o += size_t(ksplit > 1 ? ksplit - 1 : 0) * (kRingRows / 16) * 32 * 16;
   L.ctl = o;
   o += (sizeof(RingCtl) + 15) / 16 * 16;
   L.total = o + 1024;  // room to align the base
@@ -633,15 +639,50 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
-__device__ __forceinline__ float4 ld_cluster_f4(const void *local, uint32_t rank) {
+// The address of `local` (this CTA's shared memory) in CTA `rank` of the
+// cluster (every CTA of the kernel lays its shared memory out the same way).
+__device__ __forceinline__ uint32_t cluster_addr(const void *local, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(remote)
+  return remote;
+}
+
+__device__ __forceinline__ void st_cluster_f4(uint32_t remote, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
                : "memory");
-  return v;
+}
+
+// Arrival on an mbarrier of another CTA of the cluster, ordered after this
+// thread's earlier writes (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+
+// Bounded wait (the bounds of mbar_wait) on a barrier that other CTAs of the
+// cluster arrive at (acquire at cluster scope).
+__device__ __forceinline__ bool ring_wait_cluster(RingCtl &ctl, uint64_t *bar, uint32_t parity,
+                                                  uint32_t *err_word) {
+  auto try_wait = [&]() {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+  };
+  if (try_wait()) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (try_wait()) return true;
+    if (clock64() - t0 > kWaitCycles) break;
+  }
+  if (atomicExch(&ctl.fail, 1) == 0) report(err_word, KVQ_ERRBIT_TIMEOUT);
+  return false;
 }
 
 template <bool kInt4, bool kOne>
@@ -649,7 +690,7 @@ __global__ void __launch_bounds__(kRingThreads, 3)
     wq_ring_kernel(const __grid_constant__ CUtensorMap wmap, RingArgs a) {
   extern __shared__ __align__(128) uint8_t ring_raw[];
   uint8_t *sm = ring_raw + ((1024 - (smem_addr(ring_raw) & 1023)) & 1023);
-  const RingLayout L = ring_layout(kInt4, a.stages, a.gpc, a.M);
+  const RingLayout L = ring_layout(kInt4, a.stages, a.gpc, a.M, gridDim.y);
   uint8_t *ring = sm;
   uint4 *xs = reinterpret_cast<uint4 *>(sm + L.x);
   float2 *sc_s = reinterpret_cast<float2 *>(sm + L.sc);
@@ -671,11 +712,15 @@ __global__ void __launch_bounds__(kRingThreads, 3)
       mbar_init(&ctl.full[s], 1);
       mbar_init(&ctl.empty[s], kRingWarps);
     }
+    // split K: every lane of the other CTAs' four lead warps arrives once
+    if (gridDim.y > 1) mbar_init(&ctl.red, (gridDim.y - 1) * 32 * (kRingWarps / 2));
     ctl.fail = 0;
     fence_barrier_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
   }
   __syncthreads();
+  // split K: no CTA may arrive on the first CTA's barrier before it exists
+  if (gridDim.y > 1) cluster_sync_all();
   // The weights and their scales are constant (see kvq_wq_gemm): the
   // producer streams them and the consumers load the scales without waiting
   // for the work ahead of this kernel on the stream, so the first stages
@@ -799,9 +844,10 @@ __global__ void __launch_bounds__(kRingThreads, 3)
   }
 
   // ---- the CTA's sums: the two warps of a row block add theirs (box 1's
-  // into box 0's); with split K the cluster's first CTA then adds the
-  // others' (rank order) and stores.  Every thread reaches both cluster
-  // barriers, whatever happened above.
+  // into box 0's); with split K every other CTA of the cluster writes them
+  // into the first CTA's shared memory, arrives on its barrier and exits,
+  // and the first CTA adds them in rank order and stores.  Every CTA sends,
+  // whatever happened above, so the first CTA's wait ends.
   const bool consumer = warp < kRingWarps, lead = warp < kRingWarps / 2;
   if (consumer) {
     if (!lead) part[rb * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -815,21 +861,23 @@ __global__ void __launch_bounds__(kRingThreads, 3)
     }
   }
   bool store = lead;
-  if (gridDim.y > 1) {
-    if (lead) part[rb * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    cluster_sync_all();
+  if (gridDim.y > 1 && lead) {
     const uint32_t rank = cluster_rank();
-    store = lead && rank == 0;
-    if (store) {
-      for (uint32_t r = 1; r < gridDim.y; ++r) {
-        const float4 v = ld_cluster_f4(part + rb * 32 + lane, r);
+    float4 *recv = reinterpret_cast<float4 *>(sm + L.recv);
+    if (rank != 0) {
+      st_cluster_f4(cluster_addr(recv + (rank - 1) * 128 + rb * 32 + lane, 0),
+                    make_float4(acc[0], acc[1], acc[2], acc[3]));
+      mbar_arrive_cluster(cluster_addr(&ctl.red, 0));
+      store = false;
+    } else if (ring_wait_cluster(ctl, &ctl.red, 0, a.err_word)) {
+      for (uint32_t r = 0; r + 1 < gridDim.y; ++r) {
+        const float4 v = recv[r * 128 + rb * 32 + lane];
         acc[0] += v.x;
         acc[1] += v.y;
         acc[2] += v.z;
         acc[3] += v.w;
       }
     }
-    cluster_sync_all();  // the others' shared memory stays until it has been read
   }
   if (store) {
     const int row0 = row_base + rl;
@@ -985,8 +1033,8 @@ bool ring_plan(bool int4, int M, int N, int K, int sms, RingPlan *p) {
   const int gpc = gpc_of(ksplit);
   ksplit = (groups + gpc - 1) / gpc;  // no CTA without groups
   int stages = kRingMaxStages;
-  while (stages > 2 && ring_layout(int4, stages, gpc, M).total > budget) --stages;
-  const size_t smem = ring_layout(int4, stages, gpc, M).total;
+  while (stages > 2 && ring_layout(int4, stages, gpc, M, ksplit).total > budget) --stages;
+  const size_t smem = ring_layout(int4, stages, gpc, M, ksplit).total;
   if (smem > budget || stages < 3) return false;
   *p = RingPlan{ksplit, gpc, stages, smem};
   return true;

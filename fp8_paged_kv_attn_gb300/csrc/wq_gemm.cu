@@ -530,11 +530,12 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
 // 16 KB), so the bytes in flight do not depend on registers.  Rows past N
 // are zero-filled by the copy.  Consumers wait for a stage, read their
 // rows' words, compute, and release it; every wait is bounded.  Split-K
-// runs as a thread-block cluster along k: each CTA leaves its partial sums
-// in shared memory and the cluster's first CTA adds them in rank order
-// (distributed shared memory), so there is no memset, no atomic and the
-// result does not vary from run to run.  One token (M == 1) has its own
-// instantiation that keeps only the live accumulator elements.
+// runs as a thread-block cluster along k: every CTA but the first writes
+// its partial sums into the first CTA's shared memory (distributed shared
+// memory) and arrives on its mbarrier, and the first CTA adds them in rank
+// order, so there is no memset, no atomic and the result does not vary
+// from run to run.  One token (M == 1) has its own instantiation that keeps
+// only the live accumulator elements.
 
 constexpr int kRingWarps = 8;                          // consumer warps
 constexpr int kRingRows = 64;                          // output channels per CTA

@@ -194,6 +194,47 @@ def test_wq_gemm_wide_range_x(kvq, wdtype, M, N, K):
 
 
 @pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])
+@pytest.mark.parametrize("N,K", [(200, 1536), (70, 640)])
+def test_wq_ring_wide_range_x(kvq, wdtype, N, K):
+    """Each of the eight wide-range activation regimes through the ring
+    kernel: as one token (its own instantiation) and in pairs of tokens."""
+    rng = np.random.default_rng(N + K + 10 * wdtype)
+    w, s, _ = pins.random_wq_case(rng, wdtype, 1, N, K)
+    x8 = pins.wide_range_x(rng, 8, K)
+    for m in range(8):
+        check(wdtype, w, s, x8[m:m + 1], what=f"regime {m}, one token, {N}x{K}")
+    for m in range(0, 8, 2):
+        check(wdtype, w, s, x8[m:m + 2], what=f"regimes {m},{m + 1}, two tokens, {N}x{K}")
+
+
+@pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])
+@pytest.mark.parametrize("M", [1, 2, 9], ids=["ring1", "ring", "registers"])
+def test_wq_gemm_nan_inf_propagate(kvq, wdtype, M):
+    """NaN and infinities in x propagate as IEEE arithmetic has them: a NaN in
+    a token's k range makes every output of that token NaN; +-inf gives +-inf
+    or NaN (inf * 0, inf - inf) exactly where the fp64 oracle does; the other
+    tokens stay within the bound."""
+    rng = np.random.default_rng(50 + 3 * M + wdtype)
+    N, K = 150, 768
+    w, s, x = pins.random_wq_case(rng, wdtype, M, N, K)
+    x = x.copy()
+    nan_b, inf_b, ninf_b = np.uint16(0x7FC0), np.uint16(0x7F80), np.uint16(0xFF80)
+    x[0, 300] = nan_b
+    if M > 1:
+        x[1, 5] = inf_b
+        x[1, 700] = ninf_b
+    got = run_gpu(wdtype, w, s, x).astype(np.float64)
+    ref = oracle.wq_gemm(wdtype, w, s, x)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "NaN positions differ"
+    assert np.array_equal(np.isposinf(got), np.isposinf(ref)), "+inf positions differ"
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref)), "-inf positions differ"
+    assert np.all(np.isnan(got[0])), "a NaN input must make its token's outputs NaN"
+    if M > 2:
+        bound, _ = wq_bound(wdtype, w, s, x[2:])
+        assert np.all(np.abs(got[2:] - ref[2:]) <= bound)
+
+
+@pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])
 def test_wq_gemm_wide_range_x_full_size(kvq, wdtype):
     """The large projection (28672 x 5120) at 64 tokens with wide-range
     activations: 96 sampled output channels."""

@@ -140,18 +140,17 @@ __device__ __forceinline__ float pow2_any(int n) {
 // A lane's two B registers of steps 2q and 2q + 1 are one 16-byte word of
 // the staged x: [group][step pair q][token slot][lane class].
 
-// One group's products for NT token tiles: gacc[t] = the sum of kQ step
-// pairs (all 4 of a group, or 2: one e4m3 half-group) starting from zero.
-// w0 / w8: the lane's weight words of rows r and r + 8; xg: the lane's B
-// word of the first step pair (token slot of tile 0), Mp token slots per
-// step pair.
-template <bool kInt4, int NT, int kQ = 4>
+// One group's products for NT token tiles: gacc[t] = the group's 4 step
+// pairs (8 MMA steps) starting from zero.  w0 / w8: the lane's weight words
+// of rows r and r + 8; xg: the lane's B word of the group's first step pair
+// (token slot of tile 0), Mp token slots per step pair.
+template <bool kInt4, int NT>
 __device__ __forceinline__ void group_mma(float (&gacc)[NT][4],
-                                          const uint32_t (&w0)[kInt4 ? kQ : 2 * kQ],
-                                          const uint32_t (&w8)[kInt4 ? kQ : 2 * kQ],
-                                          const uint4 *xg, int Mp) {
+                                          const uint32_t (&w0)[kInt4 ? 4 : 8],
+                                          const uint32_t (&w8)[kInt4 ? 4 : 8], const uint4 *xg,
+                                          int Mp) {
 #pragma unroll
-  for (int q = 0; q < kQ; ++q) {
+  for (int q = 0; q < 4; ++q) {
     uint32_t af[2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -545,6 +544,7 @@ constexpr int kBoxBytes = 64;                          // a box: 64 bytes x kRin
 constexpr int kStageBoxes = 4;                         // boxes per stage (2 per consumer warp)
 constexpr int kStageBytes = kStageBoxes * kBoxBytes * kRingRows;  // 16 KB
 constexpr int kRingMaxCluster = 8;
+constexpr int kPartSlots = (kRingRows / 16) * 32;       // a float4 per row block and lane
 
 struct RingArgs {
   const void *scales;     // bf16 [N][K/128] or fp32 [N]
@@ -553,7 +553,7 @@ struct RingArgs {
   uint32_t *err_word;
   int32_t M, N, K;
   int32_t gpc;            // 128-wide k groups per CTA
-  int32_t stages;         // ring depth, 2 .. kRingMaxStages
+  int32_t stages;         // ring depth, 3 .. kRingMaxStages
 };
 
 struct RingCtl {
@@ -579,9 +579,9 @@ __host__ __device__ inline RingLayout ring_layout(bool int4, int stages, int gpc
   L.xu = o;
   o += size_t(gpc) * 8 * 4;
   L.part = o;
-  o += size_t(kRingRows / 16) * 32 * 16;
+  o += size_t(kPartSlots) * 16;
   L.recv = o;
-  o += size_t(ksplit > 1 ? ksplit - 1 : 0) * (kRingRows / 16) * 32 * 16;
+  o += size_t(ksplit > 1 ? ksplit - 1 : 0) * kPartSlots * 16;
   L.ctl = o;
   o += (sizeof(RingCtl) + 15) / 16 * 16;
   L.total = o + 1024;  // room to align the base
@@ -815,13 +815,8 @@ __global__ void __launch_bounds__(kRingThreads, 3)
             group_fold<true, 1, kOne>(acc1, gacc, scl[g], xul + g * 8);
           }
         }
-      } else if constexpr (kHB == 1) {
-        // box h = bytes 64 h .. 64 h + 63 of group k: step pairs 2h, 2h + 1
-        const uint32_t a0[4] = {u0[0].x, u0[0].y, u0[0].z, u0[0].w};
-        const uint32_t a8[4] = {u8[0].x, u8[0].y, u8[0].z, u8[0].w};
-        group_mma<false, 1, 2>(gacc, a0, a8, xl + (k * 4 + 2 * h) * Mp * 4, Mp);
-        group_fold<false, 1, kOne>(acc1, gacc, make_float2(1.f, 1.f), xul + k * 8);
       } else {
+        static_assert(kHB == 2, "an e4m3 warp takes both halves of a group");
         // boxes 2h, 2h + 1 = both halves of group 2k + h
         const int g = 2 * k + h;
         if (g < ng) {
@@ -866,13 +861,13 @@ __global__ void __launch_bounds__(kRingThreads, 3)
     const uint32_t rank = cluster_rank();
     float4 *recv = reinterpret_cast<float4 *>(sm + L.recv);
     if (rank != 0) {
-      st_cluster_f4(cluster_addr(recv + (rank - 1) * 128 + rb * 32 + lane, 0),
+      st_cluster_f4(cluster_addr(recv + (rank - 1) * kPartSlots + rb * 32 + lane, 0),
                     make_float4(acc[0], acc[1], acc[2], acc[3]));
       mbar_arrive_cluster(cluster_addr(&ctl.red, 0));
       store = false;
     } else if (ring_wait_cluster(ctl, &ctl.red, 0, a.err_word)) {
       for (uint32_t r = 0; r + 1 < gridDim.y; ++r) {
-        const float4 v = recv[r * 128 + rb * 32 + lane];
+        const float4 v = recv[r * kPartSlots + rb * 32 + lane];
         acc[0] += v.x;
         acc[1] += v.y;
         acc[2] += v.z;

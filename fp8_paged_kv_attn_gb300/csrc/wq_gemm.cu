@@ -56,6 +56,8 @@
 // in the register-ring kernel, for results below fp32's normal range, by the
 // split-K atomics, since an fp32 atomic add flushes subnormal operands).
 #include <atomic>
+#include <mutex>
+#include <unordered_map>
 
 #include <cuda_fp16.h>
 
@@ -967,6 +969,30 @@ bool wq_smem_opt_in(const void *fn, int slot, size_t bytes) {
   return true;
 }
 
+// Resident CTAs per SM of a register-ring kernel variant at a dynamic
+// shared-memory size (cached per device, variant and size: the split choice
+// asks for several sizes on every call).
+bool wq_occupancy(WqFn fn, int slot, size_t smem, int *occ) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const uint64_t key = (static_cast<uint64_t>(dev) << 40) | (static_cast<uint64_t>(slot) << 32) | smem;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) {
+      *occ = it->second;
+      return true;
+    }
+  }
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, fn, 32 * kWqWarps, smem) != cudaSuccess)
+    return false;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = *occ;
+  return true;
+}
+
 // Shared memory one CTA may use so that three of them fit on an SM (cached
 // per device).
 size_t smem_per_cta3() {
@@ -1086,27 +1112,34 @@ extern "C" kvq_status kvq_wq_gemm(int32_t w_dtype, const void *w, const void *sc
     return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
   }
 
-  // otherwise the register-ring kernel: split K so that the grid covers the
-  // GPU's resident CTAs once; each CTA's staged x must fit the budget
+  // otherwise the register-ring kernel.  Split K: shared memory sets the
+  // most groups a CTA can stage x for; among the splits from there, take the
+  // one with the least (waves of resident CTAs) x (groups per CTA), the
+  // fewest splits on a tie (occupancy depends on the staged x).
   const WqFn fn = int4 ? pick_wq<true>(nt) : pick_wq<false>(nt);
   const int row_tiles = (N + kWqRows - 1) / kWqRows;
   auto smem_of = [&](int gpc) { return wq_smem_bytes(int4, gpc, nt, M); };
-  if (!wq_smem_opt_in(reinterpret_cast<const void *>(fn), int4 ? nt - 1 : 8 + nt - 1, kWqSmemMax))
-    return KVQ_ERR_CUDA;
-  int gpc = groups;
-  while (gpc > 1 && smem_of(gpc) > kWqSmemMax) --gpc;
-  int ksplit = (groups + gpc - 1) / gpc;
-  for (int pass = 0; pass < 2; ++pass) {
+  const int slot = int4 ? nt - 1 : 8 + nt - 1;
+  if (!wq_smem_opt_in(reinterpret_cast<const void *>(fn), slot, kWqSmemMax)) return KVQ_ERR_CUDA;
+  int gpc_max = groups;
+  while (gpc_max > 1 && smem_of(gpc_max) > kWqSmemMax) --gpc_max;
+  const int ks_min = (groups + gpc_max - 1) / gpc_max;
+  int gpc = gpc_max, ksplit = ks_min;
+  int64_t best = -1;
+  for (int ks = ks_min; ks <= groups && ks <= ks_min + 16; ++ks) {
+    const int g = (groups + ks - 1) / ks;
+    const int kse = (groups + g - 1) / g;  // no CTA without groups
+    if (kse != ks) continue;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, 32 * kWqWarps, smem_of(gpc)) !=
-        cudaSuccess)
-      return KVQ_ERR_CUDA;
-    const int cap = (occ > 0 ? occ : 1) * sms;
-    int want = cap / row_tiles;
-    if (want < ksplit) want = ksplit;  // shared memory already needs this many
-    if (want > groups) want = groups;
-    gpc = (groups + want - 1) / want;
-    ksplit = (groups + gpc - 1) / gpc;
+    if (!wq_occupancy(fn, slot, smem_of(g), &occ)) return KVQ_ERR_CUDA;
+    const int64_t slots = static_cast<int64_t>(occ > 0 ? occ : 1) * sms;
+    const int64_t waves = (static_cast<int64_t>(row_tiles) * kse + slots - 1) / slots;
+    const int64_t cost = waves * g;
+    if (best < 0 || cost < best) {
+      best = cost;
+      gpc = g;
+      ksplit = kse;
+    }
   }
   const size_t smem = smem_of(gpc);
 

@@ -13,7 +13,7 @@
 // e4m3 weights with an fp32 scale per output channel.
 //
 // Two kernels, one per regime:
-//  * the TMA-ring kernel (up to 4 tokens for INT4, 2 for e4m3): 64 output
+//  * the TMA-ring kernel (one or two tokens): 64 output
 //    channels per CTA; a producer warp streams the weights into a
 //    shared-memory ring with the TMA engine, eight consumer warps read them
 //    from there; a k split is a thread-block cluster whose partial sums are
@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
 }
 
 // ---------------------------------------------------------------------------
-// TMA-ring kernel (up to 4 tokens: one token tile)
+// TMA-ring kernel (one or two tokens)
 // ---------------------------------------------------------------------------
 //
 // A CTA covers 64 output channels and a range of k groups; a ninth warp's
@@ -1035,8 +1035,8 @@ struct RingPlan {
   size_t smem;
 };
 bool ring_plan(bool int4, int M, int N, int K, int sms, RingPlan *p) {
-  // measured: more tokens run faster on the register ring
-  if (M > (int4 ? 4 : 2)) return false;
+  // measured: from three tokens on the register ring is as fast or faster
+  if (M > 2) return false;
   constexpr int kPerSm = 3;
   const size_t budget = smem_per_cta3();
   const int groups = K / kWqGroup;

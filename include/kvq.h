@@ -205,7 +205,7 @@ KVQ_API kvq_status kvq_pages_update(int32_t *free_stack, int32_t *free_count, ui
  * values are scaled by a power of two for the products (exact for every
  * value down to 2^-32 of the token's largest finite |x| in a k range,
  * smaller ones are rounded to 2^-25 of it); NaN and inf propagate.
- * Up to 8 tokens (when a CTA's share of x fits its shared memory) the
+ * For one or two tokens (when a CTA's share of x fits its shared memory) the
  * weights stream through a shared-memory ring fed by the TMA engine and a k
  * split runs as a thread-block cluster whose partial sums are added in a
  * fixed order: every run gives the same bits.  Otherwise split-K partial

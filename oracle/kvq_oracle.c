@@ -512,7 +512,7 @@ uint32_t oracle_decode_attn(int kv_dtype, const void *k_pool, const void *v_pool
     return err;
 }
 
-/* Reports whether this build has OpenMP (used to state the cores the CPU
+/* Reports whether the library was compiled with OpenMP (used to state the cores the CPU
  * baseline really ran on). */
 int oracle_has_openmp(void)
 {

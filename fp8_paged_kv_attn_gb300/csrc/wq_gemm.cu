@@ -306,9 +306,9 @@ __host__ __device__ constexpr int wq_scale_stride(int gpc) { return gpc | 1; }
 // reads row N - 1) and group g < ng.  Items e = p * ng + g go to threads in
 // order (a warp reads runs of consecutive scales), kScB per thread and
 // batch: every load of a batch is issued before any is stored, so a batch
-// costs one memory round trip.  p = e / ng is taken as floor((e + 1/2) /
-// ng) in fp32, exact for every ng up to 2048 and e below 64 ng (checked
-// exhaustively).
+// costs one memory round trip.  p = e / ng is taken as trunc((e + 1/2)
+// RN(1/ng)) in fp32, exact for every ng up to 2048 and e below 64 ng
+// (checked exhaustively; ng is at most a few hundred here).
 constexpr int kScB = 5;
 struct ScaleStage {
   const uint16_t *sp;  // bf16 scales [N][K / 128], from the CTA's first group

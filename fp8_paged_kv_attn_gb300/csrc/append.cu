@@ -35,9 +35,7 @@ struct AppendArgs {
   uint32_t *err_word;
   int64_t n_tokens;
   int32_t num_pages, P, H, B, MP;
-  float k_scale, v_scale;
-  float k_rlo, k_rhi, v_rlo, v_rhi;  // RN(RN(1 / scale) (1 -+ 8u))
-  int32_t k_fast, v_fast;            // the reciprocals are normal floats
+  QuantParams kq, vq;  // the quantiser's parameters for k_scale and v_scale
 };
 
 template <bool kFp8, int D>
@@ -105,9 +103,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
         if constexpr (kFp8) {
           uint8_t *pool = static_cast<uint8_t *>(is_v ? a.v_pool : a.k_pool);
           *reinterpret_cast<uint4 *>(pool + dst) =
-              quantise16(s[k][0], s[k][1], is_v ? a.v_scale : a.k_scale,
-                         is_v ? a.v_rlo : a.k_rlo, is_v ? a.v_rhi : a.k_rhi,
-                         is_v ? a.v_fast : a.k_fast);
+              quantise16(s[k][0], s[k][1], is_v ? a.vq : a.kq);
         } else {
           uint16_t *pool = static_cast<uint16_t *>(is_v ? a.v_pool : a.k_pool);
           *reinterpret_cast<uint4 *>(pool + dst) = s[k][0];
@@ -157,10 +153,8 @@ extern "C" kvq_status kvq_append(const kvq_cache *cache, const void *k_new, cons
   a.H = cache->num_kv_heads;
   a.B = B;
   a.MP = MP;
-  a.k_scale = cache->k_scale;
-  a.v_scale = cache->v_scale;
-  reciprocals(a.k_scale, &a.k_rlo, &a.k_rhi, &a.k_fast);
-  reciprocals(a.v_scale, &a.v_rlo, &a.v_rhi, &a.v_fast);
+  a.kq = quant_params(cache->k_scale);
+  a.vq = quant_params(cache->v_scale);
 
   const bool fp8 = cache->kv_dtype == KVQ_KV_E4M3;
   const AppendFn fn = pick_append(fp8, cache->head_dim);

@@ -11,17 +11,23 @@
 // the rounding kvq_append uses (quant_e4m3.cuh), so a token handed off and a
 // token appended during decode are stored identically.
 //
-// Work layout: grid (token blocks, requests); a CTA of 8 warps takes 64
-// consecutive tokens of one request, a warp 8 of them.  Lanes 0..7 of a warp
-// look up the prefill and decode page of its 8 tokens at once (two loads
-// each); then, token by token, the lanes take the token's K 16-byte output
-// chunks (16 codes; a head's row of D bf16 values is contiguous in the
-// prefill page), then its V chunks, each batch's source words loaded before
-// any of them is converted and stored.  The kv-head count and D are template
-// parameters, so every lane's chunk offsets are fixed before the token loop.
+// Work layout: grid (block groups, requests).  A request's positions are
+// cut into 64-aligned blocks of 64; a CTA takes kHoBlocksPerCta consecutive
+// blocks of one request, and a stage of its shared-memory ring is one
+// (block, kv head): the block's K rows and V rows of that head.  In a
+// prefill page a head's rows are contiguous, so a stage is filled by one
+// 1-D bulk copy (TMA engine) per prefill page the block touches and tensor
+// (page sizes 16..64 divide 64: one to four pages).  A producer warp looks up
+// both block tables once per block (two positions per lane), writes each
+// position's decode-pool offset into the stage's header and issues the
+// copies; eight consumer warps convert 8 values a thread (one 16-byte
+// shared-memory load, one 8-byte store; a warp stores 256 contiguous bytes)
+// and release the stage.  Two CTAs per SM keep up to six stages (~192 KB)
+// of reads in flight per SM.
 // HBM-bound: per token and kv head 2 D (2 + s) bytes (read bf16 K and V,
 // write s-byte codes), plus 4 bytes per prefill and per decode page.
 #include <algorithm>
+#include <atomic>
 
 #include "kvq_internal.h"
 #include "quant_e4m3.cuh"
@@ -34,114 +40,211 @@ struct HandoffArgs {
   const int32_t *src_bt, *dst_bt, *first, *count;
   uint32_t *err_word;
   int32_t src_pages, Ps, src_MP, dst_pages, Pd, dst_MP, H, B;
-  float k_scale, v_scale;
-  float k_rlo, k_rhi, v_rlo, v_rhi;
-  int32_t k_fast, v_fast;
+  QuantParams kq, vq;
 };
 
-constexpr int kHoWarps = 8;
-constexpr int kHoTokPerWarp = 8;
-constexpr int kHoTokPerCta = kHoWarps * kHoTokPerWarp;
+constexpr int kHoBlock = 64;          // positions per stage: one 64-aligned block
+constexpr int kHoConsumers = 8;       // consumer warps
+constexpr int kHoThreads = 32 * (kHoConsumers + 1);
+constexpr int kHoBlocksPerCta = 2;
+constexpr int kHoMaxStages = 6;
 
-template <bool kFp8, int H, int D>
-__global__ void __launch_bounds__(32 * kHoWarps, 6) handoff_kernel(HandoffArgs a) {
-  constexpr int kElems = kFp8 ? 16 : 8;             // elements per 16-byte output chunk
-  constexpr int kCpr = D / kElems;                  // chunks per (token, head) row
-  constexpr int kChunks = H * kCpr;                 // chunks of one token's K (or V)
-  constexpr int kPer = (kChunks + 31) / 32;         // chunks per lane per tensor
-  constexpr int kSrcWords = kFp8 ? 2 : 1;           // 16-byte source words per chunk
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // this lane's chunks: element offsets inside a token's (page, head 0, slot)
-  // block, the same for every token (heads are P * D elements apart)
-  int soff[kPer], doff[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int c = lane + 32 * k;
-    soff[k] = (c / kCpr) * a.Ps * D + (c % kCpr) * kElems;
-    doff[k] = (c / kCpr) * a.Pd * D + (c % kCpr) * kElems;
+template <int D>
+struct HoCfg {
+  static constexpr int ROW = 2 * D;             // bytes of one bf16 (token, head) row
+  static constexpr int TILE = kHoBlock * ROW;   // one tensor's rows of a stage
+  static constexpr int STAGE = 2 * TILE;        // K, then V
+  static constexpr int NS = D == 128 ? 3 : 6;   // ring depth: 96 KB of rows
+  static constexpr int GROUPS = kHoBlock * D / 8 / (32 * kHoConsumers);  // per thread and tensor
+  static_assert(NS <= kHoMaxStages, "ring depth");
+};
+
+struct HoCtl {
+  uint64_t full[kHoMaxStages], empty[kHoMaxStages];
+  int32_t live[kHoMaxStages];  // 1: the stage holds a (block, head); 0: nothing follows
+  int32_t fail;
+};
+
+template <int D>
+constexpr size_t ho_smem_bytes() {
+  return static_cast<size_t>(HoCfg<D>::NS) * HoCfg<D>::STAGE +
+         static_cast<size_t>(HoCfg<D>::NS) * kHoBlock * sizeof(int64_t) + sizeof(HoCtl);
+}
+
+// Bounded wait of either role: on timeout the error bit is raised once and
+// the fail flag tells the other role to leave.
+__device__ __forceinline__ bool ho_wait(HoCtl &ctl, uint64_t *bar, uint32_t parity,
+                                        uint32_t *err_word) {
+  if (*reinterpret_cast<volatile int32_t *>(&ctl.fail)) return false;
+  if (mbar_wait(bar, parity)) return true;
+  if (atomicExch(&ctl.fail, 1) == 0) report(err_word, KVQ_ERRBIT_TIMEOUT);
+  return false;
+}
+
+template <bool kFp8, int D>
+__global__ void __launch_bounds__(kHoThreads, 2) handoff_kernel(HandoffArgs a) {
+  using C = HoCfg<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t *rows = smem;  // [NS][K rows | V rows], row r of a stage = position blk*64 + r
+  int64_t *hdr = reinterpret_cast<int64_t *>(smem + C::NS * C::STAGE);  // [NS][64]
+  HoCtl &ctl = *reinterpret_cast<HoCtl *>(smem + C::NS * C::STAGE + C::NS * kHoBlock * 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(&ctl.full[i], 1);
+      mbar_init(&ctl.empty[i], kHoConsumers);
+    }
+    ctl.fail = 0;
+    fence_barrier_init();
   }
+  __syncthreads();
   grid_dependency_wait();
   allow_dependents();
 
-  for (int b = blockIdx.y; b < a.B; b += gridDim.y) {
-    const int f = a.first ? __ldg(a.first + b) : 0;
-    const int n = __ldg(a.count + b);
-    const long long end = static_cast<long long>(f) + n;
-    if (f < 0 || n < 0 || end > static_cast<long long>(a.src_MP) * a.Ps ||
-        end > static_cast<long long>(a.dst_MP) * a.Pd) {
-      if (blockIdx.x == 0 && threadIdx.x == 0) report(a.err_word, KVQ_ERRBIT_POS);
-      continue;
-    }
-    // positions fit in 32 bits from here on: both tables hold at most
-    // INT32_MAX tokens (checked by the host)
-    const long long t0l = static_cast<long long>(blockIdx.x) * kHoTokPerCta + warp * kHoTokPerWarp;
-    if (t0l >= n) continue;
-    const int t0 = static_cast<int>(t0l);
-    const int ntok = min(kHoTokPerWarp, n - t0);
-    // lanes 0..ntok-1: the prefill and decode pages of token f + t0 + lane
-    int sp = -1, dp = -1;
-    if (lane < ntok) {
-      const int p = f + t0 + lane;
-      sp = __ldg(a.src_bt + static_cast<int64_t>(b) * a.src_MP + p / a.Ps);
-      dp = __ldg(a.dst_bt + static_cast<int64_t>(b) * a.dst_MP + p / a.Pd);
-    }
-    for (int j = 0; j < ntok; ++j) {
-      const int p = f + t0 + j;
-      const int spage = __shfl_sync(0xffffffffu, sp, j);
-      const int dpage = __shfl_sync(0xffffffffu, dp, j);
-      if (spage < 0 || spage >= a.src_pages || dpage < 0 || dpage >= a.dst_pages) {
-        if (lane == 0) report(a.err_word, KVQ_ERRBIT_PAGE);
-        continue;  // uniform over the warp
+  if (warp == kHoConsumers) {
+    // ---------------------------------------------------------- producer
+    const int64_t src_head = static_cast<int64_t>(a.Ps) * D;  // elements between heads
+    const int64_t dst_head = static_cast<int64_t>(a.Pd) * D;
+    const uint64_t pol = policy_evict_first();
+    uint32_t g = 0;
+    bool ok = true;
+    for (int b = blockIdx.y; ok && b < a.B; b += gridDim.y) {
+      const int f = a.first ? __ldg(a.first + b) : 0;
+      const int n = __ldg(a.count + b);
+      const long long end = static_cast<long long>(f) + n;
+      if (f < 0 || n < 0 || end > static_cast<long long>(a.src_MP) * a.Ps ||
+          end > static_cast<long long>(a.dst_MP) * a.Pd) {
+        if (blockIdx.x == 0 && lane == 0) report(a.err_word, KVQ_ERRBIT_POS);
+        continue;
       }
-      // element offsets of the token's (page, head 0, slot, dim 0)
-      const int64_t src0 = (static_cast<int64_t>(spage) * H * a.Ps + p % a.Ps) * D;
-      const int64_t dst0 = (static_cast<int64_t>(dpage) * H * a.Pd + p % a.Pd) * D;
-      // K, then V: a batch's source words are all loaded before any is stored
+      if (n == 0) continue;
+      // positions fit in 32 bits from here on: both tables hold at most
+      // INT32_MAX tokens (checked by the host)
+      const int blk0 = f / kHoBlock + static_cast<int>(blockIdx.x) * kHoBlocksPerCta;
+      const int blk_last = (f + n - 1) / kHoBlock;
+      for (int k = 0; ok && k < kHoBlocksPerCta && blk0 + k <= blk_last; ++k) {
+        const int blk = blk0 + k;
+        const int lo = max(blk * kHoBlock, f), hi = min(blk * kHoBlock + kHoBlock, f + n);
+        // positions blk*64 + lane and + 32: the decode-pool offset (head 0;
+        // -1: not stored) and, where a prefill page's piece starts, the copy
+        int64_t doff[2], soff[2];
+        int run[2];
+        uint32_t tx = 0;
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const uint16_t *src = (t ? a.src_v : a.src_k) + src0;
-        uint4 s[kPer][kSrcWords];
+        for (int r = 0; r < 2; ++r) {
+          const int p = blk * kHoBlock + lane + 32 * r;
+          doff[r] = -1;
+          soff[r] = 0;
+          run[r] = 0;
+          if (p >= lo && p < hi) {
+            const int sp = __ldg(a.src_bt + static_cast<int64_t>(b) * a.src_MP + p / a.Ps);
+            const int dp = __ldg(a.dst_bt + static_cast<int64_t>(b) * a.dst_MP + p / a.Pd);
+            const bool src_ok = sp >= 0 && sp < a.src_pages;
+            if (!src_ok || dp < 0 || dp >= a.dst_pages) report(a.err_word, KVQ_ERRBIT_PAGE);
+            else doff[r] = (static_cast<int64_t>(dp) * a.H * a.Pd + p % a.Pd) * D;
+            if (src_ok && (p == lo || p % a.Ps == 0)) {
+              run[r] = min(hi, (p / a.Ps + 1) * a.Ps) - p;
+              soff[r] = (static_cast<int64_t>(sp) * a.H * a.Ps + p % a.Ps) * D;
+              tx += 2u * run[r] * C::ROW;
+            }
+          }
+        }
+        tx = __reduce_add_sync(0xffffffffu, tx);
+        for (int h = 0; h < a.H; ++h, ++g) {
+          const int slot = g % C::NS;
+          bool waited = true;
+          if (lane == 0 && g >= C::NS)
+            waited = ho_wait(ctl, &ctl.empty[slot], ((g / C::NS) - 1) & 1, a.err_word);
+          ok = __shfl_sync(0xffffffffu, waited ? 1 : 0, 0) != 0 &&
+               !*reinterpret_cast<volatile int32_t *>(&ctl.fail);
+          if (!ok) break;
+          int64_t *hd = hdr + slot * kHoBlock;
+          hd[lane] = doff[0] < 0 ? -1 : doff[0] + h * dst_head;
+          hd[lane + 32] = doff[1] < 0 ? -1 : doff[1] + h * dst_head;
+          __syncwarp();
+          if (lane == 0) {
+            ctl.live[slot] = 1;
+            mbar_arrive_expect_tx(&ctl.full[slot], tx);
+          }
+          __syncwarp();
 #pragma unroll
-        for (int k = 0; k < kPer; ++k)
-          if (kChunks % 32 == 0 || lane + 32 * k < kChunks)
-#pragma unroll
-            for (int w = 0; w < kSrcWords; ++w)
-              s[k][w] = __ldcs(reinterpret_cast<const uint4 *>(src + soff[k]) + w);
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          if (!(kChunks % 32 == 0 || lane + 32 * k < kChunks)) continue;
-          if constexpr (kFp8) {
-            uint8_t *dst = static_cast<uint8_t *>(t ? a.dst_v : a.dst_k) + dst0 + doff[k];
-            *reinterpret_cast<uint4 *>(dst) =
-                quantise16(s[k][0], s[k][1], t ? a.v_scale : a.k_scale, t ? a.v_rlo : a.k_rlo,
-                           t ? a.v_rhi : a.k_rhi, t ? a.v_fast : a.k_fast);
-          } else {
-            uint16_t *dst = static_cast<uint16_t *>(t ? a.dst_v : a.dst_k) + dst0 + doff[k];
-            *reinterpret_cast<uint4 *>(dst) = s[k][0];
+          for (int r = 0; r < 2; ++r) {
+            if (run[r] == 0) continue;
+            uint8_t *kdst = rows + slot * C::STAGE + (lane + 32 * r) * C::ROW;
+            const int64_t src = soff[r] + h * src_head;
+            const uint32_t bytes = static_cast<uint32_t>(run[r]) * C::ROW;
+            bulk_g2s_hint(kdst, a.src_k + src, bytes, &ctl.full[slot], pol);
+            bulk_g2s_hint(kdst + C::TILE, a.src_v + src, bytes, &ctl.full[slot], pol);
           }
         }
       }
     }
+    if (lane == 0) {
+      if (ok) {
+        // tell the consumers there is nothing more
+        const int slot = g % C::NS;
+        if (g < C::NS || ho_wait(ctl, &ctl.empty[slot], ((g / C::NS) - 1) & 1, a.err_word)) {
+          ctl.live[slot] = 0;
+          mbar_arrive(&ctl.full[slot]);
+        }
+      } else {
+        // A wait gave up: before the CTA exits, let the copies it started
+        // land (bounded waits), so that none writes into shared memory the
+        // SM may already have handed to another CTA.  Only the last NS
+        // stages can still be in flight.
+        for (uint32_t s = g > C::NS ? g - C::NS : 0; s < g; ++s)
+          mbar_wait(&ctl.full[s % C::NS], (s / C::NS) & 1);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  uint32_t g = 0;
+  while (true) {
+    const int slot = g % C::NS;
+    if (!ho_wait(ctl, &ctl.full[slot], (g / C::NS) & 1, a.err_word)) break;
+    if (!ctl.live[slot]) break;
+    const int64_t *hd = hdr + slot * kHoBlock;
+    const uint8_t *st = rows + slot * C::STAGE;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+#pragma unroll
+      for (int j = 0; j < C::GROUPS; ++j) {
+        const int e = threadIdx.x + 32 * kHoConsumers * j;  // 8-value group of the tile
+        const int row = e / (D / 8), col = (e % (D / 8)) * 8;
+        const int64_t off = hd[row];
+        if (off < 0) continue;
+        const uint4 s = *reinterpret_cast<const uint4 *>(st + t * C::TILE + row * C::ROW + col * 2);
+        if constexpr (kFp8) {
+          uint8_t *dst = static_cast<uint8_t *>(t ? a.dst_v : a.dst_k) + off + col;
+          *reinterpret_cast<uint2 *>(dst) = quantise8(s, t ? a.vq : a.kq);
+        } else {
+          uint16_t *dst = static_cast<uint16_t *>(t ? a.dst_v : a.dst_k) + off + col;
+          *reinterpret_cast<uint4 *>(dst) = s;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.empty[slot]);
+    ++g;
   }
 }
 
 using HandoffFn = void (*)(HandoffArgs);
 
-template <bool kFp8, int D>
-HandoffFn pick_handoff_h(int H) {
-  switch (H) {
-    case 1: return handoff_kernel<kFp8, 1, D>;
-    case 2: return handoff_kernel<kFp8, 2, D>;
-    case 4: return handoff_kernel<kFp8, 4, D>;
-    case 8: return handoff_kernel<kFp8, 8, D>;
-  }
-  return nullptr;
-}
-
-inline HandoffFn pick_handoff(bool fp8, int H, int D) {
-  if (D == 64) return fp8 ? pick_handoff_h<true, 64>(H) : pick_handoff_h<false, 64>(H);
-  if (D == 128) return fp8 ? pick_handoff_h<true, 128>(H) : pick_handoff_h<false, 128>(H);
-  return nullptr;
+// Opt each variant into its shared-memory size once per device.
+bool ho_smem_opt_in(HandoffFn fn, int variant, size_t bytes) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<bool> done[kMaxDev][4];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+  if (done[dev][variant].load(std::memory_order_acquire)) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes)) != cudaSuccess)
+    return false;
+  done[dev][variant].store(true, std::memory_order_release);
+  return true;
 }
 
 }  // namespace kvq
@@ -185,23 +288,26 @@ extern "C" kvq_status kvq_handoff_pages(const kvq_cache *src, const int32_t *src
   a.dst_pages = dst->num_pages;
   a.Pd = dst->page_size;
   a.dst_MP = dst_MP;
-  a.H = dst->num_kv_heads;
+  a.H = H;
   a.B = B;
-  a.k_scale = dst->k_scale;
-  a.v_scale = dst->v_scale;
-  reciprocals(a.k_scale, &a.k_rlo, &a.k_rhi, &a.k_fast);
-  reciprocals(a.v_scale, &a.v_rlo, &a.v_rhi, &a.v_fast);
+  a.kq = quant_params(dst->k_scale);
+  a.vq = quant_params(dst->v_scale);
 
-  const HandoffFn fn = pick_handoff(dst->kv_dtype == KVQ_KV_E4M3, dst->num_kv_heads, dst->head_dim);
-  if (!fn) return KVQ_ERR_UNSUPPORTED;
-  // a request moves at most min(both capacities) tokens; token blocks past
-  // its count exit at once
+  const bool fp8 = dst->kv_dtype == KVQ_KV_E4M3;
+  const bool d128 = dst->head_dim == 128;
+  const HandoffFn fn = d128 ? (fp8 ? handoff_kernel<true, 128> : handoff_kernel<false, 128>)
+                            : (fp8 ? handoff_kernel<true, 64> : handoff_kernel<false, 64>);
+  const size_t smem = d128 ? ho_smem_bytes<128>() : ho_smem_bytes<64>();
+  if (!ho_smem_opt_in(fn, (d128 ? 2 : 0) + (fp8 ? 1 : 0), smem)) return KVQ_ERR_CUDA;
+  // a request moves at most min(both capacities) tokens, which span at most
+  // ceil(that / 64) blocks; block groups past a request's last block exit at once
   const int64_t max_tok = std::min(static_cast<int64_t>(src_MP) * src->page_size,
                                    static_cast<int64_t>(dst_MP) * dst->page_size);
-  const int64_t gx = (max_tok + kHoTokPerCta - 1) / kHoTokPerCta;
+  const int64_t blocks = (max_tok + kHoBlock - 1) / kHoBlock;
+  const int64_t gx = (blocks + kHoBlocksPerCta - 1) / kHoBlocksPerCta;
   if (gx > INT32_MAX) return KVQ_ERR_INVALID_ARG;
   const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(B < 65535 ? B : 65535));
-  const cudaError_t e = launch_dependent(fn, grid, 32 * kHoWarps, 0,
+  const cudaError_t e = launch_dependent(fn, grid, kHoThreads, smem,
                                          reinterpret_cast<cudaStream_t>(stream), a);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -67,3 +67,78 @@ def test_margin_is_needed():
             naive = oracle.e4m3_encode(x[fin] * (np.float32(1.0) / s))
             wrong += int((naive != exact).sum())
     assert wrong > 0
+
+
+EXACT_AMAX = (1.75, 3.5, 5.25, 7.0, 10.5, 224.0)  # amax / 448 exact in fp32
+OTHER_AMAX = (2.0, 0.75, 96.0, 83.0, 81.5, 121.0, 0.0123, 1e5)
+
+
+def _amax_scales():
+    """amax / 448 (fp32, as the host rounds it) for amax values that make it
+    exact (a power of two times 1 or 3: many quotients then fall exactly on
+    e4m3 boundaries) and for others."""
+    return [np.float32(a / 448.0) for a in EXACT_AMAX + OTHER_AMAX]
+
+
+def test_exact_remainder_step():
+    """The second step: where the two codes differ, q = RN(x y) and
+    t = RN(x - q s) (one fma); t = 0 must mean RN(x / s) = q, so the code is
+    e4m3(q).  Checked for every bf16 input and scale (scale >= 2^-92, the
+    host's condition for the step); what is left goes to the division.  On
+    round amax / 448 scales nothing is left: every differing element is an
+    exact quotient."""
+    x = _all_bf16_as_f32()
+    fin = np.isfinite(x)
+    left_round = 0
+    with np.errstate(over="ignore", under="ignore", invalid="ignore"):
+        for s in _scales() + _amax_scales():
+            rcp = np.float32(1.0) / s
+            r_lo, r_hi = rcp * SHRINK, rcp * GROW
+            if not (np.isfinite(rcp) and np.isfinite(r_hi) and r_lo >= np.finfo(np.float32).tiny):
+                continue
+            if s < np.float32(2.0 ** -92):
+                continue
+            differ = (oracle.e4m3_encode(x * r_lo) != oracle.e4m3_encode(x * r_hi)) & fin
+            xd = x[differ]
+            q = xd * rcp  # float32 product: RN(x y)
+            # x - q s exactly (a float64 product of two floats is exact, and the
+            # difference of two values this close is exact too), rounded once
+            t = (xd.astype(np.float64) - q.astype(np.float64) * np.float64(s)).astype(np.float32)
+            exact = t == 0
+            want = oracle.e4m3_encode(xd / s)
+            got = oracle.e4m3_encode(q)
+            bad = np.nonzero(exact & (got != want))[0]
+            assert bad.size == 0, (float(s), xd[bad[:5]], got[bad[:5]], want[bad[:5]])
+            if any(s == r for r in _amax_scales()[:len(EXACT_AMAX)]):
+                left_round += int((~exact).sum())
+            else:  # quotients near a boundary but not on it: rare
+                assert (~exact).sum() <= 256, float(s)  # 0.4% of the inputs
+    assert left_round == 0
+
+
+def test_exact_remainder_step_is_needed():
+    """On an exact amax / 448 scale the bracket alone leaves about one in 16
+    values of e4m3's normal range undecided (so most 16-value groups would
+    go to the division): the exact step is what keeps them off it."""
+    x = _all_bf16_as_f32()
+    for a in EXACT_AMAX:
+        s = np.float32(a / 448.0)
+        rcp = np.float32(1.0) / s
+        with np.errstate(all="ignore"):
+            sel = np.isfinite(x) & (np.abs(x / s) >= 2.0 ** -6) & (np.abs(x / s) <= 448)
+        xs = x[sel]
+        differ = oracle.e4m3_encode(xs * (rcp * SHRINK)) != oracle.e4m3_encode(xs * (rcp * GROW))
+        assert differ.mean() > 0.05, a
+
+
+def test_power_of_two_scale_is_a_product():
+    """For a power-of-two scale (1 / scale normal) the kernel stores the code
+    of RN(x * (1 / scale)) with no bracket: the same real number as x / scale,
+    so the same code for every bf16 input."""
+    x = _all_bf16_as_f32()
+    with np.errstate(over="ignore", under="ignore", invalid="ignore"):
+        for k in (-120, -60, -9, -2, 0, 1, 3, 8, 60, 120, 126):
+            s = np.float32(2.0 ** k)
+            got = oracle.e4m3_encode(x * (np.float32(1.0) / s))
+            want = oracle.e4m3_encode(x / s)
+            assert np.array_equal(got, want), k

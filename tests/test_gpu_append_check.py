@@ -9,7 +9,10 @@ from gpu_harness import Run, dev, dev_bf16, dev_u32, SENTINEL
 
 pytestmark = pytest.mark.gpu
 
-SCALES = [1.0, 3.0, 0.1, 1.0 / 3.0, 0.0123, 37.5, 1e-3, 2.0 ** -20]
+SCALES = [1.0, 3.0, 0.1, 1.0 / 3.0, 0.0123, 37.5, 1e-3, 2.0 ** -20,
+          # amax / 448 for round amax values: a power of two (the product
+          # path) and 3 * 2^k (many quotients exactly on e4m3 boundaries)
+          0.25, 3.0 / 256, 0.75]
 # the kernel's reciprocal fast path is exact only while 1/scale is a normal
 # float: scales at and past both ends of that range, and seeded random
 # scales over 2^-40 .. 2^40

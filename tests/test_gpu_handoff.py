@@ -103,6 +103,22 @@ def test_handoff_whole_pool(kvq, src_P, dst_P, D, dtype):
     assert np.array_equal(gv, ov), "V pool differs from the oracle"
 
 
+@pytest.mark.parametrize("scale", [1.0, 0.25, 3.0 / 256, 0.0123, 1e-39])
+def test_handoff_scales(kvq, scale):
+    """The quantiser's paths: power-of-two scales (a product), 3 * 2^k (many
+    quotients exactly on e4m3 boundaries), an arbitrary scale (the bracket)
+    and one whose reciprocal overflows (the division): byte for byte."""
+    h = inputs.handoff(seed=41, lens=[300, 1000, 65], first=[0, 17, 64], Hkv=8, D=128,
+                       src_P=64, dst_P=16, decode_room=16, dst_pool_factor=1.2)
+    src, hk, hv, _, _ = _src_pools(kvq, h, range(h.B))
+    ks, vs = float(np.float32(scale)), float(np.float32(2 * scale))
+    _, gk, gv, gerr = _run(kvq, h, kvq.KV_E4M3, src, ks, vs)
+    ok, ov, oerr = _oracle(h, oracle.KV_E4M3, hk, hv, ks, vs)
+    assert gerr == 0 and oerr == 0
+    assert np.array_equal(gk, ok), "K pool differs from the oracle"
+    assert np.array_equal(gv, ov), "V pool differs from the oracle"
+
+
 def test_handoff_errors(kvq):
     """Ranges past either table, a negative count, a prefill page outside the
     pool (negative and one past the end), a decode page outside the pool:

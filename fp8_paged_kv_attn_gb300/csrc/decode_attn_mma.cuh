@@ -732,8 +732,7 @@ __global__ void __launch_bounds__(32 * (HG + 1))
       // already have handed to another CTA.  Only the last NS stages and the
       // last two query copies can still be in flight (a slot is reused only
       // after its previous copy completed and was consumed).
-      for (uint32_t k = g > NS ? g - NS : 0; k < g; ++k) mbar_wait(&ctl.full[k % NS], (k / NS) & 1);
-      for (uint32_t k = nq > 2 ? nq - 2 : 0; k < nq; ++k) mbar_wait(&ctl.qfull[k & 1], (k >> 1) & 1);
+      drain_copies(ctl.full, NS, g, ctl.qfull, nq);
     }
     return;
   }

@@ -89,6 +89,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   return false;
 }
 
+// The drain of a CTA whose wait gave up: waits (bounded) for the copies of
+// the ring stages before stage g that can still be in flight (the last ns)
+// and for the last two of a double buffer of nq copies.  Out of line: the
+// code never runs in a healthy call, and inlined it changed the split
+// kernel's steady loop enough to cost ~0.6% at 64 requests.
+static __device__ __noinline__ void drain_copies(uint64_t *full, uint32_t ns, uint32_t g,
+                                                 uint64_t *qfull, uint32_t nq) {
+  for (uint32_t k = g > ns ? g - ns : 0; k < g; ++k) mbar_wait(&full[k % ns], (k / ns) & 1);
+  for (uint32_t k = nq > 2 ? nq - 2 : 0; k < nq; ++k) mbar_wait(&qfull[k & 1], (k >> 1) & 1);
+}
+
 // ---------------------------------------------------------------------------
 // 1-D bulk copy global -> shared, completion counted on an mbarrier.
 // Both addresses 16-byte aligned, bytes a multiple of 16.

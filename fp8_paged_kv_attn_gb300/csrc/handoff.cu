@@ -20,10 +20,11 @@
 // (page sizes 16..64 divide 64: one to four pages).  A producer warp looks up
 // both block tables once per block (two positions per lane), writes each
 // position's decode-pool offset into the stage's header and issues the
-// copies; eight consumer warps convert 8 values a thread (one 16-byte
+// copies; sixteen consumer warps convert 8 values a thread (one 16-byte
 // shared-memory load, one 8-byte store; a warp stores 256 contiguous bytes)
 // and release the stage.  Two CTAs per SM keep up to six stages (~192 KB)
-// of reads in flight per SM.
+// of reads in flight per SM, and 32 consumer warps per SM hide the latency
+// of the quantiser's rare division.
 // HBM-bound: per token and kv head 2 D (2 + s) bytes (read bf16 K and V,
 // write s-byte codes), plus 4 bytes per prefill and per decode page.
 #include <algorithm>
@@ -44,7 +45,7 @@ struct HandoffArgs {
 };
 
 constexpr int kHoBlock = 64;          // positions per stage: one 64-aligned block
-constexpr int kHoConsumers = 8;       // consumer warps
+constexpr int kHoConsumers = 16;      // consumer warps
 constexpr int kHoThreads = 32 * (kHoConsumers + 1);
 constexpr int kHoBlocksPerCta = 2;
 constexpr int kHoMaxStages = 6;
@@ -100,6 +101,21 @@ __global__ void __launch_bounds__(kHoThreads, 2) handoff_kernel(HandoffArgs a) {
   __syncthreads();
   grid_dependency_wait();
   allow_dependents();
+  // The grid's x extent comes from the tables' capacity, not the prompts'
+  // lengths: a CTA with no block group of any of its requests leaves here,
+  // all of it at once (the producer below reports bad ranges, so a CTA of
+  // group 0 always stays).
+  if (blockIdx.x > 0) {
+    bool any = false;
+    for (int b = blockIdx.y; !any && b < a.B; b += gridDim.y) {
+      const int f = a.first ? __ldg(a.first + b) : 0;
+      const int n = __ldg(a.count + b);
+      any = n > 0 && f >= 0 &&
+            f / kHoBlock + static_cast<long long>(blockIdx.x) * kHoBlocksPerCta <=
+                (static_cast<long long>(f) + n - 1) / kHoBlock;
+    }
+    if (!any) return;
+  }
 
   if (warp == kHoConsumers) {
     // ---------------------------------------------------------- producer
@@ -120,10 +136,13 @@ __global__ void __launch_bounds__(kHoThreads, 2) handoff_kernel(HandoffArgs a) {
       if (n == 0) continue;
       // positions fit in 32 bits from here on: both tables hold at most
       // INT32_MAX tokens (checked by the host)
-      const int blk0 = f / kHoBlock + static_cast<int>(blockIdx.x) * kHoBlocksPerCta;
-      const int blk_last = (f + n - 1) / kHoBlock;
-      for (int k = 0; ok && k < kHoBlocksPerCta && blk0 + k <= blk_last; ++k) {
-        const int blk = blk0 + k;
+      // block groups blockIdx.x, + gridDim.x, ... of the request
+      const int blk_first = f / kHoBlock, blk_last = (f + n - 1) / kHoBlock;
+      for (int x = blockIdx.x; ok && blk_first + x * kHoBlocksPerCta <= blk_last;
+           x += gridDim.x)
+      for (int k = 0; ok && k < kHoBlocksPerCta && blk_first + x * kHoBlocksPerCta + k <= blk_last;
+           ++k) {
+        const int blk = blk_first + x * kHoBlocksPerCta + k;
         const int lo = max(blk * kHoBlock, f), hi = min(blk * kHoBlock + kHoBlock, f + n);
         // positions blk*64 + lane and + 32: the decode-pool offset (head 0;
         // -1: not stored) and, where a prefill page's piece starts, the copy
@@ -299,14 +318,21 @@ extern "C" kvq_status kvq_handoff_pages(const kvq_cache *src, const int32_t *src
                             : (fp8 ? handoff_kernel<true, 64> : handoff_kernel<false, 64>);
   const size_t smem = d128 ? ho_smem_bytes<128>() : ho_smem_bytes<64>();
   if (!ho_smem_opt_in(fn, (d128 ? 2 : 0) + (fp8 ? 1 : 0), smem)) return KVQ_ERR_CUDA;
-  // a request moves at most min(both capacities) tokens, which span at most
-  // ceil(that / 64) blocks; block groups past a request's last block exit at once
+  // A request moves at most min(both capacities) tokens, which span at most
+  // ceil(that / 64) blocks, so that many block groups a request cover any
+  // prompt.  Tables sized for long contexts would make that grid mostly CTAs
+  // with nothing to do; the x extent is capped so that the grid holds about
+  // 16 waves of CTAs, and a CTA takes block groups x, x + gridDim.x, ...
+  int sms = 0;
+  if (device_sm_count(&sms) != KVQ_OK) return KVQ_ERR_CUDA;
   const int64_t max_tok = std::min(static_cast<int64_t>(src_MP) * src->page_size,
                                    static_cast<int64_t>(dst_MP) * dst->page_size);
   const int64_t blocks = (max_tok + kHoBlock - 1) / kHoBlock;
-  const int64_t gx = (blocks + kHoBlocksPerCta - 1) / kHoBlocksPerCta;
-  if (gx > INT32_MAX) return KVQ_ERR_INVALID_ARG;
-  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(B < 65535 ? B : 65535));
+  const int64_t gy = B < 65535 ? B : 65535;
+  const int64_t waves16 = 16LL * 2 * sms;  // 2 CTAs per SM
+  const int64_t gx = std::min((blocks + kHoBlocksPerCta - 1) / kHoBlocksPerCta,
+                              std::max<int64_t>(1, (waves16 + gy - 1) / gy));
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
   const cudaError_t e = launch_dependent(fn, grid, kHoThreads, smem,
                                          reinterpret_cast<cudaStream_t>(stream), a);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

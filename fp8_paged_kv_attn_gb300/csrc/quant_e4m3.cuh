@@ -24,10 +24,15 @@
 // remainder is a multiple of min(ulp(x), ulp(q) ulp(scale)) and so at least
 // the smallest fp32 subnormal when q >= 2^-11, which a quotient next to a
 // boundary is, and scale >= 2^-92), so x / scale = q is representable,
-// RN(x / scale) = q and its code is cvt(q).  Elements left after that (a
-// quotient a few ulps off a boundary) send their group to the correctly
-// rounded division __fdiv_rn, as does every element of a scale whose
-// reciprocals are not normal.
+// RN(x / scale) = q and its code is cvt(q).  A boundary has at most 5
+// significant bits and x at most 8, so x = q scale exactly needs a scale
+// whose significand, trailing zeros dropped, has at most 8 bits: for any
+// other scale the step could never fire and is skipped.  Elements left
+// (a quotient a few ulps off a boundary) take the correctly rounded
+// division __fdiv_rn one by one: a lane loops over its own undecided
+// elements only, so a warp pays for the largest count among its lanes
+// (usually one) rather than for a whole group.  Every element of a scale
+// whose reciprocals are not normal is divided.
 //
 // A power-of-two scale (1.0, the usual uncalibrated one, among them) needs
 // none of this: y = 1 / scale is exact, x y and x / scale are the same real
@@ -47,7 +52,7 @@ constexpr float kGrow = 1.0f + 0x1p-21f;    // 1 + 8u, exact in fp32
 
 // What the quantiser may use for one scale (host-computed, see quant_params).
 constexpr int32_t kQuantBracket = 1;  // y, r_lo, r_hi normal: the two-code bracket holds
-constexpr int32_t kQuantExact = 2;    // scale >= 2^-92 as well: a zero remainder is exact
+constexpr int32_t kQuantExact = 2;    // a short significand, scale >= 2^-92: the remainder step
 constexpr int32_t kQuantPow2 = 4;     // scale a power of two with 1 / scale normal: x / scale = x y
 
 struct QuantParams {
@@ -90,10 +95,12 @@ __device__ __forceinline__ void quantise_words(const uint32_t (&w)[N], const Qua
       diff |= o[i] ^ h[i];
     }
     if (diff == 0) return;
+    uint32_t left[N / 2];  // per word of 4 codes: 0xFF where the ends differ
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) left[i] = __vcmpne4(o[i], h[i]);
     if (qp.mode & kQuantExact) {
       // elements whose codes differ and whose quotient is exact take cvt(q)
       const float2 y2 = make_float2(qp.rcp, qp.rcp);
-      uint32_t left = 0;
 #pragma unroll
       for (int i = 0; i < N / 2; ++i) {
         float x[4];
@@ -108,13 +115,27 @@ __device__ __forceinline__ void quantise_words(const uint32_t (&w)[N], const Qua
           exact |= (fmaf(-q[j], qp.scale, x[j]) == 0.0f ? 0xFFu : 0u) << (8 * j);
         const uint32_t c = static_cast<uint32_t>(f32x2_to_e4m3x2(q[0], q[1])) |
                            (static_cast<uint32_t>(f32x2_to_e4m3x2(q[2], q[3])) << 16);
-        const uint32_t differ = __vcmpne4(o[i], h[i]);
-        const uint32_t take = differ & exact;
+        const uint32_t take = left[i] & exact;
         o[i] = (o[i] & ~take) | (c & take);
-        left |= differ & ~exact;
+        left[i] &= ~exact;
       }
-      if (left == 0) return;
     }
+    // what is left, one element at a time (word i of codes: elements 4i..4i+3,
+    // from input words 2i and 2i + 1)
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      uint32_t pw = left[i] & 0x01010101u;  // bit 8j: element 4i + j
+      while (pw) {
+        const int sh = __ffs(pw) - 1;  // 8 j
+        pw &= pw - 1;
+        const uint32_t ww = (sh & 16) ? w[2 * i + 1] : w[2 * i];
+        const float x = __uint_as_float((sh & 8) ? (ww & 0xFFFF0000u) : (ww << 16));
+        const float d = __fdiv_rn(x, qp.scale);
+        const uint32_t c = static_cast<uint32_t>(f32x2_to_e4m3x2(d, d)) & 0xFFu;
+        o[i] = (o[i] & ~(0xFFu << sh)) | (c << sh);
+      }
+    }
+    return;
   }
 #pragma unroll
   for (int i = 0; i < N / 2; ++i) {
@@ -154,9 +175,14 @@ inline QuantParams quant_params(float scale) {
   qp.rhi = y * kGrow;
   const bool bracket = std::isfinite(y) && std::isfinite(qp.rhi) && qp.rlo >= FLT_MIN;
   int exp2 = 0;
-  const bool pow2 = std::frexp(scale, &exp2) == 0.5f && std::isfinite(y) && y >= FLT_MIN;
+  const float m = std::frexp(scale, &exp2);  // scale = m 2^exp2, m in [0.5, 1)
+  const bool pow2 = m == 0.5f && std::isfinite(y) && y >= FLT_MIN;
+  uint32_t sig = static_cast<uint32_t>(std::ldexp(m, 24));  // the 24-bit significand
+  while (sig != 0 && (sig & 1u) == 0) sig >>= 1;
+  const bool short_sig = sig < 256u;
   qp.mode = pow2 ? kQuantPow2
-                 : bracket ? (kQuantBracket | (scale >= 0x1p-92f ? kQuantExact : 0)) : 0;
+                 : bracket ? (kQuantBracket | (short_sig && scale >= 0x1p-92f ? kQuantExact : 0))
+                           : 0;
   return qp;
 }
 

@@ -73,6 +73,12 @@ EXACT_AMAX = (1.75, 3.5, 5.25, 7.0, 10.5, 224.0)  # amax / 448 exact in fp32
 OTHER_AMAX = (2.0, 0.75, 96.0, 83.0, 81.5, 121.0, 0.0123, 1e5)
 
 
+def _wide_scales():
+    """Seeded scales with full significands (amax / 448 for arbitrary amax)."""
+    rng = np.random.default_rng(23)
+    return [np.float32(a / 448.0) for a in rng.uniform(0.5, 500.0, 24)]
+
+
 def _amax_scales():
     """amax / 448 (fp32, as the host rounds it) for amax values that make it
     exact (a power of two times 1 or 3: many quotients then fall exactly on
@@ -86,12 +92,14 @@ def test_exact_remainder_step():
     e4m3(q).  Checked for every bf16 input and scale (scale >= 2^-92, the
     host's condition for the step); what is left goes to the division.  On
     round amax / 448 scales nothing is left: every differing element is an
-    exact quotient."""
+    exact quotient.  On scales whose significand (trailing zeros dropped)
+    has 8 or more bits no differing element is exact, which is why the
+    kernel skips the step for them."""
     x = _all_bf16_as_f32()
     fin = np.isfinite(x)
     left_round = 0
     with np.errstate(over="ignore", under="ignore", invalid="ignore"):
-        for s in _scales() + _amax_scales():
+        for s in _scales() + _amax_scales() + _wide_scales():
             rcp = np.float32(1.0) / s
             r_lo, r_hi = rcp * SHRINK, rcp * GROW
             if not (np.isfinite(rcp) and np.isfinite(r_hi) and r_lo >= np.finfo(np.float32).tiny):
@@ -113,7 +121,19 @@ def test_exact_remainder_step():
                 left_round += int((~exact).sum())
             else:  # quotients near a boundary but not on it: rare
                 assert (~exact).sum() <= 256, float(s)  # 0.4% of the inputs
+            if _odd_significand(s) >= 256:  # the kernel skips the step: it never fires
+                assert not exact.any(), float(s)
     assert left_round == 0
+
+
+def _odd_significand(s):
+    """The significand of a float32 with its trailing zero bits dropped (the
+    kernel's host test: the remainder step runs only when this is < 256)."""
+    m, _ = np.frexp(np.float64(s))
+    sig = int(m * 2 ** 24)
+    while sig and sig % 2 == 0:
+        sig //= 2
+    return sig
 
 
 def test_exact_remainder_step_is_needed():
@@ -142,3 +162,4 @@ def test_power_of_two_scale_is_a_product():
             got = oracle.e4m3_encode(x * (np.float32(1.0) / s))
             want = oracle.e4m3_encode(x / s)
             assert np.array_equal(got, want), k
+

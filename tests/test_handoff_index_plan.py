@@ -10,8 +10,7 @@ offsets and lengths:
   its addresses and size are multiples of 16 bytes (the bulk-copy rule);
 - the byte count announced to the stage's barrier equals the bytes copied;
 - the decode offsets stay inside the decode pool;
-- the launch grid reaches the last block of any request that fits both
-  tables.
+- the launch grid gives every block group of a request to exactly one CTA.
 """
 import itertools
 
@@ -90,15 +89,23 @@ def test_copy_plan_covers_each_position_once():
 
 
 def test_grid_reaches_every_block():
-    """gx = ceil(ceil(min capacity / 64) / 2) block groups: a request that fits
-    both tables spans at most ceil(min capacity / 64) blocks, counted from
-    its first block."""
+    """The grid's x extent is min(ceil(ceil(min capacity / 64) / 2), about 16
+    waves of CTAs / requests); CTA x takes block groups x, x + gx, ...: every
+    block group of every request that fits both tables falls to exactly one
+    CTA of the request's row."""
+    sms = 152
     for Ps, Pd in itertools.product((16, 32, 64), repeat=2):
-        for src_MP, dst_MP in ((1, 1), (3, 7), (40, 60), (129, 513)):
+        for src_MP, dst_MP in ((1, 1), (3, 7), (40, 60), (129, 513), (2048, 8192)):
             max_tok = min(src_MP * Ps, dst_MP * Pd)
             blocks = -(-max_tok // BLOCK)
-            gx = -(-blocks // BLOCKS_PER_CTA)
-            for f in range(0, max_tok, max(1, max_tok // 37)):
-                n = max_tok - f
-                spanned = (f + n - 1) // BLOCK - f // BLOCK + 1
-                assert spanned <= gx * BLOCKS_PER_CTA
+            for B in (1, 8, 64, 4096):
+                gy = min(B, 65535)
+                gx = min(-(-blocks // BLOCKS_PER_CTA), max(1, -(-(16 * 2 * sms) // gy)))
+                for f in range(0, max_tok, max(1, max_tok // 17)):
+                    n = max_tok - f
+                    groups = -(-((f + n - 1) // BLOCK - f // BLOCK + 1) // BLOCKS_PER_CTA)
+                    owners = [[] for _ in range(groups)]
+                    for bx in range(gx):
+                        for x in range(bx, groups, gx):
+                            owners[x].append(bx)
+                    assert all(len(o) == 1 for o in owners)

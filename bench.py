@@ -6,9 +6,10 @@ request has an 8192-token prompt already quantised into an e4m3 paged cache
 (GQA 32 query / 8 KV heads, head_dim 128, page 16, pool sized for 64
 requests x (8192 + 1000) tokens) -- decoding one token per request per step.
 One step is the whole hot path on one batch:
-    kvq_append (quantise the step's new K/V into the pages)
-    kvq_check_tags (batched page-tag integrity check -> abort mask)
-    kvq_decode_attn (plan + split paged attention with the merge fused).
+    kvq_append_check, one launch of
+        kvq_append (quantise the step's new K/V into the pages) and
+        kvq_check_tags (batched page-tag integrity check -> abort mask)
+    kvq_decode_attn (split paged attention, then the merge of split rows).
 Step i appends generated token (offset + i) mod 1000 of every request, so
 the context during the default run is ~8.6k-8.8k tokens, the mean context of
 the 1000-token generation.  All inputs are seeded synthetic data drawn by
@@ -307,10 +308,11 @@ class StepInputs:
 
 
 class DecodeStep:
-    """One decode step over a packed input row: kvq_append, kvq_check_tags
-    (when `check`; it writes `mask`) and kvq_decode_attn (which skips the
-    requests `mask` flags, when a mask is given), through the library's
-    Python binding.
+    """One decode step over a packed input row: kvq_append and
+    kvq_check_tags in one launch (kvq_append_check, when `check`; the check
+    writes `mask`; kvq_append alone otherwise) and kvq_decode_attn (which
+    skips the requests `mask` flags, when a mask is given), through the
+    library's Python binding.
 
     graph=True captures the step once over static buffers into a CUDA graph
     (the kernels are chained as programmatic dependents, which the
@@ -334,10 +336,13 @@ class DecodeStep:
     # -- the library calls
     def append_check(self, v):
         kvq = self.kvq
-        kvq.kvq_append(self.cache, v["k"], v["v"], self.req_idx, v["pos"], self.bt,
-                       err_word=self.err)
         if self.check:
-            kvq.kvq_check_tags(self.bt, v["lens"], self.P, self.tags, self.exp_tags, self.mask)
+            kvq.kvq_append_check(self.cache, v["k"], v["v"], self.req_idx, v["pos"], self.bt,
+                                 v["lens"], self.tags, self.exp_tags, self.mask,
+                                 err_word=self.err)
+        else:
+            kvq.kvq_append(self.cache, v["k"], v["v"], self.req_idx, v["pos"], self.bt,
+                           err_word=self.err)
 
     def attn(self, v):
         self.kvq.kvq_decode_attn(self.cache, v["q"], self.bt, v["lens"], self.out, self.ws,
@@ -736,7 +741,8 @@ def run_gpu(args, dist, rank, world, local):
                    if flush is None else
                    f"L2 ({flush.l2 >> 20} MB) flushed before every timed step and attention "
                    f"call ({kv_step / 1e6:.0f} MB of KV per step); each timed by its own events"),
-            "step": "kvq_append + kvq_check_tags + kvq_decode_attn",
+            "step": ("kvq_append_check (append + tag check, one launch) + kvq_decode_attn"
+                     if check else "kvq_append + kvq_decode_attn"),
             "launch": "CUDA graph per step (inputs staged with one device copy; the step's "
                       "kernels chained as programmatic dependents)" if graph
                       else "eager library calls",

@@ -18,8 +18,8 @@ LIB = os.path.join(OUT_DIR, "libkvq.so")
 
 SOURCES = ["api.cu", "append.cu", "handoff.cu", "check_tags.cu", "pages.cu", "decode_attn.cu",
            "decode_attn_static.cu", "wq_gemm.cu", "selftest.cu"]
-HEADERS = ["kvq_device.cuh", "kvq_internal.h", "quant_e4m3.cuh", "decode_common.cuh",
-           "decode_attn_mma.cuh"]
+HEADERS = ["kvq_device.cuh", "kvq_internal.h", "quant_e4m3.cuh", "check_body.cuh",
+           "decode_common.cuh", "decode_attn_mma.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--prec-div=true", "--prec-sqrt=true",
               "--ftz=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -23,6 +23,7 @@
 // stream (launch_dependent), so it waits for that work before any access.
 #include <cfloat>
 
+#include "check_body.cuh"
 #include "kvq_internal.h"
 #include "quant_e4m3.cuh"
 
@@ -38,8 +39,10 @@ struct AppendArgs {
   QuantParams kq, vq;  // the quantiser's parameters for k_scale and v_scale
 };
 
+// The append of tokens warp, warp + nwarps, ... where warp counts the warps
+// of CTAs cta, cta + nctas, ... (256 threads a CTA).
 template <bool kFp8, int D>
-__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+__device__ __forceinline__ void append_tokens(const AppendArgs &a, int64_t cta, int64_t nctas) {
   constexpr int kElems = kFp8 ? 16 : 8;    // elements per 16-byte output chunk
   constexpr int kCpr = D / kElems;         // chunks per (token, head) row: a power of 2
   constexpr int kSrcWords = kFp8 ? 2 : 1;  // 16-byte source words per chunk
@@ -48,13 +51,10 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   const int lane = threadIdx.x & 31;
   const int per_tensor = a.H * kCpr;  // chunks of one token's K (or V)
   const int total = 2 * per_tensor;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t nwarps = (nctas * blockDim.x) >> 5;
   const int64_t head_stride = static_cast<int64_t>(a.P) * D;
-  grid_dependency_wait();  // earlier work on the stream is complete and visible
-  allow_dependents();
 
-  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       t < a.n_tokens; t += nwarps) {
+  for (int64_t t = (cta * blockDim.x + threadIdx.x) >> 5; t < a.n_tokens; t += nwarps) {
     const uint4 *ksrc = reinterpret_cast<const uint4 *>(a.k_new + t * a.H * static_cast<int64_t>(D));
     const uint4 *vsrc = reinterpret_cast<const uint4 *>(a.v_new + t * a.H * static_cast<int64_t>(D));
     int req = 0, p = 0, page = 0, slot = 0;
@@ -113,7 +113,31 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
   }
 }
 
+template <bool kFp8, int D>
+__global__ void __launch_bounds__(256) append_kernel(AppendArgs a) {
+  grid_dependency_wait();  // earlier work on the stream is complete and visible
+  allow_dependents();
+  append_tokens<kFp8, D>(a, blockIdx.x, gridDim.x);
+}
+
+// kvq_append_check: CTAs below n_append append, the rest check tags.  The
+// two touch disjoint memory (the append writes pool pages; the check reads
+// the tables, the lengths and the tags and writes the mask), so side by side
+// they give what the two calls give in order, and the check no longer waits
+// for the append on the critical path of a decode step.
+template <bool kFp8, int D>
+__global__ void __launch_bounds__(256) append_check_kernel(AppendArgs a, CheckArgs c,
+                                                           int n_append) {
+  grid_dependency_wait();
+  allow_dependents();
+  if (static_cast<int>(blockIdx.x) < n_append)
+    append_tokens<kFp8, D>(a, blockIdx.x, n_append);
+  else
+    check_requests(c, blockIdx.x - n_append, gridDim.x - n_append);
+}
+
 using AppendFn = void (*)(AppendArgs);
+using AppendCheckFn = void (*)(AppendArgs, CheckArgs, int);
 
 inline AppendFn pick_append(bool fp8, int D) {
   if (D == 64) return fp8 ? append_kernel<true, 64> : append_kernel<false, 64>;
@@ -121,50 +145,99 @@ inline AppendFn pick_append(bool fp8, int D) {
   return nullptr;
 }
 
+inline AppendCheckFn pick_append_check(bool fp8, int D) {
+  if (D == 64) return fp8 ? append_check_kernel<true, 64> : append_check_kernel<false, 64>;
+  if (D == 128) return fp8 ? append_check_kernel<true, 128> : append_check_kernel<false, 128>;
+  return nullptr;
+}
+
 }  // namespace kvq
 
 using namespace kvq;
+
+namespace {
+
+// Checks of kvq_append's arguments and its kernel arguments.
+kvq_status append_args(const kvq_cache *cache, const void *k_new, const void *v_new,
+                       const int32_t *req_idx, const int32_t *pos, int32_t n_tokens,
+                       const int32_t *block_table, int32_t B, int32_t MP, uint32_t *err_word,
+                       AppendArgs *a) {
+  kvq_status st = validate_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n_tokens < 0 || B < 0 || MP <= 0) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (!k_new || !v_new || !req_idx || !pos || !block_table || B == 0))
+    return KVQ_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (!aligned16(k_new) || !aligned16(v_new))) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens > 0 && static_cast<int64_t>(MP) * cache->page_size > INT32_MAX)
+    return KVQ_ERR_INVALID_ARG;
+  a->k_pool = cache->k_pool;
+  a->v_pool = cache->v_pool;
+  a->k_new = static_cast<const uint16_t *>(k_new);
+  a->v_new = static_cast<const uint16_t *>(v_new);
+  a->req_idx = req_idx;
+  a->pos = pos;
+  a->block_table = block_table;
+  a->err_word = err_word;
+  a->n_tokens = n_tokens;
+  a->num_pages = cache->num_pages;
+  a->P = cache->page_size;
+  a->H = cache->num_kv_heads;
+  a->B = B;
+  a->MP = MP;
+  a->kq = quant_params(cache->k_scale);
+  a->vq = quant_params(cache->v_scale);
+  return KVQ_OK;
+}
+
+constexpr int kAppendThreads = 256;
+
+// CTAs for n tokens: a warp per token, at most 16 CTAs per SM.
+int append_ctas(int64_t n_tokens, int sms) {
+  const int64_t want = (n_tokens + kAppendThreads / 32 - 1) / (kAppendThreads / 32);
+  return static_cast<int>(want < 16LL * sms ? want : 16LL * sms);
+}
+
+}  // namespace
 
 extern "C" kvq_status kvq_append(const kvq_cache *cache, const void *k_new, const void *v_new,
                                  const int32_t *req_idx, const int32_t *pos, int32_t n_tokens,
                                  const int32_t *block_table, int32_t B, int32_t MP,
                                  uint32_t *err_word, kvq_stream_t stream) {
-  kvq_status st = validate_cache(cache);
-  if (st != KVQ_OK) return st;
-  if (n_tokens < 0 || B < 0 || MP <= 0) return KVQ_ERR_INVALID_ARG;
-  if (n_tokens == 0) return KVQ_OK;
-  if (!k_new || !v_new || !req_idx || !pos || !block_table || B == 0)
-    return KVQ_ERR_INVALID_ARG;
-  if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(MP) * cache->page_size > INT32_MAX) return KVQ_ERR_INVALID_ARG;
-
   AppendArgs a;
-  a.k_pool = cache->k_pool;
-  a.v_pool = cache->v_pool;
-  a.k_new = static_cast<const uint16_t *>(k_new);
-  a.v_new = static_cast<const uint16_t *>(v_new);
-  a.req_idx = req_idx;
-  a.pos = pos;
-  a.block_table = block_table;
-  a.err_word = err_word;
-  a.n_tokens = n_tokens;
-  a.num_pages = cache->num_pages;
-  a.P = cache->page_size;
-  a.H = cache->num_kv_heads;
-  a.B = B;
-  a.MP = MP;
-  a.kq = quant_params(cache->k_scale);
-  a.vq = quant_params(cache->v_scale);
-
-  const bool fp8 = cache->kv_dtype == KVQ_KV_E4M3;
-  const AppendFn fn = pick_append(fp8, cache->head_dim);
-  if (!fn) return KVQ_ERR_UNSUPPORTED;
-  constexpr int threads = 256, warps = threads / 32;
+  const kvq_status st =
+      append_args(cache, k_new, v_new, req_idx, pos, n_tokens, block_table, B, MP, err_word, &a);
+  if (st != KVQ_OK) return st;
+  if (n_tokens == 0) return KVQ_OK;
+  const AppendFn fn = pick_append(cache->kv_dtype == KVQ_KV_E4M3, cache->head_dim);
   int sms = 0;
   if (device_sm_count(&sms) != KVQ_OK) return KVQ_ERR_CUDA;
-  const int64_t want = (static_cast<int64_t>(n_tokens) + warps - 1) / warps;  // warp per token
-  const int blocks = static_cast<int>(want < 16LL * sms ? want : 16LL * sms);
-  const cudaError_t e =
-      launch_dependent(fn, blocks, threads, 0, reinterpret_cast<cudaStream_t>(stream), a);
+  const cudaError_t e = launch_dependent(fn, append_ctas(n_tokens, sms), kAppendThreads, 0,
+                                         reinterpret_cast<cudaStream_t>(stream), a);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+extern "C" kvq_status kvq_append_check(const kvq_cache *cache, const void *k_new,
+                                       const void *v_new, const int32_t *req_idx,
+                                       const int32_t *pos, int32_t n_tokens,
+                                       const int32_t *block_table, int32_t B, int32_t MP,
+                                       const int32_t *seq_lens, const uint32_t *page_tags,
+                                       const uint32_t *expected_tags, uint8_t *abort_mask,
+                                       uint32_t *err_word, kvq_stream_t stream) {
+  AppendArgs a;
+  const kvq_status st =
+      append_args(cache, k_new, v_new, req_idx, pos, n_tokens, block_table, B, MP, err_word, &a);
+  if (st != KVQ_OK) return st;
+  if (B > 0 && (!block_table || !seq_lens || !page_tags || !expected_tags || !abort_mask))
+    return KVQ_ERR_INVALID_ARG;
+  if (n_tokens == 0 && B == 0) return KVQ_OK;
+  CheckArgs c{block_table, seq_lens, page_tags, expected_tags, abort_mask, B, MP,
+              cache->page_size, cache->num_pages};
+  const AppendCheckFn fn = pick_append_check(cache->kv_dtype == KVQ_KV_E4M3, cache->head_dim);
+  int sms = 0;
+  if (device_sm_count(&sms) != KVQ_OK) return KVQ_ERR_CUDA;
+  const int n_append = n_tokens > 0 ? append_ctas(n_tokens, sms) : 0;
+  const int n_check = B < 32 * sms ? B : 32 * sms;
+  const cudaError_t e = launch_dependent(fn, n_append + n_check, kAppendThreads, 0,
+                                         reinterpret_cast<cudaStream_t>(stream), a, c, n_append);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -8,48 +8,19 @@
 // a separate batched pass and is not fused into the attention kernel (fusing
 // it would race between thread groups).
 //
-// One CTA per request (grid-strided): its threads stride over the request's
-// logical pages, compare the recorded tag with the page's current tag, and a
-// block-wide OR gives the request's abort flag.  Integer work only: the
-// result is exact by construction.  Launched as a programmatic dependent of
-// the work before it on the stream, so in a decode step its launch overlaps
-// the append kernel.
+// One CTA per request (grid-strided; check_body.cuh).  Launched as a
+// programmatic dependent of the work before it on the stream, so in a decode
+// step its launch overlaps the append kernel; kvq_append_check (append.cu)
+// runs the same work beside the append in one launch.
+#include "check_body.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
 
-struct CheckArgs {
-  const int32_t *block_table, *seq_lens;
-  const uint32_t *page_tags, *expected_tags;
-  uint8_t *abort_mask;
-  int32_t B, MP, P, num_pages;
-};
-
 __global__ void __launch_bounds__(256) check_tags_kernel(CheckArgs a) {
-  const int64_t cap = static_cast<int64_t>(a.MP) * a.P;
   grid_dependency_wait();  // earlier work on the stream is complete and visible
   allow_dependents();
-  for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-    const int L = a.seq_lens[b];
-    int bad = (L < 0 || L > cap) ? 1 : 0;
-    if (!bad) {
-      const int n_pages = (L + a.P - 1) / a.P;
-      const int32_t *bt = a.block_table + static_cast<int64_t>(b) * a.MP;
-      const uint32_t *exp = a.expected_tags + static_cast<int64_t>(b) * a.MP;
-#pragma unroll 4
-      for (int i = threadIdx.x; i < n_pages; i += blockDim.x) {
-        const int page = __ldg(bt + i);
-        const uint32_t want = __ldg(exp + i);
-        if (page < 0 || page >= a.num_pages) {
-          bad = 1;
-        } else if (__ldg(a.page_tags + page) != want) {
-          bad = 1;
-        }
-      }
-    }
-    bad = __syncthreads_or(bad);
-    if (threadIdx.x == 0) a.abort_mask[b] = static_cast<uint8_t>(bad ? 1 : 0);
-  }
+  check_requests(a, blockIdx.x, gridDim.x);
 }
 
 }  // namespace kvq

@@ -42,9 +42,9 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_WORKSPACE", 3: "KVQ
           4: "KVQ_ERR_UNSUPPORTED"}
 
 # every symbol include/kvq.h declares
-EXPORTS = ("kvq_append", "kvq_handoff_pages", "kvq_check_tags", "kvq_pages_update", "kvq_decode_attn_workspace_size",
-           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_wq_gemm", "kvq_selftest_wait",
-           "kvq_status_string")
+EXPORTS = ("kvq_append", "kvq_append_check", "kvq_handoff_pages", "kvq_check_tags",
+           "kvq_pages_update", "kvq_decode_attn_workspace_size", "kvq_decode_attn",
+           "kvq_decode_attn_static", "kvq_wq_gemm", "kvq_selftest_wait", "kvq_status_string")
 STATIC_SCRATCH_BYTES = 64 << 20
 
 
@@ -83,6 +83,8 @@ def load(build_if_missing: bool = True):
     cp = ctypes.POINTER(CCache)
     L.kvq_append.argtypes = [cp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp]
     L.kvq_append.restype = ctypes.c_int
+    L.kvq_append_check.argtypes = [cp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp]
+    L.kvq_append_check.restype = ctypes.c_int
     L.kvq_handoff_pages.argtypes = [cp, vp, i32, cp, vp, i32, vp, vp, i32, vp, vp]
     L.kvq_handoff_pages.restype = ctypes.c_int
     L.kvq_check_tags.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp, vp, vp]
@@ -194,6 +196,32 @@ def kvq_append(cache: KVCache, k_new, v_new, req_idx, pos, block_table, err_word
                       _dev(block_table, "block_table", I32, 2), B, MP,
                       _dev(err_word, "err_word", U32), _stream(stream))
     _check("kvq_append", st)
+
+
+def kvq_append_check(cache: KVCache, k_new, v_new, req_idx, pos, block_table, seq_lens,
+                     page_tags, expected_tags, abort_mask, err_word=None, stream=None) -> None:
+    """kvq_append and kvq_check_tags (the cache's page size and page count)
+    in one launch, with the same results as the two calls."""
+    L = load()
+    c = cache.c()
+    N = int(req_idx.shape[0])
+    B, MP = block_table.shape
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        if tuple(t.shape) != (N, c.num_kv_heads, c.head_dim):
+            raise ValueError(f"{n} must be [{N}, {c.num_kv_heads}, {c.head_dim}]")
+    if tuple(expected_tags.shape) != (B, MP) or abort_mask.shape[0] != B or \
+            seq_lens.shape[0] != B or page_tags.shape[0] != c.num_pages:
+        raise ValueError("expected_tags must be [B, MP], seq_lens and abort_mask [B], "
+                         "page_tags [num_pages]")
+    st = L.kvq_append_check(ctypes.byref(c), _dev(k_new, "k_new", BF16, 3),
+                            _dev(v_new, "v_new", BF16, 3), _dev(req_idx, "req_idx", I32, 1),
+                            _dev(pos, "pos", I32, 1), N, _dev(block_table, "block_table", I32, 2),
+                            B, MP, _dev(seq_lens, "seq_lens", I32, 1),
+                            _dev(page_tags, "page_tags", U32, 1),
+                            _dev(expected_tags, "expected_tags", U32, 2),
+                            _dev(abort_mask, "abort_mask", U8, 1), _dev(err_word, "err_word", U32),
+                            _stream(stream))
+    _check("kvq_append_check", st)
 
 
 def kvq_handoff_pages(src: KVCache, src_block_table, dst: KVCache, dst_block_table, count,

@@ -111,6 +111,28 @@ KVQ_API kvq_status kvq_append(const kvq_cache *cache, const void *k_new, const v
                       const int32_t *block_table, int32_t B, int32_t MP,
                       uint32_t *err_word, kvq_stream_t stream);
 
+/* kvq_append and kvq_check_tags of one decode step in one launch: the same
+ * effects, error bits and results as
+ *     kvq_append(cache, k_new, v_new, req_idx, pos, n_tokens, block_table, B, MP,
+ *                err_word, stream);
+ *     kvq_check_tags(block_table, B, MP, seq_lens, cache->page_size, page_tags,
+ *                    cache->num_pages, expected_tags, abort_mask, stream);
+ * with every argument as documented there ([GUARD]: the check is a separate
+ * batched pass before attention reads the cache; it stays one, running
+ * beside the append instead of after it).  The append writes only pool
+ * pages and the check only abort_mask, and neither reads what the other
+ * writes, so the order of the two calls does not change either result; the
+ * one launch takes the check off a decode step's critical path.  Argument
+ * errors are those of the two calls (KVQ_ERR_INVALID_ARG for a null check
+ * array when B > 0); n_tokens == 0 and B == 0 is a no-op. */
+KVQ_API kvq_status kvq_append_check(const kvq_cache *cache, const void *k_new,
+                                    const void *v_new, const int32_t *req_idx,
+                                    const int32_t *pos, int32_t n_tokens,
+                                    const int32_t *block_table, int32_t B, int32_t MP,
+                                    const int32_t *seq_lens, const uint32_t *page_tags,
+                                    const uint32_t *expected_tags, uint8_t *abort_mask,
+                                    uint32_t *err_word, kvq_stream_t stream);
+
 /* Prefill -> decode handoff of whole prompts ([KVQ]: the prefill side keeps
  * its KV cache in BF16, the decode side stores it as e4m3, so a prompt is
  * converted once when decode takes it over).  `src` is a paged BF16 cache

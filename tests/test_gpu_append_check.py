@@ -189,3 +189,79 @@ def test_check_edges(kvq, oracle_mod):
     ref = oracle_mod.check_tags(bt, lens, w.P, w.page_tags, exp)
     assert np.array_equal(got, ref)
     assert got[:6].tolist() == [0, 1, 1, 1, 0, 1]
+
+
+# ----------------------------------------------------------------------------
+# append and check in one launch
+# ----------------------------------------------------------------------------
+
+def _two_ways(kvq, w, kv_dtype, k, v, req, pos, bt, lens, tags, exp):
+    """The step's append and tag check as two calls and as one launch, each
+    on its own sentinel-filled pools: (pools, mask, error word) of both."""
+    res = []
+    for fused in (False, True):
+        fp8 = kv_dtype == kvq.KV_E4M3
+        dt = torch.uint8 if fp8 else torch.int16
+        fill = SENTINEL if fp8 else (SENTINEL | (SENTINEL << 8)) - 65536
+        kp = torch.full(w.pool_shape(), fill, dtype=dt, device="cuda")
+        vp = kp.clone()
+        if not fp8:
+            kp, vp = kp.view(torch.bfloat16), vp.view(torch.bfloat16)
+        cache = kvq.KVCache(kp, vp, 0.037, 0.041)
+        mask = torch.full((w.B,), 7, dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        args = (dev_bf16(k), dev_bf16(v), dev(req), dev(pos), dev(bt))
+        if fused:
+            kvq.kvq_append_check(cache, *args, dev(lens), dev_u32(tags), dev_u32(exp), mask,
+                                 err_word=err)
+        else:
+            kvq.kvq_append(cache, *args, err_word=err)
+            kvq.kvq_check_tags(dev(bt), dev(lens), w.P, dev_u32(tags), dev_u32(exp), mask)
+        torch.cuda.synchronize()
+        view = torch.uint8 if fp8 else torch.int16
+        res.append((kp.view(view).cpu().numpy(), vp.view(view).cpu().numpy(),
+                    mask.cpu().numpy(), int(err.item())))
+    return res
+
+
+@pytest.mark.parametrize("D,kv", [(128, "e4m3"), (64, "e4m3"), (128, "bf16")])
+def test_append_check_matches_two_calls(kvq, oracle_mod, D, kv):
+    """kvq_append_check gives what kvq_append then kvq_check_tags give: the
+    same pool bytes, the same mask (the oracle's) and the same error word, on
+    37 ragged requests with stale tags injected."""
+    w = inputs.ragged(seed=45, B=37, total=20000, lo=1, hi=2000, Hq=8, Hkv=8, D=D, P=16)
+    kv_dtype = kvq.KV_E4M3 if kv == "e4m3" else kvq.KV_BF16
+    _, k, v, req, pos = w.step_inputs(0)
+    lens = w.seq_lens_after(0)
+    exp = w.expected_tags.copy()
+    for b in (3, 17, 30):
+        exp[b, int(lens[b]) // w.P // 2] ^= 5
+    (k0, v0, m0, e0), (k1, v1, m1, e1) = _two_ways(kvq, w, kv_dtype, k, v, req, pos,
+                                                   w.block_table, lens, w.page_tags, exp)
+    ref = oracle_mod.check_tags(w.block_table, lens, w.P, w.page_tags, exp)
+    assert np.array_equal(m0, ref) and np.array_equal(m1, ref)
+    assert sorted(np.nonzero(ref)[0].tolist()) == [3, 17, 30]
+    assert np.array_equal(k0, k1) and np.array_equal(v0, v1)
+    assert e0 == e1 == 0
+
+
+def test_append_check_errors_match_two_calls(kvq, oracle_mod):
+    """Bad request, position and page in the append, impossible lengths and a
+    page id outside the pool in the check: the same error bits, bytes and
+    mask from the one launch as from the two calls."""
+    w = inputs.ragged(seed=44, B=9, total=3000, lo=1, hi=900, Hq=8, Hkv=8, D=64, P=16)
+    _, k, v, req, pos = w.step_inputs(0)
+    req, pos = req.copy(), pos.copy()
+    req[1], pos[2], pos[4] = w.B, -1, w.MP * w.P
+    lens = w.seq_lens_after(0).copy()
+    lens[0], lens[5] = -5, w.MP * w.P + 1
+    bt = w.block_table.copy()
+    bt[3, 0] = w.num_pages
+    bt[6, pos[6] // w.P] = w.num_pages + 3  # the page request 6's token goes to
+    (k0, v0, m0, e0), (k1, v1, m1, e1) = _two_ways(kvq, w, kvq.KV_E4M3, k, v, req, pos, bt,
+                                                   lens, w.page_tags, w.expected_tags)
+    ref = oracle_mod.check_tags(bt, lens, w.P, w.page_tags, w.expected_tags)
+    assert np.array_equal(m0, ref) and np.array_equal(m1, ref)
+    assert m1[[0, 3, 5, 6]].tolist() == [1, 1, 1, 1]
+    assert np.array_equal(k0, k1) and np.array_equal(v0, v1)
+    assert e0 == e1 and e1 & kvq.ERRBIT_REQ and e1 & kvq.ERRBIT_POS and e1 & kvq.ERRBIT_PAGE

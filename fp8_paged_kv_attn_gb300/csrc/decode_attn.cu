@@ -498,24 +498,26 @@ __device__ __forceinline__ void merge_parts(const CombineItem &it, int p0, int s
 //   out = v_scale * sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
 // A part whose maximum is -inf carries no weight and its values are not used;
 // a row with a part that met a page outside the pool (l < 0) is written as
-// zeros.  The work items are all output rows (row, query head), in two
-// passes that read each row's descriptor: output rows of rows in more than
-// kWarpMergeMax parts, a CTA each (a row of a short batch can have hundreds
-// of parts), its kSubsets warps folding every kSubsets-th part and warp 0
-// folding their results from shared memory; then output rows of rows in 2 to
-// kWarpMergeMax parts, a warp each.  A CTA (warp) loads the descriptors of
-// all its items at once.  Two builds: kSubsets = 16 warps uncapped (more of a
-// long row's loads in flight) for grids of at most #SMs CTAs, and 8 warps
-// capped at 64 registers (4 CTAs per SM) otherwise, small enough that one
-// CTA becomes resident beside a running split CTA and is waiting when the
-// split grid ends.
+// zeros.  The work items are all output rows (row, query head); a CTA takes
+// items blockIdx, blockIdx + grid, ... in passes of 32.  In a pass lane j of
+// warp 0 loads item j's row descriptor (one round trip for the pass) and
+// sorts the item into one of two lists: rows in more than kWarpMergeMax
+// parts (a row of a short batch can have hundreds), merged by the whole CTA
+// one item at a time, its kSubsets warps folding every kSubsets-th part and
+// warp 0 folding their results from shared memory; and rows in 2 to
+// kWarpMergeMax parts, a warp each.  Two builds: kSubsets = 16 warps uncapped
+// (more of a long row's loads in flight) for grids of at most #SMs CTAs, and
+// 8 warps capped at 64 registers (4 CTAs per SM) otherwise, small enough
+// that one CTA becomes resident beside a running split CTA and is waiting
+// when the split grid ends.
 template <int kMinBlocks, int kSubsets>
 __global__ void __launch_bounds__(32 * kSubsets, kMinBlocks) combine_kernel(CombineArgs a) {
   __shared__ float s_m[kSubsets], s_den[kSubsets];
   __shared__ float4 s_acc[kSubsets][32];
   __shared__ int s_bad[kSubsets];
-  __shared__ int4 s_items[32];  // (item, first CTA, parts, request)
-  __shared__ int s_n;
+  __shared__ int4 s_items[32];  // (item, first CTA, parts, request): CTA-merged
+  __shared__ int4 s_witems[32];  // the same for warp-merged items
+  __shared__ int s_n, s_nw;
   grid_dependency_wait();
   allow_dependents();  // e.g. the next step's append may be scheduled
   const int tid = threadIdx.x, sub = tid >> 5, lane = tid & 31;
@@ -527,23 +529,27 @@ __global__ void __launch_bounds__(32 * kSubsets, kMinBlocks) combine_kernel(Comb
   const int GD = a.G * a.D;
   const bool active = 4 * lane < a.D;
 
-  // ---- rows of many parts: a CTA per output row.  Lane j of warp 0 looks
-  // at item blockIdx + (base + j) * grid and lists it, with its row's
-  // descriptor, when the row has more than kWarpMergeMax parts; then the CTA
-  // merges the listed items one by one.
   for (int64_t base = 0; blockIdx.x + base * gridDim.x < nout; base += 32) {
     if (sub == 0) {
       const int64_t item = blockIdx.x + (base + lane) * gridDim.x;
       int4 d = make_int4(0, 0, 0, 0);
       if (item < nout) d = __ldcg(a.desc + item / heads_per_row);
-      const bool mine = d.y > kWarpMergeMax;
-      const unsigned bal = __ballot_sync(0xffffffffu, mine);
-      if (mine)
-        s_items[__popc(bal & ((1u << lane) - 1))] = make_int4(static_cast<int>(item), d.x, d.y, d.z);
-      if (lane == 0) s_n = __popc(bal);
+      const int4 li = make_int4(static_cast<int>(item), d.x, d.y, d.z);
+      const bool big = d.y > kWarpMergeMax, small = d.y >= 2 && d.y <= kWarpMergeMax;
+      const unsigned bb = __ballot_sync(0xffffffffu, big);
+      const unsigned bs = __ballot_sync(0xffffffffu, small);
+      const unsigned below = (1u << lane) - 1;
+      if (big) s_items[__popc(bb & below)] = li;
+      if (small) s_witems[__popc(bs & below)] = li;
+      if (lane == 0) {
+        s_n = __popc(bb);
+        s_nw = __popc(bs);
+      }
     }
     __syncthreads();
-    const int n = s_n;
+    const int n = s_n, nw = s_nw;
+
+    // ---- rows of many parts: the whole CTA per output row
     for (int k = 0; k < n; ++k) {
       const int4 li = s_items[k];
       const int row = li.x / heads_per_row;
@@ -592,26 +598,13 @@ __global__ void __launch_bounds__(32 * kSubsets, kMinBlocks) combine_kernel(Comb
       }
       __syncthreads();  // s_acc, s_m, s_den, s_bad are reused by the next item
     }
-    __syncthreads();  // every warp has read s_n before warp 0 lists the next pass
-  }
 
-  // ---- rows of 2..kWarpMergeMax parts: a warp per output row.  Lane j looks
-  // at item wid + (base + j) * nwarps; the warp merges the listed ones.
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kSubsets;
-  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kSubsets + sub;
-  for (int64_t base = 0; wid + base * nwarps < nout; base += 32) {
-    const int64_t item = wid + (base + lane) * nwarps;
-    int4 d = make_int4(0, 0, 0, 0);
-    if (item < nout) d = __ldcg(a.desc + item / heads_per_row);
-    unsigned todo = __ballot_sync(0xffffffffu, d.y >= 2 && d.y <= kWarpMergeMax);
-    while (todo) {
-      const int j = __ffs(todo) - 1;
-      todo &= todo - 1;
-      const int it_idx = static_cast<int>(__shfl_sync(0xffffffffu, item, j));
-      const int4 dj = make_int4(__shfl_sync(0xffffffffu, d.x, j), __shfl_sync(0xffffffffu, d.y, j),
-                                __shfl_sync(0xffffffffu, d.z, j), 0);
-      const int row = it_idx / heads_per_row;
-      const CombineItem it = combine_item(a, row, dj, it_idx % heads_per_row, slot_floats, kpart);
+    // ---- rows of 2..kWarpMergeMax parts: a warp per output row
+    for (int k = sub; k < nw; k += kSubsets) {
+      const int4 li = s_witems[k];
+      const int row = li.x / heads_per_row;
+      const CombineItem it = combine_item(a, row, make_int4(li.y, li.z, li.w, 0),
+                                          li.x % heads_per_row, slot_floats, kpart);
       float M = -INFINITY, den = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       bool bad = false;
@@ -624,6 +617,7 @@ __global__ void __launch_bounds__(32 * kSubsets, kMinBlocks) combine_kernel(Comb
                 : make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
       }
     }
+    __syncthreads();  // the lists are rewritten by the next pass
   }
 }
 

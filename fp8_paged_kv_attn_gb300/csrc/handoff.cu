@@ -135,65 +135,65 @@ __global__ void __launch_bounds__(kHoThreads, 2) handoff_kernel(HandoffArgs a) {
       }
       if (n == 0) continue;
       // positions fit in 32 bits from here on: both tables hold at most
-      // INT32_MAX tokens (checked by the host)
-      // block groups blockIdx.x, + gridDim.x, ... of the request
+      // INT32_MAX tokens (checked by the host).  Block groups blockIdx.x,
+      // blockIdx.x + gridDim.x, ... of the request are this CTA's.
       const int blk_first = f / kHoBlock, blk_last = (f + n - 1) / kHoBlock;
       for (int x = blockIdx.x; ok && blk_first + x * kHoBlocksPerCta <= blk_last;
-           x += gridDim.x)
-      for (int k = 0; ok && k < kHoBlocksPerCta && blk_first + x * kHoBlocksPerCta + k <= blk_last;
-           ++k) {
-        const int blk = blk_first + x * kHoBlocksPerCta + k;
-        const int lo = max(blk * kHoBlock, f), hi = min(blk * kHoBlock + kHoBlock, f + n);
-        // positions blk*64 + lane and + 32: the decode-pool offset (head 0;
-        // -1: not stored) and, where a prefill page's piece starts, the copy
-        int64_t doff[2], soff[2];
-        int run[2];
-        uint32_t tx = 0;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int p = blk * kHoBlock + lane + 32 * r;
-          doff[r] = -1;
-          soff[r] = 0;
-          run[r] = 0;
-          if (p >= lo && p < hi) {
-            const int sp = __ldg(a.src_bt + static_cast<int64_t>(b) * a.src_MP + p / a.Ps);
-            const int dp = __ldg(a.dst_bt + static_cast<int64_t>(b) * a.dst_MP + p / a.Pd);
-            const bool src_ok = sp >= 0 && sp < a.src_pages;
-            if (!src_ok || dp < 0 || dp >= a.dst_pages) report(a.err_word, KVQ_ERRBIT_PAGE);
-            else doff[r] = (static_cast<int64_t>(dp) * a.H * a.Pd + p % a.Pd) * D;
-            if (src_ok && (p == lo || p % a.Ps == 0)) {
-              run[r] = min(hi, (p / a.Ps + 1) * a.Ps) - p;
-              soff[r] = (static_cast<int64_t>(sp) * a.H * a.Ps + p % a.Ps) * D;
-              tx += 2u * run[r] * C::ROW;
+           x += gridDim.x) {
+        const int blk_end = min(blk_first + (x + 1) * kHoBlocksPerCta - 1, blk_last);
+        for (int blk = blk_first + x * kHoBlocksPerCta; ok && blk <= blk_end; ++blk) {
+          const int lo = max(blk * kHoBlock, f), hi = min(blk * kHoBlock + kHoBlock, f + n);
+          // positions blk*64 + lane and + 32: the decode-pool offset (head 0;
+          // -1: not stored) and, where a prefill page's piece starts, the copy
+          int64_t doff[2], soff[2];
+          int run[2];
+          uint32_t tx = 0;
+  #pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int p = blk * kHoBlock + lane + 32 * r;
+            doff[r] = -1;
+            soff[r] = 0;
+            run[r] = 0;
+            if (p >= lo && p < hi) {
+              const int sp = __ldg(a.src_bt + static_cast<int64_t>(b) * a.src_MP + p / a.Ps);
+              const int dp = __ldg(a.dst_bt + static_cast<int64_t>(b) * a.dst_MP + p / a.Pd);
+              const bool src_ok = sp >= 0 && sp < a.src_pages;
+              if (!src_ok || dp < 0 || dp >= a.dst_pages) report(a.err_word, KVQ_ERRBIT_PAGE);
+              else doff[r] = (static_cast<int64_t>(dp) * a.H * a.Pd + p % a.Pd) * D;
+              if (src_ok && (p == lo || p % a.Ps == 0)) {
+                run[r] = min(hi, (p / a.Ps + 1) * a.Ps) - p;
+                soff[r] = (static_cast<int64_t>(sp) * a.H * a.Ps + p % a.Ps) * D;
+                tx += 2u * run[r] * C::ROW;
+              }
             }
           }
-        }
-        tx = __reduce_add_sync(0xffffffffu, tx);
-        for (int h = 0; h < a.H; ++h, ++g) {
-          const int slot = g % C::NS;
-          bool waited = true;
-          if (lane == 0 && g >= C::NS)
-            waited = ho_wait(ctl, &ctl.empty[slot], ((g / C::NS) - 1) & 1, a.err_word);
-          ok = __shfl_sync(0xffffffffu, waited ? 1 : 0, 0) != 0 &&
-               !*reinterpret_cast<volatile int32_t *>(&ctl.fail);
-          if (!ok) break;
-          int64_t *hd = hdr + slot * kHoBlock;
-          hd[lane] = doff[0] < 0 ? -1 : doff[0] + h * dst_head;
-          hd[lane + 32] = doff[1] < 0 ? -1 : doff[1] + h * dst_head;
-          __syncwarp();
-          if (lane == 0) {
-            ctl.live[slot] = 1;
-            mbar_arrive_expect_tx(&ctl.full[slot], tx);
-          }
-          __syncwarp();
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            if (run[r] == 0) continue;
-            uint8_t *kdst = rows + slot * C::STAGE + (lane + 32 * r) * C::ROW;
-            const int64_t src = soff[r] + h * src_head;
-            const uint32_t bytes = static_cast<uint32_t>(run[r]) * C::ROW;
-            bulk_g2s_hint(kdst, a.src_k + src, bytes, &ctl.full[slot], pol);
-            bulk_g2s_hint(kdst + C::TILE, a.src_v + src, bytes, &ctl.full[slot], pol);
+          tx = __reduce_add_sync(0xffffffffu, tx);
+          for (int h = 0; h < a.H; ++h, ++g) {
+            const int slot = g % C::NS;
+            bool waited = true;
+            if (lane == 0 && g >= C::NS)
+              waited = ho_wait(ctl, &ctl.empty[slot], ((g / C::NS) - 1) & 1, a.err_word);
+            ok = __shfl_sync(0xffffffffu, waited ? 1 : 0, 0) != 0 &&
+                 !*reinterpret_cast<volatile int32_t *>(&ctl.fail);
+            if (!ok) break;
+            int64_t *hd = hdr + slot * kHoBlock;
+            hd[lane] = doff[0] < 0 ? -1 : doff[0] + h * dst_head;
+            hd[lane + 32] = doff[1] < 0 ? -1 : doff[1] + h * dst_head;
+            __syncwarp();
+            if (lane == 0) {
+              ctl.live[slot] = 1;
+              mbar_arrive_expect_tx(&ctl.full[slot], tx);
+            }
+            __syncwarp();
+  #pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              if (run[r] == 0) continue;
+              uint8_t *kdst = rows + slot * C::STAGE + (lane + 32 * r) * C::ROW;
+              const int64_t src = soff[r] + h * src_head;
+              const uint32_t bytes = static_cast<uint32_t>(run[r]) * C::ROW;
+              bulk_g2s_hint(kdst, a.src_k + src, bytes, &ctl.full[slot], pol);
+              bulk_g2s_hint(kdst + C::TILE, a.src_v + src, bytes, &ctl.full[slot], pol);
+            }
           }
         }
       }

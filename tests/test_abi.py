@@ -55,6 +55,9 @@ def test_bad_cache_rejected_before_launch(kw, want):
     c = _cache(**kw)
     st = lib.kvq_append(ctypes.byref(c), 16, 16, 16, 16, 1, 16, 1, 4, None, None)
     assert st == want
+    st = lib.kvq_append_check(ctypes.byref(c), 16, 16, 16, 16, 1, 16, 1, 4, 16, 16, 16, 16,
+                              None, None)
+    assert st == want
     st = lib.kvq_decode_attn(ctypes.byref(c), 16, 1, 4, 16, 4, 16, None, 0.1, 16, 256, 1 << 30,
                              None, None)
     assert st == want
@@ -87,3 +90,15 @@ def test_bad_call_arguments_rejected_before_launch():
     assert lib.kvq_check_tags(16, 1, 0, 16, 16, 16, 8, 16, 16, None) == 1
     assert lib.kvq_check_tags(None, 1, 4, 16, 16, 16, 8, 16, 16, None) == 1
     assert lib.kvq_check_tags(None, 0, 4, None, 16, None, 8, None, None, None) == 0
+    # append and check in one launch: either half's argument errors; nothing to
+    # do at all is a no-op
+    assert lib.kvq_append_check(ctypes.byref(c), None, 16, 16, 16, 1, 16, 1, 4, 16, 16, 16, 16,
+                                None, None) == 1
+    assert lib.kvq_append_check(ctypes.byref(c), 16, 16, 16, 16, 1, 16, 1, 4, None, 16, 16, 16,
+                                None, None) == 1
+    assert lib.kvq_append_check(ctypes.byref(c), 16, 16, 16, 16, 1, 16, 1, 4, 16, 16, 16, None,
+                                None, None) == 1
+    assert lib.kvq_append_check(ctypes.byref(c), 16, 16, 16, 16, 1, 16, 1, 0, 16, 16, 16, 16,
+                                None, None) == 1
+    assert lib.kvq_append_check(ctypes.byref(c), None, None, None, None, 0, None, 0, 4, None,
+                                None, None, None, None, None) == 0

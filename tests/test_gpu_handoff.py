@@ -103,6 +103,21 @@ def test_handoff_whole_pool(kvq, src_P, dst_P, D, dtype):
     assert np.array_equal(gv, ov), "V pool differs from the oracle"
 
 
+@pytest.mark.parametrize("Hkv,D,src_P,dst_P", [(1, 64, 16, 64), (2, 128, 32, 16), (4, 64, 64, 32)])
+def test_handoff_head_counts(kvq, Hkv, D, src_P, dst_P):
+    """One, two and four kv heads (a stage is one head of a 64-token block):
+    the whole decode pool byte for byte."""
+    h = inputs.handoff(seed=61 + Hkv, lens=[700, 1, 129, 64, 1000], first=[0, 3, 63, 64, 5],
+                       Hkv=Hkv, D=D, src_P=src_P, dst_P=dst_P, decode_room=20,
+                       dst_pool_factor=1.3)
+    src, hk, hv, ks, vs = _src_pools(kvq, h, range(h.B))
+    _, gk, gv, gerr = _run(kvq, h, kvq.KV_E4M3, src, ks, vs)
+    ok, ov, oerr = _oracle(h, oracle.KV_E4M3, hk, hv, ks, vs)
+    assert gerr == 0 and oerr == 0
+    assert np.array_equal(gk, ok), "K pool differs from the oracle"
+    assert np.array_equal(gv, ov), "V pool differs from the oracle"
+
+
 @pytest.mark.parametrize("scale", [1.0, 0.25, 3.0 / 256, 0.0123, 1e-39])
 def test_handoff_scales(kvq, scale):
     """The quantiser's paths: power-of-two scales (a product), 3 * 2^k (many

@@ -731,6 +731,10 @@ def run_gpu(args, dist, rank, world, local):
             stream.wait_event(ev_out[1])
             e1.record(stream)
             torch.cuda.synchronize()
+            # the last step's result as read back equals the device buffer
+            last = (args.steps - 1) % 2
+            if not torch.equal(h_res[last], results[last].cpu()):
+                raise RuntimeError("pipelined end-to-end loop: result read back differs")
             return dist_max(dist, e0.elapsed_time(e1))
 
         # value: the serial loop, as an autoregressive decode runs (the next

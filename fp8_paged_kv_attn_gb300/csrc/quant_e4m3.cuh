@@ -120,19 +120,27 @@ __device__ __forceinline__ void quantise_words(const uint32_t (&w)[N], const Qua
         left[i] &= ~exact;
       }
     }
-    // what is left, one element at a time (word i of codes: elements 4i..4i+3,
-    // from input words 2i and 2i + 1)
+    // what is left, one element at a time.  Word i of codes holds elements
+    // 4i .. 4i + 3, from input words 2i and 2i + 1; one loop per 16-byte
+    // source word (output words 2 i4 and 2 i4 + 1), bit 8j + h standing for
+    // element j of output word 2 i4 + h.
 #pragma unroll
-    for (int i = 0; i < N / 2; ++i) {
-      uint32_t pw = left[i] & 0x01010101u;  // bit 8j: element 4i + j
+    for (int i4 = 0; i4 < N / 4; ++i4) {
+      uint32_t pw = (left[2 * i4] & 0x01010101u) | ((left[2 * i4 + 1] & 0x01010101u) << 1);
       while (pw) {
-        const int sh = __ffs(pw) - 1;  // 8 j
+        const int bit = __ffs(pw) - 1;
         pw &= pw - 1;
-        const uint32_t ww = (sh & 16) ? w[2 * i + 1] : w[2 * i];
+        const int h = bit & 1, sh = bit & ~1;  // sh = 8 j
+        const uint32_t ww = h ? ((sh & 16) ? w[4 * i4 + 3] : w[4 * i4 + 2])
+                              : ((sh & 16) ? w[4 * i4 + 1] : w[4 * i4]);
         const float x = __uint_as_float((sh & 8) ? (ww & 0xFFFF0000u) : (ww << 16));
         const float d = __fdiv_rn(x, qp.scale);
-        const uint32_t c = static_cast<uint32_t>(f32x2_to_e4m3x2(d, d)) & 0xFFu;
-        o[i] = (o[i] & ~(0xFFu << sh)) | (c << sh);
+        const uint32_t c = (static_cast<uint32_t>(f32x2_to_e4m3x2(d, d)) & 0xFFu) << sh;
+        const uint32_t keep = ~(0xFFu << sh);
+        if (h)
+          o[2 * i4 + 1] = (o[2 * i4 + 1] & keep) | c;
+        else
+          o[2 * i4] = (o[2 * i4] & keep) | c;
       }
     }
     return;

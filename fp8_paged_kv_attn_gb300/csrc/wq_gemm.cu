@@ -13,7 +13,7 @@
 // e4m3 weights with an fp32 scale per output channel.
 //
 // Two kernels, one per regime:
-//  * the TMA-ring kernel (one or two tokens): 64 output
+//  * the TMA-ring kernel (up to 8 tokens, see ring_plan): 64 output
 //    channels per CTA; a producer warp streams the weights into a
 //    shared-memory ring with the TMA engine, eight consumer warps read them
 //    from there; a k split is a thread-block cluster whose partial sums are
@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(32 * kWqWarps, NT == 1 ? 3 : 2) wq_gemm_kernel
 }
 
 // ---------------------------------------------------------------------------
-// TMA-ring kernel (one or two tokens)
+// TMA-ring kernel (up to 8 tokens, one tile of token slots)
 // ---------------------------------------------------------------------------
 //
 // A CTA covers 64 output channels and a range of k groups; a ninth warp's
@@ -1035,8 +1035,9 @@ struct RingPlan {
   size_t smem;
 };
 bool ring_plan(bool int4, int M, int N, int K, int sms, RingPlan *p) {
-  // measured: from three tokens on the register ring is as fast or faster
-  if (M > 2) return false;
+  // one tile of 8 token slots; from three tokens on (below) only where the k
+  // split that the staged x needs still fits one wave
+  if (M > 8) return false;
   constexpr int kPerSm = 3;
   const size_t budget = smem_per_cta3();
   const int groups = K / kWqGroup;
@@ -1050,8 +1051,16 @@ bool ring_plan(bool int4, int M, int N, int K, int sms, RingPlan *p) {
   int ksplit = 1;
   while (ksplit <= kRingMaxCluster && x_bytes(gpc_of(ksplit)) > kXMax) ++ksplit;
   if (ksplit > kRingMaxCluster) return false;
+  // measured: with three or more tokens, a split forced past one wave (the
+  // 28672 x 5120 projection) loses to the register ring (INT4 153 -> 174 us
+  // at three tokens), while the smaller projections of a layer gain 7-20%
+  if (M > 2 && static_cast<int64_t>(tiles) * ksplit > slots) return false;
+  // (a larger cluster also needs more room for the partial sums it sends:
+  // grow only while three ring stages still fit)
   for (int k = ksplit + 1; k <= kRingMaxCluster && k <= groups; ++k)
-    if (static_cast<int64_t>(tiles) * k <= slots) ksplit = k;
+    if (static_cast<int64_t>(tiles) * k <= slots &&
+        ring_layout(int4, 3, gpc_of(k), M, k).total <= budget)
+      ksplit = k;
   const int gpc = gpc_of(ksplit);
   ksplit = (groups + gpc - 1) / gpc;  // no CTA without groups
   int stages = kRingMaxStages;

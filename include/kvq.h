@@ -227,10 +227,11 @@ KVQ_API kvq_status kvq_pages_update(int32_t *free_stack, int32_t *free_count, ui
  * values are scaled by a power of two for the products (exact for every
  * value down to 2^-32 of the token's largest finite |x| in a k range,
  * smaller ones are rounded to 2^-25 of it); NaN and inf propagate.
- * For one or two tokens (when a CTA's share of x fits its shared memory) the
- * weights stream through a shared-memory ring fed by the TMA engine and a k
- * split runs as a thread-block cluster whose partial sums are added in a
- * fixed order: every run gives the same bits.  Otherwise split-K partial
+ * For one or two tokens (when a CTA's share of x fits its shared memory), and
+ * for three to eight tokens where that share needs no k split past one wave
+ * of CTAs, the weights stream through a shared-memory ring fed by the TMA
+ * engine and a k split runs as a thread-block cluster whose partial sums are
+ * added in a fixed order: every run gives the same bits.  Otherwise split-K partial
  * sums are added with fp32 atomics: their order varies from run to run, and
  * atomics flush subnormals, so a result below 2^-126 in magnitude can be off
  * by up to (2 K/128 + 1) * 2^-126.

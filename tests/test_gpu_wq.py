@@ -126,12 +126,13 @@ def test_wq_gemm_full_size_sampled(kvq, wdtype, M, N, K):
     check(wdtype, w, s, x, rows=rows, what=f"{M}x{N}x{K}")
 
 
-# One or two tokens run the TMA-ring kernel (one token its own
-# specialisation): k split over clusters of 1 to 8 CTAs (3, 4, 5, 6 and 7
-# included), rows past N zero-filled by the copy, odd group counts per CTA,
-# one group in all.
+# Up to eight tokens run the TMA-ring kernel where the shape suits it (one
+# token its own specialisation): k split over clusters of 1 to 8 CTAs (3, 4,
+# 5, 6 and 7 included), rows past N zero-filled by the copy, odd group counts
+# per CTA, one group in all; 3 to 8 tokens on the projections of a layer.
 RING_SHAPES = [(1, 200, 1536), (2, 1000, 640), (1, 130, 3584), (2, 5000, 1536), (1, 64, 128),
-               (2, 65, 256), (1, 8000, 768), (2, 777, 2560)]
+               (2, 65, 256), (1, 8000, 768), (2, 777, 2560), (3, 300, 2560), (4, 1792, 5120),
+               (5, 1000, 1536), (7, 130, 640), (8, 5120, 1536), (8, 777, 5120)]
 
 
 @pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])
@@ -144,11 +145,12 @@ def test_wq_ring_shapes(kvq, wdtype, M, N, K):
 
 
 @pytest.mark.parametrize("wdtype", [0, 1], ids=["int4", "e4m3"])
-def test_wq_ring_deterministic(kvq, wdtype):
+@pytest.mark.parametrize("M", [2, 8])
+def test_wq_ring_deterministic(kvq, wdtype, M):
     """The split-K sums of the ring kernel are added in cluster-rank order, not
     by atomics: two calls give the same bits, and no wait gives up."""
-    rng = np.random.default_rng(90 + wdtype)
-    M, N, K = 2, 1792, 5120
+    rng = np.random.default_rng(90 + wdtype + M)
+    N, K = (1792, 5120) if M == 2 else (5120, 1536)
     w, s, x = pins.random_wq_case(rng, wdtype, M, N, K)
     sd = dev(s.view(np.int16)) if wdtype == oracle.W_INT4 else dev(s)
     xd = dev(x.view(np.int16)).view(torch.bfloat16)
